@@ -1,0 +1,265 @@
+/*
+ * Plain CPU oracle for the depth-routing read (test infrastructure only).
+ *
+ * This file is the checker, not the product: only the tests, the package's
+ * smoke check and the benchmark's CPU-baseline leg call it. It shares no
+ * code, header or constant with the CUDA path.
+ *
+ * Everything is float64 and written as the definitions read, one token at a
+ * time (tokens are independent: the attention runs over depth, not over
+ * tokens). OpenMP, when available, only splits the token loop.
+ *
+ * Notation (per token; N sources s_0..s_{N-1} in R^d; H heads):
+ *   key coordinates   : the last r of the d coordinates (r = d is the plain
+ *                       full-width key of "Multi-Head Attention Residuals",
+ *                       Eq. 3; r < d is the sliced key of "Low-Rank Attention
+ *                       Residuals", Eq. 11);
+ *   value slice of h  : coordinates [h*d/H, (h+1)*d/H)            (MHAR Eq. 3)
+ *   key slice of h    : coordinates d-r + [h*r/H, (h+1)*r/H)
+ *   inv_n             : (mean over the RMS coordinates of s_n^2 + eps)^(-1/2);
+ *                       the RMS coordinates are the key coordinates
+ *                       ("slice" norm, LR-AttnRes Eq. 13 first line) or all d
+ *                       ("full" norm: MHAR Appendix E, and the full-width-RMS
+ *                       control of LR-AttnRes Eq. 13 second line)
+ *   z_{n,h}           : inv_n * sum_{c in key slice h} q_c g_c s_{n,c}
+ *   alpha_{n,h}       : softmax over n of z_{.,h}                    (Eq. 2/3)
+ *   out_c             : sum_n alpha_{n,h(c)} s_{n,c}                   (Eq. 3)
+ *   lse_h             : max_n z + log sum_n exp(z - max)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_BAD_ARG 1
+#define ORC_NO_MEMORY 2
+
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static int check_shape(int N, int64_t T, int d, int r, int H)
+{
+    if (N < 1 || T < 0 || d < 1 || r < 1 || r > d || H < 1) return ORC_BAD_ARG;
+    if (d % H != 0 || r % H != 0) return ORC_BAD_ARG;
+    return ORC_OK;
+}
+
+/* Inverse RMS of one token's vector over the RMS coordinates.
+ * "Multi-Head Attention Residuals", Appendix E: r = (||s||^2/d + eps)^(-1/2);
+ * "Low-Rank Attention Residuals", Eq. 13 (slice: over the last r coordinates). */
+static double inv_rms_one(const double *x, int d, int r, int full_width, double eps)
+{
+    int c0 = full_width ? 0 : d - r;
+    int w = d - c0;
+    double ss = 0.0;
+    for (int c = c0; c < d; ++c) ss += x[c] * x[c];
+    return 1.0 / sqrt(ss / (double)w + eps);
+}
+
+/* inv[t] for every token of one [T,d] source. */
+int orc_inv_rms(const double *x, int64_t T, int d, int r, int full_width, double eps, double *inv)
+{
+    if (check_shape(1, T, d, r, 1)) return ORC_BAD_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) inv[t] = inv_rms_one(x + t * d, d, r, full_width, eps);
+    return ORC_OK;
+}
+
+/*
+ * Forward of one routing site ("Multi-Head Attention Residuals", Eq. 3 and
+ * Figure 3; "Low-Rank Attention Residuals", Eq. 8-11 for r < d).
+ *   src[n]  : [T,d] source n            q, g : [r]
+ *   out     : [T,d]   lse : [T,H]       alpha: [T,N,H] or NULL
+ * Softmax is the explicit two-pass form: max, then normalised exponentials.
+ */
+int orc_route_fwd(const double *const *src, int N, int64_t T, int d, int r, int H,
+                  int full_width, double eps, const double *q, const double *g,
+                  double *out, double *lse, double *alpha)
+{
+    if (check_shape(N, T, d, r, H)) return ORC_BAD_ARG;
+    const int K = d / H, Kr = r / H, c_key = d - r;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *z = (double *)malloc(sizeof(double) * (size_t)N * H);
+        double *a = (double *)malloc(sizeof(double) * (size_t)N * H);
+        if (!z || !a) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            if (!z || !a) continue;
+            /* scores z_{n,h} = q_h . RMSNorm(s_n)_[h] (g folded into the key) */
+            for (int n = 0; n < N; ++n) {
+                const double *s = src[n] + t * d;
+                double inv = inv_rms_one(s, d, r, full_width, eps);
+                for (int h = 0; h < H; ++h) {
+                    double dot = 0.0;
+                    for (int k = 0; k < Kr; ++k) {
+                        int j = h * Kr + k; /* index into q, g */
+                        dot += q[j] * (g ? g[j] : 1.0) * s[c_key + j];
+                    }
+                    z[n * H + h] = inv * dot;
+                }
+            }
+            /* softmax over sources, per head */
+            for (int h = 0; h < H; ++h) {
+                double m = z[h];
+                for (int n = 1; n < N; ++n)
+                    if (z[n * H + h] > m) m = z[n * H + h];
+                double sum = 0.0;
+                for (int n = 0; n < N; ++n) sum += exp(z[n * H + h] - m);
+                for (int n = 0; n < N; ++n) a[n * H + h] = exp(z[n * H + h] - m) / sum;
+                lse[t * H + h] = m + log(sum);
+            }
+            /* mix: each head mixes only its own value slice */
+            for (int c = 0; c < d; ++c) {
+                int h = c / K;
+                double acc = 0.0;
+                for (int n = 0; n < N; ++n) acc += a[n * H + h] * src[n][t * d + c];
+                out[t * d + c] = acc;
+            }
+            if (alpha) memcpy(alpha + t * (int64_t)N * H, a, sizeof(double) * (size_t)N * H);
+        }
+        free(z);
+        free(a);
+    }
+    return bad ? ORC_NO_MEMORY : ORC_OK;
+}
+
+/*
+ * Backward of one routing site, written from the value/routing decomposition
+ * of "Low-Rank Attention Residuals", Eq. 15 and Lemma 2 (Eq. 20), applied to
+ * each head's own softmax:
+ *   dL/ds_n = sum_h [ alpha_{n,h} G_[h]  +  alpha_{n,h} <G_[h], s_{n,[h]} - out_[h]> grad z_{n,h} ]
+ * with G = dL/dout, and the score gradient of Eq. 21 (slice norm) or Eq. 22
+ * (full-width norm), extended by the head's key slice and the norm weight g:
+ *   grad z_{n,h} = inv_n (q g) on key slice h  -  inv_n^3 zraw_{n,h} s_n / w  on the RMS coordinates,
+ *   zraw_{n,h}   = sum_{c in key slice h} q_c g_c s_{n,c},  w = width of the RMS coordinates.
+ * Query and norm-weight gradients follow from z = inv * sum q g s
+ * ("Multi-Head Attention Residuals", Appendix E, dq and dg):
+ *   dq_c = sum_{t,n} fb_{n,h(c)} inv_n g_c s_{n,c},   dg_c = sum_{t,n} fb_{n,h(c)} inv_n q_c s_{n,c},
+ * where fb_{n,h} = alpha_{n,h} <G_[h], s_{n,[h]} - out_[h]> is the routing feedback.
+ *   dsrc[n] : [T,d], ADDED to (the caller zeroes it; a row read by several
+ *             sites sums their contributions)
+ *   dq, dg  : [r], overwritten; dg may be NULL. g may be NULL (= ones).
+ */
+int orc_route_bwd(const double *const *src, int N, int64_t T, int d, int r, int H,
+                  int full_width, double eps, const double *q, const double *g,
+                  const double *dout, double *const *dsrc, double *dq, double *dg)
+{
+    if (check_shape(N, T, d, r, H)) return ORC_BAD_ARG;
+    const int K = d / H, Kr = r / H, c_key = d - r;
+    const int c_rms = full_width ? 0 : d - r, w_rms = d - c_rms;
+    for (int j = 0; j < r; ++j) {
+        dq[j] = 0.0;
+        if (dg) dg[j] = 0.0;
+    }
+    int bad = 0;
+#pragma omp parallel
+    {
+        size_t nh = (size_t)N * H;
+        double *inv = (double *)malloc(sizeof(double) * N);
+        double *zraw = (double *)malloc(sizeof(double) * nh);
+        double *a = (double *)malloc(sizeof(double) * nh);
+        double *fb = (double *)malloc(sizeof(double) * nh);
+        double *o = (double *)malloc(sizeof(double) * d);
+        double *dq_p = (double *)calloc((size_t)r, sizeof(double));
+        double *dg_p = (double *)calloc((size_t)r, sizeof(double));
+        int ok = inv && zraw && a && fb && o && dq_p && dg_p;
+        if (!ok) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            if (!ok) continue;
+            const double *G = dout + t * d;
+            /* recompute the forward of this token: inv, raw scores, alpha, out */
+            for (int n = 0; n < N; ++n) {
+                const double *s = src[n] + t * d;
+                inv[n] = inv_rms_one(s, d, r, full_width, eps);
+                for (int h = 0; h < H; ++h) {
+                    double dot = 0.0;
+                    for (int k = 0; k < Kr; ++k) {
+                        int j = h * Kr + k;
+                        dot += q[j] * (g ? g[j] : 1.0) * s[c_key + j];
+                    }
+                    zraw[n * H + h] = dot;
+                }
+            }
+            for (int h = 0; h < H; ++h) {
+                double m = inv[0] * zraw[h];
+                for (int n = 1; n < N; ++n) {
+                    double zz = inv[n] * zraw[n * H + h];
+                    if (zz > m) m = zz;
+                }
+                double sum = 0.0;
+                for (int n = 0; n < N; ++n) sum += exp(inv[n] * zraw[n * H + h] - m);
+                for (int n = 0; n < N; ++n) a[n * H + h] = exp(inv[n] * zraw[n * H + h] - m) / sum;
+            }
+            for (int c = 0; c < d; ++c) {
+                int h = c / K;
+                double acc = 0.0;
+                for (int n = 0; n < N; ++n) acc += a[n * H + h] * src[n][t * d + c];
+                o[c] = acc;
+            }
+            /* routing feedback fb_{n,h} = alpha <G_[h], s_[h] - out_[h]>  (Eq. 15, 20) */
+            for (int n = 0; n < N; ++n) {
+                const double *s = src[n] + t * d;
+                for (int h = 0; h < H; ++h) {
+                    double dot = 0.0;
+                    for (int c = h * K; c < (h + 1) * K; ++c) dot += G[c] * (s[c] - o[c]);
+                    fb[n * H + h] = a[n * H + h] * dot;
+                }
+            }
+            for (int n = 0; n < N; ++n) {
+                const double *s = src[n] + t * d;
+                double *ds = dsrc[n] + t * d;
+                /* direct value gradient alpha_{n,h(c)} G_c */
+                for (int c = 0; c < d; ++c) ds[c] += a[n * H + c / K] * G[c];
+                /* routing feedback times the score gradient (Eq. 21 / 22) */
+                double iv = inv[n], iv3 = iv * iv * iv;
+                for (int h = 0; h < H; ++h) {
+                    double f = fb[n * H + h];
+                    for (int k = 0; k < Kr; ++k) {
+                        int j = h * Kr + k, c = c_key + j;
+                        ds[c] += f * iv * q[j] * (g ? g[j] : 1.0);
+                        dq_p[j] += f * iv * (g ? g[j] : 1.0) * s[c];
+                        dg_p[j] += f * iv * q[j] * s[c];
+                    }
+                    double coef = f * iv3 * zraw[n * H + h] / (double)w_rms;
+                    for (int c = c_rms; c < d; ++c) ds[c] -= coef * s[c];
+                }
+            }
+        }
+        if (ok) {
+#pragma omp critical
+            {
+                for (int j = 0; j < r; ++j) {
+                    dq[j] += dq_p[j];
+                    if (dg) dg[j] += dg_p[j];
+                }
+            }
+        }
+        free(inv);
+        free(zraw);
+        free(a);
+        free(fb);
+        free(o);
+        free(dq_p);
+        free(dg_p);
+    }
+    return bad ? ORC_NO_MEMORY : ORC_OK;
+}

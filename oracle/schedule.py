@@ -1,0 +1,69 @@
+"""Source schedules: which bank rows each routing site reads (oracle side).
+
+Full routing ("Multi-Head Attention Residuals", Sec. 2.2 and Figure 3;
+"Low-Rank Attention Residuals", Eq. 4): the sources are the token embedding
+plus every sublayer output, N = 2L+1 in all; routing site i (1-based) reads
+the first i sources ("replacement routing": each sublayer appends its raw
+output as a new source).
+
+Block routing ("Low-Rank Attention Residuals", Eq. 5-6 and the Figure 11
+pseudocode): M = 2L sublayers are grouped into NB blocks whose last sublayers
+are ceil(M*j/NB), j = 1..NB. After sublayer t the running partial sum takes
+o_t; at a block end the partial sum becomes a completed block source and the
+partial accumulator empties. The read after sublayer t sees the embedding,
+the completed block sums and, if nonempty, the current partial sum.
+
+Bank layout used by both sides of the parity checks: row 0 holds the
+embedding; in full routing row j holds sublayer output j; in block routing
+row t (1..M) holds the partial sum right after sublayer t, kept as an
+immutable version so that the backward of every site sees the value its
+forward read (a completed block is the last version of its block).
+"""
+
+from __future__ import annotations
+
+__all__ = ["full_sites", "block_ends", "block_plan"]
+
+
+def full_sites(num_sources: int) -> list[list[int]]:
+    """Row lists of full routing: site i (i = 1..num_sources) reads rows 0..i-1."""
+    if num_sources < 1:
+        raise ValueError("need at least one source")
+    return [list(range(i)) for i in range(1, num_sources + 1)]
+
+
+def block_ends(M: int, NB: int | None = None) -> list[int]:
+    """Block end sublayers {ceil(M*j/NB) : j = 1..NB}; NB=None means NB = M."""
+    if M < 1:
+        raise ValueError("need at least one sublayer")
+    nb = M if NB is None else min(NB, M)
+    if nb < 1:
+        raise ValueError("need at least one block")
+    return sorted({(M * j + nb - 1) // nb for j in range(1, nb + 1)})
+
+
+def block_plan(M: int, NB: int | None = None) -> dict:
+    """Bank rows and per-site row lists of block routing over M sublayers.
+
+    Returns a dict with
+      ``ends``    : sorted block-end sublayers,
+      ``row_ops`` : ``row_ops[0] = ("emb",)``; for t = 1..M either
+                    ``("copy", t)`` (row t = o_t, the first write of a block)
+                    or ``("acc", p, t)`` (row t = row p + o_t),
+      ``sites``   : ``sites[0] = [0]`` (the read that feeds sublayer 1) and
+                    ``sites[t]`` = completed block rows + [current partial row]
+                    for the read after sublayer t.
+    """
+    ends = set(block_ends(M, NB))
+    blocks = [0]
+    partial = None
+    row_ops: list[tuple] = [("emb",)]
+    sites = [[0]]
+    for t in range(1, M + 1):
+        row_ops.append(("copy", t) if partial is None else ("acc", partial, t))
+        partial = t
+        if t in ends:
+            blocks.append(partial)
+            partial = None
+        sites.append(blocks + ([] if partial is None else [partial]))
+    return {"ends": sorted(ends), "row_ops": row_ops, "sites": sites}

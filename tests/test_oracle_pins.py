@@ -1,0 +1,302 @@
+"""Pins for the CPU oracle, against things other than the oracle itself.
+
+* brute force: an einsum restatement of the pages' route pseudocode
+  ("Multi-Head Attention Residuals" Figure 3 / Figure 7, "Low-Rank Attention
+  Residuals" Figure 11), softmax/logsumexp from scipy;
+* torch autograd (float64, CPU) on a torch restatement of the forward, for
+  every gradient the oracle's closed form gives;
+* central finite differences of the oracle's own forward;
+* the invariants the pages state (H=1 is single-head AttnRes, heads are
+  independent slices, weights sum to one, one-hot read, zero query gives the
+  mean, one source is the identity, permutation, scale invariance, gradient
+  support outside the key slice, orthogonal invariance of RMSNorm).
+
+Each pin is chosen so that a plausible slip in the oracle (dropped term, wrong
+sign, wrong slice index, transposed operand) fails at least one of them.
+"""
+
+import numpy as np
+import pytest
+import scipy.special as sps
+
+import synth
+
+
+def _case(seed, N, T, d, H, r, qstd=0.7, gkind="random"):
+    srcs = [synth.misc_normal(seed, 100 + n, (T, d), 1.0 / (1 + 0.3 * n)).astype(np.float64)
+            for n in range(N)]
+    q = synth.misc_normal(seed, 1, (r,), qstd).astype(np.float64)
+    if gkind == "random":
+        g = 1.0 + synth.misc_normal(seed, 2, (r,), 0.2).astype(np.float64)
+    else:
+        g = np.ones(r)
+    G = synth.misc_normal(seed, 3, (T, d)).astype(np.float64)
+    return srcs, q, g, G
+
+
+def _einsum_route(V, q, g, H, r, eps, full_width):
+    """Brute force: stack, normalise keys, per-head logits, softmax over depth, mix."""
+    N, T, d = V.shape
+    K = V[..., d - r:]
+    ms = (V * V).mean(-1, keepdims=True) if full_width else (K * K).mean(-1, keepdims=True)
+    khat = K / np.sqrt(ms + eps) * g
+    logits = np.einsum("he,nthe->nth", q.reshape(H, r // H), khat.reshape(N, T, H, r // H))
+    alpha = sps.softmax(logits, axis=0)
+    mixed = np.einsum("nth,nthe->the", alpha, V.reshape(N, T, H, d // H))
+    return mixed.reshape(T, d), sps.logsumexp(logits, axis=0), alpha
+
+
+def _torch_route(V, q, g, H, r, eps, full_width):
+    import torch
+    N, T, d = V.shape
+    K = V[..., d - r:]
+    ms = (V * V).mean(-1, keepdim=True) if full_width else (K * K).mean(-1, keepdim=True)
+    khat = K * torch.rsqrt(ms + eps) * g
+    logits = torch.einsum("he,nthe->nth", q.view(H, r // H), khat.view(N, T, H, r // H))
+    alpha = torch.softmax(logits, dim=0)
+    mixed = torch.einsum("nth,nthe->the", alpha, V.view(N, T, H, d // H))
+    return mixed.reshape(T, d)
+
+
+def _nmax(a, b):
+    a, b = np.asarray(a), np.asarray(b)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+SHAPES = [
+    # N, T, d, H, r, full_width
+    (1, 5, 8, 1, 8, False),
+    (3, 7, 8, 2, 8, False),
+    (4, 6, 16, 4, 16, False),
+    (6, 5, 32, 4, 32, False),
+    (5, 4, 32, 2, 16, False),   # low-rank keys
+    (6, 3, 32, 4, 8, False),    # low-rank keys, 2-wide key slices
+    (5, 4, 32, 2, 16, True),    # full-width-RMS control
+    (2, 9, 24, 3, 24, False),   # odd head count
+]
+
+
+@pytest.mark.parametrize("N,T,d,H,r,fw", SHAPES)
+def test_forward_matches_einsum_brute_force(orc, N, T, d, H, r, fw):
+    srcs, q, g, _ = _case(11, N, T, d, H, r)
+    out, lse, alpha = orc.route_fwd(srcs, q, g, H, r=r, eps=1e-6, full_width=fw, want_alpha=True)
+    ref_out, ref_lse, ref_alpha = _einsum_route(np.stack(srcs), q, g, H, r, 1e-6, fw)
+    assert _nmax(out, ref_out) < 1e-12
+    assert _nmax(lse, ref_lse) < 1e-12
+    assert _nmax(alpha, ref_alpha.transpose(1, 0, 2)) < 1e-12
+
+
+@pytest.mark.parametrize("N,T,d,H,r,fw", SHAPES)
+def test_backward_matches_torch_autograd(orc, N, T, d, H, r, fw):
+    import torch
+    srcs, q, g, G = _case(12, N, T, d, H, r)
+    dsrc, dq, dg = orc.route_bwd(srcs, q, g, G, H, r=r, eps=1e-6, full_width=fw)
+    V = torch.tensor(np.stack(srcs), dtype=torch.float64, requires_grad=True)
+    tq = torch.tensor(q, requires_grad=True)
+    tg = torch.tensor(g, requires_grad=True)
+    out = _torch_route(V, tq, tg, H, r, 1e-6, fw)
+    (out * torch.tensor(G)).sum().backward()
+    assert _nmax(np.stack(dsrc), V.grad.numpy()) < 1e-11
+    assert _nmax(dq, tq.grad.numpy()) < 1e-10
+    assert _nmax(dg, tg.grad.numpy()) < 1e-10
+
+
+@pytest.mark.parametrize("fw,r", [(False, 16), (False, 32), (True, 16)])
+def test_backward_finite_differences(orc, fw, r):
+    N, T, d, H = 4, 3, 32, 4 if r == 32 else 2
+    srcs, q, g, G = _case(13, N, T, d, H, r)
+    dsrc, dq, dg = orc.route_bwd(srcs, q, g, G, H, r=r, full_width=fw)
+
+    def loss(ss, qq, gg):
+        o, _ = orc.route_fwd(ss, qq, gg, H, r=r, full_width=fw)
+        return float(np.sum(o * G))
+
+    h = 1e-6
+    rng = np.random.default_rng(0)
+    for _ in range(12):
+        n, t, c = rng.integers(N), rng.integers(T), rng.integers(d)
+        sp = [s.copy() for s in srcs]
+        sm = [s.copy() for s in srcs]
+        sp[n][t, c] += h
+        sm[n][t, c] -= h
+        fd = (loss(sp, q, g) - loss(sm, q, g)) / (2 * h)
+        assert abs(fd - dsrc[n][t, c]) <= 1e-6 * max(1.0, abs(fd))
+    for j in rng.choice(r, size=6, replace=False):
+        for which, ana in (("q", dq), ("g", dg)):
+            vp, vm = (q.copy(), q.copy()) if which == "q" else (g.copy(), g.copy())
+            vp[j] += h
+            vm[j] -= h
+            if which == "q":
+                fd = (loss(srcs, vp, g) - loss(srcs, vm, g)) / (2 * h)
+            else:
+                fd = (loss(srcs, q, vp) - loss(srcs, q, vm)) / (2 * h)
+            assert abs(fd - ana[j]) <= 1e-6 * max(1.0, abs(fd))
+
+
+def test_single_head_is_attention_residuals(orc):
+    """H=1 is Eq. 2 of the MHAR page: one softmax over depth read by all d coordinates."""
+    N, T, d = 5, 6, 16
+    srcs, q, g, _ = _case(14, N, T, d, 1, d)
+    out, lse = orc.route_fwd(srcs, q, g, 1)
+    V = np.stack(srcs)
+    rms = np.sqrt((V * V).mean(-1) + 1e-6)                  # [N, T]
+    logits = np.einsum("d,ntd->nt", q * g, V) / rms         # q^T RMSNorm(s_i)
+    w = np.exp(logits - logits.max(0)) / np.exp(logits - logits.max(0)).sum(0)
+    assert _nmax(out, np.einsum("nt,ntd->td", w, V)) < 1e-13
+
+
+@pytest.mark.parametrize("d,H,r", [(16, 4, 16), (32, 2, 16), (24, 3, 12)])
+def test_heads_are_independent_single_head_reads(orc, d, H, r):
+    """Head h of MHAR equals a single-head read whose query is zero outside key slice h
+    (Eq. 3: each head scores only its own slice and mixes only its own slice)."""
+    N, T = 4, 5
+    srcs, q, g, G = _case(15, N, T, d, H, r)
+    out, lse = orc.route_fwd(srcs, q, g, H, r=r)
+    K, Kr = d // H, r // H
+    for h in range(H):
+        qm = np.zeros_like(q)
+        qm[h * Kr:(h + 1) * Kr] = q[h * Kr:(h + 1) * Kr]
+        o1, l1 = orc.route_fwd(srcs, qm, g, 1, r=r)
+        assert _nmax(out[:, h * K:(h + 1) * K], o1[:, h * K:(h + 1) * K]) < 1e-13
+        assert _nmax(lse[:, h], l1[:, 0]) < 1e-13
+        Gm = np.zeros_like(G)
+        Gm[:, h * K:(h + 1) * K] = G[:, h * K:(h + 1) * K]
+        ds_h, dq_h, dg_h = orc.route_bwd(srcs, q, g, Gm, H, r=r)
+        ds_1, dq_1, dg_1 = orc.route_bwd(srcs, qm, g, Gm, 1, r=r)
+        assert _nmax(np.stack(ds_h), np.stack(ds_1)) < 1e-12
+        sl = slice(h * Kr, (h + 1) * Kr)
+        assert _nmax(dq_h[sl], dq_1[sl]) < 1e-12
+        assert _nmax(dg_h[sl], dg_1[sl]) < 1e-12
+
+
+def test_weights_sum_to_one_and_lse(orc):
+    srcs, q, g, _ = _case(16, 7, 9, 32, 4, 32, qstd=2.0)
+    _, lse, alpha = orc.route_fwd(srcs, q, g, 4, want_alpha=True)
+    assert np.max(np.abs(alpha.sum(1) - 1.0)) < 1e-14
+    assert np.all(alpha > 0)
+
+
+def test_one_hot_read_when_query_scaled_up(orc):
+    N, T, d, H = 5, 8, 16, 2
+    srcs, q, g, G = _case(17, N, T, d, H, d, gkind="ones")
+    V = np.stack(srcs)
+    rms = np.sqrt((V * V).mean(-1) + 1e-6)
+    z = np.einsum("he,nthe->nth", q.reshape(H, d // H), V.reshape(N, T, H, d // H)) / rms[..., None]
+    zs = np.sort(z, axis=0)
+    gap = float(np.min(zs[-1] - zs[-2]))
+    assert gap > 0
+    lam = 60.0 / gap
+    out, _ = orc.route_fwd(srcs, lam * q, g, H)
+    arg = np.argmax(z, axis=0)                               # [T, H]
+    K = d // H
+    exp_out = np.empty_like(out)
+    for t in range(T):
+        for h in range(H):
+            exp_out[t, h * K:(h + 1) * K] = V[arg[t, h], t, h * K:(h + 1) * K]
+    assert _nmax(out, exp_out) < 1e-12
+    _, dq, dg = orc.route_bwd(srcs, lam * q, g, G, H)
+    assert np.max(np.abs(dq)) < 1e-12
+
+
+def test_zero_query_reads_the_mean(orc):
+    N, T, d, H = 6, 5, 16, 4
+    srcs, q, g, G = _case(18, N, T, d, H, d)
+    out, lse = orc.route_fwd(srcs, np.zeros_like(q), g, H)
+    assert _nmax(out, np.mean(np.stack(srcs), 0)) < 1e-14
+    assert np.max(np.abs(lse - np.log(N))) < 1e-14
+    _, dq, dg = orc.route_bwd(srcs, np.zeros_like(q), g, G, H)
+    assert np.all(dg == 0.0)
+    assert np.max(np.abs(dq)) > 0
+
+
+def test_single_source_is_identity(orc):
+    T, d, H = 7, 16, 4
+    srcs, q, g, G = _case(19, 1, T, d, H, d)
+    out, lse = orc.route_fwd(srcs, q, g, H)
+    assert np.array_equal(out, srcs[0])
+    ds, dq, dg = orc.route_bwd(srcs, q, g, G, H)
+    assert np.array_equal(ds[0], G)
+    assert np.all(dq == 0.0) and np.all(dg == 0.0)
+    z = orc.inv_rms(srcs[0])[:, None] * np.einsum("he,the->th", (q * g).reshape(H, 4),
+                                                 srcs[0].reshape(T, H, 4))
+    assert _nmax(lse, z) < 1e-14
+
+
+def test_permutation_equivariance(orc):
+    N, T, d, H = 5, 6, 16, 2
+    srcs, q, g, G = _case(20, N, T, d, H, d)
+    perm = [3, 0, 4, 2, 1]
+    o1, l1, a1 = orc.route_fwd(srcs, q, g, H, want_alpha=True)
+    o2, l2, a2 = orc.route_fwd([srcs[p] for p in perm], q, g, H, want_alpha=True)
+    assert _nmax(o2, o1) < 1e-14 and _nmax(l2, l1) < 1e-14
+    assert _nmax(a2, a1[:, perm, :]) < 1e-14
+    d1, q1, g1 = orc.route_bwd(srcs, q, g, G, H)
+    d2, q2, g2 = orc.route_bwd([srcs[p] for p in perm], q, g, G, H)
+    for i, p in enumerate(perm):
+        assert _nmax(d2[i], d1[p]) < 1e-13
+    assert _nmax(q2, q1) < 1e-12 and _nmax(g2, g1) < 1e-12
+
+
+def test_source_scale_does_not_change_weights(orc):
+    N, T, d, H = 4, 5, 16, 4
+    srcs, q, g, _ = _case(21, N, T, d, H, d)
+    _, _, a1 = orc.route_fwd(srcs, q, g, H, eps=0.0, want_alpha=True)
+    s2 = list(srcs)
+    s2[2] = srcs[2] * 7.5
+    _, _, a2 = orc.route_fwd(s2, q, g, H, eps=0.0, want_alpha=True)
+    assert _nmax(a2, a1) < 1e-13
+
+
+def test_outside_key_slice_gets_only_the_direct_value_gradient(orc):
+    """Cor. 2.1 of the LR-AttnRes page: with slice normalisation the gradient outside
+    the key slice is alpha * dL/dout, exactly."""
+    N, T, d, H, r = 5, 4, 32, 2, 8
+    srcs, q, g, G = _case(22, N, T, d, H, r)
+    _, _, a = orc.route_fwd(srcs, q, g, H, r=r, want_alpha=True)
+    ds, _, _ = orc.route_bwd(srcs, q, g, G, H, r=r)
+    K = d // H
+    for n in range(N):
+        direct = np.repeat(a[:, n, :], K, axis=1) * G
+        assert np.array_equal(ds[n][:, :d - r], direct[:, :d - r])
+        assert np.max(np.abs(ds[n][:, d - r:] - direct[:, d - r:])) > 0
+    # the full-width control keeps a radial term outside the slice (Eq. 16, second line)
+    ds_c, _, _ = orc.route_bwd(srcs, q, g, G, H, r=r, full_width=True)
+    _, _, ac = orc.route_fwd(srcs, q, g, H, r=r, full_width=True, want_alpha=True)
+    direct_c = np.repeat(ac[:, 0, :], K, axis=1) * G
+    assert np.max(np.abs(ds_c[0][:, :d - r] - direct_c[:, :d - r])) > 1e-6
+
+
+def test_rms_orthogonal_invariance(orc):
+    """RMSNorm(Ro) = R RMSNorm(o) for orthogonal R (LR-AttnRes Eq. 18): rotating the
+    non-key coordinates leaves the weights unchanged under the full-width norm, and
+    rotating the key slice together with the query leaves them unchanged under the
+    slice norm (H=1). A non-Euclidean norm would break either."""
+    N, T, d, r = 4, 6, 24, 8
+    srcs, q, g, _ = _case(23, N, T, d, 1, r, gkind="ones")
+    Qa, _ = np.linalg.qr(synth.misc_normal(1, 9, (d - r, d - r)).astype(np.float64))
+    rot = [np.concatenate([s[:, :d - r] @ Qa.T, s[:, d - r:]], axis=1) for s in srcs]
+    _, _, a1 = orc.route_fwd(srcs, q, g, 1, r=r, full_width=True, want_alpha=True)
+    o2, _, a2 = orc.route_fwd(rot, q, g, 1, r=r, full_width=True, want_alpha=True)
+    assert _nmax(a2, a1) < 1e-13
+    Qb, _ = np.linalg.qr(synth.misc_normal(1, 10, (r, r)).astype(np.float64))
+    rot_k = [np.concatenate([s[:, :d - r], s[:, d - r:] @ Qb.T], axis=1) for s in srcs]
+    _, _, b1 = orc.route_fwd(srcs, q, g, 1, r=r, want_alpha=True)
+    _, _, b2 = orc.route_fwd(rot_k, Qb @ q, g, 1, r=r, want_alpha=True)
+    assert _nmax(b2, b1) < 1e-13
+
+
+def test_low_rank_with_full_key_width_is_plain_routing(orc):
+    """r = d reduces LR-AttnRes to AttnRes (LR page, Sec. 3.3); the slice norm and the
+    full-width norm then coincide."""
+    srcs, q, g, G = _case(24, 4, 5, 16, 2, 16)
+    o1, l1 = orc.route_fwd(srcs, q, g, 2, r=16, full_width=False)
+    o2, l2 = orc.route_fwd(srcs, q, g, 2, r=16, full_width=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_inv_rms_definition(orc):
+    x = np.array([[3.0, 4.0, 0.0, 0.0], [1.0, 1.0, 1.0, 1.0]])
+    inv = orc.inv_rms(x, r=4, eps=0.0)
+    assert np.allclose(inv, [1.0 / np.sqrt(25.0 / 4.0), 1.0], rtol=0, atol=1e-15)
+    inv_tail = orc.inv_rms(x, r=2, eps=0.0)
+    assert inv_tail[1] == 1.0 and np.isinf(inv_tail[0])
