@@ -1,0 +1,407 @@
+"""Benchmark: routing time of one microbatch (every site's forward + backward).
+
+One step = one microbatch of the depth-routing path: the source appends
+(inverse RMS), the forward of every routing site in order, and the backward of
+every site in reverse (source gradients accumulated in the shared fp32 rows,
+dq/dg reduced). Default workload: the 1B-shaped model (d=1280, 36 layers ->
+73 sites, H=8, T=16x1024 tokens, bf16).
+
+Prints ONE JSON line (rank 0). ``value`` is whole-job tokens/s with inputs
+resident in HBM (each step captured as two CUDA graphs, forward and
+backward, replayed back to back); ``e2e`` is the same metric through the
+public API with the step's inputs copied from pinned host memory and its
+parameter gradients copied back, inside the timed region.
+
+Multi-GPU (torchrun): every rank routes its own microbatch (tokens shard with
+no exchange in the routing path), weak scaling; time = max over ranks.
+
+``--impl reference`` times the CPU oracle on the host cores instead (a bounded
+token sample of the same workload per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "route_bwd_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "routing ms per microbatch fwd+bwd (all sites), tokens/s, % of HBM roofline"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="1B")
+    p.add_argument("--heads", type=int, default=None)
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target wall time of the CPU-oracle sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--eager", action="store_true", help="no CUDA graphs")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "depth_wise_attention_ar_gb300", "csrc")
+    for name in ("kernels_bwd.cuh", "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(config: str, H: int):
+    """ncu DRAM bytes per backward launch, if measured on the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        e = rec.get(f"{config}/H{H}")
+        if e and e.get("kernel_hash") == kernel_hash():
+            return e["bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(cfg, H, seconds: float, steps: int = 1):
+    """The oracle (float64 C, OpenMP over tokens) on a token sample of the workload."""
+    import numpy as np
+
+    import oracle
+    import synth
+    from oracle import schedule, storage
+
+    oplan = schedule.block_plan(cfg.M, cfg.NB)
+    run = list(cfg.sites) if cfg.sites is not None else list(range(len(oplan["sites"])))
+    nrows = max(max(oplan["sites"][s]) for s in run) + 1
+
+    def one(Ts):
+        outs = [synth.storage_to_f64(synth.sublayer_output(1, j, Ts, cfg.d, cfg.dtype), cfg.dtype)
+                for j in range(nrows)]
+        rows = storage.block_bank(outs, {"row_ops": oplan["row_ops"][:nrows]}, cfg.dtype)
+        qs = {s: synth.site_query(1, s, cfg.r).astype(np.float64) for s in run}
+        gouts = {s: synth.storage_to_f64(synth.site_dout(1, s, Ts, cfg.d, cfg.dtype), cfg.dtype)
+                 for s in run}
+        t0 = time.perf_counter()
+        for s in run:
+            oracle.route_fwd([rows[j] for j in oplan["sites"][s]], qs[s], None, H, r=cfg.r)
+        dsrc = {j: np.zeros((Ts, cfg.d)) for j in range(nrows)}
+        for s in reversed(run):
+            oracle.route_bwd([rows[j] for j in oplan["sites"][s]], qs[s], None, gouts[s], H,
+                             r=cfg.r, dsrc=[dsrc[j] for j in oplan["sites"][s]])
+        return time.perf_counter() - t0
+
+    threads = oracle.threads()
+    probe = max(threads, 8)
+    tp = one(probe)
+    Ts = int(max(probe, min(cfg.T, probe * seconds / max(tp, 1e-6))))
+    Ts = max(threads, (Ts // threads) * threads)
+    times = [one(Ts) for _ in range(steps)]
+    dt = sum(times) / len(times)
+    return {"value": Ts / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{Ts} of {cfg.T} tokens, every site forward + backward in reverse, "
+                      f"float64 oracle, {dt:.1f} s per sample"}, dt, Ts
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    from depth_wise_attention_ar_gb300 import binding, workload
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = workload.CONFIGS[args.config]
+    H = args.heads or cfg.H
+    inputs = synth.DeviceInputs(seed=1000 + rank, device=f"cuda:{local}")
+    mb = workload.Microbatch(cfg, H, inputs, device=f"cuda:{local}")
+    stream = torch.cuda.Stream()
+    mbytes = workload.model_bytes(cfg, mb.plan, H)
+
+    # warm-up (eager): fills the launch caches, checks the device error word
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            mb.step()
+    torch.cuda.synchronize()
+    if binding.ar_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    use_graph = not args.eager
+    if use_graph:
+        g_fwd, g_bwd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_fwd, stream=stream):
+            mb.forward()
+        with torch.cuda.graph(g_bwd, stream=stream):
+            mb.backward()
+        run_fwd, run_bwd = g_fwd.replay, g_bwd.replay
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                run_fwd()
+                run_bwd()
+    else:
+        def run_fwd():
+            mb.forward()
+
+        def run_bwd():
+            mb.backward()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            ev[k][0].record(stream)
+            run_fwd()
+            ev[k][1].record(stream)
+            run_bwd()
+            ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
+    if world > 1:
+        t = torch.tensor([total_ms, fwd_ms, bwd_ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, fwd_ms, bwd_ms = t.tolist()
+    ms = total_ms / K
+    if binding.ar_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    # end to end through the public API: inputs from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, mb, stream, run_fwd, run_bwd, world, local)
+
+    hbm, peak_kind = peaks()
+    n_bwd = len(mb.plan.run_sites)
+    bwd_bytes = mbytes["bwd"]
+    achieved = bwd_bytes / (bwd_ms * 1e-3) / 1e9
+    traffic = measured_traffic(args.config, H)
+    line = {
+        "metric": METRIC,
+        "value": world * cfg.T / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded torch Philox on device; recipe of the 1B/100M/350M/LR models)",
+        "config": {"workload": f"{cfg.name}-shaped routing microbatch", "T": cfg.T, "d": cfg.d,
+                   "H": H, "r": cfg.r, "sites": n_bwd,
+                   "sources_read": sum(len(mb.plan.sites[s]) for s in mb.plan.run_sites),
+                   "global_batch_tokens": world * cfg.T, "parallelism": f"dp{world} (token shards)",
+                   "cuda_graphs": use_graph, "l2": "inputs larger than L2 (bank "
+                   f"{mb.bank.rows.numel() * mb.bank.rows.element_size() / 1e9:.2f} GB)"},
+        "phases_ms": {"forward_and_appends": fwd_ms, "backward": bwd_ms},
+        "model_bytes": mbytes,
+        "step_roofline": {"achieved": mbytes["total"] / (ms * 1e-3) / 1e9, "peak": hbm,
+                          "unit": "GB/s", "frac": mbytes["total"] / (ms * 1e-3) / 1e9 / hbm,
+                          "peak_source": peak_kind},
+        "roofline": {"kernel": "route_bwd_kernel (backward phase, incl. its dq/dg reduce)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "launches_per_step": n_bwd,
+                     "bytes_per_launch_avg": bwd_bytes / n_bwd,
+                     "ms_per_launch_avg": bwd_ms / n_bwd,
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"},
+        "gpu_launches": K * mb.kernel_launches(),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb, _, _ = cpu_baseline(cfg, H, args.cpu_seconds)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def end_to_end(args, mb, stream, run_fwd, run_bwd, world, local):
+    """Same step through the public API with host buffers: H2D of the step's
+    inputs (source rows, upstream gradients, queries, norm weights) from pinned
+    memory, the routing step, D2H of every site's dq/dg."""
+    import torch
+    import torch.distributed as dist
+
+    dev_in, host_in = [], []
+    for j in range(mb.n_rows):
+        t = mb.outputs[j] if j in mb.outputs else mb.bank.rows[j]
+        dev_in.append(t)
+    for s in mb.plan.run_sites:
+        dev_in.append(mb.dout[s])
+        dev_in.append(mb.q[s])
+        if mb.g[s] is not None:
+            dev_in.append(mb.g[s])
+    for t in dev_in:
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        host_in.append(h)
+    dev_out = [mb.dq[s] for s in mb.plan.run_sites] + \
+              [mb.dg[s] for s in mb.plan.run_sites if mb.g[s] is not None]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+    K = args.e2e_steps or max(1, min(args.steps, 5))
+
+    def step():
+        for dst, src in zip(dev_in, host_in):
+            dst.copy_(src, non_blocking=True)
+        run_fwd()
+        run_bwd()
+        for dst, src in zip(host_out, dev_out):
+            dst.copy_(src, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(K):
+            step()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / K
+    if world > 1:
+        t = torch.tensor([ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    return {"value": world * mb.cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def reference_arm(args, rank, world):
+    """The oracle as the reference implementation, on the host cores."""
+    if rank != 0:
+        return
+    sys.path.insert(0, ROOT)
+    from depth_wise_attention_ar_gb300.workload import CONFIGS  # schedule-free config table
+    cfg = CONFIGS[args.config]
+    H = args.heads or cfg.H
+    for _ in range(args.warmup):
+        pass
+    cb, dt, Ts = cpu_baseline(cfg, H, args.cpu_seconds, steps=max(1, args.steps))
+    line = {
+        "metric": METRIC,
+        "value": cb["value"],
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 * cfg.T / Ts,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded numpy Philox)",
+        "config": {"workload": f"{cfg.name}-shaped routing microbatch", "T": cfg.T, "d": cfg.d,
+                   "H": H, "r": cfg.r},
+        "impl": "reference",
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

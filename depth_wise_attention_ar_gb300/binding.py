@@ -1,0 +1,296 @@
+"""ctypes binding of libattnres_gb300.so (include/attnres.h).
+
+The ``ar_*`` functions mirror the C entry points one to one and only marshal
+arguments (tensors -> device pointers, lists -> int32 arrays, streams ->
+cudaStream_t). ``Bank`` is a convenience owner of the buffers a bank needs,
+allocated with torch; every computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing, importing this module raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBPATH = os.path.join(HERE, "libattnres_gb300.so")
+
+AR_OK = 0
+STATUS = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_SHAPE", 3: "AR_ERR_ALIGN",
+          4: "AR_ERR_CAPACITY", 5: "AR_ERR_ORDER", 6: "AR_ERR_CUDA", 7: "AR_ERR_TIMEOUT",
+          8: "AR_ERR_UNSUPPORTED"}
+AR_F32, AR_BF16 = 0, 1
+AR_NORM_KEY, AR_NORM_FULL = 0, 1
+AR_MAX_SOURCES = 256
+AR_DEVERR_WAIT_TIMEOUT = 1
+
+# Every function the header declares, with its ctypes signature.
+_P, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_I32P, _I64P, _U32P, _SZP = (ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
+                             ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_size_t))
+SIGNATURES = {
+    "ar_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "ar_inv_rms_floats": ([_I64, _I32, _I64P], ctypes.c_int),
+    "ar_bank_create": ([ctypes.POINTER(_P), _I64, _I32, _I32, _I32, ctypes.c_int, ctypes.c_int,
+                        _F32, _P, _P, _P], ctypes.c_int),
+    "ar_bank_destroy": ([_P], ctypes.c_int),
+    "ar_bank_row_count": ([_P, _I32P], ctypes.c_int),
+    "ar_bank_row_ptr": ([_P, _I32, ctypes.POINTER(_P)], ctypes.c_int),
+    "ar_bank_append": ([_P, _P, _I32, _I32P, _P], ctypes.c_int),
+    "ar_bank_zero_grad": ([_P], ctypes.c_int),
+    "ar_bank_reset": ([_P], ctypes.c_int),
+    "ar_route_fwd": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _I32, _P], ctypes.c_int),
+    "ar_route_bwd_workspace": ([_P, _I32, _SZP], ctypes.c_int),
+    "ar_route_bwd": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I32, _P],
+                     ctypes.c_int),
+    "ar_block_schedule": ([_I32, _I32, _I32P, _I32P, _I32P, _I64, _I64P], ctypes.c_int),
+    "ar_device_error": ([_U32P], ctypes.c_int),
+}
+
+if not os.path.exists(LIBPATH):
+    raise ImportError(
+        f"{LIBPATH} is not built; run depth_wise_attention_ar_gb300.build.build() "
+        "(nvcc, sm_103a). There is no CPU fallback.")
+
+_lib = ctypes.CDLL(LIBPATH)
+for _name, (_args, _res) in SIGNATURES.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+
+class ARError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        self.name = STATUS.get(status, f"status {status}")
+        super().__init__(f"{fn}: {self.name}")
+
+
+def _check(fn: str, st: int):
+    if st != AR_OK:
+        raise ARError(fn, st)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, torch.cuda.Stream):
+        return s.cuda_stream
+    return int(s)
+
+
+def _rows(rows):
+    arr = (ctypes.c_int32 * max(1, len(rows)))(*[int(r) for r in rows])
+    return arr, len(rows)
+
+
+# ---- one-to-one wrappers of the C ABI ------------------------------------------
+
+def ar_status_string(status: int) -> str:
+    return _lib.ar_status_string(status).decode()
+
+
+def ar_inv_rms_floats(T: int, capacity: int) -> int:
+    n = ctypes.c_int64()
+    _check("ar_inv_rms_floats", _lib.ar_inv_rms_floats(T, capacity, ctypes.byref(n)))
+    return n.value
+
+
+def ar_bank_create(T, d, r, capacity, dtype, norm, eps, rows, inv_rms, grad):
+    h = ctypes.c_void_p()
+    _check("ar_bank_create", _lib.ar_bank_create(ctypes.byref(h), T, d, r, capacity, dtype, norm,
+                                                 eps, _ptr(rows), _ptr(inv_rms), _ptr(grad)))
+    return h
+
+
+def ar_bank_destroy(bank):
+    _check("ar_bank_destroy", _lib.ar_bank_destroy(bank))
+
+
+def ar_bank_row_count(bank) -> int:
+    n = ctypes.c_int32()
+    _check("ar_bank_row_count", _lib.ar_bank_row_count(bank, ctypes.byref(n)))
+    return n.value
+
+
+def ar_bank_row_ptr(bank, row: int) -> int:
+    p = ctypes.c_void_p()
+    _check("ar_bank_row_ptr", _lib.ar_bank_row_ptr(bank, row, ctypes.byref(p)))
+    return p.value or 0
+
+
+def ar_bank_append(bank, src, accumulate_from: int = -1, stream=None) -> int:
+    row = ctypes.c_int32(-1)
+    _check("ar_bank_append", _lib.ar_bank_append(bank, _ptr(src), accumulate_from,
+                                                 ctypes.byref(row), _stream(stream)))
+    return row.value
+
+
+def ar_bank_zero_grad(bank):
+    _check("ar_bank_zero_grad", _lib.ar_bank_zero_grad(bank))
+
+
+def ar_bank_reset(bank):
+    _check("ar_bank_reset", _lib.ar_bank_reset(bank))
+
+
+def ar_route_fwd(bank, rows, H, q, g, out, lse, site_id, stream=None):
+    arr, n = _rows(rows)
+    _check("ar_route_fwd", _lib.ar_route_fwd(bank, arr, n, H, _ptr(q), _ptr(g), _ptr(out),
+                                             _ptr(lse), site_id, _stream(stream)))
+
+
+def ar_route_bwd_workspace(bank, H) -> int:
+    b = ctypes.c_size_t()
+    _check("ar_route_bwd_workspace", _lib.ar_route_bwd_workspace(bank, H, ctypes.byref(b)))
+    return b.value
+
+
+def ar_route_bwd(bank, rows, H, q, g, out, dout, lse, dq, dg, ws, ws_bytes, site_id, stream=None):
+    arr, n = _rows(rows)
+    _check("ar_route_bwd", _lib.ar_route_bwd(bank, arr, n, H, _ptr(q), _ptr(g), _ptr(out),
+                                             _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dg), _ptr(ws),
+                                             ws_bytes, site_id, _stream(stream)))
+
+
+def ar_block_schedule(M: int, NB: int | None):
+    """Returns (acc_from [M+1], sites: list of M+1 row lists)."""
+    acc = (ctypes.c_int32 * (M + 1))()
+    ptr = (ctypes.c_int32 * (M + 2))()
+    need = ctypes.c_int64()
+    nb = 0 if NB is None else NB
+    st = _lib.ar_block_schedule(M, nb, acc, ptr, None, 0, ctypes.byref(need))
+    if st not in (AR_OK, 4):
+        _check("ar_block_schedule", st)
+    flat = (ctypes.c_int32 * max(1, need.value))()
+    _check("ar_block_schedule", _lib.ar_block_schedule(M, nb, acc, ptr, flat, need.value,
+                                                       ctypes.byref(need)))
+    sites = [list(flat[ptr[t]:ptr[t + 1]]) for t in range(M + 1)]
+    return list(acc), sites
+
+
+def ar_device_error() -> int:
+    bits = ctypes.c_uint32()
+    _check("ar_device_error", _lib.ar_device_error(ctypes.byref(bits)))
+    return bits.value
+
+
+# ---- convenience owner of a bank's buffers -------------------------------------
+
+_TORCH_DT = {"bf16": torch.bfloat16, "f32": torch.float32}
+_AR_DT = {"bf16": AR_BF16, "f32": AR_F32}
+
+
+class Bank:
+    """A bank plus the torch buffers it points into (see ar_bank_create)."""
+
+    def __init__(self, T: int, d: int, r: int | None = None, capacity: int = 1,
+                 dtype: str = "bf16", norm: str = "key", eps: float = 1e-6,
+                 with_grad: bool = True, device=None):
+        r = d if r is None else r
+        dev = torch.device("cuda" if device is None else device)
+        self.T, self.d, self.r, self.capacity, self.dtype = T, d, r, capacity, dtype
+        self.torch_dtype = _TORCH_DT[dtype]
+        self.rows = torch.empty((capacity, T, d), dtype=self.torch_dtype, device=dev)
+        self.inv_ld = (capacity + 3) // 4 * 4
+        self.inv = torch.empty(max(1, ar_inv_rms_floats(T, capacity)), dtype=torch.float32,
+                               device=dev)
+        self.grad = (torch.empty((capacity, T, d), dtype=torch.float32, device=dev)
+                     if with_grad else None)
+        self.handle = ar_bank_create(T, d, r, capacity, _AR_DT[dtype],
+                                     AR_NORM_FULL if norm == "full" else AR_NORM_KEY, eps,
+                                     self.rows, self.inv, self.grad)
+        self._ws = {}
+
+    def close(self):
+        if self.handle is not None:
+            ar_bank_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def count(self) -> int:
+        return ar_bank_row_count(self.handle)
+
+    def slot(self, row: int) -> torch.Tensor:
+        return self.rows[row]
+
+    def append(self, src: torch.Tensor, accumulate_from: int = -1, stream=None) -> int:
+        self._check_tensor(src, (self.T, self.d), self.torch_dtype, "src")
+        return ar_bank_append(self.handle, src, accumulate_from, stream)
+
+    def zero_grad(self):
+        ar_bank_zero_grad(self.handle)
+
+    def reset(self):
+        ar_bank_reset(self.handle)
+
+    def inv_rms(self) -> torch.Tensor:
+        """The cache as [T, capacity] (token-major view)."""
+        return self.inv[: self.T * self.inv_ld].view(self.T, self.inv_ld)[:, : self.capacity]
+
+    def route_fwd(self, rows, H, q, g=None, out=None, lse=None, site_id=0, stream=None):
+        dev = self.rows.device
+        if out is None:
+            out = torch.empty((self.T, self.d), dtype=self.torch_dtype, device=dev)
+        if lse is None:
+            lse = torch.empty((self.T, H), dtype=torch.float32, device=dev)
+        self._check_tensor(out, (self.T, self.d), self.torch_dtype, "out")
+        self._check_tensor(lse, (self.T, H), torch.float32, "lse")
+        self._check_tensor(q, (self.r,), torch.float32, "q")
+        if g is not None:
+            self._check_tensor(g, (self.r,), torch.float32, "g")
+        ar_route_fwd(self.handle, rows, H, q, g, out, lse, site_id, stream)
+        return out, lse
+
+    def workspace(self, H) -> torch.Tensor:
+        nbytes = ar_route_bwd_workspace(self.handle, H)
+        ws = self._ws.get(H)
+        if ws is None or ws.numel() * 4 < nbytes:
+            ws = torch.empty(max(4, nbytes // 4), dtype=torch.float32, device=self.rows.device)
+            self._ws[H] = ws
+        return ws
+
+    def route_bwd(self, rows, H, q, g, out, dout, lse, dq=None, dg=None, site_id=0,
+                  stream=None, ws=None):
+        dev = self.rows.device
+        if dq is None:
+            dq = torch.empty(self.r, dtype=torch.float32, device=dev)
+        if dg is None and g is not None:
+            dg = torch.empty(self.r, dtype=torch.float32, device=dev)
+        for t, shape, dt, nm in ((out, (self.T, self.d), self.torch_dtype, "out"),
+                                 (dout, (self.T, self.d), self.torch_dtype, "dout"),
+                                 (lse, (self.T, H), torch.float32, "lse"),
+                                 (q, (self.r,), torch.float32, "q"),
+                                 (dq, (self.r,), torch.float32, "dq")):
+            self._check_tensor(t, shape, dt, nm)
+        if ws is None:
+            ws = self.workspace(H)
+        ar_route_bwd(self.handle, rows, H, q, g, out, dout, lse, dq, dg, ws, ws.numel() * 4,
+                     site_id, stream)
+        return dq, dg
+
+    @staticmethod
+    def _check_tensor(t, shape, dtype, name):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}, "
+                             f"got {t.dtype} {tuple(t.shape)}")

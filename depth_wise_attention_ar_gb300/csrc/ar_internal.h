@@ -1,0 +1,44 @@
+// Host-visible internals shared by the C-ABI layer and the kernel units:
+// the argument block of a routing launch and the launch entry points.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attnres.h"
+
+namespace ar {
+
+// Everything a routing launch needs, passed by value (kernel parameter space).
+struct RouteArgs {
+    const void *bank;      // rows [cap, T, d] of the storage dtype
+    const float *inv;      // inverse RMS, token-major [T, inv_ld]
+    float *grad;           // fp32 gradient rows [cap, T, d] (backward)
+    const float *q;        // [r]
+    const float *g;        // [r] or nullptr (= ones)
+    void *out;             // forward output [T, d]
+    float *lse;            // [T, H]
+    const void *fout;      // backward: forward output [T, d]
+    const void *dout;      // backward: dL/dout [T, d]
+    float *ws;             // backward: per-warp partial sums [warps, r]
+    unsigned int *err;     // device error word
+    int64_t T;
+    int d, r, H, n_src, inv_ld, norm_full;
+    int rows[AR_MAX_SOURCES];
+    uint32_t first_mask[AR_MAX_SOURCES / 32];  // backward: bit n set = store (first touch)
+};
+
+// ---- host-side launch entry points (one per kernel family) -----------------
+// Each returns cudaErrorNotSupported when no instantiation covers the shape.
+cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
+cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
+cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps);
+cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, const float *g,
+                               float *dq, float *dg, cudaStream_t s);
+cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col,
+                          int64_t T, int d, int r, int inv_ld, int norm_full, float eps,
+                          ar_dtype dt, cudaStream_t s);
+unsigned int *device_error_word();
+bool fused_shape_supported(int d, int r, int H);
+
+}  // namespace ar

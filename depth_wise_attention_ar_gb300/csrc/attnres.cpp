@@ -1,0 +1,335 @@
+// Host side of the C ABI declared in include/attnres.h: bank bookkeeping
+// (row count, first-touch flags of the gradient rows, the record of forward
+// calls that the backward must unwind in reverse), argument checks, and the
+// launches. No device memory is allocated here and nothing synchronises the
+// device except ar_device_error().
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "attnres.h"
+#include "ar_internal.h"
+
+struct ar_bank {
+    int64_t T = 0;
+    int d = 0, r = 0, cap = 0, inv_ld = 0;
+    ar_dtype dtype = AR_BF16;
+    int norm_full = 0;
+    float eps = 1e-6f;
+    void *rows = nullptr;
+    float *inv = nullptr;
+    float *grad = nullptr;
+    int count = 0;
+    std::vector<uint8_t> touched;     // gradient row written since zero_grad
+    std::vector<int32_t> fwd_record;  // site ids of forwards not yet backpropagated
+    int device = 0;
+    size_t esize = 2;
+};
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+ar_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return AR_OK;
+    if (e == cudaErrorNotSupported) return AR_ERR_UNSUPPORTED;
+    cudaGetLastError();  // clear a sticky-free launch error so the caller may retry
+    return AR_ERR_CUDA;
+}
+
+// Checks shared by the forward and the backward of a site.
+ar_status check_site(const ar_bank *b, const int32_t *rows, int32_t n_src, int32_t H,
+                     const float *q, const float *g)
+{
+    if (!b || !rows || !q) return AR_ERR_INVALID_ARG;
+    if (n_src < 1 || n_src > AR_MAX_SOURCES) return AR_ERR_INVALID_ARG;
+    if (H < 1 || b->d % H != 0 || b->r % H != 0) return AR_ERR_SHAPE;
+    if (!ar::fused_shape_supported(b->d, b->r, H)) return AR_ERR_UNSUPPORTED;
+    std::vector<uint8_t> seen(static_cast<size_t>(b->count), 0);
+    for (int i = 0; i < n_src; ++i) {
+        const int32_t row = rows[i];
+        if (row < 0 || row >= b->count) return AR_ERR_INVALID_ARG;
+        if (seen[row]) return AR_ERR_INVALID_ARG;  // duplicate source
+        seen[row] = 1;
+    }
+    if (!aligned4(q) || (g && !aligned4(g))) return AR_ERR_ALIGN;
+    return AR_OK;
+}
+
+void fill_common(ar::RouteArgs &a, const ar_bank *b, const int32_t *rows, int32_t n_src,
+                 int32_t H, const float *q, const float *g)
+{
+    std::memset(&a, 0, sizeof(a));
+    a.bank = b->rows;
+    a.inv = b->inv;
+    a.grad = b->grad;
+    a.q = q;
+    a.g = g;
+    a.T = b->T;
+    a.d = b->d;
+    a.r = b->r;
+    a.H = H;
+    a.n_src = n_src;
+    a.inv_ld = b->inv_ld;
+    a.norm_full = b->norm_full;
+    a.err = ar::device_error_word();
+    for (int i = 0; i < n_src; ++i) a.rows[i] = rows[i];
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ar_status_string(ar_status s)
+{
+    switch (s) {
+    case AR_OK: return "AR_OK";
+    case AR_ERR_INVALID_ARG: return "AR_ERR_INVALID_ARG";
+    case AR_ERR_SHAPE: return "AR_ERR_SHAPE";
+    case AR_ERR_ALIGN: return "AR_ERR_ALIGN";
+    case AR_ERR_CAPACITY: return "AR_ERR_CAPACITY";
+    case AR_ERR_ORDER: return "AR_ERR_ORDER";
+    case AR_ERR_CUDA: return "AR_ERR_CUDA";
+    case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT";
+    case AR_ERR_UNSUPPORTED: return "AR_ERR_UNSUPPORTED";
+    }
+    return "AR_ERR_UNKNOWN";
+}
+
+ar_status ar_inv_rms_floats(int64_t T, int32_t capacity, int64_t *floats)
+{
+    if (!floats || T < 0 || capacity < 1) return AR_ERR_INVALID_ARG;
+    *floats = T * (int64_t)((capacity + 3) / 4 * 4);
+    return AR_OK;
+}
+
+ar_status ar_bank_create(ar_bank **out, int64_t T, int32_t d, int32_t r, int32_t capacity,
+                         ar_dtype dtype, ar_norm norm, float eps, void *rows, float *inv_rms,
+                         float *grad)
+{
+    if (!out) return AR_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (capacity < 1 || T < 0) return AR_ERR_INVALID_ARG;
+    if (T > 0 && (!rows || !inv_rms)) return AR_ERR_INVALID_ARG;
+    if (dtype != AR_F32 && dtype != AR_BF16) return AR_ERR_INVALID_ARG;
+    if (norm != AR_NORM_KEY && norm != AR_NORM_FULL) return AR_ERR_INVALID_ARG;
+    if (d < 1 || r < 1 || r > d || d % 8 != 0 || r % 8 != 0) return AR_ERR_SHAPE;
+    if (!aligned16(rows) || !aligned16(inv_rms) || (grad && !aligned16(grad))) return AR_ERR_ALIGN;
+    int dev = -1;  // recorded for information; launches use the current device
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        dev = -1;
+    }
+    ar_bank *b = new (std::nothrow) ar_bank();
+    if (!b) return AR_ERR_INVALID_ARG;
+    b->T = T;
+    b->d = d;
+    b->r = r;
+    b->cap = capacity;
+    b->inv_ld = (capacity + 3) / 4 * 4;
+    b->dtype = dtype;
+    b->norm_full = norm == AR_NORM_FULL ? 1 : 0;
+    b->eps = eps;
+    b->rows = rows;
+    b->inv = inv_rms;
+    b->grad = grad;
+    b->touched.assign(static_cast<size_t>(capacity), 0);
+    b->device = dev;
+    b->esize = dtype == AR_BF16 ? 2 : 4;
+    *out = b;
+    return AR_OK;
+}
+
+ar_status ar_bank_destroy(ar_bank *bank)
+{
+    delete bank;
+    return AR_OK;
+}
+
+ar_status ar_bank_row_count(const ar_bank *bank, int32_t *count)
+{
+    if (!bank || !count) return AR_ERR_INVALID_ARG;
+    *count = bank->count;
+    return AR_OK;
+}
+
+ar_status ar_bank_row_ptr(const ar_bank *bank, int32_t row, void **ptr)
+{
+    if (!bank || !ptr || row < 0 || row >= bank->cap) return AR_ERR_INVALID_ARG;
+    *ptr = static_cast<unsigned char *>(bank->rows) +
+           (size_t)row * (size_t)bank->T * (size_t)bank->d * bank->esize;
+    return AR_OK;
+}
+
+ar_status ar_bank_append(ar_bank *bank, const void *src, int32_t accumulate_from,
+                         int32_t *out_row, void *stream)
+{
+    if (!bank || (!src && bank->T > 0)) return AR_ERR_INVALID_ARG;
+    if (bank->count >= bank->cap) return AR_ERR_CAPACITY;
+    if (accumulate_from < -1 || accumulate_from >= bank->count) return AR_ERR_INVALID_ARG;
+    if (!aligned16(src)) return AR_ERR_ALIGN;
+    void *dst = nullptr;
+    ar_bank_row_ptr(bank, bank->count, &dst);
+    const void *prev = nullptr;
+    if (accumulate_from >= 0) ar_bank_row_ptr(bank, accumulate_from, const_cast<void **>(&prev));
+    const cudaError_t e = ar::launch_append(src, prev, dst, bank->inv + bank->count, bank->T,
+                                            bank->d, bank->r, bank->inv_ld, bank->norm_full,
+                                            bank->eps, bank->dtype,
+                                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    if (out_row) *out_row = bank->count;
+    ++bank->count;
+    return AR_OK;
+}
+
+ar_status ar_bank_zero_grad(ar_bank *bank)
+{
+    if (!bank) return AR_ERR_INVALID_ARG;
+    std::fill(bank->touched.begin(), bank->touched.end(), 0);
+    return AR_OK;
+}
+
+ar_status ar_bank_reset(ar_bank *bank)
+{
+    if (!bank) return AR_ERR_INVALID_ARG;
+    bank->count = 0;
+    bank->fwd_record.clear();
+    std::fill(bank->touched.begin(), bank->touched.end(), 0);
+    return AR_OK;
+}
+
+ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                       const float *q, const float *g, void *out, float *lse, int32_t site_id,
+                       void *stream)
+{
+    ar_status st = check_site(bank, rows, n_src, H, q, g);
+    if (st != AR_OK) return st;
+    if (bank->T > 0 && (!out || !lse)) return AR_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned4(lse)) return AR_ERR_ALIGN;
+    if (bank->T > 0) {
+        ar::RouteArgs a;
+        fill_common(a, bank, rows, n_src, H, q, g);
+        a.out = out;
+        a.lse = lse;
+        const cudaError_t e = ar::launch_route_fwd(a, bank->dtype, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    bank->fwd_record.push_back(site_id);
+    return AR_OK;
+}
+
+ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
+{
+    if (!bank || !bytes) return AR_ERR_INVALID_ARG;
+    if (H < 1 || bank->d % H != 0 || bank->r % H != 0) return AR_ERR_SHAPE;
+    if (!ar::fused_shape_supported(bank->d, bank->r, H)) return AR_ERR_UNSUPPORTED;
+    ar::RouteArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.d = bank->d;
+    a.r = bank->r;
+    a.H = H;
+    int warps = 0;
+    const cudaError_t e = ar::route_bwd_grid(a, bank->dtype, &warps);
+    if (e != cudaSuccess) return from_cuda(e);
+    *bytes = (size_t)warps * (size_t)bank->r * sizeof(float);
+    return AR_OK;
+}
+
+ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                       const float *q, const float *g, const void *out, const void *dout,
+                       const float *lse, float *dq, float *dg, void *ws, size_t ws_bytes,
+                       int32_t site_id, void *stream)
+{
+    if (bank && !bank->grad) return AR_ERR_INVALID_ARG;
+    ar_status st = check_site(bank, rows, n_src, H, q, g);
+    if (st != AR_OK) return st;
+    if (!dq || (bank->T > 0 && (!out || !dout || !lse || !ws))) return AR_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(dout) || !aligned4(lse) || !aligned4(dq) ||
+        (dg && !aligned4(dg)) || !aligned16(ws))
+        return AR_ERR_ALIGN;
+    if (bank->fwd_record.empty() || bank->fwd_record.back() != site_id) return AR_ERR_ORDER;
+    size_t need = 0;
+    st = ar_route_bwd_workspace(bank, H, &need);
+    if (st != AR_OK) return st;
+    if (bank->T > 0 && ws_bytes < need) return AR_ERR_CAPACITY;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (bank->T == 0) {
+        cudaError_t e = cudaMemsetAsync(dq, 0, (size_t)bank->r * sizeof(float), s);
+        if (e == cudaSuccess && dg) e = cudaMemsetAsync(dg, 0, (size_t)bank->r * sizeof(float), s);
+        if (e != cudaSuccess) return from_cuda(e);
+    } else {
+        ar::RouteArgs a;
+        fill_common(a, bank, rows, n_src, H, q, g);
+        a.fout = out;
+        a.dout = dout;
+        a.lse = const_cast<float *>(lse);
+        a.ws = static_cast<float *>(ws);
+        for (int i = 0; i < n_src; ++i)
+            if (!bank->touched[rows[i]]) a.first_mask[i >> 5] |= 1u << (i & 31);
+        cudaError_t e = ar::launch_route_bwd(a, bank->dtype, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), (int)(need / sizeof(float) / bank->r),
+                                   bank->r, q, g, dq, dg, s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    for (int i = 0; i < n_src; ++i) bank->touched[rows[i]] = 1;
+    bank->fwd_record.pop_back();
+    return AR_OK;
+}
+
+ar_status ar_block_schedule(int32_t M, int32_t NB, int32_t *acc_from, int32_t *site_ptr,
+                            int32_t *site_rows, int64_t site_rows_cap, int64_t *site_rows_len)
+{
+    if (M < 1 || !acc_from || !site_ptr || !site_rows_len) return AR_ERR_INVALID_ARG;
+    const int64_t nb = (NB <= 0 || NB >= M) ? M : NB;
+    std::vector<uint8_t> is_end(static_cast<size_t>(M) + 1, 0);
+    for (int64_t j = 1; j <= nb; ++j) is_end[(M * j + nb - 1) / nb] = 1;  // ceil(M j / NB)
+    std::vector<int32_t> blocks{0};
+    int32_t partial = -1;
+    std::vector<int32_t> flat{0};
+    std::vector<int32_t> ptr{0, 1};
+    acc_from[0] = -1;
+    for (int32_t t = 1; t <= M; ++t) {
+        acc_from[t] = partial;  // -1 at a block start
+        partial = t;
+        if (is_end[t]) {
+            blocks.push_back(partial);
+            partial = -1;
+        }
+        flat.insert(flat.end(), blocks.begin(), blocks.end());
+        if (partial >= 0) flat.push_back(partial);
+        ptr.push_back(static_cast<int32_t>(flat.size()));
+    }
+    *site_rows_len = static_cast<int64_t>(flat.size());
+    for (int32_t t = 0; t <= M + 1; ++t) site_ptr[t] = ptr[t];
+    if (!site_rows || site_rows_cap < (int64_t)flat.size()) return AR_ERR_CAPACITY;
+    std::memcpy(site_rows, flat.data(), flat.size() * sizeof(int32_t));
+    return AR_OK;
+}
+
+ar_status ar_device_error(uint32_t *bits)
+{
+    if (!bits) return AR_ERR_INVALID_ARG;
+    unsigned int *w = ar::device_error_word();
+    if (!w) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    unsigned int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(w, 0, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    *bits = v;
+    return AR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,204 @@
+// Shared device helpers of the GB300 depth-routing kernels: argument block,
+// PTX wrappers for mbarriers and 1-D bulk (TMA) copies, and 8-element chunk
+// conversions between the storage dtype and fp32 registers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ar_internal.h"
+#include "attnres.h"
+
+namespace ar {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// Online-softmax rescale threshold (log2 units): the running maximum is only
+// moved when a score exceeds it by more than this, so the exponentials stay
+// below 2^8 and most sources skip the rescale of the accumulator.
+constexpr float kRescaleTau = 8.0f;
+// Bound on mbarrier polls before a wait is declared lost (no device trap).
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase with `parity` completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit)
+{
+    for (uint32_t it = 0; it < limit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void report_error(unsigned int *err, unsigned int bits)
+{
+    if (err) atomicOr(err, bits);
+}
+
+// ---- 8-element chunks ------------------------------------------------------
+// A chunk is 8 consecutive elements of a row: 16 bytes in bf16, 32 in fp32.
+
+template <typename T> struct ChunkBytes;
+template <> struct ChunkBytes<__nv_bfloat16> { static constexpr int value = 16; };
+template <> struct ChunkBytes<float> { static constexpr int value = 32; };
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 u, float v[8])
+{
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xffff0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xffff0000u);
+    v[4] = __uint_as_float(u.z << 16);
+    v[5] = __uint_as_float(u.z & 0xffff0000u);
+    v[6] = __uint_as_float(u.w << 16);
+    v[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+// 16-byte shared-memory load issued exactly where written (volatile), so a
+// second pass over a staged row re-reads shared memory instead of pinning the
+// first pass's values in registers.
+__device__ __forceinline__ uint4 lds128(const void *p)
+{
+    uint4 u;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                 : "r"(smem_u32(p))
+                 : "memory");
+    return u;
+}
+
+// Load a chunk from shared memory (any generic pointer to smem).
+__device__ __forceinline__ void ld_chunk_s(const __nv_bfloat16 *p, float v[8])
+{
+    unpack_bf16x8(lds128(p), v);
+}
+__device__ __forceinline__ void ld_chunk_s(const float *p, float v[8])
+{
+    const uint4 a = lds128(p);
+    const uint4 b = lds128(p + 4);
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+    v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+    v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+}
+
+// Load a chunk from global memory through the read-only path.
+__device__ __forceinline__ void ld_chunk_g(const __nv_bfloat16 *p, float v[8])
+{
+    unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(p)), v);
+}
+__device__ __forceinline__ void ld_chunk_g(const float *p, float v[8])
+{
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Store a chunk (rounded to nearest even for bf16).
+__device__ __forceinline__ void st_chunk_g(__nv_bfloat16 *p, const float v[8])
+{
+    uint4 u;
+    u.x = pack_bf16x2(v[0], v[1]);
+    u.y = pack_bf16x2(v[2], v[3]);
+    u.z = pack_bf16x2(v[4], v[5]);
+    u.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4 *>(p) = u;
+}
+__device__ __forceinline__ void st_chunk_g(float *p, const float v[8])
+{
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// fp32 chunk (gradient rows) in shared / global memory.
+__device__ __forceinline__ void ld_f32x8_s(const float *p, float v[8]) { ld_chunk_s(p, v); }
+__device__ __forceinline__ void st_f32x8_s(float *p, const float v[8])
+{
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void st_f32x8_g(float *p, const float v[8]) { st_chunk_g(p, v); }
+
+// Sum over the `lph` lanes of this lane's aligned group (lph a power of two).
+__device__ __forceinline__ float group_sum(float x, int lph)
+{
+    for (int o = 1; o < lph; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace ar

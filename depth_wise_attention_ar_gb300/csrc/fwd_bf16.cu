@@ -1,0 +1,6 @@
+// Forward routing kernels instantiated for the bf16 storage dtype.
+#include "kernels_fwd.cuh"
+
+namespace ar {
+template cudaError_t dispatch_fwd<__nv_bfloat16>(const RouteArgs &a, cudaStream_t s);
+}  // namespace ar

@@ -1,0 +1,261 @@
+// Fused routing backward for sm_103a, full-width keys (r = d).
+//
+// For one routing site, given dL/dout, emits dL/ds_n for every listed source
+// into the shared fp32 gradient rows (store on a row's first touch, in-place
+// accumulation afterwards: "Multi-Head Attention Residuals", Appendix E,
+// Figure 10) and per-warp partial sums for dL/dq and dL/dg.
+//
+// Per token t, source n, head h (w = softmax weight, recomputed from the
+// saved log-sum-exp; G = dL/dout):
+//   P[n,h]   = <G_[h], s_{n,[h]}>
+//   zr[n,h]  = sum_{c in slice h} q_c g_c s_{n,c}       (z = inv_n * zr)
+//   S[h]     = sum_n w P = <G_[h], out_[h]>  (the softmax coupling term, read
+//              from the forward output instead of a second pass over the
+//              sources: out_[h] is exactly sum_n w s_{n,[h]})
+//   dz[n,h]  = w (P - S)                      (routing feedback,
+//              "Low-Rank Attention Residuals", Eq. 15 / Lemma 2)
+//   dL/ds_n  = w G + inv dz (q g)   on slice h
+//            - inv^3 / d * (sum_h dz zr) * s_n   on all coordinates
+//              (score gradient through the RMS: MHAR Appendix E, LR-AttnRes
+//              Eq. 21 with r = d)
+//   dq_c = g_c U_c, dg_c = q_c U_c with U_c = sum_{t,n} inv dz s_{n,c}.
+// Every (token, source) item is independent once S[h] and lse[h] are known,
+// so each warp takes an equal contiguous range of the T*N items
+// (token-major): the work splits evenly over the grid whatever T is.
+//
+// GB300 mapping: one warp per item stream with a private ring of
+// shared-memory stages, as in the forward; a stage holds the source row
+// (storage dtype) and, unless this is the row's first touch, its fp32
+// gradient row, both brought in by 1-D bulk copies on one mbarrier. The new
+// gradient row goes back with 16-byte stores. G and U stay in registers,
+// q*g sits in a block-wide shared table, and the staged source row is read
+// twice from shared memory (dots, then gradient).
+#pragma once
+
+#include "common.cuh"
+#include "launch_util.cuh"
+
+namespace ar {
+
+constexpr int kBwdWarps = 4;
+constexpr int kBwdStages = 3;
+
+inline size_t bwd_smem_bytes(int d, size_t esize)
+{
+    return (size_t)kBwdWarps * kBwdStages * ((size_t)d * esize + (size_t)d * 4) +
+           (size_t)kBwdWarps * kBwdStages * 8 + (size_t)kBwdWarps * AR_MAX_SOURCES * 4 +
+           (size_t)d * 4;
+}
+
+template <typename T, int CPL>
+__global__ void __launch_bounds__(kBwdWarps * 32)
+    route_bwd_kernel(const __grid_constant__ RouteArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_rows[AR_MAX_SOURCES];
+    __shared__ uint32_t s_first[AR_MAX_SOURCES / 32];
+    constexpr int S = kBwdStages;
+    constexpr int CB = ChunkBytes<T>::value;
+    constexpr unsigned FULL = 0xffffffffu;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = a.d, N = a.n_src, H = a.H;
+    const int64_t TT = a.T;
+    const uint32_t vbytes = (uint32_t)d * (uint32_t)sizeof(T);
+    const uint32_t gbytes = (uint32_t)d * 4u;
+    const uint32_t slot_bytes = vbytes + gbytes;
+
+    unsigned char *rings = smem;
+    uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + (size_t)kBwdWarps * S * slot_bytes);
+    float *inv_all = reinterpret_cast<float *>(bars_all + kBwdWarps * S);
+    float *s_qg = inv_all + kBwdWarps * AR_MAX_SOURCES;  // [d], q * g
+
+    for (int i = threadIdx.x; i < N; i += blockDim.x) s_rows[i] = a.rows[i];
+    for (int i = threadIdx.x; i < AR_MAX_SOURCES / 32; i += blockDim.x) s_first[i] = a.first_mask[i];
+    for (int c = threadIdx.x; c < d; c += blockDim.x)
+        s_qg[c] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f);
+    unsigned char *ring = rings + (size_t)warp * S * slot_bytes;
+    uint64_t *bars = bars_all + warp * S;
+    float *cur_inv = inv_all + warp * AR_MAX_SOURCES;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ---- lane -> head and chunk mapping (same as the forward)
+    const int LPH = 32 / H;
+    const int h = lane / LPH, sub = lane - h * LPH;
+    int cidx[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) cidx[j] = h * (CPL * LPH) + sub + LPH * ((j + h) % CPL);
+    const float inv_d = 1.0f / (float)d;
+
+    // ---- this warp's contiguous range of (token, source) items
+    const int64_t GW = (int64_t)gridDim.x * kBwdWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kBwdWarps + warp;
+    const int64_t total = TT * N;
+    const int64_t lo = total * gw / GW, hi = total * (gw + 1) / GW;
+    const uint64_t pol = l2_policy_evict_first();
+
+    int64_t issued = lo, tok_p = lo / N;
+    int n_p = (int)(lo - tok_p * N), slot_p = 0;
+    auto issue_next = [&]() {
+        if (lane == 0) {
+            const bool first = (s_first[n_p >> 5] >> (n_p & 31)) & 1u;
+            const int64_t off = (int64_t)s_rows[n_p] * TT + tok_p;
+            unsigned char *dst = ring + (size_t)slot_p * slot_bytes;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[slot_p], vbytes + (first ? 0u : gbytes));
+            bulk_g2s(dst, static_cast<const unsigned char *>(a.bank) + off * vbytes, vbytes,
+                     &bars[slot_p], pol);
+            if (!first) bulk_g2s(dst + vbytes, a.grad + off * d, gbytes, &bars[slot_p], pol);
+        }
+        ++issued;
+        if (++n_p == N) { n_p = 0; ++tok_p; }
+        if (++slot_p == S) slot_p = 0;
+    };
+    for (int s = 0; s < S && issued < hi; ++s) issue_next();
+
+    float U[CPL][8];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) U[j][e] = 0.f;
+
+    float G[CPL][8];
+    float S_h = 0.f, lse2 = 0.f;
+    int64_t tok = lo / N, i = lo;
+    int n = (int)(lo - tok * N), slot = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (; i < hi; ++i) {
+        if (i == lo || n == 0) {
+            // token-level data: dL/dout, the coupling term S, lse, inverse RMS
+            const T *grow = static_cast<const T *>(a.dout) + tok * d;
+            const T *orow = static_cast<const T *>(a.fout) + tok * d;
+            float sp = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                float o[8];
+                ld_chunk_g(grow + cidx[j] * 8, G[j]);
+                ld_chunk_g(orow + cidx[j] * 8, o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sp = fmaf(G[j][e], o[e], sp);
+            }
+            S_h = group_sum(sp, LPH);
+            lse2 = __ldg(a.lse + tok * H + h) * kLog2e;
+            __syncwarp();
+            for (int nn = lane; nn < N; nn += 32)
+                cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+            __syncwarp();
+        }
+        const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
+        if (!__all_sync(FULL, got)) { ok = false; break; }
+        phase ^= 1u << slot;
+        const unsigned char *vb = ring + (size_t)slot * slot_bytes;
+        const float *gb = reinterpret_cast<const float *>(vb + vbytes);
+        const bool first = (s_first[n >> 5] >> (n & 31)) & 1u;
+
+        // pass 1: value dot with G and raw score
+        float P = 0.f, zr = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            float v[8], qgc[8];
+            ld_chunk_s(reinterpret_cast<const T *>(vb + cidx[j] * CB), v);
+            ld_chunk_s(s_qg + cidx[j] * 8, qgc);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                P = fmaf(G[j][e], v[e], P);
+                zr = fmaf(qgc[e], v[e], zr);
+            }
+        }
+        P = group_sum(P, LPH);
+        zr = group_sum(zr, LPH);
+        const float iv = cur_inv[n];
+        const float w = exp2f(fmaf(iv * zr, kLog2e, -lse2));
+        const float dz = w * (P - S_h);
+        const float C = (H == 1) ? dz * zr : warp_sum(sub == 0 ? dz * zr : 0.f);
+        const float coef = iv * iv * iv * C * inv_d;
+        const float ak = iv * dz;
+        float *grad_row = a.grad + ((int64_t)s_rows[n] * TT + tok) * d;
+
+        // pass 2: gradient row
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            float v[8], qgc[8], nv[8];
+            ld_chunk_s(reinterpret_cast<const T *>(vb + cidx[j] * CB), v);
+            ld_chunk_s(s_qg + cidx[j] * 8, qgc);
+            if (first) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) nv[e] = 0.f;
+            } else {
+                ld_chunk_s(gb + cidx[j] * 8, nv);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                nv[e] = fmaf(w, G[j][e], nv[e]);
+                nv[e] = fmaf(ak, qgc[e], nv[e]);
+                nv[e] = fmaf(-coef, v[e], nv[e]);
+                U[j][e] = fmaf(ak, v[e], U[j][e]);
+            }
+            st_f32x8_g(grad_row + cidx[j] * 8, nv);
+        }
+        __syncwarp();
+        if (issued < hi) issue_next();
+        if (++n == N) { n = 0; ++tok; }
+        if (++slot == S) slot = 0;
+    }
+
+    if (!ok) {
+        if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
+        for (int64_t j = i; j < issued; ++j) {
+            mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+            phase ^= 1u << slot;
+            if (++slot == S) slot = 0;
+        }
+    }
+
+    // per-warp partial sums U -> workspace row gw
+    float *wrow = a.ws + gw * d;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) st_f32x8_g(wrow + cidx[j] * 8, U[j]);
+}
+
+template <typename T, int CPL>
+cudaError_t bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_warps)
+{
+    const void *k = reinterpret_cast<const void *>(&route_bwd_kernel<T, CPL>);
+    const size_t smem = bwd_smem_bytes(a->d, sizeof(T));
+    int grid = 0;
+    cudaError_t e = persistent_grid(k, kBwdWarps * 32, smem, &grid);
+    if (e != cudaSuccess) return e;
+    if (grid_warps) {
+        *grid_warps = grid * kBwdWarps;
+        return cudaSuccess;
+    }
+    route_bwd_kernel<T, CPL><<<grid, kBwdWarps * 32, smem, s>>>(*a);
+    return cudaGetLastError();
+}
+
+// Same shapes as the forward. With grid_warps != nullptr only the grid (in
+// warps = workspace rows) is computed and nothing is launched.
+template <typename T>
+cudaError_t dispatch_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps)
+{
+    if (a->r != a->d) return cudaErrorNotSupported;
+    switch (a->d / 256) {
+    case 1: return bwd_inst<T, 1>(a, s, grid_warps);
+    case 2: return bwd_inst<T, 2>(a, s, grid_warps);
+    case 3: return bwd_inst<T, 3>(a, s, grid_warps);
+    case 4: return bwd_inst<T, 4>(a, s, grid_warps);
+    case 5: return bwd_inst<T, 5>(a, s, grid_warps);
+    case 6: return bwd_inst<T, 6>(a, s, grid_warps);
+    case 7: return bwd_inst<T, 7>(a, s, grid_warps);
+    case 8: return bwd_inst<T, 8>(a, s, grid_warps);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace ar

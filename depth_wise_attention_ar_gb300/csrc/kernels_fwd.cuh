@@ -1,0 +1,239 @@
+// Fused routing forward for sm_103a, full-width keys (r = d).
+//
+// Computes, for one routing site and every token t, the per-head softmax
+// over the listed sources and the mixed output ("Multi-Head Attention
+// Residuals", Eq. 3; the fused online-softmax design of its Appendix E,
+// Figure 9), with the RMSNorm key taken from the cached inverse RMS.
+//
+// GB300 mapping
+// - One warp owns one token at a time and walks its N source rows. Each row
+//   (d elements, contiguous) is brought into a per-warp ring of shared-memory
+//   stages by a single 1-D bulk copy (cp.async.bulk, completion on an
+//   mbarrier); lane 0 refills a stage as soon as the warp has consumed it, so
+//   every warp keeps kFwdStages rows in flight and no warp waits on another.
+// - Lane l serves head h = l / (32/H); the head's d/H coordinates are spread
+//   over its 32/H lanes in 8-element chunks (CPL = d/256 chunks per lane), so
+//   the per-head score is a reduction over 32/H lanes (log2(32/H) shuffles)
+//   and the lane's head weight needs no broadcast. Chunk order is rotated by
+//   the head index so that the lanes of the two heads that share a
+//   quarter-warp hit different shared-memory banks.
+// - The accumulator (8*CPL floats) and q*g (8*CPL floats) live in registers;
+//   the staged row is read twice from shared memory (score, then mix).
+// - The softmax is online in log2 units; the running maximum only moves when
+//   a score exceeds it by kRescaleTau, so the accumulator is rarely rescaled.
+// - Grid: persistent, SM count x resident blocks; tokens strided over warps.
+#pragma once
+
+#include "common.cuh"
+#include "launch_util.cuh"
+
+namespace ar {
+
+constexpr int kFwdWarps = 4;
+constexpr int kFwdStages = 4;
+
+inline size_t fwd_smem_bytes(int d, size_t esize)
+{
+    return (size_t)kFwdWarps * kFwdStages * d * esize + (size_t)kFwdWarps * kFwdStages * 8 +
+           (size_t)kFwdWarps * AR_MAX_SOURCES * 4;
+}
+
+template <typename T, int CPL>
+__global__ void __launch_bounds__(kFwdWarps * 32)
+    route_fwd_kernel(const __grid_constant__ RouteArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_rows[AR_MAX_SOURCES];
+    constexpr int S = kFwdStages;
+    constexpr int CB = ChunkBytes<T>::value;
+    constexpr unsigned FULL = 0xffffffffu;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = a.d, N = a.n_src, H = a.H;
+    const int64_t TT = a.T;
+    const uint32_t row_bytes = (uint32_t)d * (uint32_t)sizeof(T);
+
+    for (int i = threadIdx.x; i < N; i += blockDim.x) s_rows[i] = a.rows[i];
+    unsigned char *ring = smem + (size_t)warp * S * row_bytes;
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + (size_t)kFwdWarps * S * row_bytes) + warp * S;
+    float *cur_inv = reinterpret_cast<float *>(smem + (size_t)kFwdWarps * S * row_bytes +
+                                               (size_t)kFwdWarps * S * 8) +
+                     warp * AR_MAX_SOURCES;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ---- lane -> head and chunk mapping
+    const int LPH = 32 / H;
+    const int h = lane / LPH, sub = lane - h * LPH;
+    int cidx[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) cidx[j] = h * (CPL * LPH) + sub + LPH * ((j + h) % CPL);
+    // query times norm weight, in log2 units, over this lane's coordinates
+    float qg[CPL][8];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = cidx[j] * 8 + e;
+            qg[j][e] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) * kLog2e;
+        }
+
+    // ---- work: tokens gw, gw + GW, ...
+    const int64_t GW = (int64_t)gridDim.x * kFwdWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kFwdWarps + warp;
+    const int64_t ntok = gw < TT ? (TT - 1 - gw) / GW + 1 : 0;
+    const int64_t total = ntok * N;
+    const uint64_t pol = l2_policy_evict_first();
+
+    // producer cursor (all lanes track it; lane 0 issues)
+    int64_t issued = 0, tok_p = gw;
+    int n_p = 0, slot_p = 0;
+    auto issue_next = [&]() {
+        if (lane == 0) {
+            const unsigned char *src = static_cast<const unsigned char *>(a.bank) +
+                                       ((int64_t)s_rows[n_p] * TT + tok_p) * row_bytes;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[slot_p], row_bytes);
+            bulk_g2s(ring + (size_t)slot_p * row_bytes, src, row_bytes, &bars[slot_p], pol);
+        }
+        ++issued;
+        if (++n_p == N) { n_p = 0; tok_p += GW; }
+        if (++slot_p == S) slot_p = 0;
+    };
+    for (int s = 0; s < S && issued < total; ++s) issue_next();
+
+    // inverse RMS of the next token's sources, prefetched into registers
+    float pre_inv[AR_MAX_SOURCES / 32];
+    auto prefetch_inv = [&](int64_t tok) {
+#pragma unroll
+        for (int u = 0; u < AR_MAX_SOURCES / 32; ++u) {
+            const int nn = lane + 32 * u;
+            if (nn < N) pre_inv[u] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+        }
+    };
+    if (ntok > 0) prefetch_inv(gw);
+
+    int n = 0, slot = 0;
+    uint32_t phase = 0;
+    int64_t tok = gw, i = 0;
+    float m = 0.f, l = 0.f;
+    float acc[CPL][8];
+    bool ok = true;
+    for (; i < total; ++i) {
+        if (n == 0) {
+#pragma unroll
+            for (int u = 0; u < AR_MAX_SOURCES / 32; ++u) {
+                const int nn = lane + 32 * u;
+                if (nn < N) cur_inv[nn] = pre_inv[u];
+            }
+            __syncwarp();
+            if (tok + GW < TT) prefetch_inv(tok + GW);
+        }
+        const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
+        if (!__all_sync(FULL, got)) { ok = false; break; }
+        phase ^= 1u << slot;
+        const unsigned char *buf = ring + (size_t)slot * row_bytes;
+
+        // score of this lane's head: q_h . (g * s_n)_[h], times inv_n
+        float zr = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            float v[8];
+            ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) zr = fmaf(qg[j][e], v[e], zr);
+        }
+        zr = group_sum(zr, LPH);
+        const float z2 = zr * cur_inv[n];  // score in log2 units
+
+        float p = 1.f;
+        if (n == 0) {
+            m = z2;
+            l = 1.f;
+        } else {
+            const bool need = z2 > m + kRescaleTau;
+            if (__any_sync(FULL, need)) {
+                const float sc = need ? exp2f(m - z2) : 1.f;
+                m = need ? z2 : m;
+                l *= sc;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[j][e] *= sc;
+            }
+            p = exp2f(z2 - m);
+            l += p;
+        }
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            float v[8];
+            ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j][e] = (n == 0) ? v[e] : fmaf(p, v[e], acc[j][e]);
+        }
+        __syncwarp();
+        if (issued < total) issue_next();  // refill the stage just consumed
+
+        if (n == N - 1) {
+            const float rl = 1.f / l;
+            T *orow = static_cast<T *>(a.out) + tok * d;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
+                st_chunk_g(orow + cidx[j] * 8, o);
+            }
+            if (sub == 0) a.lse[tok * H + h] = (m + log2f(l)) * kLn2;
+        }
+        if (++n == N) { n = 0; tok += GW; }
+        if (++slot == S) slot = 0;
+    }
+
+    if (!ok) {
+        if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
+        // wait briefly for this warp's copies still in flight, then leave
+        for (int64_t j = i; j < issued; ++j) {
+            mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+            phase ^= 1u << slot;
+            if (++slot == S) slot = 0;
+        }
+    }
+}
+
+template <typename T, int CPL>
+cudaError_t launch_fwd_inst(const RouteArgs &a, cudaStream_t s)
+{
+    const void *k = reinterpret_cast<const void *>(&route_fwd_kernel<T, CPL>);
+    const size_t smem = fwd_smem_bytes(a.d, sizeof(T));
+    int grid = 0;
+    cudaError_t e = persistent_grid(k, kFwdWarps * 32, smem, &grid);
+    if (e != cudaSuccess) return e;
+    route_fwd_kernel<T, CPL><<<grid, kFwdWarps * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// Full-width keys with d = 256 * CPL, CPL in 1..8.
+template <typename T>
+cudaError_t dispatch_fwd(const RouteArgs &a, cudaStream_t s)
+{
+    if (a.r != a.d) return cudaErrorNotSupported;
+    switch (a.d / 256) {
+    case 1: return launch_fwd_inst<T, 1>(a, s);
+    case 2: return launch_fwd_inst<T, 2>(a, s);
+    case 3: return launch_fwd_inst<T, 3>(a, s);
+    case 4: return launch_fwd_inst<T, 4>(a, s);
+    case 5: return launch_fwd_inst<T, 5>(a, s);
+    case 6: return launch_fwd_inst<T, 6>(a, s);
+    case 7: return launch_fwd_inst<T, 7>(a, s);
+    case 8: return launch_fwd_inst<T, 8>(a, s);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace ar

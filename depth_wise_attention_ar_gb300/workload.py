@@ -1,0 +1,186 @@
+"""Microbatch driver: the whole routing path of one microbatch through the C ABI.
+
+A microbatch is what one training step of a model with depth routing asks of
+this library ("Multi-Head Attention Residuals", Figure 3 and Appendix E;
+"Low-Rank Attention Residuals", Figure 11):
+
+1. forward, in model order: append each new source row (its inverse RMS is
+   computed once here) and run the forward of every routing site;
+2. backward, in reverse order: run the backward of every site, accumulating
+   dL/ds into the shared fp32 gradient rows and producing dL/dq, dL/dg.
+
+Bank layout: row 0 holds the embedding, row t the state after sublayer t —
+the sublayer output itself (full routing) or the block partial sum
+(block routing). Rows that are plain sublayer outputs are written in place by
+their producer (here: filled before the step) and appended without a copy;
+block partial sums are appended as row p + o_t from a separate output buffer.
+
+The schedule comes from the library's own bookkeeping (``ar_block_schedule``);
+full routing is the schedule with one block per sublayer.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+
+__all__ = ["Config", "CONFIGS", "Plan", "make_plan", "Microbatch", "model_bytes"]
+
+
+@dataclass(frozen=True)
+class Config:
+    name: str
+    T: int                      # tokens per microbatch (batch x sequence)
+    d: int                      # width
+    H: int                      # routing heads
+    r: int                      # key width (r = d: full keys)
+    dtype: str                  # "bf16" | "f32"
+    M: int                      # residual-writing sublayers (2L)
+    NB: int | None = None       # blocks (None: full routing)
+    sites: tuple | None = None  # restrict to these site indices (None: all)
+    q_std: float = 0.02
+    note: str = ""
+
+
+CONFIGS = {
+    "tiny": Config("tiny", T=256, d=512, H=4, r=512, dtype="f32", M=4, sites=(4,),
+                   note="one MHAR site over N=5 sources, fp32"),
+    "100M": Config("100M", T=8 * 2048, d=512, H=4, r=512, dtype="bf16", M=24,
+                   note="d=512, L=12: 25 sites, site i reads the first i sources"),
+    "350M": Config("350M", T=16 * 1024, d=1024, H=8, r=1024, dtype="bf16", M=48,
+                   note="d=1024, L=24: 49 sites"),
+    "1B": Config("1B", T=16 * 1024, d=1280, H=8, r=1280, dtype="bf16", M=72,
+                 note="d=1280, L=36: 73 sites"),
+    "lr_block": Config("lr_block", T=8192, d=4096, H=8, r=1024, dtype="bf16", M=64, NB=8,
+                       note="32 layers in 8 blocks, keys = last 1024 coordinates"),
+}
+
+
+@dataclass
+class Plan:
+    acc_from: list            # per bank row: -1 (stored as is) or the row it accumulates onto
+    sites: list               # per site: row list
+    run_sites: list           # site indices that run
+
+    @property
+    def rows(self) -> int:
+        return len(self.acc_from)
+
+
+def make_plan(cfg: Config) -> Plan:
+    from . import binding as B
+    acc, sites = B.ar_block_schedule(cfg.M, cfg.NB)
+    run = list(cfg.sites) if cfg.sites is not None else list(range(len(sites)))
+    return Plan(acc_from=acc, sites=sites, run_sites=run)
+
+
+def model_bytes(cfg: Config, plan: Plan, H: int | None = None) -> dict:
+    """Algorithmic bytes of one microbatch (what the method must move).
+
+    forward site : T (N b d + 4 N + b d + 4 H)   (rows, inverse RMS, out, lse)
+    backward site: T (b d + b d + 4 H + 4 N + N b d + N d (8, or 4 on a row's
+                   first touch))                 (dout, out, lse, inverse RMS,
+                                                   rows once, gradient rows)
+    append       : T (b r + 4) for a row written in place by its producer
+                   (key read for the inverse RMS), T (3 b d + 4) for a partial
+                   sum (two reads, one write).
+    """
+    H = cfg.H if H is None else H
+    b = 2 if cfg.dtype == "bf16" else 4
+    T, d, r = cfg.T, cfg.d, cfg.r
+    fwd = bwd = app = 0
+    touched = set()
+    needed = sorted({row for s in plan.run_sites for row in plan.sites[s]})
+    for row in needed:
+        app += T * (3 * b * d + 4) if plan.acc_from[row] >= 0 else T * (b * r + 4)
+    for s in plan.run_sites:
+        N = len(plan.sites[s])
+        fwd += T * (N * b * d + 4 * N + b * d + 4 * H)
+    for s in reversed(plan.run_sites):
+        rows = plan.sites[s]
+        N = len(rows)
+        g = sum(4 * d if row in touched else 0 for row in rows) + 4 * d * N
+        touched.update(rows)
+        bwd += T * (2 * b * d + 4 * H + 4 * N + N * b * d) + T * g
+    return {"fwd": fwd, "bwd": bwd, "append": app, "total": fwd + bwd + app}
+
+
+@dataclass
+class Microbatch:
+    """Device buffers and launch sequence of one microbatch of a config."""
+
+    cfg: Config
+    H: int
+    inputs: object            # provides output(j,T,d,dtype), query(site,r),
+                              # norm_weight(site,r) (None = ones), dout(site,T,d,dtype)
+    device: str = "cuda"
+    plan: Plan = field(init=False)
+
+    def __post_init__(self):
+        import torch
+
+        from . import binding as B
+        cfg, dev, src = self.cfg, torch.device(self.device), self.inputs
+        self.plan = make_plan(cfg)
+        needed = sorted({row for s in self.plan.run_sites for row in self.plan.sites[s]})
+        self.n_rows = max(needed) + 1
+        self.bank = B.Bank(cfg.T, cfg.d, cfg.r, self.n_rows, cfg.dtype, eps=1e-6, device=dev)
+        tdt = self.bank.torch_dtype
+        # sublayer outputs: written in place into their bank rows, or kept in
+        # separate buffers when the row is a block partial sum
+        self.outputs = {}
+        for j in range(self.n_rows):
+            x = src.output(j, cfg.T, cfg.d, cfg.dtype)
+            if self.plan.acc_from[j] >= 0:
+                self.outputs[j] = x
+            else:
+                self.bank.rows[j].copy_(x)
+            del x
+        self.q = {s: src.query(s, cfg.r) for s in self.plan.run_sites}
+        self.g = {s: src.norm_weight(s, cfg.r) for s in self.plan.run_sites}
+        self.dout = {s: src.dout(s, cfg.T, cfg.d, cfg.dtype) for s in self.plan.run_sites}
+        self.out = {s: torch.empty((cfg.T, cfg.d), dtype=tdt, device=dev)
+                    for s in self.plan.run_sites}
+        self.lse = {s: torch.empty((cfg.T, self.H), dtype=torch.float32, device=dev)
+                    for s in self.plan.run_sites}
+        self.dq = {s: torch.empty(cfg.r, device=dev) for s in self.plan.run_sites}
+        self.dg = {s: torch.empty(cfg.r, device=dev) for s in self.plan.run_sites}
+        self.ws = self.bank.workspace(self.H)
+
+    def forward(self, stream=None, on_site=None):
+        bank, plan = self.bank, self.plan
+        bank.reset()
+        appended = 0
+        run = set(plan.run_sites)
+        last = max(plan.run_sites)
+        for t in range(last + 1):
+            if t < self.n_rows:
+                src = self.outputs.get(t, bank.rows[t])
+                bank.append(src, plan.acc_from[t], stream)
+                appended += 1
+            if t in run:
+                bank.route_fwd(plan.sites[t], self.H, self.q[t], self.g[t], self.out[t],
+                               self.lse[t], site_id=t, stream=stream)
+                if on_site:
+                    on_site("fwd", t)
+        return appended
+
+    def backward(self, stream=None, on_site=None):
+        bank, plan = self.bank, self.plan
+        bank.zero_grad()
+        for t in reversed(plan.run_sites):
+            if on_site:
+                on_site("bwd_begin", t)
+            bank.route_bwd(plan.sites[t], self.H, self.q[t], self.g[t], self.out[t], self.dout[t],
+                           self.lse[t], self.dq[t], self.dg[t] if self.g[t] is not None else None,
+                           site_id=t, stream=stream, ws=self.ws)
+            if on_site:
+                on_site("bwd_end", t)
+
+    def step(self, stream=None):
+        self.forward(stream)
+        self.backward(stream)
+
+    def kernel_launches(self) -> int:
+        """Kernels one step launches: appends, forwards, backward + reduce per site."""
+        return self.n_rows + 3 * len(self.plan.run_sites)

@@ -1,0 +1,232 @@
+/*
+ * attnres.h — C ABI of the GB300 depth-routing library (libattnres_gb300.so).
+ *
+ * The depth-routing read of attention residuals: at every routing site each
+ * token reads a learned softmax mixture over a bank of earlier sublayer
+ * outputs ("Multi-Head Attention Residuals", Sec. 2.2 Eq. 2 and Sec. 2.3
+ * Eq. 3; "Low-Rank Attention Residuals", Sec. 3.1-3.3 Eq. 2-12).
+ *
+ *   key of source n, token t : RMSNorm over the key coordinates, times g.
+ *                              The key coordinates are the last r of the d
+ *                              coordinates (r = d: plain AttnRes / MHAR keys;
+ *                              r < d: the sliced keys of LR-AttnRes, Eq. 11).
+ *   head h (H heads)         : value slice = coordinates [h*d/H, (h+1)*d/H),
+ *                              key slice   = coordinates d-r + [h*r/H, (h+1)*r/H).
+ *   score    z[n,h]  = inv[n] * sum_{c in key slice h} q[c'] g[c'] s_n[c]
+ *                      (c' = c - (d - r): q and g are indexed over the key
+ *                      coordinates), inv[n] = (mean_{key coords} s_n^2 + eps)^(-1/2)
+ *   weights  a[n,h]  = softmax over n of z[.,h]            (per head; Eq. 3)
+ *   output   out[c]  = sum_n a[n,h(c)] s_n[c]                          (Eq. 3)
+ *   lse[h]           = log sum_n exp z[n,h]          (saved for the backward)
+ * H = 1 is single-head AttnRes (MHAR Appendix B, Figure 7); r = d with H > 1 is
+ * MHAR; r < d is LR-AttnRes with the heads laid over the key slice.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Memory: the caller owns all device memory and every stream. The library
+ *   never allocates device memory and never synchronises the device, except
+ *   in ar_device_error(), which says so. Compute calls are asynchronous on
+ *   the given stream (a cudaStream_t passed as void*; NULL = legacy default).
+ * - Pointers named "device" must be device-accessible; "host" pointers are
+ *   read before the call returns and may be reused at once.
+ * - Every call returns an ar_status. Argument checks happen on the host
+ *   before anything is launched; a failed check launches nothing and leaves
+ *   the bank unchanged. A CUDA launch error returns AR_ERR_CUDA.
+ * - A device-side wait that runs out (a copy that never lands) does not trap:
+ *   the kernel records it in a device error word and returns; read it with
+ *   ar_device_error().
+ * - Banks are not thread-safe; distinct banks may be used from distinct
+ *   threads.
+ *
+ * Shapes the fused routing kernels cover: r = d, d a multiple of 256 up to
+ * 2048, H in {1,2,4,8,16,32}, 1 <= n_src <= AR_MAX_SOURCES, row/output
+ * pointers 16-byte aligned. Other shapes return AR_ERR_UNSUPPORTED (or
+ * AR_ERR_ALIGN for a misaligned pointer). Appends accept any d, r that are
+ * multiples of 8.
+ */
+#ifndef ATTNRES_H
+#define ATTNRES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AR_MAX_SOURCES 256
+
+typedef enum {
+    AR_OK = 0,
+    AR_ERR_INVALID_ARG = 1, /* null/duplicate/out-of-range argument        */
+    AR_ERR_SHAPE = 2,       /* inconsistent sizes (d % H, r > d, ...)       */
+    AR_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned      */
+    AR_ERR_CAPACITY = 4,    /* bank full, or workspace too small            */
+    AR_ERR_ORDER = 5,       /* backward not in reverse forward order        */
+    AR_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed         */
+    AR_ERR_TIMEOUT = 7,     /* a device-side wait ran out (see ar_device_error) */
+    AR_ERR_UNSUPPORTED = 8  /* valid, but outside the fused kernels' shapes */
+} ar_status;
+
+typedef enum { AR_F32 = 0, AR_BF16 = 1 } ar_dtype;
+
+/* Which coordinates the RMS statistic of a key runs over.
+ * AR_NORM_KEY : the key coordinates (last r) — LR-AttnRes Eq. 13, first line;
+ *               with r = d this is the full-width RMS of MHAR Appendix E.
+ * AR_NORM_FULL: all d coordinates with the sliced numerator — the
+ *               full-width-RMS control of LR-AttnRes Eq. 13, second line. */
+typedef enum { AR_NORM_KEY = 0, AR_NORM_FULL = 1 } ar_norm;
+
+/* Device error bits reported by ar_device_error(). */
+#define AR_DEVERR_WAIT_TIMEOUT 1u
+
+typedef struct ar_bank ar_bank; /* opaque host-side handle */
+
+/* Human-readable name of a status. Never NULL. */
+const char *ar_status_string(ar_status s);
+
+/* Number of floats the inverse-RMS cache of a bank needs: T * ld, where
+ * ld = capacity rounded up to a multiple of 4 (token-major layout, below). */
+ar_status ar_inv_rms_floats(int64_t T, int32_t capacity, int64_t *floats);
+
+/*
+ * Create a bank: the shared source buffer of MHAR Appendix E ("Shared source
+ * buffer": one [2L+1, B, T, d] buffer written once per source) plus the
+ * per-row inverse-RMS cache and the shared fp32 gradient accumulator
+ * (Appendix E, backward: "one shared fp32 buffer, in place").
+ *   T        : tokens (batch x sequence), T >= 0. T = 0 makes every compute
+ *              call a no-op (the backward still zeroes dq/dg), and then every
+ *              per-token pointer (rows, inv_rms, src, out, lse, dout, ws) may
+ *              be NULL.
+ *   d, r     : width and key width (1 <= r <= d)
+ *   capacity : rows the bank can hold (1 <= capacity)
+ *   dtype    : storage type of rows, outputs and dout
+ *   norm     : RMS coordinates of the keys (ar_norm)
+ *   eps      : RMSNorm epsilon (> 0 recommended; 1e-6 in the pages' models)
+ *   rows     : device [capacity, T, d] of dtype (row-major: row j's token t
+ *              starts at (j*T + t)*d elements)
+ *   inv_rms  : device float [T, ld] (token-major; ld from ar_inv_rms_floats)
+ *   grad     : device float [capacity, T, d], or NULL for forward-only use
+ * On success *out receives a handle owned by the caller (ar_bank_destroy).
+ * The pointed-to buffers must outlive the bank. Errors: AR_ERR_INVALID_ARG
+ * (null out/rows/inv_rms, capacity < 1), AR_ERR_SHAPE (r > d, d < 1),
+ * AR_ERR_ALIGN. Creating a bank touches no device; the first launch does.
+ */
+ar_status ar_bank_create(ar_bank **out, int64_t T, int32_t d, int32_t r, int32_t capacity,
+                         ar_dtype dtype, ar_norm norm, float eps, void *rows,
+                         float *inv_rms, float *grad);
+
+/* Release the handle (not the caller's buffers). NULL is accepted. */
+ar_status ar_bank_destroy(ar_bank *bank);
+
+/* Rows appended so far. */
+ar_status ar_bank_row_count(const ar_bank *bank, int32_t *count);
+
+/* Device address of row `row` (0 <= row < capacity): lets a producer write
+ * its sublayer output straight into the next bank slot (then append it with
+ * src = that address, which copies nothing). */
+ar_status ar_bank_row_ptr(const ar_bank *bank, int32_t row, void **ptr);
+
+/*
+ * Append one source row (MHAR Sec. 2.2: "each later source is the raw output
+ * of one attention or MLP sublayer"; LR-AttnRes Eq. 5-6 and Figure 11 for
+ * the block variant) and cache its per-token inverse RMS once, for reuse by
+ * every later site.
+ *   src             : device [T, d] of the bank dtype. It may be the address
+ *                     of the slot being filled (ar_bank_row_ptr), then
+ *                     nothing is copied.
+ *   accumulate_from : -1 to store src as is; otherwise a row index p already
+ *                     appended: the new row is rows[p] + src computed in fp32
+ *                     and rounded once to the storage dtype (a new immutable
+ *                     partial-sum version; "accumulation precedes slicing and
+ *                     normalization", LR-AttnRes Sec. 3.3).
+ *   out_row         : receives the new row's index (may be NULL).
+ * Errors: AR_ERR_CAPACITY (bank full), AR_ERR_INVALID_ARG (bad p, null src),
+ * AR_ERR_ALIGN, AR_ERR_CUDA.
+ */
+ar_status ar_bank_append(ar_bank *bank, const void *src, int32_t accumulate_from,
+                         int32_t *out_row, void *stream);
+
+/* Start a new backward pass: mark every gradient row untouched, so that the
+ * first backward that reaches a row stores into it and later ones accumulate
+ * (MHAR Appendix E, FIRST_CALL). No memset is issued. */
+ar_status ar_bank_zero_grad(ar_bank *bank);
+
+/* Forget all rows, routing records and gradient flags (next microbatch). */
+ar_status ar_bank_reset(ar_bank *bank);
+
+/*
+ * Forward of one routing site: online softmax over the listed sources with
+ * the RMSNorm key fused in (MHAR Appendix E, "Forward: online softmax over
+ * depth with the norm fused in", Figure 9), each source row read once.
+ *   rows, n_src : host int32 list of distinct appended rows, 1..AR_MAX_SOURCES
+ *   H           : routing heads
+ *   q           : device float [r], the site's query
+ *   g           : device float [r] RMSNorm weight, or NULL for ones
+ *   out         : device [T, d] of the bank dtype
+ *   lse         : device float [T, H], per-head log-sum-exp (natural log)
+ *   site_id     : caller's id of this site; pushed on the bank's call record
+ *                 so that the backward can check reverse order.
+ * Errors: AR_ERR_INVALID_ARG (row not appended, duplicate row, n_src out of
+ * range, null pointers), AR_ERR_SHAPE (d % H or r % H nonzero),
+ * AR_ERR_UNSUPPORTED, AR_ERR_ALIGN, AR_ERR_CUDA.
+ */
+ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                       const float *q, const float *g, void *out, float *lse,
+                       int32_t site_id, void *stream);
+
+/* Bytes of device workspace ar_route_bwd needs for this bank and H (the
+ * per-block partial sums of dq/dg). Depends on the current device. */
+ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes);
+
+/*
+ * Backward of one routing site (MHAR Appendix E, "Backward: one kernel,
+ * norms recomputed, gradients accumulated in place", Figure 10; the
+ * value/routing split of LR-AttnRes Eq. 15 with the score gradient of
+ * Eq. 21/22). Given dL/dout it emits dL/ds_n for every listed source into the
+ * bank's fp32 gradient rows — a store on a row's first touch since
+ * ar_bank_zero_grad, an in-place accumulation afterwards — and dL/dq, dL/dg.
+ *   rows, n_src, H, q, g : exactly as in the forward of this site
+ *   out   : device [T, d], this site's forward output (its per-head dot with
+ *           dout is the softmax coupling term)
+ *   dout  : device [T, d] of the bank dtype, dL/dout
+ *   lse   : device float [T, H] written by this site's forward
+ *   dq    : device float [r], overwritten with dL/dq
+ *   dg    : device float [r] overwritten with dL/dg, or NULL to skip
+ *   ws    : device workspace of ws_bytes >= ar_route_bwd_workspace()
+ *   site_id: must equal the most recent forward's site_id not yet
+ *           backpropagated (reverse forward order, MHAR Appendix E);
+ *           otherwise AR_ERR_ORDER and nothing runs.
+ * Errors: as the forward, plus AR_ERR_ORDER, AR_ERR_CAPACITY (workspace too
+ * small), AR_ERR_INVALID_ARG (bank created without grad).
+ */
+ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                       const float *q, const float *g, const void *out, const void *dout,
+                       const float *lse, float *dq, float *dg, void *ws, size_t ws_bytes,
+                       int32_t site_id, void *stream);
+
+/*
+ * Block schedule of LR-AttnRes (Figure 11): M sublayers in NB blocks whose
+ * last sublayers are ceil(M*j/NB); NB <= 0 or NB >= M means full routing.
+ * Bank row 0 is the embedding; row t (1..M) is the partial sum after
+ * sublayer t. Outputs (host arrays):
+ *   acc_from  [M+1] : -1 if row t is stored as is (row 0, or the first
+ *                     sublayer of a block), else the row it accumulates onto
+ *   site_ptr  [M+2] : CSR offsets; site t (0..M) reads
+ *                     site_rows[site_ptr[t] .. site_ptr[t+1])
+ *   site_rows [cap] : row lists; *site_rows_len receives the total length
+ * Errors: AR_ERR_INVALID_ARG (M < 1, null outputs), AR_ERR_CAPACITY
+ * (site_rows_cap too small; *site_rows_len still receives the need).
+ */
+ar_status ar_block_schedule(int32_t M, int32_t NB, int32_t *acc_from, int32_t *site_ptr,
+                            int32_t *site_rows, int64_t site_rows_cap, int64_t *site_rows_len);
+
+/* Read and clear the device error word of the current device (bit mask of
+ * AR_DEVERR_*; 0 = none). This call synchronises the device. */
+ar_status ar_device_error(uint32_t *bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNRES_H */

@@ -143,3 +143,103 @@ def site_dout(seed: int, site: int, T: int, d: int, dtype: str) -> np.ndarray:
 def misc_normal(seed: int, tag: int, shape, std: float = 1.0) -> np.ndarray:
     """A float32 draw for tests that need extra independent values."""
     return normal_f32(seed, (_TAGS["misc"], tag), shape, std)
+
+
+# ---- device-side generation for full-size workloads -----------------------------
+# Full-size microbatches hold billions of values; they are drawn on the GPU by
+# torch's seeded Philox generator, one generator per tensor (keyed like the host
+# streams above). The oracle side of a parity check reads the same values back
+# for the tokens it samples, so both sides still see identical bits.
+
+def _key64(seed: int, *ids: int) -> int:
+    h = hashlib.blake2b(digest_size=8)
+    h.update(int(seed).to_bytes(8, "little", signed=True))
+    for i in ids:
+        h.update(int(i).to_bytes(8, "little", signed=True))
+    return int.from_bytes(h.digest(), "little") & ((1 << 63) - 1)
+
+
+class DeviceInputs:
+    """Seeded synthetic inputs drawn on a CUDA device (same recipe as above).
+
+    Methods return torch tensors on ``device``; ``dtype`` is "bf16" or "f32"
+    (rounded to nearest even by torch's conversion)."""
+
+    def __init__(self, seed: int = 0, device="cuda", q_std: float = 0.02,
+                 g_kind: str = "ones"):
+        import torch
+        self.torch = torch
+        self.seed, self.device, self.q_std, self.g_kind = seed, torch.device(device), q_std, g_kind
+
+    def _randn(self, shape, *ids):
+        torch = self.torch
+        g = torch.Generator(device=self.device)
+        g.manual_seed(_key64(self.seed, *ids))
+        return torch.randn(shape, generator=g, device=self.device, dtype=torch.float32)
+
+    def _cast(self, x, dtype):
+        return x.to(self.torch.bfloat16 if dtype == "bf16" else self.torch.float32)
+
+    def output(self, j: int, T: int, d: int, dtype: str):
+        return self._cast(self._randn((T, d), _TAGS["source"], j) * layer_scale(j), dtype)
+
+    def query(self, site: int, r: int):
+        return self._randn((r,), _TAGS["query"], site) * self.q_std
+
+    def norm_weight(self, site: int, r: int):
+        if self.g_kind == "ones":
+            return None
+        return 1.0 + 0.1 * self._randn((r,), _TAGS["normw"], site)
+
+    def dout(self, site: int, T: int, d: int, dtype: str):
+        return self._cast(self._randn((T, d), _TAGS["dout"], site), dtype)
+
+
+class HostInputs:
+    """The host (numpy Philox) streams above, served as CUDA tensors.
+
+    Same interface as ``DeviceInputs``; ``host_*`` methods return the float64
+    values the oracle consumes (exact widenings of the stored values)."""
+
+    def __init__(self, seed: int = 0, device="cuda", q_std: float = 0.02,
+                 g_kind: str = "ones"):
+        import torch
+        self.torch = torch
+        self.seed, self.device, self.q_std, self.g_kind = seed, torch.device(device), q_std, g_kind
+
+    def _to_dev(self, a: np.ndarray, dtype: str):
+        torch = self.torch
+        if dtype == "bf16":
+            t = torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32).copy())
+        return t.to(self.device)
+
+    def output(self, j, T, d, dtype):
+        return self._to_dev(sublayer_output(self.seed, j, T, d, dtype), dtype)
+
+    def query(self, site, r):
+        return self._to_dev(site_query(self.seed, site, r, self.q_std), "f32")
+
+    def norm_weight(self, site, r):
+        if self.g_kind == "ones":
+            return None
+        return self._to_dev(site_norm_weight(self.seed, site, r, self.g_kind), "f32")
+
+    def dout(self, site, T, d, dtype):
+        return self._to_dev(site_dout(self.seed, site, T, d, dtype), dtype)
+
+    # float64 views for the oracle
+    def host_output(self, j, T, d, dtype):
+        return storage_to_f64(sublayer_output(self.seed, j, T, d, dtype), dtype)
+
+    def host_query(self, site, r):
+        return site_query(self.seed, site, r, self.q_std).astype(np.float64)
+
+    def host_norm_weight(self, site, r):
+        if self.g_kind == "ones":
+            return None
+        return site_norm_weight(self.seed, site, r, self.g_kind).astype(np.float64)
+
+    def host_dout(self, site, T, d, dtype):
+        return storage_to_f64(site_dout(self.seed, site, T, d, dtype), dtype)

@@ -1,0 +1,290 @@
+"""GPU path against the CPU oracle, element by element, through the C ABI.
+
+Tolerances (normalised max-abs error, max|x - ref| / max|ref|): 1e-5 for
+fp32 storage, 2e-2 for bf16 storage. Bank contents and row bookkeeping are
+compared bit for bit. Inputs come from ``synth`` (the shared seeded
+generators); expected values come from ``oracle`` only.
+"""
+
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def W():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from depth_wise_attention_ar_gb300 import build
+    build.build()
+    from depth_wise_attention_ar_gb300 import binding, workload
+    return binding, workload
+
+
+def nmax(x, ref):
+    x, ref = np.asarray(x, dtype=np.float64), np.asarray(ref, dtype=np.float64)
+    den = max(float(np.max(np.abs(ref))), 1e-30)
+    return float(np.max(np.abs(x - ref))) / den
+
+
+def to64(t):
+    import torch
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def oracle_chain(inputs, cfg, H, plan, orc):
+    """Oracle run of the whole microbatch: rows, per-site out/lse, dsrc rows, dq, dg."""
+    from oracle import schedule, storage
+    T, d, r = cfg.T, cfg.d, cfg.r
+    oplan = schedule.block_plan(cfg.M, cfg.NB)
+    assert oplan["sites"] == plan.sites               # bit-exact bookkeeping
+    needed = sorted({row for s in plan.run_sites for row in plan.sites[s]})
+    nrows = max(needed) + 1
+    outs = [inputs.host_output(j, T, d, cfg.dtype) for j in range(nrows)]
+    rows = storage.block_bank(outs, {"row_ops": oplan["row_ops"][:nrows]}, cfg.dtype)
+    res = {"rows": rows, "out": {}, "lse": {}, "dq": {}, "dg": {}}
+    for s in plan.run_sites:
+        src = [rows[j] for j in plan.sites[s]]
+        res["out"][s], res["lse"][s] = orc.route_fwd(src, inputs.host_query(s, r),
+                                                     inputs.host_norm_weight(s, r), H, r=r)
+    dsrc = {j: np.zeros((T, d)) for j in range(nrows)}
+    for s in reversed(plan.run_sites):
+        src = [rows[j] for j in plan.sites[s]]
+        _, dq, dg = orc.route_bwd(src, inputs.host_query(s, r), inputs.host_norm_weight(s, r),
+                                  inputs.host_dout(s, T, d, cfg.dtype), H, r=r,
+                                  dsrc=[dsrc[j] for j in plan.sites[s]])
+        res["dq"][s], res["dg"][s] = dq, dg
+    res["dsrc"] = dsrc
+    return res
+
+
+def run_and_compare(W, orc, cfg, H, q_std=0.02, g_kind="ones", seed=0, check_dg=True):
+    import torch
+    B, wl = W
+    inputs = synth.HostInputs(seed=seed, q_std=q_std, g_kind=g_kind)
+    mb = wl.Microbatch(cfg, H, inputs)
+    mb.step()
+    torch.cuda.synchronize()
+    assert B.ar_device_error() == 0
+    ref = oracle_chain(inputs, cfg, H, mb.plan, orc)
+    tol = TOL[cfg.dtype]
+    worst = {}
+    for s in mb.plan.run_sites:
+        worst[f"out{s}"] = nmax(to64(mb.out[s]), ref["out"][s])
+        worst[f"lse{s}"] = nmax(to64(mb.lse[s]), ref["lse"][s])
+        worst[f"dq{s}"] = nmax(to64(mb.dq[s]), ref["dq"][s])
+        if g_kind != "ones" and check_dg:
+            worst[f"dg{s}"] = nmax(to64(mb.dg[s]), ref["dg"][s])
+    for j in range(mb.n_rows):
+        worst[f"dV{j}"] = nmax(to64(mb.bank.grad[j]), ref["dsrc"][j])
+    bad = {k: v for k, v in worst.items() if not v <= tol}
+    assert not bad, f"over tolerance {tol}: {bad}"
+    return mb, ref, worst
+
+
+def small(wl, name, T, d, H, dtype, M, NB=None, sites=None, r=None):
+    return wl.Config(name, T=T, d=d, H=H, r=d if r is None else r, dtype=dtype, M=M, NB=NB,
+                     sites=sites)
+
+
+def test_tiny_config_fp32(W, orc):
+    """The tiny MHAR site: T=256, d=512, H=4, N=5, fp32, query std 0.02."""
+    _, wl = W
+    run_and_compare(W, orc, wl.CONFIGS["tiny"], 4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("q_std", [0.02, 0.3, 2.0])
+def test_full_schedule_chain(W, orc, dtype, q_std):
+    """A whole microbatch (8 sites, site i reads the first i sources), ragged T,
+    random norm weights; q_std=2 makes the softmax peaked (exercises the
+    online rescale)."""
+    _, wl = W
+    cfg = small(wl, "chain", T=333, d=512, H=4, dtype=dtype, M=7)
+    run_and_compare(W, orc, cfg, 4, q_std=q_std, g_kind="random")
+
+
+@pytest.mark.parametrize("d,H", [(256, 1), (256, 32), (768, 2), (768, 8), (1280, 1), (1280, 4),
+                                 (1280, 8), (1280, 16), (1024, 8), (2048, 16), (1792, 4)])
+def test_widths_and_heads(W, orc, d, H):
+    _, wl = W
+    cfg = small(wl, "wh", T=211, d=d, H=H, dtype="bf16", M=4)
+    run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
+
+
+@pytest.mark.parametrize("d,H", [(512, 4), (1280, 8)])
+def test_widths_fp32(W, orc, d, H):
+    _, wl = W
+    cfg = small(wl, "wh32", T=150, d=d, H=H, dtype="f32", M=5)
+    run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
+
+
+def test_single_source_site_is_identity(W, orc):
+    import torch
+    B, wl = W
+    cfg = small(wl, "n1", T=97, d=512, H=4, dtype="bf16", M=0 + 1, sites=(0,))
+    inputs = synth.HostInputs(seed=3, q_std=1.0, g_kind="random")
+    mb = wl.Microbatch(cfg, 4, inputs)
+    mb.step()
+    torch.cuda.synchronize()
+    assert torch.equal(mb.out[0], mb.bank.rows[0])               # bit-exact copy
+    assert torch.all(mb.dq[0] == 0) and torch.all(mb.dg[0] == 0)
+    dout = mb.dout[0].float()
+    assert nmax(to64(mb.bank.grad[0]), to64(dout)) < 1e-6       # w = 1 up to rounding
+
+
+def test_many_sources_and_tiny_T(W, orc):
+    """n_src = 256 (the maximum) and T = 1."""
+    _, wl = W
+    cfg = small(wl, "wide", T=1, d=256, H=8, dtype="f32", M=255, sites=(255,))
+    run_and_compare(W, orc, cfg, 8, q_std=0.5, g_kind="random")
+
+
+def test_empty_token_count(W):
+    import torch
+    B, _ = W
+    bank = B.Bank(0, 512, 512, 2, "bf16")
+    src = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
+    bank.append(src)
+    bank.append(src)
+    q = torch.randn(512, device="cuda")
+    out, lse = bank.route_fwd([0, 1], 4, q, site_id=1)
+    dq = torch.full((512,), 7.0, device="cuda")
+    bank.zero_grad()
+    bank.route_bwd([0, 1], 4, q, None, out, out, lse, dq=dq, site_id=1)
+    torch.cuda.synchronize()
+    assert torch.all(dq == 0)
+
+
+def test_repeatable_bits(W):
+    """Two runs of the same microbatch give identical bits (no atomics)."""
+    import torch
+    _, wl = W
+    cfg = small(wl, "rep", T=1000, d=1280, H=8, dtype="bf16", M=9)
+    inputs = synth.HostInputs(seed=5, q_std=0.5, g_kind="random")
+    mb = wl.Microbatch(cfg, 8, inputs)
+    mb.step()
+    a = [t.clone() for t in (*mb.out.values(), *mb.lse.values(), *mb.dq.values(),
+                              *mb.dg.values(), mb.bank.grad)]
+    mb.step()
+    b = [t.clone() for t in (*mb.out.values(), *mb.lse.values(), *mb.dq.values(),
+                              *mb.dg.values(), mb.bank.grad)]
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("r", [512, 256])
+def test_block_bank_rows_and_inverse_rms(W, orc, dtype, r):
+    """Block-routing appends: every row (copy or accumulate) is bit-exact against
+    the oracle's storage rounding; the cached inverse RMS (over the last r
+    coordinates) matches the oracle."""
+    import torch
+    from oracle import schedule, storage
+    B, wl = W
+    T, d, M, NB = 300, 512, 12, 3
+    acc, sites = B.ar_block_schedule(M, NB)
+    bank = B.Bank(T, d, r, M + 1, dtype)
+    inputs = synth.HostInputs(seed=7)
+    for t in range(M + 1):
+        o = inputs.output(t, T, d, dtype)
+        if acc[t] < 0:
+            bank.rows[t].copy_(o)
+            bank.append(bank.rows[t])
+        else:
+            bank.append(o, acc[t])
+    torch.cuda.synchronize()
+    oplan = schedule.block_plan(M, NB)
+    ref = storage.block_bank([inputs.host_output(t, T, d, dtype) for t in range(M + 1)], oplan,
+                             dtype)
+    got = bank.rows.cpu()
+    inv = bank.inv_rms().cpu().numpy().astype(np.float64)
+    for t in range(M + 1):
+        bits = storage.storage_bits(ref[t], dtype)
+        mine = (got[t].view(torch.int16).numpy().view(np.uint16) if dtype == "bf16"
+                else got[t].numpy().view(np.uint32))
+        assert np.array_equal(mine, bits), f"row {t}"
+        assert nmax(inv[:, t], orc.inv_rms(ref[t], r=r)) < 2e-6
+
+
+def test_error_paths_on_device(W):
+    import torch
+    B, _ = W
+    bank = B.Bank(64, 512, 512, 3, "bf16")
+    x = torch.zeros((64, 512), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        bank.append(x)
+    with pytest.raises(B.ARError) as e:
+        bank.append(x)
+    assert e.value.name == "AR_ERR_CAPACITY"
+    q = torch.zeros(512, device="cuda")
+    with pytest.raises(B.ARError) as e:
+        bank.route_fwd([0, 0], 4, q)
+    assert e.value.name == "AR_ERR_INVALID_ARG"                   # duplicate source
+    out1, lse1 = bank.route_fwd([0, 1], 4, q, site_id=1)
+    out2, lse2 = bank.route_fwd([0, 1, 2], 4, q, site_id=2)
+    bank.zero_grad()
+    with pytest.raises(B.ARError) as e:                          # not reverse order
+        bank.route_bwd([0, 1], 4, q, None, out1, out1, lse1, site_id=1)
+    assert e.value.name == "AR_ERR_ORDER"
+    ws = bank.workspace(4)
+    with pytest.raises(B.ARError) as e:
+        bank.route_bwd([0, 1, 2], 4, q, None, out2, out2, lse2, site_id=2, ws=ws[:4])
+    assert e.value.name == "AR_ERR_CAPACITY"
+    bank.route_bwd([0, 1, 2], 4, q, None, out2, out2, lse2, site_id=2)
+    bank.route_bwd([0, 1], 4, q, None, out1, out1, lse1, site_id=1)
+    torch.cuda.synchronize()
+    assert B.ar_device_error() == 0
+
+
+def test_full_size_1b_sampled_tokens(W, orc):
+    """The 1B-shaped microbatch at full size (T=16384, d=1280, H=8, 73 sites), in
+    the launch configuration the benchmark times: outputs, lse and source
+    gradients of 48 sampled tokens against the oracle, dq/dg of the last site
+    (all 73 sources, all tokens) against the oracle in token chunks."""
+    import torch
+    _, wl = W
+    cfg = wl.CONFIGS["1B"]
+    inputs = synth.DeviceInputs(seed=11, q_std=0.3, g_kind="random")
+    mb = wl.Microbatch(cfg, cfg.H, inputs)
+    mb.step()
+    torch.cuda.synchronize()
+    T, d, H = cfg.T, cfg.d, cfg.H
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(T, size=48, replace=False))
+    toks[0], toks[-1] = 0, T - 1
+    ti = torch.as_tensor(toks, device="cuda")
+    rows = [to64(mb.bank.rows[j][ti]) for j in range(mb.n_rows)]
+    dsrc = {j: np.zeros((len(toks), d)) for j in range(mb.n_rows)}
+    tol = TOL["bf16"]
+    for s in mb.plan.run_sites:
+        src = [rows[j] for j in mb.plan.sites[s]]
+        q, g = to64(mb.q[s]), to64(mb.g[s])
+        o, l = orc.route_fwd(src, q, g, H)
+        assert nmax(to64(mb.out[s][ti]), o) < tol, s
+        assert nmax(to64(mb.lse[s][ti]), l) < tol, s
+    for s in reversed(mb.plan.run_sites):
+        src = [rows[j] for j in mb.plan.sites[s]]
+        orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][ti]), H,
+                      dsrc=[dsrc[j] for j in mb.plan.sites[s]])
+    for j in range(mb.n_rows):
+        assert nmax(to64(mb.bank.grad[j][ti]), dsrc[j]) < tol, j
+    # dq / dg of the last site over every token, oracle run chunk by chunk
+    s = mb.plan.run_sites[-1]
+    dq = np.zeros(d)
+    dg = np.zeros(d)
+    for t0 in range(0, T, 2048):
+        sl = slice(t0, min(T, t0 + 2048))
+        src = [to64(mb.bank.rows[j][sl]) for j in mb.plan.sites[s]]
+        _, a, b = orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][sl]), H)
+        dq += a
+        dg += b
+    assert nmax(to64(mb.dq[s]), dq) < tol
+    assert nmax(to64(mb.dg[s]), dg) < tol
