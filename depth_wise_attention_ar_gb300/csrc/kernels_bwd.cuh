@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         for (int e = 0; e < 8; ++e) U[j][e] = 0.f;
 
     float G[CPL][8];
-    float S_h = 0.f, lse2 = 0.f;
+    float S_h = 0.f, lse_h = 0.f;
     int64_t tok = lo / N, i = lo;
     int n = (int)(lo - tok * N), slot = 0;
     uint32_t phase = 0;
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
                 for (int e = 0; e < 8; ++e) sp = fmaf(G[j][e], o[e], sp);
             }
             S_h = group_sum(sp, LPH);
-            lse2 = __ldg(a.lse + tok * H + h) * kLog2e;
+            lse_h = __ldg(a.lse + tok * H + h);
             __syncwarp();
             for (int nn = lane; nn < N; nn += 32)
                 cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         P = group_sum(P, LPH);
         zr = group_sum(zr, LPH);
         const float iv = cur_inv[n];
-        const float w = exp2f(fmaf(iv * zr, kLog2e, -lse2));
+        const float w = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
         const float dz = w * (P - S_h);
         const float C = (H == 1) ? dz * zr : warp_sum(sub == 0 ? dz * zr : 0.f);
         const float coef = iv * iv * iv * C * inv_d;

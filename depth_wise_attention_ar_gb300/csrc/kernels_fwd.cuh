@@ -19,8 +19,10 @@
 //   quarter-warp hit different shared-memory banks.
 // - The accumulator (8*CPL floats) and q*g (8*CPL floats) live in registers;
 //   the staged row is read twice from shared memory (score, then mix).
-// - The softmax is online in log2 units; the running maximum only moves when
-//   a score exceeds it by kRescaleTau, so the accumulator is rarely rescaled.
+// - The softmax is online; the running maximum only moves when a score
+//   exceeds it by kRescaleTau, so the accumulator is rarely rescaled. Scores
+//   stay in natural units (exp2 only inside the exponent) so that the
+//   backward's recomputed score matches bit for bit.
 // - Grid: persistent, SM count x resident blocks; tokens strided over warps.
 #pragma once
 
@@ -73,14 +75,14 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     int cidx[CPL];
 #pragma unroll
     for (int j = 0; j < CPL; ++j) cidx[j] = h * (CPL * LPH) + sub + LPH * ((j + h) % CPL);
-    // query times norm weight, in log2 units, over this lane's coordinates
+    // query times norm weight over this lane's coordinates
     float qg[CPL][8];
 #pragma unroll
     for (int j = 0; j < CPL; ++j)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = cidx[j] * 8 + e;
-            qg[j][e] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) * kLog2e;
+            qg[j][e] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f);
         }
 
     // ---- work: tokens gw, gw + GW, ...
@@ -149,24 +151,26 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
             for (int e = 0; e < 8; ++e) zr = fmaf(qg[j][e], v[e], zr);
         }
         zr = group_sum(zr, LPH);
-        const float z2 = zr * cur_inv[n];  // score in log2 units
+        // score; __fmul_rn keeps the product uncontracted so that the backward
+        // recomputes the same bits
+        const float z = __fmul_rn(zr, cur_inv[n]);
 
         float p = 1.f;
         if (n == 0) {
-            m = z2;
+            m = z;
             l = 1.f;
         } else {
-            const bool need = z2 > m + kRescaleTau;
+            const bool need = z > m + kRescaleTau;
             if (__any_sync(FULL, need)) {
-                const float sc = need ? exp2f(m - z2) : 1.f;
-                m = need ? z2 : m;
+                const float sc = need ? exp2f((m - z) * kLog2e) : 1.f;
+                m = need ? z : m;
                 l *= sc;
 #pragma unroll
                 for (int j = 0; j < CPL; ++j)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) acc[j][e] *= sc;
             }
-            p = exp2f(z2 - m);
+            p = exp2f((z - m) * kLog2e);
             l += p;
         }
 #pragma unroll
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
                 for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
                 st_chunk_g(orow + cidx[j] * 8, o);
             }
-            if (sub == 0) a.lse[tok * H + h] = (m + log2f(l)) * kLn2;
+            if (sub == 0) a.lse[tok * H + h] = m + log2f(l) * kLn2;
         }
         if (++n == N) { n = 0; tok += GW; }
         if (++slot == S) slot = 0;

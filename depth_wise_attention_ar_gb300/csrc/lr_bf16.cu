@@ -1,0 +1,7 @@
+// Sliced-key (r < d) routing kernels instantiated for the bf16 storage dtype.
+#include "kernels_lr.cuh"
+
+namespace ar {
+template cudaError_t dispatch_lr_fwd<__nv_bfloat16>(const RouteArgs &a, cudaStream_t s);
+template cudaError_t dispatch_lr_bwd<__nv_bfloat16>(const RouteArgs *a, cudaStream_t s, int *grid_warps);
+}  // namespace ar

@@ -7,6 +7,8 @@ namespace ar {
 
 template <typename T> cudaError_t dispatch_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
+template <typename T> cudaError_t dispatch_lr_fwd(const RouteArgs &a, cudaStream_t s);
+template <typename T> cudaError_t dispatch_lr_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
 
 // Device error word; kernels get its address as an argument.
 __device__ unsigned int g_device_error = 0;
@@ -146,29 +148,41 @@ cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q,
     return cudaGetLastError();
 }
 
-// ---- dtype dispatch ------------------------------------------------------------
+// ---- dtype / key-width dispatch ------------------------------------------------
+// r = d: full-width keys (online-softmax forward, register-resident state);
+// r < d: sliced keys (two-sweep forward with a key cache, blocked backward).
 cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 {
+    if (a.r < a.d)
+        return dt == AR_BF16 ? dispatch_lr_fwd<__nv_bfloat16>(a, s) : dispatch_lr_fwd<float>(a, s);
     return dt == AR_BF16 ? dispatch_fwd<__nv_bfloat16>(a, s) : dispatch_fwd<float>(a, s);
 }
 
 cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 {
+    if (a.r < a.d)
+        return dt == AR_BF16 ? dispatch_lr_bwd<__nv_bfloat16>(&a, s, nullptr)
+                             : dispatch_lr_bwd<float>(&a, s, nullptr);
     return dt == AR_BF16 ? dispatch_bwd<__nv_bfloat16>(&a, s, nullptr)
                          : dispatch_bwd<float>(&a, s, nullptr);
 }
 
 cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps)
 {
+    if (a.r < a.d)
+        return dt == AR_BF16 ? dispatch_lr_bwd<__nv_bfloat16>(&a, nullptr, grid_warps)
+                             : dispatch_lr_bwd<float>(&a, nullptr, grid_warps);
     return dt == AR_BF16 ? dispatch_bwd<__nv_bfloat16>(&a, nullptr, grid_warps)
                          : dispatch_bwd<float>(&a, nullptr, grid_warps);
 }
 
 bool fused_shape_supported(int d, int r, int H)
 {
-    // full-width keys, d = 256 * CPL with CPL in 1..8, H a power of two <= 32
-    if (d <= 0 || r != d || d % 256 != 0 || d > 2048) return false;
-    return H >= 1 && H <= 32 && (32 % H) == 0;
+    if (H < 1 || H > 32 || (32 % H) != 0) return false;
+    if (d <= 0 || r <= 0 || r > d || d % 256 != 0 || r % 256 != 0) return false;
+    if (r == d) return d <= 2048;                  // full keys: d = 256 * (1..8)
+    const int kcpl = r / 256;                      // sliced keys: r = 256 * {1,2,4,8}
+    return d <= 4096 && (kcpl == 1 || kcpl == 2 || kcpl == 4 || kcpl == 8);
 }
 
 }  // namespace ar

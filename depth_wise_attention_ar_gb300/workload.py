@@ -39,6 +39,7 @@ class Config:
     NB: int | None = None       # blocks (None: full routing)
     sites: tuple | None = None  # restrict to these site indices (None: all)
     q_std: float = 0.02
+    norm: str = "key"           # RMS over the key coordinates, or "full" width
     note: str = ""
 
 
@@ -124,7 +125,8 @@ class Microbatch:
         self.plan = make_plan(cfg)
         needed = sorted({row for s in self.plan.run_sites for row in self.plan.sites[s]})
         self.n_rows = max(needed) + 1
-        self.bank = B.Bank(cfg.T, cfg.d, cfg.r, self.n_rows, cfg.dtype, eps=1e-6, device=dev)
+        self.bank = B.Bank(cfg.T, cfg.d, cfg.r, self.n_rows, cfg.dtype, norm=cfg.norm, eps=1e-6,
+                           device=dev)
         tdt = self.bank.torch_dtype
         # sublayer outputs: written in place into their bank rows, or kept in
         # separate buffers when the row is a block partial sum

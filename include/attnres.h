@@ -38,9 +38,11 @@
  * - Banks are not thread-safe; distinct banks may be used from distinct
  *   threads.
  *
- * Shapes the fused routing kernels cover: r = d, d a multiple of 256 up to
- * 2048, H in {1,2,4,8,16,32}, 1 <= n_src <= AR_MAX_SOURCES, row/output
- * pointers 16-byte aligned. Other shapes return AR_ERR_UNSUPPORTED (or
+ * Shapes the fused routing kernels cover: H in {1,2,4,8,16,32},
+ * 1 <= n_src <= AR_MAX_SOURCES, row/output pointers 16-byte aligned, and
+ * either full keys (r = d, d a multiple of 256 up to 2048) or sliced keys
+ * (r < d, d a multiple of 256 up to 4096, r in {256, 512, 1024, 2048}, with
+ * the forward's key cache 2*n_src*r*sizeof(dtype) bytes within 200 KB). Other shapes return AR_ERR_UNSUPPORTED (or
  * AR_ERR_ALIGN for a misaligned pointer). Appends accept any d, r that are
  * multiples of 8.
  */

@@ -109,9 +109,10 @@ def test_route_argument_checks_precede_launch(B):
     assert _err(B.ar_route_fwd, h, [0], 64, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
     assert _err(B.ar_route_fwd, h, [0], 4, None, None, FAKE, FAKE, 1, 0) == "AR_ERR_INVALID_ARG"
     B.ar_bank_destroy(h)
-    h = _bank(B, d=4096, r=1024)
-    assert _err(B.ar_route_fwd, h, [0], 8, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
-    B.ar_bank_destroy(h)
+    for d, r in ((4096, 4096), (1024, 768), (8192, 1024), (1000, 1000)):
+        h = _bank(B, d=d, r=r)
+        assert _err(B.ar_route_fwd, h, [0], 8, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
+        B.ar_bank_destroy(h)
 
 
 def test_failed_append_leaves_bank_unchanged_without_gpu(B):

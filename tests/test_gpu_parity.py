@@ -52,12 +52,14 @@ def oracle_chain(inputs, cfg, H, plan, orc):
     for s in plan.run_sites:
         src = [rows[j] for j in plan.sites[s]]
         res["out"][s], res["lse"][s] = orc.route_fwd(src, inputs.host_query(s, r),
-                                                     inputs.host_norm_weight(s, r), H, r=r)
+                                                     inputs.host_norm_weight(s, r), H, r=r,
+                                                     full_width=cfg.norm == "full")
     dsrc = {j: np.zeros((T, d)) for j in range(nrows)}
     for s in reversed(plan.run_sites):
         src = [rows[j] for j in plan.sites[s]]
         _, dq, dg = orc.route_bwd(src, inputs.host_query(s, r), inputs.host_norm_weight(s, r),
                                   inputs.host_dout(s, T, d, cfg.dtype), H, r=r,
+                                  full_width=cfg.norm == "full",
                                   dsrc=[dsrc[j] for j in plan.sites[s]])
         res["dq"][s], res["dg"][s] = dq, dg
     res["dsrc"] = dsrc
@@ -88,9 +90,9 @@ def run_and_compare(W, orc, cfg, H, q_std=0.02, g_kind="ones", seed=0, check_dg=
     return mb, ref, worst
 
 
-def small(wl, name, T, d, H, dtype, M, NB=None, sites=None, r=None):
+def small(wl, name, T, d, H, dtype, M, NB=None, sites=None, r=None, norm="key"):
     return wl.Config(name, T=T, d=d, H=H, r=d if r is None else r, dtype=dtype, M=M, NB=NB,
-                     sites=sites)
+                     sites=sites, norm=norm)
 
 
 def test_tiny_config_fp32(W, orc):
@@ -122,6 +124,24 @@ def test_widths_and_heads(W, orc, d, H):
 def test_widths_fp32(W, orc, d, H):
     _, wl = W
     cfg = small(wl, "wh32", T=150, d=d, H=H, dtype="f32", M=5)
+    run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("norm", ["key", "full"])
+def test_block_routing_chain_sliced_keys(W, orc, dtype, norm):
+    """Block routing (12 sublayers in 3 blocks: partial-sum appends) with sliced
+    keys r = d/4, both RMS choices of LR-AttnRes Eq. 13."""
+    _, wl = W
+    cfg = small(wl, "blk", T=300, d=1024, H=4, dtype=dtype, M=12, NB=3, r=256, norm=norm)
+    run_and_compare(W, orc, cfg, 4, q_std=0.5, g_kind="random")
+
+
+@pytest.mark.parametrize("d,r,H", [(512, 256, 8), (2048, 512, 4), (4096, 1024, 8),
+                                   (4096, 2048, 16), (1280, 256, 1), (768, 512, 32)])
+def test_sliced_key_shapes(W, orc, d, r, H):
+    _, wl = W
+    cfg = small(wl, "lr", T=129, d=d, H=H, dtype="bf16", M=5, NB=2, r=r)
     run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
 
 
@@ -284,6 +304,61 @@ def test_full_size_1b_sampled_tokens(W, orc):
         sl = slice(t0, min(T, t0 + 2048))
         src = [to64(mb.bank.rows[j][sl]) for j in mb.plan.sites[s]]
         _, a, b = orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][sl]), H)
+        dq += a
+        dg += b
+    assert nmax(to64(mb.dq[s]), dq) < tol
+    assert nmax(to64(mb.dg[s]), dg) < tol
+
+
+def test_full_size_lr_block_sampled_tokens(W, orc):
+    """The low-rank block workload at full size (T=8192, d=4096, r=1024, H=8,
+    65 sites over 9 completed + partial block sums) in the benchmark's launch
+    configuration: bank rows (bit-exact, oracle rounding of the partial sums),
+    outputs, lse and source gradients of 32 sampled tokens, dq/dg of the last
+    site over all tokens."""
+    import torch
+    from oracle import schedule, storage
+    _, wl = W
+    cfg = wl.CONFIGS["lr_block"]
+    inputs = synth.DeviceInputs(seed=12, q_std=0.3, g_kind="random")
+    mb = wl.Microbatch(cfg, cfg.H, inputs)
+    mb.step()
+    torch.cuda.synchronize()
+    T, d, r, H = cfg.T, cfg.d, cfg.r, cfg.H
+    rng = np.random.default_rng(1)
+    toks = np.sort(rng.choice(T, size=32, replace=False))
+    toks[0], toks[-1] = 0, T - 1
+    ti = torch.as_tensor(toks, device="cuda")
+    oplan = schedule.block_plan(cfg.M, cfg.NB)
+    outs = [to64((mb.outputs[j] if j in mb.outputs else mb.bank.rows[j])[ti])
+            for j in range(mb.n_rows)]
+    # rows stored as is are the producer's outputs; partial sums are recomputed
+    outs_raw = []
+    for j in range(mb.n_rows):
+        outs_raw.append(outs[j])
+    rows = storage.block_bank(outs_raw, oplan, "bf16")
+    for j in range(mb.n_rows):
+        assert np.array_equal(to64(mb.bank.rows[j][ti]), rows[j]), j
+    tol = TOL["bf16"]
+    dsrc = {j: np.zeros((len(toks), d)) for j in range(mb.n_rows)}
+    for s in mb.plan.run_sites:
+        src = [rows[j] for j in mb.plan.sites[s]]
+        o, l = orc.route_fwd(src, to64(mb.q[s]), to64(mb.g[s]), H, r=r)
+        assert nmax(to64(mb.out[s][ti]), o) < tol, s
+        assert nmax(to64(mb.lse[s][ti]), l) < tol, s
+    for s in reversed(mb.plan.run_sites):
+        src = [rows[j] for j in mb.plan.sites[s]]
+        orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][ti]), H, r=r,
+                      dsrc=[dsrc[j] for j in mb.plan.sites[s]])
+    for j in range(mb.n_rows):
+        assert nmax(to64(mb.bank.grad[j][ti]), dsrc[j]) < tol, j
+    s = mb.plan.run_sites[-1]
+    dq = np.zeros(r)
+    dg = np.zeros(r)
+    for t0 in range(0, T, 1024):
+        sl = slice(t0, min(T, t0 + 1024))
+        src = [to64(mb.bank.rows[j][sl]) for j in mb.plan.sites[s]]
+        _, a, b = orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][sl]), H, r=r)
         dq += a
         dg += b
     assert nmax(to64(mb.dq[s]), dq) < tol
