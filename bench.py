@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="1B")
     p.add_argument("--heads", type=int, default=None)
+    p.add_argument("--tokens", type=int, default=None, help="override T (profiling cases)")
+    p.add_argument("--sites", choices=["all", "last"], default="all",
+                   help="run every routing site, or only the last one (profiling cases)")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target wall time of the CPU-oracle sample")
@@ -175,6 +178,16 @@ def cpu_baseline(cfg, H, seconds: float, steps: int = 1):
                       f"float64 oracle, {dt:.1f} s per sample"}, dt, Ts
 
 
+def config_of(args, workload):
+    import dataclasses
+    cfg = workload.CONFIGS[args.config]
+    if args.tokens:
+        cfg = dataclasses.replace(cfg, T=args.tokens)
+    if args.sites == "last":
+        cfg = dataclasses.replace(cfg, sites=(cfg.M,))
+    return cfg
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -193,7 +206,7 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    cfg = workload.CONFIGS[args.config]
+    cfg = config_of(args, workload)
     H = args.heads or cfg.H
     inputs = synth.DeviceInputs(seed=1000 + rank, device=f"cuda:{local}")
     mb = workload.Microbatch(cfg, H, inputs, device=f"cuda:{local}")
@@ -374,8 +387,8 @@ def reference_arm(args, rank, world):
     if rank != 0:
         return
     sys.path.insert(0, ROOT)
-    from depth_wise_attention_ar_gb300.workload import CONFIGS  # schedule-free config table
-    cfg = CONFIGS[args.config]
+    from depth_wise_attention_ar_gb300 import workload
+    cfg = config_of(args, workload)
     H = args.heads or cfg.H
     for _ in range(args.warmup):
         pass
