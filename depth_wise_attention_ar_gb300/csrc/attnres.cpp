@@ -246,7 +246,7 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
                        const float *lse, float *dq, float *dg, void *ws, size_t ws_bytes,
                        int32_t site_id, void *stream)
 {
-    if (bank && !bank->grad) return AR_ERR_INVALID_ARG;
+    if (bank && !bank->grad && bank->T > 0) return AR_ERR_INVALID_ARG;
     ar_status st = check_site(bank, rows, n_src, H, q, g);
     if (st != AR_OK) return st;
     if (!dq || (bank->T > 0 && (!out || !dout || !lse || !ws))) return AR_ERR_INVALID_ARG;

@@ -79,9 +79,12 @@ def model_bytes(cfg: Config, plan: Plan, H: int | None = None) -> dict:
     """Algorithmic bytes of one microbatch (what the method must move).
 
     forward site : T (N b d + 4 N + b d + 4 H)   (rows, inverse RMS, out, lse)
-    backward site: T (b d + b d + 4 H + 4 N + N b d + N d (8, or 4 on a row's
-                   first touch))                 (dout, out, lse, inverse RMS,
-                                                   rows once, gradient rows)
+    backward site: T (b d + 4 H + 4 N + N b d + N d (8, or 4 on a row's first
+                   touch))                       (dout, lse, inverse RMS, rows
+                                                  once, gradient rows)
+    The backward kernel also reads the forward output once per token (its
+    softmax coupling term); that T b d is not part of the method's bytes and
+    is not counted.
     append       : T (b r + 4) for a row written in place by its producer
                    (key read for the inverse RMS), T (3 b d + 4) for a partial
                    sum (two reads, one write).
@@ -102,7 +105,7 @@ def model_bytes(cfg: Config, plan: Plan, H: int | None = None) -> dict:
         N = len(rows)
         g = sum(4 * d if row in touched else 0 for row in rows) + 4 * d * N
         touched.update(rows)
-        bwd += T * (2 * b * d + 4 * H + 4 * N + N * b * d) + T * g
+        bwd += T * (b * d + 4 * H + 4 * N + N * b * d) + T * g
     return {"fwd": fwd, "bwd": bwd, "append": app, "total": fwd + bwd + app}
 
 
