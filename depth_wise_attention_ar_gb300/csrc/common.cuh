@@ -178,6 +178,76 @@ __device__ __forceinline__ void st_chunk_g(float *p, const float v[8])
     reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// Dot product of two 8-element chunks as (low half) + (high half), each half
+// a fixed chain. Exchanging the halves (lane-swapped order below) gives the
+// same bits, because the final addition commutes exactly.
+__device__ __forceinline__ float dot8(const float a[8], const float b[8])
+{
+    float lo = __fmul_rn(a[0], b[0]);
+    lo = fmaf(a[1], b[1], lo);
+    lo = fmaf(a[2], b[2], lo);
+    lo = fmaf(a[3], b[3], lo);
+    float hi = __fmul_rn(a[4], b[4]);
+    hi = fmaf(a[5], b[5], hi);
+    hi = fmaf(a[6], b[6], hi);
+    hi = fmaf(a[7], b[7], hi);
+    return __fadd_rn(lo, hi);
+}
+
+// ---- chunks in lane-swapped element order -----------------------------------
+// A warp reading 32-byte fp32 chunks, one per lane, with 16-byte loads hits
+// every shared-memory bank twice per quarter-warp if all lanes read the same
+// half first. Lanes with sw = 4 therefore read the upper half first and keep
+// their chunk's elements in swapped order: register element e holds memory
+// element e ^ sw. Every per-element operand of such a lane (source values,
+// dL/dout, q*g, partial sums) is kept in the same order, so the arithmetic is
+// unchanged and only loads and stores see the swap.
+
+__device__ __forceinline__ uint4 swap_halves(uint4 u, int sw)
+{
+    return sw ? make_uint4(u.z, u.w, u.x, u.y) : u;
+}
+
+__device__ __forceinline__ void ld_chunk_s_sw(const __nv_bfloat16 *p, int sw, float v[8])
+{
+    unpack_bf16x8(swap_halves(lds128(p), sw), v);
+}
+__device__ __forceinline__ void ld_chunk_s_sw(const float *p, int sw, float v[8])
+{
+    const uint4 a = lds128(p + sw);
+    const uint4 b = lds128(p + (sw ^ 4));
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+    v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+    v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+}
+__device__ __forceinline__ void ld_chunk_g_sw(const __nv_bfloat16 *p, int sw, float v[8])
+{
+    unpack_bf16x8(swap_halves(__ldg(reinterpret_cast<const uint4 *>(p)), sw), v);
+}
+__device__ __forceinline__ void ld_chunk_g_sw(const float *p, int sw, float v[8])
+{
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p + sw));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p + (sw ^ 4)));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void st_f32x8_g_sw(float *p, int sw, const float v[8])
+{
+    *reinterpret_cast<float4 *>(p + sw) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4 *>(p + (sw ^ 4)) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Chunk order of a lane inside its head: rotating by the head index keeps the
+// head groups that share a quarter-warp on different banks when d/256 (CPL)
+// is even; for odd CPL the plain order already does.
+template <int CPL>
+__device__ __forceinline__ int chunk_of(int h, int sub, int LPH, int j)
+{
+    constexpr int rot = (CPL & 1) ? 0 : 1;
+    return h * (CPL * LPH) + sub + LPH * ((j + rot * h) % CPL);
+}
+
 // fp32 chunk (gradient rows) in shared / global memory.
 __device__ __forceinline__ void ld_f32x8_s(const float *p, float v[8]) { ld_chunk_s(p, v); }
 __device__ __forceinline__ void st_f32x8_s(float *p, const float v[8])

@@ -27,9 +27,11 @@
 // shared-memory stages, as in the forward; a stage holds the source row
 // (storage dtype) and, unless this is the row's first touch, its fp32
 // gradient row, both brought in by 1-D bulk copies on one mbarrier. The new
-// gradient row goes back with 16-byte stores. G and U stay in registers,
-// q*g sits in a block-wide shared table, and the staged source row is read
-// twice from shared memory (dots, then gradient).
+// gradient row goes back with 16-byte stores. G, q*g, U and the staged row's
+// values stay in registers (8*CPL floats each). Lanes whose bit 2 is set keep
+// each chunk's two halves swapped, so that their 16-byte reads of the fp32
+// gradient row fall on the other half of the banks; dot products are summed
+// as (low half) + (high half), which gives the forward's bits either way.
 #pragma once
 
 #include "common.cuh"
@@ -43,8 +45,7 @@ constexpr int kBwdStages = 3;
 inline size_t bwd_smem_bytes(int d, size_t esize)
 {
     return (size_t)kBwdWarps * kBwdStages * ((size_t)d * esize + (size_t)d * 4) +
-           (size_t)kBwdWarps * kBwdStages * 8 + (size_t)kBwdWarps * AR_MAX_SOURCES * 4 +
-           (size_t)d * 4;
+           (size_t)kBwdWarps * kBwdStages * 8 + (size_t)kBwdWarps * AR_MAX_SOURCES * 4;
 }
 
 template <typename T, int CPL>
@@ -68,12 +69,9 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
     unsigned char *rings = smem;
     uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + (size_t)kBwdWarps * S * slot_bytes);
     float *inv_all = reinterpret_cast<float *>(bars_all + kBwdWarps * S);
-    float *s_qg = inv_all + kBwdWarps * AR_MAX_SOURCES;  // [d], q * g
 
     for (int i = threadIdx.x; i < N; i += blockDim.x) s_rows[i] = a.rows[i];
     for (int i = threadIdx.x; i < AR_MAX_SOURCES / 32; i += blockDim.x) s_first[i] = a.first_mask[i];
-    for (int c = threadIdx.x; c < d; c += blockDim.x)
-        s_qg[c] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f);
     unsigned char *ring = rings + (size_t)warp * S * slot_bytes;
     uint64_t *bars = bars_all + warp * S;
     float *cur_inv = inv_all + warp * AR_MAX_SOURCES;
@@ -84,12 +82,22 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
     }
     __syncthreads();
 
-    // ---- lane -> head and chunk mapping (same as the forward)
+    // ---- lane -> head and chunk mapping (same chunks as the forward); lanes
+    // with sw = 4 keep their chunks' halves swapped (conflict-free fp32 reads)
     const int LPH = 32 / H;
     const int h = lane / LPH, sub = lane - h * LPH;
+    const int sw = ((lane >> 2) & 1) * 4;
     int cidx[CPL];
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) cidx[j] = h * (CPL * LPH) + sub + LPH * ((j + h) % CPL);
+    for (int j = 0; j < CPL; ++j) cidx[j] = chunk_of<CPL>(h, sub, LPH, j);
+    float qg[CPL][8];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = cidx[j] * 8 + (e ^ sw);
+            qg[j][e] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f);
+        }
     const float inv_d = 1.0f / (float)d;
 
     // ---- this warp's contiguous range of (token, source) items
@@ -139,10 +147,9 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float o[8];
-                ld_chunk_g(grow + cidx[j] * 8, G[j]);
-                ld_chunk_g(orow + cidx[j] * 8, o);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) sp = fmaf(G[j][e], o[e], sp);
+                ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
+                ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
+                sp = __fadd_rn(sp, dot8(G[j], o));
             }
             S_h = group_sum(sp, LPH);
             lse_h = __ldg(a.lse + tok * H + h);
@@ -158,18 +165,14 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         const float *gb = reinterpret_cast<const float *>(vb + vbytes);
         const bool first = (s_first[n >> 5] >> (n & 31)) & 1u;
 
-        // pass 1: value dot with G and raw score
+        // pass 1: value dot with G and raw score (the forward's sum order)
+        float v[CPL][8];
         float P = 0.f, zr = 0.f;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            float v[8], qgc[8];
-            ld_chunk_s(reinterpret_cast<const T *>(vb + cidx[j] * CB), v);
-            ld_chunk_s(s_qg + cidx[j] * 8, qgc);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                P = fmaf(G[j][e], v[e], P);
-                zr = fmaf(qgc[e], v[e], zr);
-            }
+            ld_chunk_s_sw(reinterpret_cast<const T *>(vb + cidx[j] * CB), sw, v[j]);
+            P = __fadd_rn(P, dot8(G[j], v[j]));
+            zr = __fadd_rn(zr, dot8(qg[j], v[j]));
         }
         P = group_sum(P, LPH);
         zr = group_sum(zr, LPH);
@@ -184,23 +187,21 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         // pass 2: gradient row
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            float v[8], qgc[8], nv[8];
-            ld_chunk_s(reinterpret_cast<const T *>(vb + cidx[j] * CB), v);
-            ld_chunk_s(s_qg + cidx[j] * 8, qgc);
+            float nv[8];
             if (first) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) nv[e] = 0.f;
             } else {
-                ld_chunk_s(gb + cidx[j] * 8, nv);
+                ld_chunk_s_sw(gb + cidx[j] * 8, sw, nv);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 nv[e] = fmaf(w, G[j][e], nv[e]);
-                nv[e] = fmaf(ak, qgc[e], nv[e]);
-                nv[e] = fmaf(-coef, v[e], nv[e]);
-                U[j][e] = fmaf(ak, v[e], U[j][e]);
+                nv[e] = fmaf(ak, qg[j][e], nv[e]);
+                nv[e] = fmaf(-coef, v[j][e], nv[e]);
+                U[j][e] = fmaf(ak, v[j][e], U[j][e]);
             }
-            st_f32x8_g(grad_row + cidx[j] * 8, nv);
+            st_f32x8_g_sw(grad_row + cidx[j] * 8, sw, nv);
         }
         __syncwarp();
         if (issued < hi) issue_next();
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
     // per-warp partial sums U -> workspace row gw
     float *wrow = a.ws + gw * d;
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) st_f32x8_g(wrow + cidx[j] * 8, U[j]);
+    for (int j = 0; j < CPL; ++j) st_f32x8_g_sw(wrow + cidx[j] * 8, sw, U[j]);
 }
 
 template <typename T, int CPL>

@@ -17,8 +17,8 @@
 //   and the lane's head weight needs no broadcast. Chunk order is rotated by
 //   the head index so that the lanes of the two heads that share a
 //   quarter-warp hit different shared-memory banks.
-// - The accumulator (8*CPL floats) and q*g (8*CPL floats) live in registers;
-//   the staged row is read twice from shared memory (score, then mix).
+// - The accumulator, q*g and the staged row's values (8*CPL floats each)
+//   live in registers; a staged row is read from shared memory once.
 // - The softmax is online; the running maximum only moves when a score
 //   exceeds it by kRescaleTau, so the accumulator is rarely rescaled. Scores
 //   stay in natural units (exp2 only inside the exponent) so that the
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     const int h = lane / LPH, sub = lane - h * LPH;
     int cidx[CPL];
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) cidx[j] = h * (CPL * LPH) + sub + LPH * ((j + h) % CPL);
+    for (int j = 0; j < CPL; ++j) cidx[j] = chunk_of<CPL>(h, sub, LPH, j);
     // query times norm weight over this lane's coordinates
     float qg[CPL][8];
 #pragma unroll
@@ -142,44 +142,41 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
         const unsigned char *buf = ring + (size_t)slot * row_bytes;
 
         // score of this lane's head: q_h . (g * s_n)_[h], times inv_n
+        float v[CPL][8];
         float zr = 0.f;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            float v[8];
-            ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) zr = fmaf(qg[j][e], v[e], zr);
+            ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
+            zr = __fadd_rn(zr, dot8(qg[j], v[j]));
         }
         zr = group_sum(zr, LPH);
-        // score; __fmul_rn keeps the product uncontracted so that the backward
-        // recomputes the same bits
+        // __fmul_rn keeps the product uncontracted: the backward recomputes
+        // the same bits
         const float z = __fmul_rn(zr, cur_inv[n]);
-
-        float p = 1.f;
-        if (n == 0) {
+        if (n == 0) {  // first source of the token: weight exp(0) = 1 below
             m = z;
-            l = 1.f;
-        } else {
-            const bool need = z > m + kRescaleTau;
-            if (__any_sync(FULL, need)) {
-                const float sc = need ? exp2f((m - z) * kLog2e) : 1.f;
-                m = need ? z : m;
-                l *= sc;
+            l = 0.f;
 #pragma unroll
-                for (int j = 0; j < CPL; ++j)
+            for (int j = 0; j < CPL; ++j)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[j][e] *= sc;
-            }
-            p = exp2f((z - m) * kLog2e);
-            l += p;
+                for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
         }
+        const bool need = z > m + kRescaleTau;
+        if (__any_sync(FULL, need)) {
+            const float sc = need ? exp2f((m - z) * kLog2e) : 1.f;
+            m = need ? z : m;
+            l *= sc;
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            float v[8];
-            ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v);
+            for (int j = 0; j < CPL; ++j)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[j][e] = (n == 0) ? v[e] : fmaf(p, v[e], acc[j][e]);
+                for (int e = 0; e < 8; ++e) acc[j][e] *= sc;
         }
+        const float p = exp2f((z - m) * kLog2e);
+        l += p;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, v[j][e], acc[j][e]);
         __syncwarp();
         if (issued < total) issue_next();  // refill the stage just consumed
 
