@@ -45,6 +45,8 @@ SIGNATURES = {
     "ar_route_bwd_workspace": ([_P, _I32, _SZP], ctypes.c_int),
     "ar_route_bwd": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I32, _P],
                      ctypes.c_int),
+    "ar_route_bwd_noalloc": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
+                             ctypes.c_int),
     "ar_block_schedule": ([_I32, _I32, _I32P, _I32P, _I32P, _I64, _I64P], ctypes.c_int),
     "ar_device_error": ([_U32P], ctypes.c_int),
 }
@@ -161,6 +163,17 @@ def ar_route_bwd(bank, rows, H, q, g, out, dout, lse, dq, dg, ws, ws_bytes, site
     _check("ar_route_bwd", _lib.ar_route_bwd(bank, arr, n, H, _ptr(q), _ptr(g), _ptr(out),
                                              _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dg), _ptr(ws),
                                              ws_bytes, site_id, _stream(stream)))
+
+
+def ar_route_bwd_noalloc(bank, rows, H, q, g, out, dout, lse, dq, dg, site_id, stream=None):
+    arr, n = _rows(rows)
+    _check("ar_route_bwd_noalloc", _lib.ar_route_bwd_noalloc(bank, arr, n, H, _ptr(q), _ptr(g),
+                                                             _ptr(out), _ptr(dout), _ptr(lse),
+                                                             _ptr(dq), _ptr(dg), site_id,
+                                                             _stream(stream)))
+
+
+AR_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def ar_block_schedule(M: int, NB: int | None):

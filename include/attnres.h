@@ -223,6 +223,33 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
 ar_status ar_block_schedule(int32_t M, int32_t NB, int32_t *acc_from, int32_t *site_ptr,
                             int32_t *site_rows, int64_t site_rows_cap, int64_t *site_rows_len);
 
+/*
+ * ar_route_bwd_noalloc: ar_route_bwd with no caller workspace. There is no
+ * counterpart in the papers; this entry point exists for callers that cannot
+ * allocate device memory (for example an engine plugin whose execute hook may
+ * not call cudaMalloc, or code embedded in a process whose device memory
+ * belongs to another framework's pool).
+ *   Arguments, results and checks are those of ar_route_bwd, minus ws and
+ *   ws_bytes: the backward's scratch (its per-warp dq/dg partial sums) lives
+ *   in a fixed device array inside this library, AR_NOALLOC_SCRATCH_BYTES
+ *   large, which every GPU that loads the library holds until the process
+ *   exits. The call allocates nothing.
+ *   - If ar_route_bwd_workspace() for this bank and H exceeds
+ *     AR_NOALLOC_SCRATCH_BYTES, the call returns AR_ERR_CAPACITY and runs
+ *     nothing; use ar_route_bwd with a workspace instead.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero). Calls whose kernels can overlap
+ *     on the GPU (unordered streams) race on it: serialise them.
+ */
+#define AR_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+ar_status ar_route_bwd_noalloc(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                               const float *q, const float *g, const void *out, const void *dout,
+                               const float *lse, float *dq, float *dg, int32_t site_id,
+                               void *stream);
+
 /* Read and clear the device error word of the current device (bit mask of
  * AR_DEVERR_*; 0 = none). This call synchronises the device. */
 ar_status ar_device_error(uint32_t *bits);
