@@ -178,6 +178,18 @@ def cpu_baseline(cfg, H, seconds: float, steps: int = 1):
                       f"float64 oracle, {dt:.1f} s per sample"}, dt, Ts
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the
+    step time); identity on a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def config_of(args, workload):
     import dataclasses
     cfg = workload.CONFIGS[args.config]
@@ -264,9 +276,8 @@ def main():
     fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
     bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
     if world > 1:
-        t = torch.tensor([total_ms, fwd_ms, bwd_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, fwd_ms, bwd_ms = t.tolist()
+        total_ms, fwd_ms, bwd_ms = max_over_ranks([total_ms, fwd_ms, bwd_ms],
+                                                  device=f"cuda:{local}")
     ms = total_ms / K
     if binding.ar_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
@@ -375,9 +386,7 @@ def end_to_end(args, mb, stream, run_fwd, run_bwd, world, local):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / K
     if world > 1:
-        t = torch.tensor([ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+        (ms,) = max_over_ranks([ms], device=f"cuda:{local}")
     return {"value": world * mb.cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
