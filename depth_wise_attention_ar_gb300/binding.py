@@ -47,6 +47,7 @@ SIGNATURES = {
                      ctypes.c_int),
     "ar_route_bwd_noalloc": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
                              ctypes.c_int),
+    "ar_bank_grad_fold": ([_P, _I32, _I32, _P], ctypes.c_int),
     "ar_block_schedule": ([_I32, _I32, _I32P, _I32P, _I32P, _I64, _I64P], ctypes.c_int),
     "ar_device_error": ([_U32P], ctypes.c_int),
 }
@@ -174,6 +175,10 @@ def ar_route_bwd_noalloc(bank, rows, H, q, g, out, dout, lse, dq, dg, site_id, s
 
 
 AR_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def ar_bank_grad_fold(bank, dst_row: int, src_row: int, stream=None):
+    _check("ar_bank_grad_fold", _lib.ar_bank_grad_fold(bank, dst_row, src_row, _stream(stream)))
 
 
 def ar_block_schedule(M: int, NB: int | None):

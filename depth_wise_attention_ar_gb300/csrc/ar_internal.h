@@ -38,7 +38,23 @@ cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q,
 cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col,
                           int64_t T, int d, int r, int inv_ld, int norm_full, float eps,
                           ar_dtype dt, cudaStream_t s);
+cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
+                             bool dst_valid, cudaStream_t s);
 unsigned int *device_error_word();
 bool fused_shape_supported(int d, int r, int H);
+
+// Shapes of the four-warp kernels: d = 1024 * CPL (CPL in 1..8), H a multiple
+// of 4 with H/4 heads per warp a power of two <= 32; r = d, or r = k * d/4
+// (k in 1..3) with H/k a power of two <= 32.
+inline bool coop_supported(int d, int r, int H)
+{
+    if (d <= 0 || d % 1024 != 0 || d / 1024 > 8) return false;
+    if (H < 4 || H % 4 != 0 || H / 4 > 32 || (32 % (H / 4)) != 0) return false;
+    if (r == d) return true;
+    const int CG = d / 4;
+    if (r <= 0 || r % CG != 0 || r > d) return false;
+    const int kw = r / CG;
+    return H % kw == 0 && H / kw <= 32 && (32 % (H / kw)) == 0;
+}
 
 }  // namespace ar

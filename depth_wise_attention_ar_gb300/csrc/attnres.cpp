@@ -283,6 +283,23 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
     return AR_OK;
 }
 
+ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, void *stream)
+{
+    if (!bank || dst_row < 0 || src_row < 0 || dst_row >= bank->count ||
+        src_row >= bank->count || dst_row == src_row)
+        return AR_ERR_INVALID_ARG;
+    if (!bank->grad) return bank->T == 0 ? AR_OK : AR_ERR_INVALID_ARG;
+    const int64_t n = bank->T * (int64_t)bank->d;
+    float *dst = bank->grad + (int64_t)dst_row * n;
+    const float *src = bank->grad + (int64_t)src_row * n;
+    const cudaError_t e = ar::launch_grad_fold(dst, src, n, bank->touched[src_row] != 0,
+                                               bank->touched[dst_row] != 0,
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    bank->touched[dst_row] = 1;
+    return AR_OK;
+}
+
 ar_status ar_block_schedule(int32_t M, int32_t NB, int32_t *acc_from, int32_t *site_ptr,
                             int32_t *site_rows, int64_t site_rows_cap, int64_t *site_rows_len)
 {

@@ -1,0 +1,526 @@
+// Routing kernels for wide rows: four warps of a block share every item.
+//
+// Same mathematics as the full-key kernels ("Multi-Head Attention Residuals",
+// Eq. 3 and Appendix E; "Low-Rank Attention Residuals", Eq. 8-13 and 15-22),
+// for rows too wide for one warp's registers (d > 2048) and for sliced keys
+// on wide rows. The row is split into four column groups of CG = d/4 columns;
+// warp w owns group w and whole value heads (H/4 of them). One staged row
+// (source row, plus its fp32 gradient row in the backward) is shared by the
+// block; thread 0 refills a stage once all four warps are past it.
+//
+// Key handling
+// - r = d (full keys): a warp's key heads are its value heads, so the
+//   forward needs no exchange; the backward sums the RMS coupling term
+//   sum_h dz*zr over the four warps through shared memory.
+// - r < d (sliced keys, r a multiple of CG): the key tail is owned by the last
+//   r/CG warps. They compute every head's raw score and publish it; the
+//   backward also publishes dz per head, and the key-path terms on the tail
+//   are staged in the shared gradient row before the owning lanes write it.
+// Score bits match between the passes (same lanes, same order, dot8 sums).
+#pragma once
+
+#include "common.cuh"
+#include "launch_util.cuh"
+
+namespace ar {
+
+constexpr int kCoopWarps = 4;
+constexpr int kCoopFwdStages = 4;
+constexpr int kCoopBwdStages = 3;
+
+struct CoopMap {
+    int Hw, LPH, hl, sub, h;      // value heads per warp, lanes per head, local head, lane in head, head
+    int kw, Hk, LPHk, hk, ksub;   // key warps, key heads per key warp, lanes per key head, key head
+    bool key_warp;
+};
+
+__device__ __forceinline__ CoopMap coop_map(int w, int lane, int H, int d, int r)
+{
+    CoopMap m;
+    m.Hw = H / kCoopWarps;
+    m.LPH = 32 / m.Hw;
+    m.hl = lane / m.LPH;
+    m.sub = lane - m.hl * m.LPH;
+    m.h = w * m.Hw + m.hl;
+    const int CG = d / kCoopWarps;
+    m.kw = r / CG;
+    m.Hk = H / m.kw;
+    m.LPHk = 32 / m.Hk;
+    const int kwi = w - (kCoopWarps - m.kw);
+    m.key_warp = kwi >= 0;
+    m.hk = m.key_warp ? kwi * m.Hk + lane / m.LPHk : 0;
+    m.ksub = lane % m.LPHk;
+    return m;
+}
+
+inline size_t coop_fwd_smem_bytes(int d, size_t esize)
+{
+    return (size_t)kCoopFwdStages * d * esize + kCoopFwdStages * 8 + 2 * 32 * 4 +
+           AR_MAX_SOURCES * 4;
+}
+
+template <typename T, int CPL, bool LR>
+__global__ void __launch_bounds__(kCoopWarps * 32)
+    route_fwd_coop_kernel(const __grid_constant__ RouteArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_rows[AR_MAX_SOURCES];
+    constexpr int S = kCoopFwdStages;
+    constexpr int CB = ChunkBytes<T>::value;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = a.d, r = a.r, N = a.n_src, H = a.H;
+    const int64_t TT = a.T;
+    const uint32_t row_bytes = (uint32_t)d * (uint32_t)sizeof(T);
+
+    for (int i = threadIdx.x; i < N; i += blockDim.x) s_rows[i] = a.rows[i];
+    unsigned char *ring = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)S * row_bytes);
+    float *zs = reinterpret_cast<float *>(bars + S);   // [2][32] scores per head
+    float *cur_inv = zs + 64;                           // [AR_MAX_SOURCES]
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const CoopMap mp = coop_map(w, lane, H, d, r);
+    const int gchunk = w * CPL * 32;                    // first chunk of this warp's group
+    int cidx[CPL], kidx[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        cidx[j] = gchunk + chunk_of<CPL>(mp.hl, mp.sub, mp.LPH, j);
+        kidx[j] = gchunk + chunk_of<CPL>(mp.hk % mp.Hk, mp.ksub, mp.LPHk, j);
+    }
+    const int key0 = (d - r) / 8;
+    float qg[CPL][8];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = (LR ? kidx[j] : cidx[j]) * 8 + e - key0 * 8;
+            const bool have = !LR || mp.key_warp;
+            qg[j][e] = have ? __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) : 0.f;
+        }
+
+    const int64_t GB = gridDim.x, gb = blockIdx.x;
+    const int64_t ntok = gb < TT ? (TT - 1 - gb) / GB + 1 : 0;
+    const int64_t total = ntok * N;
+    const uint64_t pol = l2_policy_evict_first();
+
+    int64_t issued = 0, tok_p = gb;
+    int n_p = 0, slot_p = 0;
+    auto issue_next = [&]() {
+        if (threadIdx.x == 0) {
+            const unsigned char *src = static_cast<const unsigned char *>(a.bank) +
+                                       ((int64_t)s_rows[n_p] * TT + tok_p) * row_bytes;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[slot_p], row_bytes);
+            bulk_g2s(ring + (size_t)slot_p * row_bytes, src, row_bytes, &bars[slot_p], pol);
+        }
+        ++issued;
+        if (++n_p == N) { n_p = 0; tok_p += GB; }
+        if (++slot_p == S) slot_p = 0;
+    };
+    for (int s = 0; s < S && issued < total; ++s) issue_next();
+
+    int n = 0, slot = 0, par = 0;
+    uint32_t phase = 0;
+    int64_t tok = gb, i = 0;
+    float m = 0.f, l = 0.f;
+    float acc[CPL][8];
+    bool ok = true;
+    for (; i < total; ++i) {
+        if (n == 0) {
+            for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
+                cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+            __syncthreads();
+        }
+        const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
+        if (__syncthreads_or(!got)) { ok = false; break; }
+        phase ^= 1u << slot;
+        const unsigned char *buf = ring + (size_t)slot * row_bytes;
+        const float iv = cur_inv[n];
+
+        float v[CPL][8];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
+        float z;
+        if constexpr (!LR) {
+            float zr = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) zr = __fadd_rn(zr, dot8(qg[j], v[j]));
+            zr = group_sum(zr, mp.LPH);
+            z = __fmul_rn(zr, iv);
+        } else {
+            if (mp.key_warp) {
+                float zr = 0.f;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    float kv[8];
+                    ld_chunk_s(reinterpret_cast<const T *>(buf + kidx[j] * CB), kv);
+                    zr = __fadd_rn(zr, dot8(qg[j], kv));
+                }
+                zr = group_sum(zr, mp.LPHk);
+                if (mp.ksub == 0) zs[par * 32 + mp.hk] = __fmul_rn(zr, iv);
+            }
+            __syncthreads();
+            z = zs[par * 32 + mp.h];
+        }
+        if (n == 0) {
+            m = z;
+            l = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+        }
+        const bool need = z > m + kRescaleTau;
+        if (__any_sync(0xffffffffu, need)) {
+            const float sc = need ? exp2f((m - z) * kLog2e) : 1.f;
+            m = need ? z : m;
+            l *= sc;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[j][e] *= sc;
+        }
+        const float p = exp2f((z - m) * kLog2e);
+        l += p;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, v[j][e], acc[j][e]);
+        __syncthreads();  // every warp is past this stage
+        if (issued < total) issue_next();
+
+        if (n == N - 1) {
+            const float rl = 1.f / l;
+            T *orow = static_cast<T *>(a.out) + tok * d;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
+                st_chunk_g(orow + cidx[j] * 8, o);
+            }
+            if (mp.sub == 0) a.lse[tok * H + mp.h] = m + log2f(l) * kLn2;
+        }
+        par ^= 1;
+        if (++n == N) { n = 0; tok += GB; }
+        if (++slot == S) slot = 0;
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) {
+            report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
+            for (int64_t j = i; j < issued; ++j) {
+                mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+                phase ^= 1u << slot;
+                if (++slot == S) slot = 0;
+            }
+        }
+    }
+}
+
+inline size_t coop_bwd_smem_bytes(int d, size_t esize)
+{
+    return (size_t)kCoopBwdStages * ((size_t)d * esize + (size_t)d * 4) + kCoopBwdStages * 8 +
+           3 * 2 * 32 * 4 + AR_MAX_SOURCES * 4;
+}
+
+template <typename T, int CPL, bool LR>
+__global__ void __launch_bounds__(kCoopWarps * 32)
+    route_bwd_coop_kernel(const __grid_constant__ RouteArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_rows[AR_MAX_SOURCES];
+    __shared__ uint32_t s_first[AR_MAX_SOURCES / 32];
+    constexpr int S = kCoopBwdStages;
+    constexpr int CB = ChunkBytes<T>::value;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = a.d, r = a.r, N = a.n_src, H = a.H;
+    const int64_t TT = a.T;
+    const uint32_t vbytes = (uint32_t)d * (uint32_t)sizeof(T), gbytes = (uint32_t)d * 4u;
+    const uint32_t slot_bytes = vbytes + gbytes;
+
+    for (int i = threadIdx.x; i < N; i += blockDim.x) s_rows[i] = a.rows[i];
+    for (int i = threadIdx.x; i < AR_MAX_SOURCES / 32; i += blockDim.x) s_first[i] = a.first_mask[i];
+    unsigned char *ring = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)S * slot_bytes);
+    float *zsm = reinterpret_cast<float *>(bars + S);  // [2][32] raw scores (sliced keys)
+    float *dzs = zsm + 64;                              // [2][32] dz per head (sliced keys)
+    float *cws = dzs + 64;                              // [2][32] per-warp coupling sums
+    float *cur_inv = cws + 64;                          // [AR_MAX_SOURCES]
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const CoopMap mp = coop_map(w, lane, H, d, r);
+    const int sw = ((lane >> 2) & 1) * 4;
+    const int gchunk = w * CPL * 32;
+    int cidx[CPL], kidx[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        cidx[j] = gchunk + chunk_of<CPL>(mp.hl, mp.sub, mp.LPH, j);
+        kidx[j] = gchunk + chunk_of<CPL>(mp.hk % mp.Hk, mp.ksub, mp.LPHk, j);
+    }
+    const int key0 = (d - r) / 8;
+    float qg[CPL][8], U[CPL][8];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = (LR ? kidx[j] : cidx[j]) * 8 + (e ^ sw) - key0 * 8;
+            const bool have = !LR || mp.key_warp;
+            qg[j][e] = have ? __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) : 0.f;
+            U[j][e] = 0.f;
+        }
+    const float inv_width = 1.0f / (float)(a.norm_full ? d : r);
+
+    const int64_t GB = gridDim.x, gb = blockIdx.x;
+    const int64_t total = TT * N;
+    const int64_t lo = total * gb / GB, hi = total * (gb + 1) / GB;
+    const uint64_t pol = l2_policy_evict_first();
+
+    int64_t issued = lo, tok_p = lo / N;
+    int n_p = (int)(lo - tok_p * N), slot_p = 0;
+    auto issue_next = [&]() {
+        if (threadIdx.x == 0) {
+            const bool first = (s_first[n_p >> 5] >> (n_p & 31)) & 1u;
+            const int64_t off = (int64_t)s_rows[n_p] * TT + tok_p;
+            unsigned char *dst = ring + (size_t)slot_p * slot_bytes;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[slot_p], vbytes + (first ? 0u : gbytes));
+            bulk_g2s(dst, static_cast<const unsigned char *>(a.bank) + off * vbytes, vbytes,
+                     &bars[slot_p], pol);
+            if (!first) bulk_g2s(dst + vbytes, a.grad + off * d, gbytes, &bars[slot_p], pol);
+        }
+        ++issued;
+        if (++n_p == N) { n_p = 0; ++tok_p; }
+        if (++slot_p == S) slot_p = 0;
+    };
+    for (int s = 0; s < S && issued < hi; ++s) issue_next();
+
+    float G[CPL][8];
+    float S_h = 0.f, lse_h = 0.f;
+    int64_t tok = lo / N, i = lo;
+    int n = (int)(lo - tok * N), slot = 0, par = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (; i < hi; ++i) {
+        if (i == lo || n == 0) {
+            const T *grow = static_cast<const T *>(a.dout) + tok * d;
+            const T *orow = static_cast<const T *>(a.fout) + tok * d;
+            float sp = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                float o[8];
+                ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
+                ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
+                sp = __fadd_rn(sp, dot8(G[j], o));
+            }
+            S_h = group_sum(sp, mp.LPH);
+            lse_h = __ldg(a.lse + tok * H + mp.h);
+            for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
+                cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+            __syncthreads();
+        }
+        const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
+        if (__syncthreads_or(!got)) { ok = false; break; }
+        phase ^= 1u << slot;
+        unsigned char *vb = ring + (size_t)slot * slot_bytes;
+        float *gb_s = reinterpret_cast<float *>(vb + vbytes);
+        const bool first = (s_first[n >> 5] >> (n & 31)) & 1u;
+        const float iv = cur_inv[n];
+
+        // pass A: value dots, raw scores
+        float v[CPL][8];
+        float P = 0.f, zr = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            ld_chunk_s_sw(reinterpret_cast<const T *>(vb + cidx[j] * CB), sw, v[j]);
+            P = __fadd_rn(P, dot8(G[j], v[j]));
+            if constexpr (!LR) zr = __fadd_rn(zr, dot8(qg[j], v[j]));
+        }
+        P = group_sum(P, mp.LPH);
+        if constexpr (!LR) {
+            zr = group_sum(zr, mp.LPH);
+        } else {
+            if (mp.key_warp) {
+                float zk = 0.f;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    float kv[8];
+                    ld_chunk_s_sw(reinterpret_cast<const T *>(vb + kidx[j] * CB), sw, kv);
+                    zk = __fadd_rn(zk, dot8(qg[j], kv));
+                }
+                zk = group_sum(zk, mp.LPHk);
+                if (mp.ksub == 0) zsm[par * 32 + mp.hk] = zk;
+            }
+            __syncthreads();
+            zr = zsm[par * 32 + mp.h];
+        }
+        const float wgt = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
+        const float dz = wgt * (P - S_h);
+        const float cpart = warp_sum(mp.sub == 0 ? dz * zr : 0.f);
+        if (lane == 0) cws[par * 32 + w] = cpart;
+        if (LR && mp.sub == 0) dzs[par * 32 + mp.h] = dz;
+        __syncthreads();
+        float C = 0.f;
+#pragma unroll
+        for (int k = 0; k < kCoopWarps; ++k) C += cws[par * 32 + k];
+        const float coef = iv * iv * iv * C * inv_width;
+        float *grad_row = a.grad + ((int64_t)s_rows[n] * TT + tok) * d;
+
+        if constexpr (!LR) {
+            const float ak = iv * dz;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                float nv[8];
+                if (first) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) nv[e] = 0.f;
+                } else {
+                    ld_chunk_s_sw(gb_s + cidx[j] * 8, sw, nv);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    nv[e] = fmaf(wgt, G[j][e], nv[e]);
+                    nv[e] = fmaf(ak, qg[j][e], nv[e]);
+                    nv[e] = fmaf(-coef, v[j][e], nv[e]);
+                    U[j][e] = fmaf(ak, v[j][e], U[j][e]);
+                }
+                st_f32x8_g_sw(grad_row + cidx[j] * 8, sw, nv);
+            }
+        } else {
+            // key-path terms on the tail, staged in the shared gradient row
+            if (mp.key_warp) {
+                const float ak = iv * dzs[par * 32 + mp.hk];
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    float kv[8], nv[8];
+                    ld_chunk_s_sw(reinterpret_cast<const T *>(vb + kidx[j] * CB), sw, kv);
+                    if (first) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) nv[e] = 0.f;
+                    } else {
+                        ld_chunk_s_sw(gb_s + kidx[j] * 8, sw, nv);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        nv[e] = fmaf(ak, qg[j][e], nv[e]);
+                        nv[e] = fmaf(-coef, kv[e], nv[e]);
+                        U[j][e] = fmaf(ak, kv[e], U[j][e]);
+                    }
+                    float *dst = gb_s + kidx[j] * 8;
+                    *reinterpret_cast<float4 *>(dst + sw) = make_float4(nv[0], nv[1], nv[2], nv[3]);
+                    *reinterpret_cast<float4 *>(dst + (sw ^ 4)) = make_float4(nv[4], nv[5], nv[6], nv[7]);
+                }
+                __syncwarp();
+            }
+            // value path (and the radial term off the slice for the full norm)
+            const float cv = a.norm_full ? coef : 0.f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const bool tail = cidx[j] >= key0;
+                float nv[8];
+                if (tail || !first) {
+                    ld_chunk_s_sw(gb_s + cidx[j] * 8, sw, nv);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) nv[e] = 0.f;
+                }
+                const float c2 = tail ? 0.f : cv;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    nv[e] = fmaf(wgt, G[j][e], nv[e]);
+                    nv[e] = fmaf(-c2, v[j][e], nv[e]);
+                }
+                st_f32x8_g_sw(grad_row + cidx[j] * 8, sw, nv);
+            }
+        }
+        __syncthreads();  // every warp is past this stage
+        if (issued < hi) issue_next();
+        par ^= 1;
+        if (++n == N) { n = 0; ++tok; }
+        if (++slot == S) slot = 0;
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) {
+            report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
+            for (int64_t j = i; j < issued; ++j) {
+                mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+                phase ^= 1u << slot;
+                if (++slot == S) slot = 0;
+            }
+        }
+    }
+    // per-block partial sums U over the key coordinates -> workspace row gb
+    if (!LR || mp.key_warp) {
+        float *wrow = a.ws + gb * r;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+            st_f32x8_g_sw(wrow + ((LR ? kidx[j] : cidx[j]) - key0) * 8, sw, U[j]);
+    }
+}
+
+template <typename T, int CPL, bool LR>
+cudaError_t coop_fwd_inst(const RouteArgs &a, cudaStream_t s)
+{
+    const void *k = reinterpret_cast<const void *>(&route_fwd_coop_kernel<T, CPL, LR>);
+    const size_t smem = coop_fwd_smem_bytes(a.d, sizeof(T));
+    int grid = 0;
+    cudaError_t e = persistent_grid(k, kCoopWarps * 32, smem, &grid);
+    if (e != cudaSuccess) return e;
+    route_fwd_coop_kernel<T, CPL, LR><<<grid, kCoopWarps * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int CPL, bool LR>
+cudaError_t coop_bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_rows)
+{
+    const void *k = reinterpret_cast<const void *>(&route_bwd_coop_kernel<T, CPL, LR>);
+    const size_t smem = coop_bwd_smem_bytes(a->d, sizeof(T));
+    int grid = 0;
+    cudaError_t e = persistent_grid(k, kCoopWarps * 32, smem, &grid);
+    if (e != cudaSuccess) return e;
+    if (grid_rows) {
+        *grid_rows = grid;
+        return cudaSuccess;
+    }
+    route_bwd_coop_kernel<T, CPL, LR><<<grid, kCoopWarps * 32, smem, s>>>(*a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_coop_fwd(const RouteArgs &a, cudaStream_t s)
+{
+    const bool lr = a.r < a.d;
+#define AR_COOP_CASE(C) \
+    case C: return lr ? coop_fwd_inst<T, C, true>(a, s) : coop_fwd_inst<T, C, false>(a, s);
+    switch (a.d / 1024) {
+        AR_COOP_CASE(1) AR_COOP_CASE(2) AR_COOP_CASE(3) AR_COOP_CASE(4)
+        AR_COOP_CASE(5) AR_COOP_CASE(6) AR_COOP_CASE(7) AR_COOP_CASE(8)
+    default: return cudaErrorNotSupported;
+    }
+#undef AR_COOP_CASE
+}
+
+template <typename T>
+cudaError_t dispatch_coop_bwd(const RouteArgs *a, cudaStream_t s, int *grid_rows)
+{
+    const bool lr = a->r < a->d;
+#define AR_COOP_CASE(C)                                                   \
+    case C:                                                               \
+        return lr ? coop_bwd_inst<T, C, true>(a, s, grid_rows)            \
+                  : coop_bwd_inst<T, C, false>(a, s, grid_rows);
+    switch (a->d / 1024) {
+        AR_COOP_CASE(1) AR_COOP_CASE(2) AR_COOP_CASE(3) AR_COOP_CASE(4)
+        AR_COOP_CASE(5) AR_COOP_CASE(6) AR_COOP_CASE(7) AR_COOP_CASE(8)
+    default: return cudaErrorNotSupported;
+    }
+#undef AR_COOP_CASE
+}
+
+}  // namespace ar

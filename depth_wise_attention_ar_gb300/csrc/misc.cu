@@ -9,6 +9,8 @@ template <typename T> cudaError_t dispatch_fwd(const RouteArgs &a, cudaStream_t 
 template <typename T> cudaError_t dispatch_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
 template <typename T> cudaError_t dispatch_lr_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_lr_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
+template <typename T> cudaError_t dispatch_coop_fwd(const RouteArgs &a, cudaStream_t s);
+template <typename T> cudaError_t dispatch_coop_bwd(const RouteArgs *a, cudaStream_t s, int *grid_rows);
 
 // Device error word; kernels get its address as an argument.
 __device__ unsigned int g_device_error = 0;
@@ -116,6 +118,43 @@ cudaError_t launch_append(const void *src, const void *prev, void *dst, float *i
     return cudaGetLastError();
 }
 
+// ---- gradient fold (block-sum fan-out) -----------------------------------------
+// dst += src over one [T, d] pair of fp32 gradient rows (dst = src when dst
+// has not been written since zero_grad; dst = 0 when neither has). A block
+// partial-sum version t+1 = version t + o_{t+1} passes its whole adjoint on to
+// version t ("Low-Rank Attention Residuals", Appendix B.4: every write of a
+// block receives the block sum's adjoint).
+__global__ void __launch_bounds__(256) grad_fold_kernel(float *dst, const float *src, int64_t n4,
+                                                        int mode)
+{
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (mode & 1) v = s4[i];                  // src has content
+        if (mode & 2) {                           // dst has content
+            const float4 o = d4[i];
+            v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+        }
+        d4[i] = v;
+    }
+}
+
+cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
+                             bool dst_valid, cudaStream_t s)
+{
+    if (n == 0) return cudaSuccess;
+    int grid = 0;
+    cudaError_t e = persistent_grid(reinterpret_cast<const void *>(&grad_fold_kernel), 256, 0, &grid);
+    if (e != cudaSuccess) return e;
+    const int64_t n4 = n / 4;
+    const int64_t need = (n4 + 255) / 256;
+    if (need < grid) grid = (int)need;
+    grad_fold_kernel<<<grid, 256, 0, s>>>(dst, src, n4, (src_valid ? 1 : 0) | (dst_valid ? 2 : 0));
+    return cudaGetLastError();
+}
+
 // ---- dq / dg -----------------------------------------------------------------
 // dq_c = g_c * sum_w ws[w, c], dg_c = q_c * sum_w ws[w, c]; the sum over the
 // backward's warps runs in a fixed order (8 strided groups, then the groups
@@ -148,41 +187,62 @@ cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q,
     return cudaGetLastError();
 }
 
-// ---- dtype / key-width dispatch ------------------------------------------------
-// r = d: full-width keys (online-softmax forward, register-resident state);
-// r < d: sliced keys (two-sweep forward with a key cache, blocked backward).
+// ---- dtype / shape dispatch ----------------------------------------------------
+// r = d, d <= 2048: one warp per token (online softmax, register-resident).
+// d > 2048, or r < d with d a multiple of 1024: four warps share each row.
+// Other sliced-key shapes (d <= 4096): one warp per token, two-sweep forward.
+enum class Family { kFull, kCoop, kSliced, kNone };
+
+static Family family_of(int d, int r, int H)
+{
+    if (H < 1 || d <= 0 || r <= 0 || r > d || d % 256 != 0 || r % 256 != 0) return Family::kNone;
+    const bool pow2_h = H <= 32 && (32 % H) == 0;
+    if (r == d && d <= 2048 && pow2_h) return Family::kFull;
+    if (coop_supported(d, r, H)) return Family::kCoop;
+    const int kcpl = r / 256;
+    if (r < d && d <= 4096 && pow2_h && (kcpl == 1 || kcpl == 2 || kcpl == 4 || kcpl == 8))
+        return Family::kSliced;
+    return Family::kNone;
+}
+
 cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 {
-    if (a.r < a.d)
-        return dt == AR_BF16 ? dispatch_lr_fwd<__nv_bfloat16>(a, s) : dispatch_lr_fwd<float>(a, s);
-    return dt == AR_BF16 ? dispatch_fwd<__nv_bfloat16>(a, s) : dispatch_fwd<float>(a, s);
+    const bool bf = dt == AR_BF16;
+    switch (family_of(a.d, a.r, a.H)) {
+    case Family::kFull: return bf ? dispatch_fwd<__nv_bfloat16>(a, s) : dispatch_fwd<float>(a, s);
+    case Family::kCoop:
+        return bf ? dispatch_coop_fwd<__nv_bfloat16>(a, s) : dispatch_coop_fwd<float>(a, s);
+    case Family::kSliced:
+        return bf ? dispatch_lr_fwd<__nv_bfloat16>(a, s) : dispatch_lr_fwd<float>(a, s);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+static cudaError_t bwd_any(const RouteArgs &a, ar_dtype dt, cudaStream_t s, int *rows)
+{
+    const bool bf = dt == AR_BF16;
+    switch (family_of(a.d, a.r, a.H)) {
+    case Family::kFull:
+        return bf ? dispatch_bwd<__nv_bfloat16>(&a, s, rows) : dispatch_bwd<float>(&a, s, rows);
+    case Family::kCoop:
+        return bf ? dispatch_coop_bwd<__nv_bfloat16>(&a, s, rows)
+                  : dispatch_coop_bwd<float>(&a, s, rows);
+    case Family::kSliced:
+        return bf ? dispatch_lr_bwd<__nv_bfloat16>(&a, s, rows) : dispatch_lr_bwd<float>(&a, s, rows);
+    default: return cudaErrorNotSupported;
+    }
 }
 
 cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 {
-    if (a.r < a.d)
-        return dt == AR_BF16 ? dispatch_lr_bwd<__nv_bfloat16>(&a, s, nullptr)
-                             : dispatch_lr_bwd<float>(&a, s, nullptr);
-    return dt == AR_BF16 ? dispatch_bwd<__nv_bfloat16>(&a, s, nullptr)
-                         : dispatch_bwd<float>(&a, s, nullptr);
+    return bwd_any(a, dt, s, nullptr);
 }
 
-cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps)
+cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_rows)
 {
-    if (a.r < a.d)
-        return dt == AR_BF16 ? dispatch_lr_bwd<__nv_bfloat16>(&a, nullptr, grid_warps)
-                             : dispatch_lr_bwd<float>(&a, nullptr, grid_warps);
-    return dt == AR_BF16 ? dispatch_bwd<__nv_bfloat16>(&a, nullptr, grid_warps)
-                         : dispatch_bwd<float>(&a, nullptr, grid_warps);
+    return bwd_any(a, dt, nullptr, grid_rows);
 }
 
-bool fused_shape_supported(int d, int r, int H)
-{
-    if (H < 1 || H > 32 || (32 % H) != 0) return false;
-    if (d <= 0 || r <= 0 || r > d || d % 256 != 0 || r % 256 != 0) return false;
-    if (r == d) return d <= 2048;                  // full keys: d = 256 * (1..8)
-    const int kcpl = r / 256;                      // sliced keys: r = 256 * {1,2,4,8}
-    return d <= 4096 && (kcpl == 1 || kcpl == 2 || kcpl == 4 || kcpl == 8);
-}
+bool fused_shape_supported(int d, int r, int H) { return family_of(d, r, H) != Family::kNone; }
 
 }  // namespace ar

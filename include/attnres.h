@@ -208,6 +208,20 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
                        int32_t site_id, void *stream);
 
 /*
+ * Fold one gradient row into another: grad[dst_row] += grad[src_row] over all
+ * T x d entries (fp32). A row that has not been written since
+ * ar_bank_zero_grad counts as zero, and dst_row is marked written.
+ * Use: block partial sums are stored as versions, row t+1 = row t + o_{t+1};
+ * version t+1's adjoint reaches version t (and so every write of the block)
+ * through this fold, run after the backward of every site that reads row
+ * t+1 ("Low-Rank Attention Residuals", Appendix B.4: every write of a block
+ * receives the adjoint of the block sum; Figure 11's partial += y).
+ * Errors: AR_ERR_INVALID_ARG (rows not appended, equal rows, bank without
+ * gradient rows), AR_ERR_CUDA.
+ */
+ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, void *stream);
+
+/*
  * Block schedule of LR-AttnRes (Figure 11): M sublayers in NB blocks whose
  * last sublayers are ceil(M*j/NB); NB <= 0 or NB >= M means full routing.
  * Bank row 0 is the embedding; row t (1..M) is the partial sum after

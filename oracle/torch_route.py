@@ -1,0 +1,60 @@
+"""Plain PyTorch (float64, CPU) restatement of one routing site and of a whole
+routed model chain — test infrastructure only.
+
+``route`` restates the route pseudocode of "Multi-Head Attention Residuals"
+(Figure 3; Figure 7 at H = 1) and of "Low-Rank Attention Residuals"
+(Figure 11, sliced keys): stack the sources, normalise the keys, one logit per
+(source, head), softmax over depth, mix each head's value slice. Being plain
+torch ops, it is differentiable by autograd, so a routed model chain built
+from it gives reference gradients for every parameter.
+
+Pinned by tests/test_oracle_pins.py against the C oracle (forward values and,
+through autograd, the closed-form gradients).
+"""
+
+from __future__ import annotations
+
+import torch
+
+__all__ = ["route", "chain"]
+
+
+def route(sources, q, g, H: int, r: int | None = None, eps: float = 1e-6,
+          full_width: bool = False):
+    """sources: list of N tensors [T, d]; q, g: [r] (g None = ones)."""
+    V = torch.stack(list(sources))
+    N, T, d = V.shape
+    r = d if r is None else r
+    K = V[..., d - r:]
+    ms = (V * V).mean(-1, keepdim=True) if full_width else (K * K).mean(-1, keepdim=True)
+    khat = K * torch.rsqrt(ms + eps)
+    if g is not None:
+        khat = khat * g
+    logits = torch.einsum("he,nthe->nth", q.view(H, r // H), khat.view(N, T, H, r // H))
+    alpha = torch.softmax(logits, dim=0)
+    mixed = torch.einsum("nth,nthe->the", alpha, V.view(N, T, H, d // H))
+    return mixed.reshape(T, d)
+
+
+def chain(x, sublayers, queries, norm_weights, H: int, r: int | None = None, NB: int | None = None,
+          eps: float = 1e-6, full_width: bool = False):
+    """A routed model (LR-AttnRes Figure 11 with MHAR heads): h = x; after each
+    sublayer, route over the embedding, the completed block sums and the
+    current partial sum. ``NB=None`` keeps every output as its own source
+    (full routing, MHAR Figure 3). ``queries``/``norm_weights`` hold one entry
+    per read (len(sublayers) + 1, the first for the read that feeds sublayer
+    1). Returns the final read."""
+    from .schedule import block_ends
+    M = len(sublayers)
+    ends = set(block_ends(M, NB))
+    blocks, partial = [x], None
+    h = route([x], queries[0], norm_weights[0], H, r, eps, full_width)
+    for t, f in enumerate(sublayers, start=1):
+        y = f(h)
+        partial = y if partial is None else partial + y
+        if t in ends:
+            blocks.append(partial)
+            partial = None
+        srcs = blocks + ([] if partial is None else [partial])
+        h = route(srcs, queries[t], norm_weights[t], H, r, eps, full_width)
+    return h

@@ -145,6 +145,18 @@ def test_sliced_key_shapes(W, orc, d, r, H):
     run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
 
 
+@pytest.mark.parametrize("d,r,H,dtype", [(3072, 3072, 8, "bf16"), (4096, 4096, 8, "bf16"),
+                                         (4096, 4096, 16, "f32"), (8192, 8192, 32, "bf16"),
+                                         (2048, 1024, 8, "bf16"), (4096, 2048, 8, "f32"),
+                                         (1024, 512, 4, "f32"), (7168, 1792, 4, "bf16")])
+def test_wide_rows_four_warp_kernels(W, orc, d, r, H, dtype):
+    """Rows split over the four warps of a block (full keys up to d = 8192, and
+    sliced keys owned by the last warps)."""
+    _, wl = W
+    cfg = small(wl, "wide", T=97, d=d, H=H, dtype=dtype, M=4, NB=2, r=r)
+    run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
+
+
 def test_single_source_site_is_identity(W, orc):
     import torch
     B, wl = W

@@ -3,8 +3,9 @@
 * brute force: an einsum restatement of the pages' route pseudocode
   ("Multi-Head Attention Residuals" Figure 3 / Figure 7, "Low-Rank Attention
   Residuals" Figure 11), softmax/logsumexp from scipy;
-* torch autograd (float64, CPU) on a torch restatement of the forward, for
-  every gradient the oracle's closed form gives;
+* torch autograd (float64, CPU) on the torch restatement of the forward
+  (oracle/torch_route.py), for every gradient the oracle's closed form gives
+  (this also pins that restatement, which the model-chain tests use);
 * central finite differences of the oracle's own forward;
 * the invariants the pages state (H=1 is single-head AttnRes, heads are
   independent slices, weights sum to one, one-hot read, zero query gives the
@@ -47,15 +48,8 @@ def _einsum_route(V, q, g, H, r, eps, full_width):
 
 
 def _torch_route(V, q, g, H, r, eps, full_width):
-    import torch
-    N, T, d = V.shape
-    K = V[..., d - r:]
-    ms = (V * V).mean(-1, keepdim=True) if full_width else (K * K).mean(-1, keepdim=True)
-    khat = K * torch.rsqrt(ms + eps) * g
-    logits = torch.einsum("he,nthe->nth", q.view(H, r // H), khat.view(N, T, H, r // H))
-    alpha = torch.softmax(logits, dim=0)
-    mixed = torch.einsum("nth,nthe->the", alpha, V.view(N, T, H, d // H))
-    return mixed.reshape(T, d)
+    from oracle import torch_route
+    return torch_route.route(list(V.unbind(0)), q, g, H, r, eps, full_width)
 
 
 def _nmax(a, b):
@@ -300,3 +294,36 @@ def test_inv_rms_definition(orc):
     assert np.allclose(inv, [1.0 / np.sqrt(25.0 / 4.0), 1.0], rtol=0, atol=1e-15)
     inv_tail = orc.inv_rms(x, r=2, eps=0.0)
     assert inv_tail[1] == 1.0 and np.isinf(inv_tail[0])
+
+
+@pytest.mark.parametrize("NB", [None, 2, 3])
+def test_torch_chain_matches_schedule_and_c_oracle(orc, NB):
+    """The float64 model chain (oracle/torch_route.chain) against the block
+    schedule, the storage of partial sums and the C oracle, read by read."""
+    import torch
+    from oracle import schedule, torch_route
+    T, d, H, M = 5, 16, 2, 6
+    Ws = [synth.misc_normal(31, t, (d, d), 0.3).astype(np.float64) for t in range(M)]
+    qs = [synth.misc_normal(32, t, (d,), 0.8).astype(np.float64) for t in range(M + 1)]
+    x = synth.misc_normal(33, 0, (T, d)).astype(np.float64)
+    subs = [lambda hh, w=torch.tensor(w): torch.tanh(hh @ w) for w in Ws]
+    h_chain = torch_route.chain(torch.tensor(x), subs, [torch.tensor(q) for q in qs],
+                                [None] * (M + 1), H, NB=NB).numpy()
+    plan = schedule.block_plan(M, NB)
+    outs = [x]
+    h, _ = orc.route_fwd([x], qs[0], None, H)
+    for t in range(1, M + 1):
+        outs.append(np.tanh(h @ Ws[t - 1]))
+        rows = _exact_block_rows(outs, plan, t)     # block sums without rounding
+        h, _ = orc.route_fwd([rows[j] for j in plan["sites"][t]], qs[t], None, H)
+    assert np.max(np.abs(h - h_chain)) < 1e-12
+
+
+def _exact_block_rows(outs, plan, t):
+    rows = []
+    for op in plan["row_ops"][:t + 1]:
+        if op[0] in ("emb", "copy"):
+            rows.append(outs[0] if op[0] == "emb" else outs[op[1]])
+        else:
+            rows.append(rows[op[1]] + outs[op[2]])
+    return rows
