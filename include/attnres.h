@@ -38,11 +38,15 @@
  * - Banks are not thread-safe; distinct banks may be used from distinct
  *   threads.
  *
- * Shapes the fused routing kernels cover: H in {1,2,4,8,16,32},
- * 1 <= n_src <= AR_MAX_SOURCES, row/output pointers 16-byte aligned, and
- * either full keys (r = d, d a multiple of 256 up to 2048) or sliced keys
- * (r < d, d a multiple of 256 up to 4096, r in {256, 512, 1024, 2048}, with
- * the forward's key cache 2*n_src*r*sizeof(dtype) bytes within 200 KB). Other shapes return AR_ERR_UNSUPPORTED (or
+ * Shapes the fused routing kernels cover (1 <= n_src <= AR_MAX_SOURCES,
+ * row/output pointers 16-byte aligned, d and r multiples of 256):
+ *   - r = d <= 2048, H in {1,2,4,8,16,32};
+ *   - d a multiple of 1024 up to 8192, H a multiple of 4 with H/4 in
+ *     {1,2,4,8,16,32}, and r = d or r = k*d/4 (k = 1, 2) with H/k a power of
+ *     two <= 32;
+ *   - other r < d with d <= 4096, H in {1,...,32} a power of two and
+ *     r in {256, 512, 1024, 2048} (the forward's key cache,
+ *     2*n_src*r*sizeof(dtype) bytes, within 200 KB). Other shapes return AR_ERR_UNSUPPORTED (or
  * AR_ERR_ALIGN for a misaligned pointer). Appends accept any d, r that are
  * multiples of 8.
  */
