@@ -352,12 +352,18 @@ def end_to_end(args, mb, stream, run_fwd, run_bwd, world, local):
         dev_in.append(mb.q[s])
         if mb.g[s] is not None:
             dev_in.append(mb.g[s])
+        if mb.cfg.delta:
+            dev_in += [mb.partial[s], mb.alpha[s]]
+    if mb.cfg.delta:
+        dev_in.append(mb.null)
     for t in dev_in:
         h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         h.copy_(t)
         host_in.append(h)
     dev_out = [mb.dq[s] for s in mb.plan.run_sites] + \
               [mb.dg[s] for s in mb.plan.run_sites if mb.g[s] is not None]
+    if mb.cfg.delta:
+        dev_out += [mb.dalpha[s] for s in mb.plan.run_sites] + [mb.dnull]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
     h2d = sum(h.numel() * h.element_size() for h in host_in)
     d2h = sum(h.numel() * h.element_size() for h in host_out)

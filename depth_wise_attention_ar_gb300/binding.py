@@ -42,12 +42,19 @@ SIGNATURES = {
     "ar_bank_zero_grad": ([_P], ctypes.c_int),
     "ar_bank_reset": ([_P], ctypes.c_int),
     "ar_route_fwd": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _I32, _P], ctypes.c_int),
+    "ar_route_fwd_delta": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
+                           ctypes.c_int),
+    "ar_route_bwd_delta": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                            _I32, _P], ctypes.c_int),
+    "ar_bank_append_broadcast": ([_P, _P, _I32P, _P], ctypes.c_int),
+    "ar_bank_grad_token_sum": ([_P, _I32, _P, _P], ctypes.c_int),
     "ar_route_bwd_workspace": ([_P, _I32, _SZP], ctypes.c_int),
     "ar_route_bwd": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I32, _P],
                      ctypes.c_int),
     "ar_route_bwd_noalloc": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
                              ctypes.c_int),
     "ar_bank_grad_fold": ([_P, _I32, _I32, _P], ctypes.c_int),
+    "ar_route_merge": ([_P, _I32, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "ar_block_schedule": ([_I32, _I32, _I32P, _I32P, _I32P, _I64, _I64P], ctypes.c_int),
     "ar_device_error": ([_U32P], ctypes.c_int),
 }
@@ -153,6 +160,38 @@ def ar_route_fwd(bank, rows, H, q, g, out, lse, site_id, stream=None):
                                              _ptr(lse), site_id, _stream(stream)))
 
 
+def ar_route_fwd_delta(bank, rows, H, q, g, partial, alpha, out, routed, lse, site_id,
+                       stream=None):
+    arr, n = _rows(rows)
+    _check("ar_route_fwd_delta", _lib.ar_route_fwd_delta(bank, arr, n, H, _ptr(q), _ptr(g),
+                                                         _ptr(partial), _ptr(alpha), _ptr(out),
+                                                         _ptr(routed), _ptr(lse), site_id,
+                                                         _stream(stream)))
+
+
+def ar_route_bwd_delta(bank, rows, H, q, g, routed, dout, lse, alpha, dq, dg, dalpha, ws,
+                       ws_bytes, site_id, stream=None):
+    arr, n = _rows(rows)
+    _check("ar_route_bwd_delta", _lib.ar_route_bwd_delta(bank, arr, n, H, _ptr(q), _ptr(g),
+                                                         _ptr(routed), _ptr(dout), _ptr(lse),
+                                                         _ptr(alpha), _ptr(dq), _ptr(dg),
+                                                         _ptr(dalpha), _ptr(ws), ws_bytes,
+                                                         site_id, _stream(stream)))
+
+
+def ar_bank_append_broadcast(bank, vec, stream=None) -> int:
+    row = ctypes.c_int32(-1)
+    _check("ar_bank_append_broadcast", _lib.ar_bank_append_broadcast(bank, _ptr(vec),
+                                                                     ctypes.byref(row),
+                                                                     _stream(stream)))
+    return row.value
+
+
+def ar_bank_grad_token_sum(bank, row, out, stream=None):
+    _check("ar_bank_grad_token_sum", _lib.ar_bank_grad_token_sum(bank, row, _ptr(out),
+                                                                 _stream(stream)))
+
+
 def ar_route_bwd_workspace(bank, H) -> int:
     b = ctypes.c_size_t()
     _check("ar_route_bwd_workspace", _lib.ar_route_bwd_workspace(bank, H, ctypes.byref(b)))
@@ -179,6 +218,12 @@ AR_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 def ar_bank_grad_fold(bank, dst_row: int, src_row: int, stream=None):
     _check("ar_bank_grad_fold", _lib.ar_bank_grad_fold(bank, dst_row, src_row, _stream(stream)))
+
+
+def ar_route_merge(bank, H, out_a, lse_a, out_b, lse_b, out, lse, stream=None):
+    _check("ar_route_merge", _lib.ar_route_merge(bank, H, _ptr(out_a), _ptr(lse_a), _ptr(out_b),
+                                                 _ptr(lse_b), _ptr(out), _ptr(lse),
+                                                 _stream(stream)))
 
 
 def ar_block_schedule(M: int, NB: int | None):
@@ -275,6 +320,45 @@ class Bank:
             self._check_tensor(g, (self.r,), torch.float32, "g")
         ar_route_fwd(self.handle, rows, H, q, g, out, lse, site_id, stream)
         return out, lse
+
+    def route_fwd_delta(self, rows, H, q, g, partial, alpha, out=None, routed=None, lse=None,
+                        site_id=0, stream=None):
+        """Delta form: out = partial + alpha * routed (see ar_route_fwd_delta)."""
+        dev = self.rows.device
+        shape = (self.T, self.d)
+        out = torch.empty(shape, dtype=self.torch_dtype, device=dev) if out is None else out
+        routed = torch.empty(shape, dtype=self.torch_dtype, device=dev) if routed is None else routed
+        lse = torch.empty((self.T, H), dtype=torch.float32, device=dev) if lse is None else lse
+        for t, sh, dt, nm in ((partial, shape, self.torch_dtype, "partial"),
+                              (out, shape, self.torch_dtype, "out"),
+                              (routed, shape, self.torch_dtype, "routed"),
+                              (lse, (self.T, H), torch.float32, "lse"),
+                              (alpha, (1,), torch.float32, "alpha")):
+            self._check_tensor(t, sh, dt, nm)
+        ar_route_fwd_delta(self.handle, rows, H, q, g, partial, alpha, out, routed, lse, site_id,
+                           stream)
+        return out, routed, lse
+
+    def route_bwd_delta(self, rows, H, q, g, routed, dout, lse, alpha, dq=None, dg=None,
+                        dalpha=None, site_id=0, stream=None, ws=None):
+        dev = self.rows.device
+        dq = torch.empty(self.r, dtype=torch.float32, device=dev) if dq is None else dq
+        if dg is None and g is not None:
+            dg = torch.empty(self.r, dtype=torch.float32, device=dev)
+        dalpha = torch.empty(1, dtype=torch.float32, device=dev) if dalpha is None else dalpha
+        ws = self.workspace(H) if ws is None else ws
+        ar_route_bwd_delta(self.handle, rows, H, q, g, routed, dout, lse, alpha, dq, dg, dalpha,
+                           ws, ws.numel() * 4, site_id, stream)
+        return dq, dg, dalpha
+
+    def append_broadcast(self, vec, stream=None) -> int:
+        self._check_tensor(vec, (self.d,), self.torch_dtype, "vec")
+        return ar_bank_append_broadcast(self.handle, vec, stream)
+
+    def grad_token_sum(self, row, out=None, stream=None):
+        out = torch.empty(self.d, dtype=torch.float32, device=self.rows.device) if out is None else out
+        ar_bank_grad_token_sum(self.handle, row, out, stream)
+        return out
 
     def workspace(self, H) -> torch.Tensor:
         nbytes = ar_route_bwd_workspace(self.handle, H)

@@ -22,6 +22,11 @@ struct RouteArgs {
     const void *dout;      // backward: dL/dout [T, d]
     float *ws;             // backward: per-warp partial sums [warps, r]
     unsigned int *err;     // device error word
+    // delta form (h = partial + alpha * routed): forward epilogue and backward
+    const void *partial;   // forward: residual stream [T, d], or nullptr
+    const float *alpha;    // gate (device scalar), or nullptr (= 1)
+    void *routed;          // forward: also store the routed mix here, or nullptr
+    float *dalpha;         // backward: dL/dalpha (device scalar), or nullptr
     int64_t T;
     int d, r, H, n_src, inv_ld, norm_full;
     int rows[AR_MAX_SOURCES];
@@ -34,14 +39,18 @@ cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
 cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
 cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps);
 cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, const float *g,
-                               float *dq, float *dg, cudaStream_t s);
+                               float *dq, float *dg, float *dalpha, cudaStream_t s);
+cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const float *lb,
+                         void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s);
+cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cudaStream_t s);
 cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col,
                           int64_t T, int d, int r, int inv_ld, int norm_full, float eps,
-                          ar_dtype dt, cudaStream_t s);
+                          ar_dtype dt, cudaStream_t s, bool broadcast = false);
 cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
                              bool dst_valid, cudaStream_t s);
 unsigned int *device_error_word();
 bool fused_shape_supported(int d, int r, int H);
+bool delta_supported(int d, int r, int H);
 
 // Shapes of the four-warp kernels: d = 1024 * CPL (CPL in 1..8), H a multiple
 // of 4 with H/4 heads per warp a power of two <= 32; r = d, or r = k * d/4

@@ -204,24 +204,53 @@ ar_status ar_bank_reset(ar_bank *bank)
     return AR_OK;
 }
 
-ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
-                       const float *q, const float *g, void *out, float *lse, int32_t site_id,
-                       void *stream)
+namespace {
+
+ar_status route_fwd_impl(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                         const float *q, const float *g, const void *partial, const float *alpha,
+                         void *out, void *routed, float *lse, int32_t site_id, void *stream)
 {
     ar_status st = check_site(bank, rows, n_src, H, q, g);
     if (st != AR_OK) return st;
     if (bank->T > 0 && (!out || !lse)) return AR_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned4(lse)) return AR_ERR_ALIGN;
+    if (!aligned16(out) || !aligned4(lse) || !aligned16(partial) || !aligned16(routed) ||
+        !aligned4(alpha))
+        return AR_ERR_ALIGN;
+    if ((partial || alpha || routed) && !ar::delta_supported(bank->d, bank->r, H))
+        return AR_ERR_UNSUPPORTED;
     if (bank->T > 0) {
         ar::RouteArgs a;
         fill_common(a, bank, rows, n_src, H, q, g);
         a.out = out;
         a.lse = lse;
+        a.partial = partial;
+        a.alpha = alpha;
+        a.routed = routed;
         const cudaError_t e = ar::launch_route_fwd(a, bank->dtype, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return from_cuda(e);
     }
     bank->fwd_record.push_back(site_id);
     return AR_OK;
+}
+
+}  // namespace
+
+ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                       const float *q, const float *g, void *out, float *lse, int32_t site_id,
+                       void *stream)
+{
+    return route_fwd_impl(bank, rows, n_src, H, q, g, nullptr, nullptr, out, nullptr, lse, site_id,
+                          stream);
+}
+
+ar_status ar_route_fwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                             const float *q, const float *g, const void *partial,
+                             const float *alpha, void *out, void *routed, float *lse,
+                             int32_t site_id, void *stream)
+{
+    if (bank && bank->T > 0 && (!partial || !alpha || !routed)) return AR_ERR_INVALID_ARG;
+    return route_fwd_impl(bank, rows, n_src, H, q, g, partial, alpha, out, routed, lse, site_id,
+                          stream);
 }
 
 ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
@@ -237,22 +266,26 @@ ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
     int warps = 0;
     const cudaError_t e = ar::route_bwd_grid(a, bank->dtype, &warps);
     if (e != cudaSuccess) return from_cuda(e);
-    *bytes = (size_t)warps * (size_t)bank->r * sizeof(float);
+    // [rows, r] partial sums of dq/dg, then a [rows, 4] tail for dL/dalpha
+    *bytes = (size_t)warps * ((size_t)bank->r + 4) * sizeof(float);
     return AR_OK;
 }
 
-ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
-                       const float *q, const float *g, const void *out, const void *dout,
-                       const float *lse, float *dq, float *dg, void *ws, size_t ws_bytes,
-                       int32_t site_id, void *stream)
+namespace {
+
+ar_status route_bwd_impl(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                         const float *q, const float *g, const void *out, const void *dout,
+                         const float *lse, const float *alpha, float *dq, float *dg,
+                         float *dalpha, void *ws, size_t ws_bytes, int32_t site_id, void *stream)
 {
     if (bank && !bank->grad && bank->T > 0) return AR_ERR_INVALID_ARG;
     ar_status st = check_site(bank, rows, n_src, H, q, g);
     if (st != AR_OK) return st;
     if (!dq || (bank->T > 0 && (!out || !dout || !lse || !ws))) return AR_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(dout) || !aligned4(lse) || !aligned4(dq) ||
-        (dg && !aligned4(dg)) || !aligned16(ws))
+        (dg && !aligned4(dg)) || !aligned16(ws) || !aligned4(alpha) || !aligned4(dalpha))
         return AR_ERR_ALIGN;
+    if ((alpha || dalpha) && !ar::delta_supported(bank->d, bank->r, H)) return AR_ERR_UNSUPPORTED;
     if (bank->fwd_record.empty() || bank->fwd_record.back() != site_id) return AR_ERR_ORDER;
     size_t need = 0;
     st = ar_route_bwd_workspace(bank, H, &need);
@@ -262,6 +295,7 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
     if (bank->T == 0) {
         cudaError_t e = cudaMemsetAsync(dq, 0, (size_t)bank->r * sizeof(float), s);
         if (e == cudaSuccess && dg) e = cudaMemsetAsync(dg, 0, (size_t)bank->r * sizeof(float), s);
+        if (e == cudaSuccess && dalpha) e = cudaMemsetAsync(dalpha, 0, sizeof(float), s);
         if (e != cudaSuccess) return from_cuda(e);
     } else {
         ar::RouteArgs a;
@@ -270,17 +304,74 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
         a.dout = dout;
         a.lse = const_cast<float *>(lse);
         a.ws = static_cast<float *>(ws);
+        a.alpha = alpha;
+        a.dalpha = dalpha;
         for (int i = 0; i < n_src; ++i)
             if (!bank->touched[rows[i]]) a.first_mask[i >> 5] |= 1u << (i & 31);
         cudaError_t e = ar::launch_route_bwd(a, bank->dtype, s);
         if (e != cudaSuccess) return from_cuda(e);
-        e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), (int)(need / sizeof(float) / bank->r),
-                                   bank->r, q, g, dq, dg, s);
+        const int ws_rows = (int)(need / sizeof(float) / ((size_t)bank->r + 4));
+        e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), ws_rows, bank->r, q, g, dq, dg,
+                                   dalpha, s);
         if (e != cudaSuccess) return from_cuda(e);
     }
     for (int i = 0; i < n_src; ++i) bank->touched[rows[i]] = 1;
     bank->fwd_record.pop_back();
     return AR_OK;
+}
+
+}  // namespace
+
+ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                       const float *q, const float *g, const void *out, const void *dout,
+                       const float *lse, float *dq, float *dg, void *ws, size_t ws_bytes,
+                       int32_t site_id, void *stream)
+{
+    return route_bwd_impl(bank, rows, n_src, H, q, g, out, dout, lse, nullptr, dq, dg, nullptr,
+                          ws, ws_bytes, site_id, stream);
+}
+
+ar_status ar_route_bwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                             const float *q, const float *g, const void *routed,
+                             const void *dout, const float *lse, const float *alpha, float *dq,
+                             float *dg, float *dalpha, void *ws, size_t ws_bytes, int32_t site_id,
+                             void *stream)
+{
+    if (!alpha || !dalpha) return AR_ERR_INVALID_ARG;
+    return route_bwd_impl(bank, rows, n_src, H, q, g, routed, dout, lse, alpha, dq, dg, dalpha, ws,
+                          ws_bytes, site_id, stream);
+}
+
+ar_status ar_bank_append_broadcast(ar_bank *bank, const void *vec, int32_t *out_row, void *stream)
+{
+    if (!bank || !vec) return AR_ERR_INVALID_ARG;
+    if (bank->count >= bank->cap) return AR_ERR_CAPACITY;
+    if (!aligned16(vec)) return AR_ERR_ALIGN;
+    void *dst = nullptr;
+    ar_bank_row_ptr(bank, bank->count, &dst);
+    const cudaError_t e = ar::launch_append(vec, nullptr, dst, bank->inv + bank->count, bank->T,
+                                            bank->d, bank->r, bank->inv_ld, bank->norm_full,
+                                            bank->eps, bank->dtype,
+                                            static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (out_row) *out_row = bank->count;
+    ++bank->count;
+    return AR_OK;
+}
+
+ar_status ar_bank_grad_token_sum(const ar_bank *bank, int32_t row, float *out, void *stream)
+{
+    if (!bank || !out || row < 0 || row >= bank->count) return AR_ERR_INVALID_ARG;
+    if (!bank->grad && bank->T > 0) return AR_ERR_INVALID_ARG;
+    if (!aligned4(out)) return AR_ERR_ALIGN;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (bank->T == 0 || !bank->touched[row])
+        e = cudaMemsetAsync(out, 0, (size_t)bank->d * sizeof(float), s);
+    else
+        e = ar::launch_token_sum(bank->grad + (int64_t)row * bank->T * bank->d, bank->T, bank->d,
+                                 out, s);
+    return e == cudaSuccess ? AR_OK : from_cuda(e);
 }
 
 ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, void *stream)
@@ -298,6 +389,21 @@ ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, voi
     if (e != cudaSuccess) return from_cuda(e);
     bank->touched[dst_row] = 1;
     return AR_OK;
+}
+
+ar_status ar_route_merge(const ar_bank *bank, int32_t H, const void *out_a, const float *lse_a,
+                         const void *out_b, const float *lse_b, void *out, float *lse, void *stream)
+{
+    if (!bank) return AR_ERR_INVALID_ARG;
+    if (H < 1 || bank->d % H != 0) return AR_ERR_SHAPE;
+    if (bank->T > 0 && (!out_a || !lse_a || !out_b || !lse_b || !out || !lse))
+        return AR_ERR_INVALID_ARG;
+    if (!aligned16(out_a) || !aligned16(out_b) || !aligned16(out) || !aligned4(lse_a) ||
+        !aligned4(lse_b) || !aligned4(lse))
+        return AR_ERR_ALIGN;
+    const cudaError_t e = ar::launch_merge(out_a, lse_a, out_b, lse_b, out, lse, bank->T, bank->d,
+                                           H, bank->dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AR_OK : from_cuda(e);
 }
 
 ar_status ar_block_schedule(int32_t M, int32_t NB, int32_t *acc_from, int32_t *site_ptr,

@@ -257,6 +257,27 @@ __device__ __forceinline__ void st_f32x8_s(float *p, const float v[8])
 }
 __device__ __forceinline__ void st_f32x8_g(float *p, const float v[8]) { st_chunk_g(p, v); }
 
+// Forward epilogue of one 8-element chunk of the routed mix o at element
+// offset off: out = o, or out = partial + alpha * o in the delta form
+// ("Multi-Head Attention Residuals", Appendix E, Figure 9: the kernel adds
+// the residual stream in delta modes); the plain mix also goes to routed when
+// asked for (the delta backward needs it).
+template <typename T>
+__device__ __forceinline__ void store_output(const RouteArgs &a, int64_t off, const float o[8])
+{
+    if (a.routed) st_chunk_g(static_cast<T *>(a.routed) + off, o);
+    if (a.partial) {
+        const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
+        float p[8], y[8];
+        ld_chunk_g(static_cast<const T *>(a.partial) + off, p);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = fmaf(alpha, o[e], p[e]);
+        st_chunk_g(static_cast<T *>(a.out) + off, y);
+    } else {
+        st_chunk_g(static_cast<T *>(a.out) + off, o);
+    }
+}
+
 // Sum over the `lph` lanes of this lane's aligned group (lph a power of two).
 __device__ __forceinline__ float group_sum(float x, int lph)
 {

@@ -133,7 +133,8 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         for (int e = 0; e < 8; ++e) U[j][e] = 0.f;
 
     float G[CPL][8];
-    float S_h = 0.f, lse_h = 0.f;
+    float S_h = 0.f, lse_h = 0.f, dal = 0.f;
+    const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
     int64_t tok = lo / N, i = lo;
     int n = (int)(lo - tok * N), slot = 0;
     uint32_t phase = 0;
@@ -143,15 +144,21 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
             // token-level data: dL/dout, the coupling term S, lse, inverse RMS
             const T *grow = static_cast<const T *>(a.dout) + tok * d;
             const T *orow = static_cast<const T *>(a.fout) + tok * d;
-            float sp = 0.f;
+            float sp = 0.f, raw = 0.f;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float o[8];
                 ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
                 ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
+                if (a.dalpha) raw = __fadd_rn(raw, dot8(G[j], o));
+                if (a.alpha) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) G[j][e] *= alpha;  // delta form: G = alpha dL/dh
+                }
                 sp = __fadd_rn(sp, dot8(G[j], o));
             }
             S_h = group_sum(sp, LPH);
+            if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted by the warp owning (t, 0)
             lse_h = __ldg(a.lse + tok * H + h);
             __syncwarp();
             for (int nn = lane; nn < N; nn += 32)
@@ -218,10 +225,12 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         }
     }
 
-    // per-warp partial sums U -> workspace row gw
+    // per-warp partial sums U -> workspace row gw; dL/dalpha partial -> tail
     float *wrow = a.ws + gw * d;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) st_f32x8_g_sw(wrow + cidx[j] * 8, sw, U[j]);
+    if (a.dalpha && lane == 0)
+        *reinterpret_cast<float4 *>(a.ws + GW * d + gw * 4) = make_float4(dal, 0.f, 0.f, 0.f);
 }
 
 template <typename T, int CPL>

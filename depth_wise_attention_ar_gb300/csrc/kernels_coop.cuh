@@ -195,13 +195,12 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
 
         if (n == N - 1) {
             const float rl = 1.f / l;
-            T *orow = static_cast<T *>(a.out) + tok * d;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
-                st_chunk_g(orow + cidx[j] * 8, o);
+                store_output<T>(a, tok * d + cidx[j] * 8, o);
             }
             if (mp.sub == 0) a.lse[tok * H + mp.h] = m + log2f(l) * kLn2;
         }
@@ -303,7 +302,8 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     for (int s = 0; s < S && issued < hi; ++s) issue_next();
 
     float G[CPL][8];
-    float S_h = 0.f, lse_h = 0.f;
+    float S_h = 0.f, lse_h = 0.f, dal = 0.f;
+    const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
     int64_t tok = lo / N, i = lo;
     int n = (int)(lo - tok * N), slot = 0, par = 0;
     uint32_t phase = 0;
@@ -312,15 +312,21 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         if (i == lo || n == 0) {
             const T *grow = static_cast<const T *>(a.dout) + tok * d;
             const T *orow = static_cast<const T *>(a.fout) + tok * d;
-            float sp = 0.f;
+            float sp = 0.f, raw = 0.f;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float o[8];
                 ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
                 ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
+                if (a.dalpha) raw = __fadd_rn(raw, dot8(G[j], o));
+                if (a.alpha) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) G[j][e] *= alpha;  // delta form: G = alpha dL/dh
+                }
                 sp = __fadd_rn(sp, dot8(G[j], o));
             }
             S_h = group_sum(sp, mp.LPH);
+            if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted once
             lse_h = __ldg(a.lse + tok * H + mp.h);
             for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
                 cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
@@ -456,13 +462,15 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             }
         }
     }
-    // per-block partial sums U over the key coordinates -> workspace row gb
+    // per-block partial sums U over the key coordinates -> workspace row gb;
+    // dL/dalpha partials (one per warp) -> tail
     if (!LR || mp.key_warp) {
         float *wrow = a.ws + gb * r;
 #pragma unroll
         for (int j = 0; j < CPL; ++j)
             st_f32x8_g_sw(wrow + ((LR ? kidx[j] : cidx[j]) - key0) * 8, sw, U[j]);
     }
+    if (a.dalpha && lane == 0) a.ws[GB * r + gb * 4 + w] = dal;
 }
 
 template <typename T, int CPL, bool LR>

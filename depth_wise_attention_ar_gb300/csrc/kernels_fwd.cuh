@@ -182,13 +182,12 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
 
         if (n == N - 1) {
             const float rl = 1.f / l;
-            T *orow = static_cast<T *>(a.out) + tok * d;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
-                st_chunk_g(orow + cidx[j] * 8, o);
+                store_output<T>(a, tok * d + cidx[j] * 8, o);
             }
             if (sub == 0) a.lse[tok * H + h] = m + log2f(l) * kLn2;
         }

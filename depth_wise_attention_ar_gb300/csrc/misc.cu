@@ -39,7 +39,7 @@ unsigned int *device_error_word()
 template <typename T>
 __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev, T *dst, float *inv,
                                                      int64_t TT, int d, int r, int inv_ld,
-                                                     int norm_full, float eps)
+                                                     int norm_full, float eps, int src_tok_stride)
 {
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -47,9 +47,9 @@ __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev
     const int nch = d / 8;
     const int c0 = norm_full ? 0 : (d - r) / 8;
     const float inv_w = 1.0f / (float)(norm_full ? d : r);
-    const bool write = (src != dst) || prev != nullptr;
+    const bool write = (src != dst) || prev != nullptr || src_tok_stride != d;
     for (int64_t t = w0; t < TT; t += nw) {
-        const T *s = src + t * d;
+        const T *s = src + t * src_tok_stride;
         T *o = dst + t * d;
         float ss = 0.f;
         if (write) {
@@ -96,8 +96,9 @@ __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev
 
 cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col, int64_t T,
                           int d, int r, int inv_ld, int norm_full, float eps, ar_dtype dt,
-                          cudaStream_t s)
+                          cudaStream_t s, bool broadcast)
 {
+    const int stride = broadcast ? 0 : d;
     if (T == 0) return cudaSuccess;
     int grid = 0;
     const void *k = dt == AR_BF16 ? reinterpret_cast<const void *>(&append_kernel<__nv_bfloat16>)
@@ -109,12 +110,12 @@ cudaError_t launch_append(const void *src, const void *prev, void *dst, float *i
     if (dt == AR_BF16)
         append_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
             static_cast<const __nv_bfloat16 *>(src), static_cast<const __nv_bfloat16 *>(prev),
-            static_cast<__nv_bfloat16 *>(dst), inv_col, T, d, r, inv_ld, norm_full, eps);
+            static_cast<__nv_bfloat16 *>(dst), inv_col, T, d, r, inv_ld, norm_full, eps, stride);
     else
         append_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(src),
                                                   static_cast<const float *>(prev),
                                                   static_cast<float *>(dst), inv_col, T, d, r,
-                                                  inv_ld, norm_full, eps);
+                                                  inv_ld, norm_full, eps, stride);
     return cudaGetLastError();
 }
 
@@ -155,15 +156,120 @@ cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_v
     return cudaGetLastError();
 }
 
+// ---- gradient of a broadcast row ----------------------------------------------
+// out[c] = sum_t grad[t, c] over one [T, d] fp32 gradient row: the gradient of
+// a source that is the same vector for every token (the learnable null source
+// of the delta form, "Multi-Head Attention Residuals", Sec. 3.3). One block per
+// 32 columns; warp w sums tokens w, w + 8, ..., then the 8 warps in order.
+__global__ void __launch_bounds__(256) token_sum_kernel(const float *grad, int64_t TT, int d,
+                                                        float *out)
+{
+    __shared__ float part[8][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + lane;
+    float s = 0.f;
+    if (c < d)
+        for (int64_t t = w; t < TT; t += 8) s += grad[t * d + c];
+    part[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && c < d) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t += part[k][lane];
+        out[c] = t;
+    }
+}
+
+cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cudaStream_t s)
+{
+    token_sum_kernel<<<(d + 31) / 32, 256, 0, s>>>(grad, T, d, out);
+    return cudaGetLastError();
+}
+
+// ---- merge of two partial reads (two-phase block inference) --------------------
+// For two disjoint source sets A and B of one site, with per-head results
+// (out_A, lse_A) and (out_B, lse_B), the read over A u B is
+//   lse = m + log(e^(lse_A - m) + e^(lse_B - m)),  m = max(lse_A, lse_B)
+//   out = (e^(lse_A - lse) out_A + e^(lse_B - lse) out_B)   on each head's slice
+// ("Low-Rank Attention Residuals", Sec. 3.4: inter-block and intra-block
+// results merge with an online-softmax update). One warp per token.
+template <typename T>
+__global__ void __launch_bounds__(256) merge_kernel(const T *oa, const float *la, const T *ob,
+                                                    const float *lb, T *out, float *lse,
+                                                    int64_t TT, int d, int H)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int K = d / H, nch = d / 8;
+    for (int64_t t = w0; t < TT; t += nw) {
+        for (int c = lane; c < nch; c += 32) {
+            const int h = (c * 8) / K;
+            const float a = la[t * H + h], b = lb[t * H + h];
+            const float m = fmaxf(a, b);
+            const float ea = exp2f((a - m) * kLog2e), eb = exp2f((b - m) * kLog2e);
+            const float inv = 1.f / (ea + eb);
+            float x[8], y[8], z[8];
+            ld_chunk_g(oa + t * d + c * 8, x);
+            ld_chunk_g(ob + t * d + c * 8, y);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) z[e] = fmaf(ea * inv, x[e], eb * inv * y[e]);
+            st_chunk_g(out + t * d + c * 8, z);
+        }
+        for (int h = lane; h < H; h += 32) {
+            const float a = la[t * H + h], b = lb[t * H + h];
+            const float m = fmaxf(a, b);
+            lse[t * H + h] = m + log2f(exp2f((a - m) * kLog2e) + exp2f((b - m) * kLog2e)) * kLn2;
+        }
+    }
+}
+
+cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const float *lb,
+                         void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s)
+{
+    if (T == 0) return cudaSuccess;
+    const void *k = dt == AR_BF16 ? reinterpret_cast<const void *>(&merge_kernel<__nv_bfloat16>)
+                                  : reinterpret_cast<const void *>(&merge_kernel<float>);
+    int grid = 0;
+    cudaError_t e = persistent_grid(k, 256, 0, &grid);
+    if (e != cudaSuccess) return e;
+    const int64_t need = (T + 7) / 8;
+    if (need < grid) grid = (int)need;
+    if (dt == AR_BF16)
+        merge_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(oa), la, static_cast<const __nv_bfloat16 *>(ob), lb,
+            static_cast<__nv_bfloat16 *>(out), lse, T, d, H);
+    else
+        merge_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(oa), la,
+                                                 static_cast<const float *>(ob), lb,
+                                                 static_cast<float *>(out), lse, T, d, H);
+    return cudaGetLastError();
+}
+
 // ---- dq / dg -----------------------------------------------------------------
 // dq_c = g_c * sum_w ws[w, c], dg_c = q_c * sum_w ws[w, c]; the sum over the
 // backward's warps runs in a fixed order (8 strided groups, then the groups
 // in order), so repeated runs give identical bits.
 __global__ void __launch_bounds__(256) dqdg_reduce_kernel(const float *ws, int rows, int r,
                                                           const float *q, const float *g,
-                                                          float *dq, float *dg)
+                                                          float *dq, float *dg, float *dalpha)
 {
     __shared__ float part[8][33];
+    if (dalpha && blockIdx.x == 0) {
+        // dL/dalpha of the delta form: the rows * 4 tail partials, fixed order
+        __shared__ float red[256];
+        const float *tail = ws + (int64_t)rows * r;
+        float s = 0.f;
+        for (int k = threadIdx.x; k < rows * 4; k += 256) s += tail[k];
+        red[threadIdx.x] = s;
+        __syncthreads();
+        for (int o = 128; o > 0; o >>= 1) {
+            if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) *dalpha = red[0];
+        __syncthreads();
+    }
     const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
     float s = 0.f;
@@ -181,9 +287,9 @@ __global__ void __launch_bounds__(256) dqdg_reduce_kernel(const float *ws, int r
 }
 
 cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, const float *g,
-                               float *dq, float *dg, cudaStream_t s)
+                               float *dq, float *dg, float *dalpha, cudaStream_t s)
 {
-    dqdg_reduce_kernel<<<(r + 31) / 32, 256, 0, s>>>(ws, rows, r, q, g, dq, dg);
+    dqdg_reduce_kernel<<<(r + 31) / 32, 256, 0, s>>>(ws, rows, r, q, g, dq, dg, dalpha);
     return cudaGetLastError();
 }
 
@@ -244,5 +350,11 @@ cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_rows)
 }
 
 bool fused_shape_supported(int d, int r, int H) { return family_of(d, r, H) != Family::kNone; }
+
+bool delta_supported(int d, int r, int H)
+{
+    const Family f = family_of(d, r, H);
+    return f == Family::kFull || f == Family::kCoop;
+}
 
 }  // namespace ar

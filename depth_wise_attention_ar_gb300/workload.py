@@ -40,6 +40,8 @@ class Config:
     sites: tuple | None = None  # restrict to these site indices (None: all)
     q_std: float = 0.02
     norm: str = "key"           # RMS over the key coordinates, or "full" width
+    delta: bool = False         # delta form: row 0 is a learnable null source, every
+                                # site returns partial + alpha * routed
     note: str = ""
 
 
@@ -54,6 +56,10 @@ CONFIGS = {
                  note="d=1280, L=36: 73 sites"),
     "lr_block": Config("lr_block", T=8192, d=4096, H=8, r=1024, dtype="bf16", M=64, NB=8,
                        note="32 layers in 8 blocks, keys = last 1024 coordinates"),
+    "delta_8b": Config("delta_8b", T=2 * 4096, d=4096, H=8, r=4096, dtype="bf16", M=64, NB=8,
+                       delta=True,
+                       note="delta form of the 8B mid-training model: null source + 8 block "
+                            "deltas (at most 9 sources), H=8, full-width keys"),
 }
 
 
@@ -88,6 +94,9 @@ def model_bytes(cfg: Config, plan: Plan, H: int | None = None) -> dict:
     append       : T (b r + 4) for a row written in place by its producer
                    (key read for the inverse RMS), T (3 b d + 4) for a partial
                    sum (two reads, one write).
+    delta form   : each forward also reads the residual stream and writes the
+                   routed mix (2 T b d); the null source is a broadcast fill
+                   (T (b d + 4)) and its gradient a token sum (T d 4).
     """
     H = cfg.H if H is None else H
     b = 2 if cfg.dtype == "bf16" else 4
@@ -96,10 +105,15 @@ def model_bytes(cfg: Config, plan: Plan, H: int | None = None) -> dict:
     touched = set()
     needed = sorted({row for s in plan.run_sites for row in plan.sites[s]})
     for row in needed:
-        app += T * (3 * b * d + 4) if plan.acc_from[row] >= 0 else T * (b * r + 4)
+        if row == 0 and cfg.delta:
+            app += T * (b * d + 4) + T * d * 4     # broadcast fill; its gradient's token sum
+        else:
+            app += T * (3 * b * d + 4) if plan.acc_from[row] >= 0 else T * (b * r + 4)
     for s in plan.run_sites:
         N = len(plan.sites[s])
         fwd += T * (N * b * d + 4 * N + b * d + 4 * H)
+        if cfg.delta:
+            fwd += 2 * T * b * d                    # partial read, routed mix written
     for s in reversed(plan.run_sites):
         rows = plan.sites[s]
         N = len(rows)
@@ -135,6 +149,10 @@ class Microbatch:
         # separate buffers when the row is a block partial sum
         self.outputs = {}
         for j in range(self.n_rows):
+            if j == 0 and cfg.delta:
+                # learnable null source: one vector, broadcast over the tokens
+                self.null = src.output(0, 1, cfg.d, cfg.dtype).reshape(cfg.d).contiguous()
+                continue
             x = src.output(j, cfg.T, cfg.d, cfg.dtype)
             if self.plan.acc_from[j] >= 0:
                 self.outputs[j] = x
@@ -151,6 +169,14 @@ class Microbatch:
         self.dq = {s: torch.empty(cfg.r, device=dev) for s in self.plan.run_sites}
         self.dg = {s: torch.empty(cfg.r, device=dev) for s in self.plan.run_sites}
         self.ws = self.bank.workspace(self.H)
+        if cfg.delta:
+            self.partial = {s: src.output(1000 + s, cfg.T, cfg.d, cfg.dtype)
+                            for s in self.plan.run_sites}
+            self.alpha = {s: src.query(2000 + s, 1) for s in self.plan.run_sites}
+            self.routed = {s: torch.empty((cfg.T, cfg.d), dtype=tdt, device=dev)
+                           for s in self.plan.run_sites}
+            self.dalpha = {s: torch.empty(1, device=dev) for s in self.plan.run_sites}
+            self.dnull = torch.empty(cfg.d, device=dev)
 
     def forward(self, stream=None, on_site=None):
         bank, plan = self.bank, self.plan
@@ -158,14 +184,23 @@ class Microbatch:
         appended = 0
         run = set(plan.run_sites)
         last = max(plan.run_sites)
+        delta = self.cfg.delta
         for t in range(last + 1):
             if t < self.n_rows:
-                src = self.outputs.get(t, bank.rows[t])
-                bank.append(src, plan.acc_from[t], stream)
+                if t == 0 and delta:
+                    bank.append_broadcast(self.null, stream)
+                else:
+                    src = self.outputs.get(t, bank.rows[t])
+                    bank.append(src, plan.acc_from[t], stream)
                 appended += 1
             if t in run:
-                bank.route_fwd(plan.sites[t], self.H, self.q[t], self.g[t], self.out[t],
-                               self.lse[t], site_id=t, stream=stream)
+                if delta:
+                    bank.route_fwd_delta(plan.sites[t], self.H, self.q[t], self.g[t],
+                                         self.partial[t], self.alpha[t], self.out[t],
+                                         self.routed[t], self.lse[t], site_id=t, stream=stream)
+                else:
+                    bank.route_fwd(plan.sites[t], self.H, self.q[t], self.g[t], self.out[t],
+                                   self.lse[t], site_id=t, stream=stream)
                 if on_site:
                     on_site("fwd", t)
         return appended
@@ -176,11 +211,19 @@ class Microbatch:
         for t in reversed(plan.run_sites):
             if on_site:
                 on_site("bwd_begin", t)
-            bank.route_bwd(plan.sites[t], self.H, self.q[t], self.g[t], self.out[t], self.dout[t],
-                           self.lse[t], self.dq[t], self.dg[t] if self.g[t] is not None else None,
-                           site_id=t, stream=stream, ws=self.ws)
+            dg = self.dg[t] if self.g[t] is not None else None
+            if self.cfg.delta:
+                bank.route_bwd_delta(plan.sites[t], self.H, self.q[t], self.g[t], self.routed[t],
+                                     self.dout[t], self.lse[t], self.alpha[t], self.dq[t], dg,
+                                     self.dalpha[t], site_id=t, stream=stream, ws=self.ws)
+            else:
+                bank.route_bwd(plan.sites[t], self.H, self.q[t], self.g[t], self.out[t],
+                               self.dout[t], self.lse[t], self.dq[t], dg, site_id=t,
+                               stream=stream, ws=self.ws)
             if on_site:
                 on_site("bwd_end", t)
+        if self.cfg.delta:
+            bank.grad_token_sum(0, self.dnull, stream)   # the null source's gradient
 
     def step(self, stream=None):
         self.forward(stream)
@@ -188,4 +231,4 @@ class Microbatch:
 
     def kernel_launches(self) -> int:
         """Kernels one step launches: appends, forwards, backward + reduce per site."""
-        return self.n_rows + 3 * len(self.plan.run_sites)
+        return self.n_rows + 3 * len(self.plan.run_sites) + (1 if self.cfg.delta else 0)

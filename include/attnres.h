@@ -181,8 +181,33 @@ ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
                        const float *q, const float *g, void *out, float *lse,
                        int32_t site_id, void *stream);
 
-/* Bytes of device workspace ar_route_bwd needs for this bank and H (the
- * per-block partial sums of dq/dg). Depends on the current device. */
+/*
+ * Forward of one routing site in the delta form of attention residuals:
+ *   out = partial + alpha * routed,   routed = the read of ar_route_fwd
+ * ("Multi-Head Attention Residuals", Sec. 3.3 "Identity-preserving
+ * conversion": h = partial + alpha * routed with a zero-initialised gate, so
+ * that alpha = 0 leaves the residual stream untouched; Appendix E, Figure 9:
+ * the fused kernel adds the residual stream in delta modes).
+ *   partial : device [T, d] of the bank dtype, the intact residual stream
+ *   alpha   : device float, the site's gate
+ *   out     : device [T, d] of the bank dtype (may not alias partial)
+ *   routed  : device [T, d] of the bank dtype; receives the routed mix, which
+ *             the backward needs
+ *   other arguments as ar_route_fwd. In the pages' mid-training setup the
+ *   sources are a per-call stack: a learnable null source
+ *   (ar_bank_append_broadcast) plus one delta per block.
+ * Errors: as ar_route_fwd; AR_ERR_INVALID_ARG for a null partial, alpha or
+ * routed; AR_ERR_UNSUPPORTED for shapes served by the one-warp sliced-key
+ * kernels (r < d with d not a multiple of 1024).
+ */
+ar_status ar_route_fwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                             const float *q, const float *g, const void *partial,
+                             const float *alpha, void *out, void *routed, float *lse,
+                             int32_t site_id, void *stream);
+
+/* Bytes of device workspace ar_route_bwd (and ar_route_bwd_delta) needs for
+ * this bank and H: per-warp (or per-block) partial sums of dq/dg and of
+ * dL/dalpha. Depends on the current device. */
 ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes);
 
 /*
@@ -226,6 +251,22 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
 ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, void *stream);
 
 /*
+ * Merge two partial reads of one site over disjoint source sets A and B into
+ * the read over A u B, per head, by the online-softmax update:
+ *   lse = log(e^lse_A + e^lse_B),
+ *   out = e^(lse_A - lse) out_A + e^(lse_B - lse) out_B   on the head's slice.
+ * This is the merge of two-phase block inference ("Low-Rank Attention
+ * Residuals", Sec. 3.4: input-independent queries let the inter-block reads
+ * of a whole block be done first; each site's intra-block read is merged in).
+ *   out_a, out_b, out : device [T, d] of the bank dtype (out may alias either)
+ *   lse_a, lse_b, lse : device float [T, H] (lse may alias either)
+ * The bank supplies T, d and the dtype only. Errors: AR_ERR_INVALID_ARG,
+ * AR_ERR_SHAPE (d % H), AR_ERR_ALIGN, AR_ERR_CUDA.
+ */
+ar_status ar_route_merge(const ar_bank *bank, int32_t H, const void *out_a, const float *lse_a,
+                         const void *out_b, const float *lse_b, void *out, float *lse, void *stream);
+
+/*
  * Block schedule of LR-AttnRes (Figure 11): M sublayers in NB blocks whose
  * last sublayers are ceil(M*j/NB); NB <= 0 or NB >= M means full routing.
  * Bank row 0 is the embedding; row t (1..M) is the partial sum after
@@ -240,6 +281,43 @@ ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, voi
  */
 ar_status ar_block_schedule(int32_t M, int32_t NB, int32_t *acc_from, int32_t *site_ptr,
                             int32_t *site_rows, int64_t site_rows_cap, int64_t *site_rows_len);
+
+/*
+ * Backward of ar_route_fwd_delta. With G = dL/dout: the routed mix receives
+ * alpha * G, so the source gradients, dq and dg are those of ar_route_bwd for
+ * upstream gradient alpha * G; dL/dalpha = sum over tokens of <G, routed>; and
+ * dL/dpartial = G (the caller uses dout directly, nothing is computed).
+ *   routed : device [T, d], written by this site's forward
+ *   alpha  : device float, the gate the forward used
+ *   dalpha : device float, overwritten with dL/dalpha
+ *   other arguments as ar_route_bwd (same workspace size). In the pages'
+ *   per-call form every call owns fresh gradient rows: call ar_bank_zero_grad
+ *   (or use a bank per call) before it, so that every row is stored, not
+ *   accumulated.
+ * Errors: as ar_route_bwd; AR_ERR_INVALID_ARG for a null alpha or dalpha.
+ */
+ar_status ar_route_bwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                             const float *q, const float *g, const void *routed,
+                             const void *dout, const float *lse, const float *alpha, float *dq,
+                             float *dg, float *dalpha, void *ws, size_t ws_bytes, int32_t site_id,
+                             void *stream);
+
+/*
+ * Append a row that holds the same vector for every token (the learnable null
+ * source of the delta form, "Multi-Head Attention Residuals", Sec. 3.3), and
+ * cache its inverse RMS.
+ *   vec : device [d] of the bank dtype. Errors as ar_bank_append.
+ */
+ar_status ar_bank_append_broadcast(ar_bank *bank, const void *vec, int32_t *out_row, void *stream);
+
+/*
+ * out[c] = sum over tokens of the gradient row `row` (the gradient of a
+ * broadcast source such as the null source), in a fixed summation order.
+ *   out : device float [d], overwritten (zeros if the row was not written
+ *         since ar_bank_zero_grad). Errors: AR_ERR_INVALID_ARG, AR_ERR_ALIGN,
+ *         AR_ERR_CUDA.
+ */
+ar_status ar_bank_grad_token_sum(const ar_bank *bank, int32_t row, float *out, void *stream);
 
 /*
  * ar_route_bwd_noalloc: ar_route_bwd with no caller workspace. There is no

@@ -155,5 +155,26 @@ def route_bwd(sources, q, g, dout, H: int, r: int | None = None, eps: float = 1e
     return dsrc, dq, dg
 
 
+def route_fwd_delta(sources, q, g, H: int, partial, alpha: float, r: int | None = None,
+                    eps: float = 1e-6, full_width: bool = False):
+    """Delta form of one site ("Multi-Head Attention Residuals", Sec. 3.3,
+    identity-preserving conversion): h = partial + alpha * routed.
+    Returns ``(h, routed, lse)``."""
+    routed, lse = route_fwd(sources, q, g, H, r=r, eps=eps, full_width=full_width)
+    return _f64(partial) + float(alpha) * routed, routed, lse
+
+
+def route_bwd_delta(sources, q, g, dout, H: int, alpha: float, r: int | None = None,
+                    eps: float = 1e-6, full_width: bool = False, dsrc=None):
+    """Backward of ``route_fwd_delta``: the routed read receives alpha * dout.
+    Returns ``(dsrc, dq, dg, dalpha, dpartial)`` with dalpha = sum <dout, routed>
+    and dpartial = dout."""
+    G = _f64(dout)
+    routed, _ = route_fwd(sources, q, g, H, r=r, eps=eps, full_width=full_width)
+    dsrc, dq, dg = route_bwd(sources, q, g, float(alpha) * G, H, r=r, eps=eps,
+                             full_width=full_width, dsrc=dsrc)
+    return dsrc, dq, dg, float(np.sum(G * routed)), G
+
+
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))

@@ -109,10 +109,16 @@ def test_route_argument_checks_precede_launch(B):
     assert _err(B.ar_route_fwd, h, [0], 64, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
     assert _err(B.ar_route_fwd, h, [0], 4, None, None, FAKE, FAKE, 1, 0) == "AR_ERR_INVALID_ARG"
     B.ar_bank_destroy(h)
-    for d, r in ((4096, 4096), (1024, 768), (8192, 1024), (1000, 1000)):
+    for d, r, H in ((4096, 4096, 2), (1024, 768, 8), (8192, 1024, 8), (1000, 1000, 8),
+                    (16384, 16384, 8), (512, 256, 64)):
         h = _bank(B, d=d, r=r)
-        assert _err(B.ar_route_fwd, h, [0], 8, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
+        assert _err(B.ar_route_fwd, h, [0], H, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
         B.ar_bank_destroy(h)
+    # the delta form is served by the full-key and four-warp kernels only
+    h = _bank(B, d=1280, r=256)
+    assert _err(B.ar_route_fwd_delta, h, [0], 8, q, None, FAKE, FAKE, FAKE, FAKE, FAKE, 1,
+                0) == "AR_ERR_INVALID_ARG"   # nothing appended yet
+    B.ar_bank_destroy(h)
 
 
 def test_failed_append_leaves_bank_unchanged_without_gpu(B):

@@ -1,0 +1,73 @@
+"""Two-phase block inference ("Low-Rank Attention Residuals", Sec. 3.4): each
+site's read is split into the inter-block part (embedding + completed block
+sums, all available when the block starts) and the intra-block part (the
+current partial sum); ar_route_merge combines the two by their per-head
+log-sum-exp. The merged read must equal the oracle's read over all the site's
+sources."""
+
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from depth_wise_attention_ar_gb300 import build
+    build.build()
+    from depth_wise_attention_ar_gb300 import binding
+    return binding
+
+
+def _t64(t):
+    import torch
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def _nmax(x, ref):
+    return float(np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+@pytest.mark.parametrize("d,r,H,dtype", [(512, 512, 4, "f32"), (1024, 256, 4, "bf16"),
+                                         (4096, 1024, 8, "bf16")])
+def test_two_phase_block_read_equals_single_read(B, orc, d, r, H, dtype):
+    import torch
+    from oracle import schedule, storage
+    T, M, NB = 200, 12, 3
+    acc, sites = B.ar_block_schedule(M, NB)
+    inp = synth.HostInputs(seed=17, q_std=0.8, g_kind="random")
+    bank = B.Bank(T, d, r, M + 1, dtype)
+    for t in range(M + 1):
+        o = inp.output(t, T, d, dtype)
+        if acc[t] < 0:
+            bank.rows[t].copy_(o)
+            bank.append(bank.rows[t])
+        else:
+            bank.append(o, acc[t])
+    ref_rows = storage.block_bank([inp.host_output(t, T, d, dtype) for t in range(M + 1)],
+                                  schedule.block_plan(M, NB), dtype)
+    tol = 1e-5 if dtype == "f32" else 2e-2
+    checked = 0
+    for t in range(1, M + 1):
+        rows = sites[t]
+        if t in schedule.block_ends(M, NB):
+            continue              # right after a block end there is no partial sum
+        inter, partial = rows[:-1], rows[-1]
+        q, g = inp.query(t, r), inp.norm_weight(t, r)
+        out_a, lse_a = bank.route_fwd(inter, H, q, g, site_id=t)
+        out_b, lse_b = bank.route_fwd([partial], H, q, g, site_id=t)
+        out = torch.empty_like(out_a)
+        lse = torch.empty_like(lse_a)
+        B.ar_route_merge(bank.handle, H, out_a, lse_a, out_b, lse_b, out, lse)
+        torch.cuda.synchronize()
+        ref_out, ref_lse = orc.route_fwd([ref_rows[j] for j in rows], inp.host_query(t, r),
+                                         inp.host_norm_weight(t, r), H, r=r)
+        assert _nmax(_t64(out), ref_out) < tol, t
+        assert _nmax(_t64(lse), ref_lse) < tol, t
+        checked += 1
+    assert checked >= 6

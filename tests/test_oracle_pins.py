@@ -327,3 +327,55 @@ def _exact_block_rows(outs, plan, t):
         else:
             rows.append(rows[op[1]] + outs[op[2]])
     return rows
+
+
+def test_delta_form_closed_gate_is_identity(orc):
+    """alpha = 0: the delta form returns the residual stream exactly (the
+    identity-preserving conversion of the MHAR page, Sec. 3.3); its dalpha is
+    <dout, routed> summed, the source gradients vanish and dpartial = dout."""
+    srcs, q, g, G = _case(40, 4, 6, 16, 4, 16)
+    P = synth.misc_normal(40, 99, (6, 16)).astype(np.float64)
+    h, routed, lse = orc.route_fwd_delta(srcs, q, g, 4, P, 0.0)
+    assert np.array_equal(h, P)
+    ds, dq, dg, dalpha, dpart = orc.route_bwd_delta(srcs, q, g, G, 4, 0.0)
+    assert all(np.all(x == 0) for x in ds) and np.all(dq == 0) and np.all(dg == 0)
+    assert abs(dalpha - float(np.sum(G * routed))) == 0.0 and np.array_equal(dpart, G)
+
+
+def test_delta_form_matches_autograd_and_finite_differences(orc):
+    import torch
+    from oracle import torch_route
+    srcs, q, g, G = _case(41, 5, 7, 32, 4, 16)
+    P = synth.misc_normal(41, 98, (7, 32)).astype(np.float64)
+    alpha = 0.37
+    ds, dq, dg, dalpha, dpart = orc.route_bwd_delta(srcs, q, g, G, 4, alpha, r=16)
+    V = [torch.tensor(s_, requires_grad=True) for s_ in srcs]
+    tq, tg = torch.tensor(q, requires_grad=True), torch.tensor(g, requires_grad=True)
+    ta, tp = torch.tensor(alpha, dtype=torch.float64, requires_grad=True), torch.tensor(P, requires_grad=True)
+    h = tp + ta * torch_route.route(V, tq, tg, 4, r=16)
+    (h * torch.tensor(G)).sum().backward()
+    for n in range(5):
+        assert _nmax(ds[n], V[n].grad.numpy()) < 1e-11
+    assert _nmax(dq, tq.grad.numpy()) < 1e-10 and _nmax(dg, tg.grad.numpy()) < 1e-10
+    assert abs(dalpha - ta.grad.item()) < 1e-10 * max(1.0, abs(dalpha))
+    assert np.array_equal(dpart, G)
+    eps = 1e-6
+    hp, _, _ = orc.route_fwd_delta(srcs, q, g, 4, P, alpha + eps, r=16)
+    hm, _, _ = orc.route_fwd_delta(srcs, q, g, 4, P, alpha - eps, r=16)
+    fd = float(np.sum((hp - hm) * G)) / (2 * eps)
+    assert abs(fd - dalpha) <= 1e-6 * max(1.0, abs(fd))
+
+
+def test_lse_merge_of_disjoint_source_sets(orc):
+    """The read over A u B is the log-sum-exp merge of the reads over A and B,
+    per head (the online-softmax update two-phase inference relies on)."""
+    srcs, q, g, _ = _case(42, 7, 5, 16, 4, 16, qstd=1.5)
+    oa, la = orc.route_fwd(srcs[:4], q, g, 4)
+    ob, lb = orc.route_fwd(srcs[4:], q, g, 4)
+    o, l = orc.route_fwd(srcs, q, g, 4)
+    lse = np.logaddexp(la, lb)
+    K = 4
+    wa = np.repeat(np.exp(la - lse), K, axis=1)
+    wb = np.repeat(np.exp(lb - lse), K, axis=1)
+    assert _nmax(lse, l) < 1e-14
+    assert _nmax(wa * oa + wb * ob, o) < 1e-13
