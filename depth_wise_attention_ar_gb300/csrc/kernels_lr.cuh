@@ -7,8 +7,9 @@
 //   sweep 1: the key tails of the N listed rows (r coordinates each) land in a
 //            per-warp shared-memory cache by 1-D bulk copies; every head's
 //            scores, softmax weights and lse follow from the cache;
-//   sweep 2: the value rows are mixed in column blocks of CW = 256*CPB
-//            columns with those weights: blocks left of the tail stream through
+//   sweep 2: the value rows are mixed in column blocks of CW columns (at most
+//            1024; CW divides both d - r and r) with those weights: blocks left
+//            of the tail stream through
 //            a ring of shared-memory stages, tail blocks come from the cache,
 //            so every source coordinate is read from HBM once.
 //   The cache is double-buffered: the next token's key tails are requested as
@@ -31,19 +32,21 @@ namespace ar {
 constexpr int kLrFwdStages = 4;
 constexpr int kLrBwdStages = 2;
 
-// Column-block width in chunks per lane: the largest of 4, 2, 1 that divides
-// both the non-key width and the key width (in units of 256 columns).
-__host__ __device__ inline int lr_cpb(int d, int r)
+// Column-block width of the mixing sweep: the largest multiple of 8 columns,
+// at most 1024, that divides both the non-key width d - r and the key width r
+// (blocks never straddle the start of the key tail).
+__host__ __device__ inline int lr_block_cols(int d, int r)
 {
-    const int a = (d - r) / 256, b = r / 256;
-    for (int c = 4; c > 1; c >>= 1)
-        if (a % c == 0 && b % c == 0) return c;
-    return 1;
+    int x = d - r, y = r;
+    while (y) { const int t = x % y; x = y; y = t; }   // gcd(d - r, r) (= r when r = d)
+    for (int c = 1024; c >= 8; c -= 8)
+        if (x % c == 0) return c;
+    return 8;
 }
 
 inline size_t lr_fwd_smem_bytes(int d, int r, int N, int H, size_t esize)
 {
-    const size_t cw = (size_t)256 * lr_cpb(d, r);
+    const size_t cw = (size_t)lr_block_cols(d, r);
     return 2 * (size_t)N * r * esize            // key cache, double-buffered
            + (size_t)kLrFwdStages * cw * esize  // value ring
            + 2 * (size_t)N * H * 4              // scores, weights
@@ -51,7 +54,7 @@ inline size_t lr_fwd_smem_bytes(int d, int r, int N, int H, size_t esize)
            + (size_t)AR_MAX_SOURCES * 4 * 2;    // inverse RMS (current, next)
 }
 
-template <typename T, int KCPL>
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant__ RouteArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -61,8 +64,8 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
     const int lane = threadIdx.x;
     const int d = a.d, r = a.r, N = a.n_src, H = a.H;
     const int64_t TT = a.T;
-    const int cpb = lr_cpb(d, r);
-    const int CW = 256 * cpb;                       // columns per block
+    const int CW = lr_block_cols(d, r);             // columns per block
+    const int cwc = CW / 8;                         // chunks per block
     const uint32_t eb = (uint32_t)sizeof(T);
     const uint32_t key_bytes = (uint32_t)r * eb, blk_bytes = (uint32_t)CW * eb;
     const int nblk_v = (d - r) / CW, nblk_k = r / CW;  // value-only and tail blocks
@@ -86,16 +89,20 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
     const int LPH = 32 / H;
     const int h = lane / LPH, sub = lane - h * LPH;
     const int K = d / H;                            // value slice width
-    // key chunks of this lane (relative to the first key coordinate)
-    int kidx[KCPL];
-    float qg[KCPL][8];
+    // key chunks of this lane (relative to the first key coordinate): chunk
+    // sub + LPH*j of its head's r/(8H) key chunks, where that exists
+    const int ckh = r / 8 / H;
+    int kidx[KMAX];
+    bool kval[KMAX];
+    float qg[KMAX][8];
 #pragma unroll
-    for (int j = 0; j < KCPL; ++j) {
-        kidx[j] = h * (KCPL * LPH) + sub + LPH * j;
+    for (int j = 0; j < KMAX; ++j) {
+        kval[j] = sub + LPH * j < ckh;
+        kidx[j] = h * ckh + sub + LPH * j;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = kidx[j] * 8 + e;
-            qg[j][e] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f);
+            qg[j][e] = kval[j] ? __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) : 0.f;
         }
     }
 
@@ -167,11 +174,12 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
             const T *kr = reinterpret_cast<const T *>(keys + (size_t)n * key_bytes);
             float zr = 0.f;
 #pragma unroll
-            for (int j = 0; j < KCPL; ++j) {
-                float v[8];
-                ld_chunk_s(kr + kidx[j] * 8, v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) zr = fmaf(qg[j][e], v[e], zr);
+            for (int j = 0; j < KMAX; ++j) {
+                if (kval[j]) {
+                    float v[8];
+                    ld_chunk_s(kr + kidx[j] * 8, v);
+                    zr = __fadd_rn(zr, dot8(qg[j], v));
+                }
             }
             zr = group_sum(zr, LPH);
             if (sub == 0) zs[n * H + h] = __fmul_rn(zr, cinv[n]);
@@ -213,8 +221,8 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    if (j < cpb) {
-                        const int c = lane + 32 * j;               // chunk within the block
+                    const int c = lane + 32 * j;                   // chunk within the block
+                    if (c < cwc) {
                         const int col = b * CW + c * 8;
                         const float wn = ws[n * H + col / K];
                         float v[8];
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
             if (!ok) break;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if (j < cpb) st_chunk_g(orow + b * CW + (lane + 32 * j) * 8, acc[j]);
+                if (lane + 32 * j < cwc) st_chunk_g(orow + b * CW + (lane + 32 * j) * 8, acc[j]);
         }
     }
     if (!ok) {
@@ -255,7 +263,7 @@ inline size_t lr_bwd_smem_bytes(int d, size_t esize)
            + (size_t)kLrBwdStages * 8 + (size_t)AR_MAX_SOURCES * 4;
 }
 
-template <typename T, int KCPL>
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant__ RouteArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -285,15 +293,18 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
     const int h = lane / LPH, sub = lane - h * LPH;
     const int cpl = d / 256;                        // value chunks per lane
     const int key0 = (d - r) / 8;                   // first key chunk
-    int kidx[KCPL];
-    float qg[KCPL][8], U[KCPL][8];
+    const int ckh = r / 8 / H;                      // key chunks per head
+    int kidx[KMAX];
+    bool kval[KMAX];
+    float qg[KMAX][8], U[KMAX][8];
 #pragma unroll
-    for (int j = 0; j < KCPL; ++j) {
-        kidx[j] = key0 + h * (KCPL * LPH) + sub + LPH * j;
+    for (int j = 0; j < KMAX; ++j) {
+        kval[j] = sub + LPH * j < ckh;
+        kidx[j] = key0 + h * ckh + sub + LPH * j;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = (kidx[j] - key0) * 8 + e;
-            qg[j][e] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f);
+            qg[j][e] = kval[j] ? __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) : 0.f;
             U[j][e] = 0.f;
         }
     }
@@ -383,11 +394,12 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
             for (int e = 0; e < 8; ++e) P = fmaf(gv[e], v[e], P);
         }
 #pragma unroll
-        for (int j = 0; j < KCPL; ++j) {
-            float v[8];
-            ld_chunk_s(V + kidx[j] * 8, v);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) zr = fmaf(qg[j][e], v[e], zr);
+        for (int j = 0; j < KMAX; ++j) {
+            if (kval[j]) {
+                float v[8];
+                ld_chunk_s(V + kidx[j] * 8, v);
+                zr = __fadd_rn(zr, dot8(qg[j], v));
+            }
         }
         P = group_sum(P, LPH);
         zr = group_sum(zr, LPH);
@@ -400,7 +412,8 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 
         // pass B: key-path terms on the tail, into the staged gradient row
 #pragma unroll
-        for (int j = 0; j < KCPL; ++j) {
+        for (int j = 0; j < KMAX; ++j) {
+            if (!kval[j]) continue;
             float v[8], nv[8];
             ld_chunk_s(V + kidx[j] * 8, v);
             if (first) {
@@ -457,26 +470,27 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
     }
     float *wrow = a.ws + gw * r;
 #pragma unroll
-    for (int j = 0; j < KCPL; ++j) st_f32x8_g(wrow + (kidx[j] - key0) * 8, U[j]);
+    for (int j = 0; j < KMAX; ++j)
+        if (kval[j]) st_f32x8_g(wrow + (kidx[j] - key0) * 8, U[j]);
 }
 
-template <typename T, int KCPL>
+template <typename T, int KMAX>
 cudaError_t launch_lr_fwd_inst(const RouteArgs &a, cudaStream_t s)
 {
-    const void *k = reinterpret_cast<const void *>(&route_fwd_lr_kernel<T, KCPL>);
+    const void *k = reinterpret_cast<const void *>(&route_fwd_lr_kernel<T, KMAX>);
     const size_t smem = lr_fwd_smem_bytes(a.d, a.r, a.n_src, a.H, sizeof(T));
     if (smem > 200 * 1024) return cudaErrorNotSupported;
     int grid = 0;
     cudaError_t e = persistent_grid(k, 32, smem, &grid);
     if (e != cudaSuccess) return e;
-    route_fwd_lr_kernel<T, KCPL><<<grid, 32, smem, s>>>(a);
+    route_fwd_lr_kernel<T, KMAX><<<grid, 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-template <typename T, int KCPL>
+template <typename T, int KMAX>
 cudaError_t lr_bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_warps)
 {
-    const void *k = reinterpret_cast<const void *>(&route_bwd_lr_kernel<T, KCPL>);
+    const void *k = reinterpret_cast<const void *>(&route_bwd_lr_kernel<T, KMAX>);
     const size_t smem = lr_bwd_smem_bytes(a->d, sizeof(T));
     int grid = 0;
     cudaError_t e = persistent_grid(k, 32, smem, &grid);
@@ -485,34 +499,34 @@ cudaError_t lr_bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_warps)
         *grid_warps = grid;
         return cudaSuccess;
     }
-    route_bwd_lr_kernel<T, KCPL><<<grid, 32, smem, s>>>(*a);
+    route_bwd_lr_kernel<T, KMAX><<<grid, 32, smem, s>>>(*a);
     return cudaGetLastError();
 }
 
-// Sliced keys: r = 256 * KCPL with KCPL in {1, 2, 4, 8}, r < d <= 4096,
-// d a multiple of 256.
+// Key chunks per lane (at most): ceil(r / 256). Served: r a multiple of 8 with
+// r/H a multiple of 8, r <= d <= 4096 with d a multiple of 256.
+__host__ __device__ inline int lr_kmax(int r) { return (r + 255) / 256; }
+
+#define AR_LR_KMAX_CASES(X) X(1) X(2) X(3) X(4) X(5) X(6) X(8) X(10) X(12) X(14) X(16)
+
 template <typename T>
 cudaError_t dispatch_lr_fwd(const RouteArgs &a, cudaStream_t s)
 {
-    switch (a.r / 256) {
-    case 1: return launch_lr_fwd_inst<T, 1>(a, s);
-    case 2: return launch_lr_fwd_inst<T, 2>(a, s);
-    case 4: return launch_lr_fwd_inst<T, 4>(a, s);
-    case 8: return launch_lr_fwd_inst<T, 8>(a, s);
-    default: return cudaErrorNotSupported;
-    }
+    const int km = lr_kmax(a.r);
+#define AR_CASE(K) if (km <= K) return launch_lr_fwd_inst<T, K>(a, s);
+    AR_LR_KMAX_CASES(AR_CASE)
+#undef AR_CASE
+    return cudaErrorNotSupported;
 }
 
 template <typename T>
 cudaError_t dispatch_lr_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps)
 {
-    switch (a->r / 256) {
-    case 1: return lr_bwd_inst<T, 1>(a, s, grid_warps);
-    case 2: return lr_bwd_inst<T, 2>(a, s, grid_warps);
-    case 4: return lr_bwd_inst<T, 4>(a, s, grid_warps);
-    case 8: return lr_bwd_inst<T, 8>(a, s, grid_warps);
-    default: return cudaErrorNotSupported;
-    }
+    const int km = lr_kmax(a->r);
+#define AR_CASE(K) if (km <= K) return lr_bwd_inst<T, K>(a, s, grid_warps);
+    AR_LR_KMAX_CASES(AR_CASE)
+#undef AR_CASE
+    return cudaErrorNotSupported;
 }
 
 }  // namespace ar

@@ -301,13 +301,13 @@ enum class Family { kFull, kCoop, kSliced, kNone };
 
 static Family family_of(int d, int r, int H)
 {
-    if (H < 1 || d <= 0 || r <= 0 || r > d || d % 256 != 0 || r % 256 != 0) return Family::kNone;
+    if (H < 1 || d <= 0 || r <= 0 || r > d || d % 256 != 0 || r % 8 != 0) return Family::kNone;
     const bool pow2_h = H <= 32 && (32 % H) == 0;
     if (r == d && d <= 2048 && pow2_h) return Family::kFull;
-    if (coop_supported(d, r, H)) return Family::kCoop;
-    const int kcpl = r / 256;
-    if (r < d && d <= 4096 && pow2_h && (kcpl == 1 || kcpl == 2 || kcpl == 4 || kcpl == 8))
-        return Family::kSliced;
+    if (r % 256 == 0 && coop_supported(d, r, H)) return Family::kCoop;
+    // one warp per token, two sweeps: any key width with whole 8-column chunks
+    // per head (r = d included, for widths the other families leave out)
+    if (d <= 4096 && pow2_h && (r / H) % 8 == 0 && (r + 255) / 256 <= 16) return Family::kSliced;
     return Family::kNone;
 }
 

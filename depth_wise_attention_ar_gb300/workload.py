@@ -56,6 +56,10 @@ CONFIGS = {
                  note="d=1280, L=36: 73 sites"),
     "lr_block": Config("lr_block", T=8192, d=4096, H=8, r=1024, dtype="bf16", M=64, NB=8,
                        note="32 layers in 8 blocks, keys = last 1024 coordinates"),
+    "lr_page_1b": Config("lr_page_1b", T=2 * 2048, d=1536, H=1, r=384, dtype="bf16", M=48, NB=8,
+                         note="the LR page's 1B model: 24 layers, 8 blocks, r = d/4, one head"),
+    "lr_page_4b": Config("lr_page_4b", T=2 * 2048, d=2560, H=1, r=640, dtype="bf16", M=88, NB=8,
+                         note="the LR page's 4B model: 44 layers, 8 blocks, r = d/4, one head"),
     "delta_8b": Config("delta_8b", T=2 * 4096, d=4096, H=8, r=4096, dtype="bf16", M=64, NB=8,
                        delta=True,
                        note="delta form of the 8B mid-training model: null source + 8 block "

@@ -157,6 +157,19 @@ def test_wide_rows_four_warp_kernels(W, orc, d, r, H, dtype):
     run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
 
 
+@pytest.mark.parametrize("d,r,H,dtype", [(1536, 384, 1, "bf16"), (2560, 640, 1, "bf16"),
+                                         (2560, 2560, 1, "bf16"), (1536, 384, 8, "f32"),
+                                         (2560, 640, 8, "bf16"), (1024, 128, 4, "bf16"),
+                                         (3584, 896, 2, "bf16")])
+def test_low_rank_page_shapes(W, orc, d, r, H, dtype):
+    """Key widths that are not multiples of 256 (the LR page's 1B and 4B models:
+    d = 1536, r = 384 and d = 2560, r = 640, single-head) and r = d at widths the
+    other kernel families leave out."""
+    _, wl = W
+    cfg = small(wl, "lrp", T=113, d=d, H=H, dtype=dtype, M=6, NB=2, r=r)
+    run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
+
+
 def test_single_source_site_is_identity(W, orc):
     import torch
     B, wl = W
