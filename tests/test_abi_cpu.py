@@ -109,7 +109,7 @@ def test_route_argument_checks_precede_launch(B):
     assert _err(B.ar_route_fwd, h, [0], 64, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
     assert _err(B.ar_route_fwd, h, [0], 4, None, None, FAKE, FAKE, 1, 0) == "AR_ERR_INVALID_ARG"
     B.ar_bank_destroy(h)
-    for d, r, H in ((4096, 4096, 2), (1024, 760, 8), (8192, 1024, 8), (1000, 1000, 8),
+    for d, r, H in ((8192, 8192, 2), (1024, 760, 8), (8192, 1024, 8), (1000, 1000, 8),
                     (16384, 16384, 8), (512, 256, 64)):
         h = _bank(B, d=d, r=r)
         assert _err(B.ar_route_fwd, h, [0], H, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
