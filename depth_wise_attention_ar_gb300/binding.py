@@ -30,6 +30,15 @@ AR_DEVERR_WAIT_TIMEOUT = 1
 _P, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 _I32P, _I64P, _U32P, _SZP = (ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
                              ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_size_t))
+class ArSite(ctypes.Structure):
+    """struct ar_site: a routing site with strided query / norm weight."""
+    _fields_ = [("rows", ctypes.POINTER(ctypes.c_int32)), ("n_src", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("q", ctypes.c_void_p), ("q_stride", ctypes.c_int64),
+                ("g", ctypes.c_void_p), ("g_stride", ctypes.c_int64),
+                ("site_id", ctypes.c_int32)]
+
+
+_SITEP = ctypes.POINTER(ArSite)
 SIGNATURES = {
     "ar_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "ar_inv_rms_floats": ([_I64, _I32, _I64P], ctypes.c_int),
@@ -39,6 +48,9 @@ SIGNATURES = {
     "ar_bank_row_count": ([_P, _I32P], ctypes.c_int),
     "ar_bank_row_ptr": ([_P, _I32, ctypes.POINTER(_P)], ctypes.c_int),
     "ar_bank_append": ([_P, _P, _I32, _I32P, _P], ctypes.c_int),
+    "ar_bank_append_strided": ([_P, _P, _I64, _I64, _I32, _I32P, _P], ctypes.c_int),
+    "ar_route_fwd_site": ([_P, _SITEP, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "ar_route_bwd_site": ([_P, _SITEP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "ar_bank_zero_grad": ([_P], ctypes.c_int),
     "ar_bank_reset": ([_P], ctypes.c_int),
     "ar_route_fwd": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _I32, _P], ctypes.c_int),
@@ -144,6 +156,42 @@ def ar_bank_append(bank, src, accumulate_from: int = -1, stream=None) -> int:
     _check("ar_bank_append", _lib.ar_bank_append(bank, _ptr(src), accumulate_from,
                                                  ctypes.byref(row), _stream(stream)))
     return row.value
+
+
+def ar_bank_append_strided(bank, src, token_stride: int, elem_stride: int,
+                           accumulate_from: int = -1, stream=None) -> int:
+    row = ctypes.c_int32(-1)
+    _check("ar_bank_append_strided",
+           _lib.ar_bank_append_strided(bank, _ptr(src), token_stride, elem_stride,
+                                       accumulate_from, ctypes.byref(row), _stream(stream)))
+    return row.value
+
+
+def make_site(rows, H, q, g=None, site_id=0, q_stride=None, g_stride=None):
+    """An ArSite (plus the row array it points to, which must stay alive).
+    Strides default to those of the q / g tensors."""
+    arr, n = _rows(rows)
+    qs = q_stride if q_stride is not None else (q.stride(0) if isinstance(q, torch.Tensor) else 1)
+    gs = g_stride if g_stride is not None else (
+        g.stride(0) if isinstance(g, torch.Tensor) else 1)
+    site = ArSite(ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32)), n, H, _ptr(q), qs, _ptr(g),
+                  gs, site_id)
+    site._keep = arr
+    return site
+
+
+def ar_route_fwd_site(bank, site: ArSite, partial, alpha, out, routed, lse, stream=None):
+    _check("ar_route_fwd_site", _lib.ar_route_fwd_site(bank, ctypes.byref(site), _ptr(partial),
+                                                       _ptr(alpha), _ptr(out), _ptr(routed),
+                                                       _ptr(lse), _stream(stream)))
+
+
+def ar_route_bwd_site(bank, site: ArSite, out, dout, lse, alpha, dq, dg, dalpha, ws, ws_bytes,
+                      stream=None):
+    _check("ar_route_bwd_site", _lib.ar_route_bwd_site(bank, ctypes.byref(site), _ptr(out),
+                                                       _ptr(dout), _ptr(lse), _ptr(alpha),
+                                                       _ptr(dq), _ptr(dg), _ptr(dalpha), _ptr(ws),
+                                                       ws_bytes, _stream(stream)))
 
 
 def ar_bank_zero_grad(bank):
@@ -294,6 +342,11 @@ class Bank:
         return self.rows[row]
 
     def append(self, src: torch.Tensor, accumulate_from: int = -1, stream=None) -> int:
+        """Append a [T, d] source; a strided view goes through ar_bank_append_strided."""
+        if isinstance(src, torch.Tensor) and not src.is_contiguous() and src.dim() == 2:
+            self._check_tensor(src, (self.T, self.d), self.torch_dtype, "src", contiguous=False)
+            return ar_bank_append_strided(self.handle, src, src.stride(0), src.stride(1),
+                                          accumulate_from, stream)
         self._check_tensor(src, (self.T, self.d), self.torch_dtype, "src")
         return ar_bank_append(self.handle, src, accumulate_from, stream)
 
@@ -315,10 +368,14 @@ class Bank:
             lse = torch.empty((self.T, H), dtype=torch.float32, device=dev)
         self._check_tensor(out, (self.T, self.d), self.torch_dtype, "out")
         self._check_tensor(lse, (self.T, H), torch.float32, "lse")
-        self._check_tensor(q, (self.r,), torch.float32, "q")
+        self._check_tensor(q, (self.r,), torch.float32, "q", contiguous=False)
         if g is not None:
-            self._check_tensor(g, (self.r,), torch.float32, "g")
-        ar_route_fwd(self.handle, rows, H, q, g, out, lse, site_id, stream)
+            self._check_tensor(g, (self.r,), torch.float32, "g", contiguous=False)
+        if _strided(q, g):
+            ar_route_fwd_site(self.handle, make_site(rows, H, q, g, site_id), None, None, out,
+                              None, lse, stream)
+        else:
+            ar_route_fwd(self.handle, rows, H, q, g, out, lse, site_id, stream)
         return out, lse
 
     def route_fwd_delta(self, rows, H, q, g, partial, alpha, out=None, routed=None, lse=None,
@@ -371,28 +428,43 @@ class Bank:
     def route_bwd(self, rows, H, q, g, out, dout, lse, dq=None, dg=None, site_id=0,
                   stream=None, ws=None):
         dev = self.rows.device
-        if dq is None:
-            dq = torch.empty(self.r, dtype=torch.float32, device=dev)
+        strided = _strided(q, g)
+        if dq is None:  # laid out like q (dq is written with q's stride)
+            dq = torch.empty_strided((self.r,), (q.stride(0),), dtype=torch.float32, device=dev)
         if dg is None and g is not None:
-            dg = torch.empty(self.r, dtype=torch.float32, device=dev)
+            dg = torch.empty_strided((self.r,), (g.stride(0),), dtype=torch.float32, device=dev)
         for t, shape, dt, nm in ((out, (self.T, self.d), self.torch_dtype, "out"),
                                  (dout, (self.T, self.d), self.torch_dtype, "dout"),
-                                 (lse, (self.T, H), torch.float32, "lse"),
-                                 (q, (self.r,), torch.float32, "q"),
-                                 (dq, (self.r,), torch.float32, "dq")):
+                                 (lse, (self.T, H), torch.float32, "lse")):
             self._check_tensor(t, shape, dt, nm)
+        for t, ref, nm in ((q, q, "q"), (dq, q, "dq"), (g, g, "g"), (dg, g, "dg")):
+            if t is not None:
+                self._check_tensor(t, (self.r,), torch.float32, nm, contiguous=False)
+                if ref is not None and t.stride(0) != ref.stride(0):
+                    raise ValueError(f"{nm} must have the stride of {'q' if nm[-1] == 'q' else 'g'}")
         if ws is None:
             ws = self.workspace(H)
-        ar_route_bwd(self.handle, rows, H, q, g, out, dout, lse, dq, dg, ws, ws.numel() * 4,
-                     site_id, stream)
+        if strided:
+            ar_route_bwd_site(self.handle, make_site(rows, H, q, g, site_id), out, dout, lse, None,
+                              dq, dg, None, ws, ws.numel() * 4, stream)
+        else:
+            ar_route_bwd(self.handle, rows, H, q, g, out, dout, lse, dq, dg, ws, ws.numel() * 4,
+                         site_id, stream)
         return dq, dg
 
     @staticmethod
-    def _check_tensor(t, shape, dtype, name):
+    def _check_tensor(t, shape, dtype, name, contiguous=True):
         if not isinstance(t, torch.Tensor):
             raise TypeError(f"{name} must be a torch tensor")
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-        if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous():
-            raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}, "
-                             f"got {t.dtype} {tuple(t.shape)}")
+        if tuple(t.shape) != tuple(shape) or t.dtype != dtype or (contiguous and
+                                                                  not t.is_contiguous()):
+            raise ValueError(f"{name}: expected {'contiguous ' if contiguous else ''}{dtype} "
+                             f"{tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+        if not contiguous and any(st < 1 for st in t.stride()[-1:]):
+            raise ValueError(f"{name}: element stride must be positive")
+
+
+def _strided(q, g) -> bool:
+    return q.stride(0) != 1 or (g is not None and g.stride(0) != 1)

@@ -14,8 +14,8 @@ struct RouteArgs {
     const void *bank;      // rows [cap, T, d] of the storage dtype
     const float *inv;      // inverse RMS, token-major [T, inv_ld]
     float *grad;           // fp32 gradient rows [cap, T, d] (backward)
-    const float *q;        // [r]
-    const float *g;        // [r] or nullptr (= ones)
+    const float *q;        // [r], element stride q_stride
+    const float *g;        // [r], element stride g_stride, or nullptr (= ones)
     void *out;             // forward output [T, d]
     float *lse;            // [T, H]
     const void *fout;      // backward: forward output [T, d]
@@ -28,8 +28,13 @@ struct RouteArgs {
     void *routed;          // forward: also store the routed mix here, or nullptr
     float *dalpha;         // backward: dL/dalpha (device scalar), or nullptr
     int64_t T;
+    int64_t q_stride, g_stride;  // elements between consecutive entries of q, g
     int d, r, H, n_src, inv_ld, norm_full;
     int rows[AR_MAX_SOURCES];
+    // a row listed k > 1 times in a site enters once with log k added to its
+    // score (softmax over the list = softmax over distinct rows with weights k)
+    int has_bias;
+    float bias[AR_MAX_SOURCES];
     uint32_t first_mask[AR_MAX_SOURCES / 32];  // backward: bit n set = store (first touch)
 };
 
@@ -38,19 +43,28 @@ struct RouteArgs {
 cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
 cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
 cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps);
-cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, const float *g,
-                               float *dq, float *dg, float *dalpha, cudaStream_t s);
+// dq and dg are written with the strides of q and g respectively.
+cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, int64_t q_stride,
+                               const float *g, int64_t g_stride, float *dq, float *dg,
+                               float *dalpha, cudaStream_t s);
 cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const float *lb,
                          void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s);
 cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cudaStream_t s);
+// src is a strided [T, d] view: element (t, c) at src[t * ld + c * es]
+// (ld = 0: the same vector for every token).
 cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col,
                           int64_t T, int d, int r, int inv_ld, int norm_full, float eps,
-                          ar_dtype dt, cudaStream_t s, bool broadcast = false);
+                          ar_dtype dt, cudaStream_t s, int64_t ld, int64_t es);
 cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
                              bool dst_valid, cudaStream_t s);
 unsigned int *device_error_word();
-bool fused_shape_supported(int d, int r, int H);
-bool delta_supported(int d, int r, int H);
+// Some kernel family serves n_src distinct rows at this shape.
+bool route_supported(int d, int r, int H, int n_src, ar_dtype dt);
+// The family serving one source may hand sites with many sources to the
+// scalar-access kernels (whose workspace differs).
+bool may_fall_back_to_generic(int d, int r, int H, ar_dtype dt);
+// Workspace rows (warps) of the scalar-access backward on the current device.
+cudaError_t generic_bwd_rows(int *rows);
 
 // Shapes of the four-warp kernels: d = 1024 * CPL (CPL in 1..8), H a multiple
 // of 4 with H/4 heads per warp a power of two <= 32; r = d, or r = k * d/4

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -50,27 +51,54 @@ ar_status check_site(const ar_bank *b, const int32_t *rows, int32_t n_src, int32
     if (!b || !rows || !q) return AR_ERR_INVALID_ARG;
     if (n_src < 1 || n_src > AR_MAX_SOURCES) return AR_ERR_INVALID_ARG;
     if (H < 1 || b->d % H != 0 || b->r % H != 0) return AR_ERR_SHAPE;
-    if (!ar::fused_shape_supported(b->d, b->r, H)) return AR_ERR_UNSUPPORTED;
-    std::vector<uint8_t> seen(static_cast<size_t>(b->count), 0);
+    int distinct = 0;
     for (int i = 0; i < n_src; ++i) {
-        const int32_t row = rows[i];
-        if (row < 0 || row >= b->count) return AR_ERR_INVALID_ARG;
-        if (seen[row]) return AR_ERR_INVALID_ARG;  // duplicate source
-        seen[row] = 1;
+        int k = 0;
+        while (k < i && rows[k] != rows[i]) ++k;
+        distinct += k == i;
     }
+    if (!ar::route_supported(b->d, b->r, H, distinct, b->dtype)) return AR_ERR_UNSUPPORTED;
+    for (int i = 0; i < n_src; ++i)
+        if (rows[i] < 0 || rows[i] >= b->count) return AR_ERR_INVALID_ARG;
     if (!aligned4(q) || (g && !aligned4(g))) return AR_ERR_ALIGN;
     return AR_OK;
 }
 
-void fill_common(ar::RouteArgs &a, const ar_bank *b, const int32_t *rows, int32_t n_src,
-                 int32_t H, const float *q, const float *g)
+// The site's distinct rows in order of first appearance, each with the number
+// of times the list names it.
+void distinct_rows(const int32_t *rows, int32_t n_src, std::vector<int32_t> &uniq,
+                   std::vector<int32_t> &mult)
 {
+    uniq.clear();
+    mult.clear();
+    for (int i = 0; i < n_src; ++i) {
+        size_t k = 0;
+        while (k < uniq.size() && uniq[k] != rows[i]) ++k;
+        if (k == uniq.size()) {
+            uniq.push_back(rows[i]);
+            mult.push_back(1);
+        } else {
+            ++mult[k];
+        }
+    }
+}
+
+void fill_common(ar::RouteArgs &a, const ar_bank *b, const int32_t *rows_in, int32_t n_in,
+                 int32_t H, const float *q, const float *g, int64_t q_stride = 1,
+                 int64_t g_stride = 1)
+{
+    std::vector<int32_t> uniq, mult;
+    distinct_rows(rows_in, n_in, uniq, mult);
+    const int32_t *rows = uniq.data();
+    const int32_t n_src = static_cast<int32_t>(uniq.size());
     std::memset(&a, 0, sizeof(a));
     a.bank = b->rows;
     a.inv = b->inv;
     a.grad = b->grad;
     a.q = q;
     a.g = g;
+    a.q_stride = q_stride;
+    a.g_stride = g_stride;
     a.T = b->T;
     a.d = b->d;
     a.r = b->r;
@@ -79,7 +107,13 @@ void fill_common(ar::RouteArgs &a, const ar_bank *b, const int32_t *rows, int32_
     a.inv_ld = b->inv_ld;
     a.norm_full = b->norm_full;
     a.err = ar::device_error_word();
-    for (int i = 0; i < n_src; ++i) a.rows[i] = rows[i];
+    for (int i = 0; i < n_src; ++i) {
+        a.rows[i] = rows[i];
+        if (mult[i] > 1) {
+            a.has_bias = 1;
+            a.bias[i] = std::log(static_cast<float>(mult[i]));
+        }
+    }
 }
 
 }  // namespace
@@ -119,7 +153,7 @@ ar_status ar_bank_create(ar_bank **out, int64_t T, int32_t d, int32_t r, int32_t
     if (T > 0 && (!rows || !inv_rms)) return AR_ERR_INVALID_ARG;
     if (dtype != AR_F32 && dtype != AR_BF16) return AR_ERR_INVALID_ARG;
     if (norm != AR_NORM_KEY && norm != AR_NORM_FULL) return AR_ERR_INVALID_ARG;
-    if (d < 1 || r < 1 || r > d || d % 8 != 0 || r % 8 != 0) return AR_ERR_SHAPE;
+    if (d < 1 || r < 1 || r > d) return AR_ERR_SHAPE;
     if (!aligned16(rows) || !aligned16(inv_rms) || (grad && !aligned16(grad))) return AR_ERR_ALIGN;
     int dev = -1;  // recorded for information; launches use the current device
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -167,13 +201,15 @@ ar_status ar_bank_row_ptr(const ar_bank *bank, int32_t row, void **ptr)
     return AR_OK;
 }
 
-ar_status ar_bank_append(ar_bank *bank, const void *src, int32_t accumulate_from,
-                         int32_t *out_row, void *stream)
+ar_status ar_bank_append_strided(ar_bank *bank, const void *src, int64_t token_stride,
+                                 int64_t elem_stride, int32_t accumulate_from, int32_t *out_row,
+                                 void *stream)
 {
     if (!bank || (!src && bank->T > 0)) return AR_ERR_INVALID_ARG;
+    if (token_stride < 0 || elem_stride < 1) return AR_ERR_INVALID_ARG;
     if (bank->count >= bank->cap) return AR_ERR_CAPACITY;
     if (accumulate_from < -1 || accumulate_from >= bank->count) return AR_ERR_INVALID_ARG;
-    if (!aligned16(src)) return AR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(src) % bank->esize) != 0) return AR_ERR_ALIGN;
     void *dst = nullptr;
     ar_bank_row_ptr(bank, bank->count, &dst);
     const void *prev = nullptr;
@@ -181,11 +217,19 @@ ar_status ar_bank_append(ar_bank *bank, const void *src, int32_t accumulate_from
     const cudaError_t e = ar::launch_append(src, prev, dst, bank->inv + bank->count, bank->T,
                                             bank->d, bank->r, bank->inv_ld, bank->norm_full,
                                             bank->eps, bank->dtype,
-                                            static_cast<cudaStream_t>(stream));
+                                            static_cast<cudaStream_t>(stream), token_stride,
+                                            elem_stride);
     if (e != cudaSuccess) return from_cuda(e);
     if (out_row) *out_row = bank->count;
     ++bank->count;
     return AR_OK;
+}
+
+ar_status ar_bank_append(ar_bank *bank, const void *src, int32_t accumulate_from,
+                         int32_t *out_row, void *stream)
+{
+    return ar_bank_append_strided(bank, src, bank ? bank->d : 0, 1, accumulate_from, out_row,
+                                  stream);
 }
 
 ar_status ar_bank_zero_grad(ar_bank *bank)
@@ -206,21 +250,23 @@ ar_status ar_bank_reset(ar_bank *bank)
 
 namespace {
 
-ar_status route_fwd_impl(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
-                         const float *q, const float *g, const void *partial, const float *alpha,
-                         void *out, void *routed, float *lse, int32_t site_id, void *stream)
+ar_status route_fwd_impl(ar_bank *bank, const ar_site &st_, const void *partial,
+                         const float *alpha, void *out, void *routed, float *lse, void *stream)
 {
+    const int32_t *rows = st_.rows;
+    const int32_t n_src = st_.n_src, H = st_.H;
+    const float *q = st_.q, *g = st_.g;
+    if (st_.q_stride < 1 || (g && st_.g_stride < 1)) return AR_ERR_INVALID_ARG;
     ar_status st = check_site(bank, rows, n_src, H, q, g);
     if (st != AR_OK) return st;
     if (bank->T > 0 && (!out || !lse)) return AR_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned4(lse) || !aligned16(partial) || !aligned16(routed) ||
         !aligned4(alpha))
         return AR_ERR_ALIGN;
-    if ((partial || alpha || routed) && !ar::delta_supported(bank->d, bank->r, H))
-        return AR_ERR_UNSUPPORTED;
+    if ((partial || alpha || routed) && !(partial && alpha && routed)) return AR_ERR_INVALID_ARG;
     if (bank->T > 0) {
         ar::RouteArgs a;
-        fill_common(a, bank, rows, n_src, H, q, g);
+        fill_common(a, bank, rows, n_src, H, q, g, st_.q_stride, st_.g_stride);
         a.out = out;
         a.lse = lse;
         a.partial = partial;
@@ -229,8 +275,23 @@ ar_status route_fwd_impl(ar_bank *bank, const int32_t *rows, int32_t n_src, int3
         const cudaError_t e = ar::launch_route_fwd(a, bank->dtype, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return from_cuda(e);
     }
-    bank->fwd_record.push_back(site_id);
+    bank->fwd_record.push_back(st_.site_id);
     return AR_OK;
+}
+
+ar_site make_site(const int32_t *rows, int32_t n_src, int32_t H, const float *q, const float *g,
+                  int32_t site_id)
+{
+    ar_site s;
+    s.rows = rows;
+    s.n_src = n_src;
+    s.H = H;
+    s.q = q;
+    s.q_stride = 1;
+    s.g = g;
+    s.g_stride = 1;
+    s.site_id = site_id;
+    return s;
 }
 
 }  // namespace
@@ -239,8 +300,8 @@ ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
                        const float *q, const float *g, void *out, float *lse, int32_t site_id,
                        void *stream)
 {
-    return route_fwd_impl(bank, rows, n_src, H, q, g, nullptr, nullptr, out, nullptr, lse, site_id,
-                          stream);
+    return route_fwd_impl(bank, make_site(rows, n_src, H, q, g, site_id), nullptr, nullptr, out,
+                          nullptr, lse, stream);
 }
 
 ar_status ar_route_fwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
@@ -249,23 +310,38 @@ ar_status ar_route_fwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, 
                              int32_t site_id, void *stream)
 {
     if (bank && bank->T > 0 && (!partial || !alpha || !routed)) return AR_ERR_INVALID_ARG;
-    return route_fwd_impl(bank, rows, n_src, H, q, g, partial, alpha, out, routed, lse, site_id,
-                          stream);
+    return route_fwd_impl(bank, make_site(rows, n_src, H, q, g, site_id), partial, alpha, out,
+                          routed, lse, stream);
+}
+
+ar_status ar_route_fwd_site(ar_bank *bank, const ar_site *site, const void *partial,
+                            const float *alpha, void *out, void *routed, float *lse, void *stream)
+{
+    if (!site) return AR_ERR_INVALID_ARG;
+    return route_fwd_impl(bank, *site, partial, alpha, out, routed, lse, stream);
 }
 
 ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
 {
     if (!bank || !bytes) return AR_ERR_INVALID_ARG;
     if (H < 1 || bank->d % H != 0 || bank->r % H != 0) return AR_ERR_SHAPE;
-    if (!ar::fused_shape_supported(bank->d, bank->r, H)) return AR_ERR_UNSUPPORTED;
+    if (!ar::route_supported(bank->d, bank->r, H, 1, bank->dtype)) return AR_ERR_UNSUPPORTED;
     ar::RouteArgs a;
     std::memset(&a, 0, sizeof(a));
     a.d = bank->d;
     a.r = bank->r;
     a.H = H;
+    a.n_src = 1;
     int warps = 0;
-    const cudaError_t e = ar::route_bwd_grid(a, bank->dtype, &warps);
+    cudaError_t e = ar::route_bwd_grid(a, bank->dtype, &warps);
     if (e != cudaSuccess) return from_cuda(e);
+    if (ar::may_fall_back_to_generic(bank->d, bank->r, H, bank->dtype)) {
+        // sites with many sources may run on the scalar-access kernels
+        int gw = 0;
+        e = ar::generic_bwd_rows(&gw);
+        if (e != cudaSuccess) return from_cuda(e);
+        warps = std::max(warps, gw);
+    }
     // [rows, r] partial sums of dq/dg, then a [rows, 4] tail for dL/dalpha
     *bytes = (size_t)warps * ((size_t)bank->r + 4) * sizeof(float);
     return AR_OK;
@@ -273,11 +349,14 @@ ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
 
 namespace {
 
-ar_status route_bwd_impl(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
-                         const float *q, const float *g, const void *out, const void *dout,
+ar_status route_bwd_impl(ar_bank *bank, const ar_site &st_, const void *out, const void *dout,
                          const float *lse, const float *alpha, float *dq, float *dg,
-                         float *dalpha, void *ws, size_t ws_bytes, int32_t site_id, void *stream)
+                         float *dalpha, void *ws, size_t ws_bytes, void *stream)
 {
+    const int32_t *rows = st_.rows;
+    const int32_t n_src = st_.n_src, H = st_.H;
+    const float *q = st_.q, *g = st_.g;
+    if (st_.q_stride < 1 || (g && st_.g_stride < 1)) return AR_ERR_INVALID_ARG;
     if (bank && !bank->grad && bank->T > 0) return AR_ERR_INVALID_ARG;
     ar_status st = check_site(bank, rows, n_src, H, q, g);
     if (st != AR_OK) return st;
@@ -285,34 +364,37 @@ ar_status route_bwd_impl(ar_bank *bank, const int32_t *rows, int32_t n_src, int3
     if (!aligned16(out) || !aligned16(dout) || !aligned4(lse) || !aligned4(dq) ||
         (dg && !aligned4(dg)) || !aligned16(ws) || !aligned4(alpha) || !aligned4(dalpha))
         return AR_ERR_ALIGN;
-    if ((alpha || dalpha) && !ar::delta_supported(bank->d, bank->r, H)) return AR_ERR_UNSUPPORTED;
-    if (bank->fwd_record.empty() || bank->fwd_record.back() != site_id) return AR_ERR_ORDER;
-    size_t need = 0;
-    st = ar_route_bwd_workspace(bank, H, &need);
-    if (st != AR_OK) return st;
-    if (bank->T > 0 && ws_bytes < need) return AR_ERR_CAPACITY;
+    if ((alpha != nullptr) != (dalpha != nullptr)) return AR_ERR_INVALID_ARG;
+    if (bank->fwd_record.empty() || bank->fwd_record.back() != st_.site_id) return AR_ERR_ORDER;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (bank->T == 0) {
-        cudaError_t e = cudaMemsetAsync(dq, 0, (size_t)bank->r * sizeof(float), s);
-        if (e == cudaSuccess && dg) e = cudaMemsetAsync(dg, 0, (size_t)bank->r * sizeof(float), s);
-        if (e == cudaSuccess && dalpha) e = cudaMemsetAsync(dalpha, 0, sizeof(float), s);
+        // no tokens: the reduction over zero workspace rows writes zeros
+        const cudaError_t e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), 0, bank->r, q,
+                                                     st_.q_stride, g, st_.g_stride, dq, dg,
+                                                     dalpha, s);
         if (e != cudaSuccess) return from_cuda(e);
     } else {
         ar::RouteArgs a;
-        fill_common(a, bank, rows, n_src, H, q, g);
+        fill_common(a, bank, rows, n_src, H, q, g, st_.q_stride, st_.g_stride);
         a.fout = out;
         a.dout = dout;
         a.lse = const_cast<float *>(lse);
         a.ws = static_cast<float *>(ws);
         a.alpha = alpha;
         a.dalpha = dalpha;
-        for (int i = 0; i < n_src; ++i)
-            if (!bank->touched[rows[i]]) a.first_mask[i >> 5] |= 1u << (i & 31);
-        cudaError_t e = ar::launch_route_bwd(a, bank->dtype, s);
+        for (int i = 0; i < a.n_src; ++i)
+            if (!bank->touched[a.rows[i]]) a.first_mask[i >> 5] |= 1u << (i & 31);
+        // workspace rows of the family serving this site (at most what
+        // ar_route_bwd_workspace reports)
+        int ws_rows = 0;
+        cudaError_t e = ar::route_bwd_grid(a, bank->dtype, &ws_rows);
         if (e != cudaSuccess) return from_cuda(e);
-        const int ws_rows = (int)(need / sizeof(float) / ((size_t)bank->r + 4));
-        e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), ws_rows, bank->r, q, g, dq, dg,
-                                   dalpha, s);
+        if (ws_bytes < (size_t)ws_rows * ((size_t)bank->r + 4) * sizeof(float))
+            return AR_ERR_CAPACITY;
+        e = ar::launch_route_bwd(a, bank->dtype, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), ws_rows, bank->r, q,
+                                   st_.q_stride, g, st_.g_stride, dq, dg, dalpha, s);
         if (e != cudaSuccess) return from_cuda(e);
     }
     for (int i = 0; i < n_src; ++i) bank->touched[rows[i]] = 1;
@@ -327,32 +409,40 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
                        const float *lse, float *dq, float *dg, void *ws, size_t ws_bytes,
                        int32_t site_id, void *stream)
 {
-    return route_bwd_impl(bank, rows, n_src, H, q, g, out, dout, lse, nullptr, dq, dg, nullptr,
-                          ws, ws_bytes, site_id, stream);
+    return route_bwd_impl(bank, make_site(rows, n_src, H, q, g, site_id), out, dout, lse, nullptr,
+                          dq, dg, nullptr, ws, ws_bytes, stream);
 }
 
 ar_status ar_route_bwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
-                             const float *q, const float *g, const void *routed,
-                             const void *dout, const float *lse, const float *alpha, float *dq,
-                             float *dg, float *dalpha, void *ws, size_t ws_bytes, int32_t site_id,
+                             const float *q, const float *g, const void *routed, const void *dout,
+                             const float *lse, const float *alpha, float *dq, float *dg,
+                             float *dalpha, void *ws, size_t ws_bytes, int32_t site_id,
                              void *stream)
 {
     if (!alpha || !dalpha) return AR_ERR_INVALID_ARG;
-    return route_bwd_impl(bank, rows, n_src, H, q, g, routed, dout, lse, alpha, dq, dg, dalpha, ws,
-                          ws_bytes, site_id, stream);
+    return route_bwd_impl(bank, make_site(rows, n_src, H, q, g, site_id), routed, dout, lse, alpha,
+                          dq, dg, dalpha, ws, ws_bytes, stream);
+}
+
+ar_status ar_route_bwd_site(ar_bank *bank, const ar_site *site, const void *out, const void *dout,
+                            const float *lse, const float *alpha, float *dq, float *dg,
+                            float *dalpha, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!site) return AR_ERR_INVALID_ARG;
+    return route_bwd_impl(bank, *site, out, dout, lse, alpha, dq, dg, dalpha, ws, ws_bytes, stream);
 }
 
 ar_status ar_bank_append_broadcast(ar_bank *bank, const void *vec, int32_t *out_row, void *stream)
 {
     if (!bank || !vec) return AR_ERR_INVALID_ARG;
     if (bank->count >= bank->cap) return AR_ERR_CAPACITY;
-    if (!aligned16(vec)) return AR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(vec) % bank->esize) != 0) return AR_ERR_ALIGN;
     void *dst = nullptr;
     ar_bank_row_ptr(bank, bank->count, &dst);
     const cudaError_t e = ar::launch_append(vec, nullptr, dst, bank->inv + bank->count, bank->T,
                                             bank->d, bank->r, bank->inv_ld, bank->norm_full,
                                             bank->eps, bank->dtype,
-                                            static_cast<cudaStream_t>(stream), true);
+                                            static_cast<cudaStream_t>(stream), 0, 1);
     if (e != cudaSuccess) return from_cuda(e);
     if (out_row) *out_row = bank->count;
     ++bank->count;

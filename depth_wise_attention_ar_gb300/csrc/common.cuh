@@ -278,6 +278,12 @@ __device__ __forceinline__ void store_output(const RouteArgs &a, int64_t off, co
     }
 }
 
+// One element of the storage dtype, as fp32 / rounded from fp32 (to nearest even).
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void st_elem(float *p, float v) { *p = v; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
 // Sum over the `lph` lanes of this lane's aligned group (lph a power of two).
 __device__ __forceinline__ float group_sum(float x, int lph)
 {

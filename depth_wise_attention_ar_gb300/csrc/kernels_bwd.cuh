@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = cidx[j] * 8 + (e ^ sw);
-            qg[j][e] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f);
+            qg[j][e] = __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f);
         }
     const float inv_d = 1.0f / (float)d;
 
@@ -184,7 +184,9 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         P = group_sum(P, LPH);
         zr = group_sum(zr, LPH);
         const float iv = cur_inv[n];
-        const float w = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
+        float z = __fmul_rn(iv, zr);
+        if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
+        const float w = exp2f((z - lse_h) * kLog2e);
         const float dz = w * (P - S_h);
         const float C = (H == 1) ? dz * zr : warp_sum(sub == 0 ? dz * zr : 0.f);
         const float coef = iv * iv * iv * C * inv_d;

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         for (int e = 0; e < 8; ++e) {
             const int c = (LR ? kidx[j] : cidx[j]) * 8 + e - key0 * 8;
             const bool have = !LR || mp.key_warp;
-            qg[j][e] = have ? __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) : 0.f;
+            qg[j][e] = have ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
         }
 
     const int64_t GB = gridDim.x, gb = blockIdx.x;
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             for (int j = 0; j < CPL; ++j) zr = __fadd_rn(zr, dot8(qg[j], v[j]));
             zr = group_sum(zr, mp.LPH);
             z = __fmul_rn(zr, iv);
+            if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
         } else {
             if (mp.key_warp) {
                 float zr = 0.f;
@@ -161,7 +162,11 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                     zr = __fadd_rn(zr, dot8(qg[j], kv));
                 }
                 zr = group_sum(zr, mp.LPHk);
-                if (mp.ksub == 0) zs[par * 32 + mp.hk] = __fmul_rn(zr, iv);
+                if (mp.ksub == 0) {
+                    float zz = __fmul_rn(zr, iv);
+                    if (a.has_bias) zz = __fadd_rn(zz, a.bias[n]);
+                    zs[par * 32 + mp.hk] = zz;
+                }
             }
             __syncthreads();
             z = zs[par * 32 + mp.h];
@@ -272,7 +277,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         for (int e = 0; e < 8; ++e) {
             const int c = (LR ? kidx[j] : cidx[j]) * 8 + (e ^ sw) - key0 * 8;
             const bool have = !LR || mp.key_warp;
-            qg[j][e] = have ? __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) : 0.f;
+            qg[j][e] = have ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
             U[j][e] = 0.f;
         }
     const float inv_width = 1.0f / (float)(a.norm_full ? d : r);
@@ -367,7 +372,9 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             __syncthreads();
             zr = zsm[par * 32 + mp.h];
         }
-        const float wgt = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
+        float zb = __fmul_rn(iv, zr);
+        if (a.has_bias) zb = __fadd_rn(zb, a.bias[n]);
+        const float wgt = exp2f((zb - lse_h) * kLog2e);
         const float dz = wgt * (P - S_h);
         const float cpart = warp_sum(mp.sub == 0 ? dz * zr : 0.f);
         if (lane == 0) cws[par * 32 + w] = cpart;

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = cidx[j] * 8 + e;
-            qg[j][e] = __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f);
+            qg[j][e] = __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f);
         }
 
     // ---- work: tokens gw, gw + GW, ...
@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
         zr = group_sum(zr, LPH);
         // __fmul_rn keeps the product uncontracted: the backward recomputes
         // the same bits
-        const float z = __fmul_rn(zr, cur_inv[n]);
+        float z = __fmul_rn(zr, cur_inv[n]);
+        if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
         if (n == 0) {  // first source of the token: weight exp(0) = 1 below
             m = z;
             l = 0.f;

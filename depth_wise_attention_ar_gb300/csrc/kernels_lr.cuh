@@ -26,33 +26,9 @@
 
 #include "common.cuh"
 #include "launch_util.cuh"
+#include "shapes.h"
 
 namespace ar {
-
-constexpr int kLrFwdStages = 4;
-constexpr int kLrBwdStages = 2;
-
-// Column-block width of the mixing sweep: the largest multiple of 8 columns,
-// at most 1024, that divides both the non-key width d - r and the key width r
-// (blocks never straddle the start of the key tail).
-__host__ __device__ inline int lr_block_cols(int d, int r)
-{
-    int x = d - r, y = r;
-    while (y) { const int t = x % y; x = y; y = t; }   // gcd(d - r, r) (= r when r = d)
-    for (int c = 1024; c >= 8; c -= 8)
-        if (x % c == 0) return c;
-    return 8;
-}
-
-inline size_t lr_fwd_smem_bytes(int d, int r, int N, int H, size_t esize)
-{
-    const size_t cw = (size_t)lr_block_cols(d, r);
-    return 2 * (size_t)N * r * esize            // key cache, double-buffered
-           + (size_t)kLrFwdStages * cw * esize  // value ring
-           + 2 * (size_t)N * H * 4              // scores, weights
-           + (size_t)(2 + kLrFwdStages) * 8     // mbarriers
-           + (size_t)AR_MAX_SOURCES * 4 * 2;    // inverse RMS (current, next)
-}
 
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant__ RouteArgs a)
@@ -102,7 +78,7 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = kidx[j] * 8 + e;
-            qg[j][e] = kval[j] ? __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) : 0.f;
+            qg[j][e] = kval[j] ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
         }
     }
 
@@ -182,7 +158,11 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
                 }
             }
             zr = group_sum(zr, LPH);
-            if (sub == 0) zs[n * H + h] = __fmul_rn(zr, cinv[n]);
+            if (sub == 0) {
+                float zz = __fmul_rn(zr, cinv[n]);
+                if (a.has_bias) zz = __fadd_rn(zz, a.bias[n]);
+                zs[n * H + h] = zz;
+            }
         }
         __syncwarp();
         if (sub == 0) {  // exact softmax over the N sources of head h
@@ -201,7 +181,6 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
             load_inv(k + 1, inv2 + (1 - buf) * AR_MAX_SOURCES);
         }
         // ---- sweep 2: mix column blocks with the weights
-        T *orow = static_cast<T *>(a.out) + tok * d;
         for (int b = 0; b < nblk_v + nblk_k && ok; ++b) {
             float acc[4][8];
 #pragma unroll
@@ -241,7 +220,8 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
             if (!ok) break;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if (lane + 32 * j < cwc) st_chunk_g(orow + b * CW + (lane + 32 * j) * 8, acc[j]);
+                if (lane + 32 * j < cwc)
+                    store_output<T>(a, tok * d + b * CW + (lane + 32 * j) * 8, acc[j]);
         }
     }
     if (!ok) {
@@ -304,7 +284,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = (kidx[j] - key0) * 8 + e;
-            qg[j][e] = kval[j] ? __ldg(a.q + c) * (a.g ? __ldg(a.g + c) : 1.0f) : 0.f;
+            qg[j][e] = kval[j] ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
             U[j][e] = 0.f;
         }
     }
@@ -336,7 +316,10 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
     };
     for (int s = 0; s < S && issued < hi; ++s) issue_next();
 
-    float S_h = 0.f, lse_h = 0.f;
+    // delta form: G = alpha dL/dh enters linearly, so G stays in the storage
+    // dtype and alpha scales the dot products and the w G term
+    float S_h = 0.f, lse_h = 0.f, dal = 0.f;
+    const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
     int64_t tok = lo / N, i = lo;
     int n = (int)(lo - tok * N), slot = 0;
     uint32_t phase = 0;
@@ -369,7 +352,9 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 #pragma unroll
                 for (int e = 0; e < 8; ++e) sp = fmaf(gv[e], o[e], sp);
             }
-            S_h = group_sum(sp, LPH);
+            // each token's <dL/dh, routed> counted by the warp owning (t, 0)
+            if (a.dalpha && n == 0) dal += warp_sum(sp);
+            S_h = alpha * group_sum(sp, LPH);
             lse_h = __ldg(a.lse + tok * H + h);
             for (int nn = lane; nn < N; nn += 32)
                 cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
@@ -401,14 +386,17 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
                 zr = __fadd_rn(zr, dot8(qg[j], v));
             }
         }
-        P = group_sum(P, LPH);
+        P = alpha * group_sum(P, LPH);
         zr = group_sum(zr, LPH);
         const float iv = cur_inv[n];
-        const float w = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
+        float z = __fmul_rn(iv, zr);
+        if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
+        const float w = exp2f((z - lse_h) * kLog2e);
         const float dz = w * (P - S_h);
         const float C = (H == 1) ? dz * zr : warp_sum(sub == 0 ? dz * zr : 0.f);
         const float coef = iv * iv * iv * C * inv_width;
         const float ak = iv * dz;
+        const float wa = w * alpha;
 
         // pass B: key-path terms on the tail, into the staged gradient row
 #pragma unroll
@@ -452,7 +440,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
                 for (int e = 0; e < 8; ++e) nv[e] = fmaf(-cv, v[e], nv[e]);
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) nv[e] = fmaf(w, gv[e], nv[e]);
+            for (int e = 0; e < 8; ++e) nv[e] = fmaf(wa, gv[e], nv[e]);
             st_f32x8_g(grad_row + c * 8, nv);
         }
         __syncwarp();
@@ -472,6 +460,8 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
         if (kval[j]) st_f32x8_g(wrow + (kidx[j] - key0) * 8, U[j]);
+    if (a.dalpha && lane == 0)
+        *reinterpret_cast<float4 *>(a.ws + GW * r + gw * 4) = make_float4(dal, 0.f, 0.f, 0.f);
 }
 
 template <typename T, int KMAX>
@@ -505,7 +495,6 @@ cudaError_t lr_bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_warps)
 
 // Key chunks per lane (at most): ceil(r / 256). Served: r a multiple of 8 with
 // r/H a multiple of 8, r <= d <= 4096 with d a multiple of 256.
-__host__ __device__ inline int lr_kmax(int r) { return (r + 255) / 256; }
 
 #define AR_LR_KMAX_CASES(X) X(1) X(2) X(3) X(4) X(5) X(6) X(8) X(10) X(12) X(14) X(16)
 

@@ -2,6 +2,7 @@
 // error word, and the dtype dispatch of the routing launches.
 #include "common.cuh"
 #include "launch_util.cuh"
+#include "shapes.h"
 
 namespace ar {
 
@@ -11,6 +12,8 @@ template <typename T> cudaError_t dispatch_lr_fwd(const RouteArgs &a, cudaStream
 template <typename T> cudaError_t dispatch_lr_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
 template <typename T> cudaError_t dispatch_coop_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_coop_bwd(const RouteArgs *a, cudaStream_t s, int *grid_rows);
+template <typename T> cudaError_t dispatch_generic_fwd(const RouteArgs &a, cudaStream_t s);
+template <typename T> cudaError_t dispatch_generic_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
 
 // Device error word; kernels get its address as an argument.
 __device__ unsigned int g_device_error = 0;
@@ -36,57 +39,65 @@ unsigned int *device_error_word()
 // inverse RMS is taken over the stored (rounded) values of the RMS
 // coordinates: the last r ("Low-Rank Attention Residuals" Eq. 11/13), or all
 // d for the full-width norm ("Multi-Head Attention Residuals" Appendix E).
-template <typename T>
+// The source is a strided [T, d] view: element (t, c) at src[t * ld + c * es]
+// (ld = 0 broadcasts one vector to every token). VEC: 16-byte accesses
+// (d a multiple of 8, es = 1, aligned rows); otherwise one element at a time.
+// Both walk the row in the same 8-column chunks (lane-strided, columns in
+// order within a chunk), so they give the same bits.
+__device__ __forceinline__ float round_bf16(float x)
+{
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev, T *dst, float *inv,
                                                      int64_t TT, int d, int r, int inv_ld,
-                                                     int norm_full, float eps, int src_tok_stride)
+                                                     int norm_full, float eps, int64_t ld,
+                                                     int64_t es, bool in_place)
 {
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int nch = d / 8;
-    const int c0 = norm_full ? 0 : (d - r) / 8;
+    const int nch = (d + 7) / 8;
+    const int col0 = norm_full ? 0 : d - r;  // first RMS coordinate
     const float inv_w = 1.0f / (float)(norm_full ? d : r);
-    const bool write = (src != dst) || prev != nullptr || src_tok_stride != d;
     for (int64_t t = w0; t < TT; t += nw) {
-        const T *s = src + t * src_tok_stride;
+        const T *s = src + t * ld;
         T *o = dst + t * d;
         float ss = 0.f;
-        if (write) {
-            for (int c = lane; c < nch; c += 32) {
-                float x[8];
-                ld_chunk_g(s + c * 8, x);
+        // a row already in its slot is only read for its RMS coordinates
+        for (int c = (in_place ? col0 / 8 : 0) + lane; c < nch; c += 32) {
+            float x[8];
+            if constexpr (VEC) {
+                ld_chunk_g(in_place ? o + c * 8 : s + c * 8, x);
                 if (prev) {
                     float p[8];
                     ld_chunk_g(prev + t * d + c * 8, p);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] += p[e];
                 }
-                st_chunk_g(o + c * 8, x);
-                if (c >= c0) {
-                    if constexpr (sizeof(T) == 2) {
-                        // square the stored (rounded) value
-                        float xr[8];
-                        uint4 u;
-                        u.x = pack_bf16x2(x[0], x[1]);
-                        u.y = pack_bf16x2(x[2], x[3]);
-                        u.z = pack_bf16x2(x[4], x[5]);
-                        u.w = pack_bf16x2(x[6], x[7]);
-                        unpack_bf16x8(u, xr);
+                if (!in_place) st_chunk_g(o + c * 8, x);
+            } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) ss = fmaf(xr[e], xr[e], ss);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                for (int e = 0; e < 8; ++e) {
+                    const int col = c * 8 + e;
+                    x[e] = 0.f;
+                    if (col < d) {
+                        float v = to_f32(in_place ? o[col] : s[col * es]);
+                        if (prev) v += to_f32(prev[t * d + col]);
+                        if (!in_place) st_elem(o + col, v);
+                        x[e] = v;
                     }
                 }
             }
-        } else {
-            for (int c = c0 + lane; c < nch; c += 32) {
-                float x[8];
-                ld_chunk_g(o + c * 8, x);
+            if (c * 8 + 8 > col0) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                for (int e = 0; e < 8; ++e) {
+                    const int col = c * 8 + e;
+                    // square the stored (rounded) value
+                    const float xr = sizeof(T) == 2 ? round_bf16(x[e]) : x[e];
+                    if (col >= col0 && col < d) ss = fmaf(xr, xr, ss);
+                }
             }
         }
         ss = warp_sum(ss);
@@ -94,29 +105,42 @@ __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev
     }
 }
 
-cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col, int64_t T,
-                          int d, int r, int inv_ld, int norm_full, float eps, ar_dtype dt,
-                          cudaStream_t s, bool broadcast)
+template <typename E>
+static cudaError_t append_t(const void *src, const void *prev, void *dst, float *inv_col, int64_t T,
+                            int d, int r, int inv_ld, int norm_full, float eps, int64_t ld,
+                            int64_t es, cudaStream_t s)
 {
-    const int stride = broadcast ? 0 : d;
-    if (T == 0) return cudaSuccess;
+    const bool in_place = src == dst && prev == nullptr && ld == d && es == 1;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
+                         reinterpret_cast<uintptr_t>(prev);
+    const bool vec = d % 8 == 0 && es == 1 && (ld * (int64_t)sizeof(E)) % 16 == 0 && (al & 15) == 0;
+    const void *k = vec ? reinterpret_cast<const void *>(&append_kernel<E, true>)
+                        : reinterpret_cast<const void *>(&append_kernel<E, false>);
     int grid = 0;
-    const void *k = dt == AR_BF16 ? reinterpret_cast<const void *>(&append_kernel<__nv_bfloat16>)
-                                  : reinterpret_cast<const void *>(&append_kernel<float>);
     cudaError_t e = persistent_grid(k, 256, 0, &grid);
     if (e != cudaSuccess) return e;
     const int64_t need = (T + 7) / 8;
     if (need < grid) grid = (int)need;
-    if (dt == AR_BF16)
-        append_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(src), static_cast<const __nv_bfloat16 *>(prev),
-            static_cast<__nv_bfloat16 *>(dst), inv_col, T, d, r, inv_ld, norm_full, eps, stride);
+    const E *sp = static_cast<const E *>(src), *pp = static_cast<const E *>(prev);
+    E *dp = static_cast<E *>(dst);
+    if (vec)
+        append_kernel<E, true><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld, norm_full,
+                                                    eps, ld, es, in_place);
     else
-        append_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(src),
-                                                  static_cast<const float *>(prev),
-                                                  static_cast<float *>(dst), inv_col, T, d, r,
-                                                  inv_ld, norm_full, eps, stride);
+        append_kernel<E, false><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld,
+                                                     norm_full, eps, ld, es, in_place);
     return cudaGetLastError();
+}
+
+cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col, int64_t T,
+                          int d, int r, int inv_ld, int norm_full, float eps, ar_dtype dt,
+                          cudaStream_t s, int64_t ld, int64_t es)
+{
+    if (T == 0) return cudaSuccess;
+    return dt == AR_BF16 ? append_t<__nv_bfloat16>(src, prev, dst, inv_col, T, d, r, inv_ld,
+                                                   norm_full, eps, ld, es, s)
+                         : append_t<float>(src, prev, dst, inv_col, T, d, r, inv_ld, norm_full,
+                                           eps, ld, es, s);
 }
 
 // ---- gradient fold (block-sum fan-out) -----------------------------------------
@@ -125,6 +149,14 @@ cudaError_t launch_append(const void *src, const void *prev, void *dst, float *i
 // partial-sum version t+1 = version t + o_{t+1} passes its whole adjoint on to
 // version t ("Low-Rank Attention Residuals", Appendix B.4: every write of a
 // block receives the block sum's adjoint).
+__global__ void __launch_bounds__(256) grad_fold_scalar_kernel(float *dst, const float *src,
+                                                               int64_t n, int mode)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = ((mode & 1) ? src[i] : 0.f) + ((mode & 2) ? dst[i] : 0.f);
+}
+
 __global__ void __launch_bounds__(256) grad_fold_kernel(float *dst, const float *src, int64_t n4,
                                                         int mode)
 {
@@ -146,13 +178,24 @@ cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_v
                              bool dst_valid, cudaStream_t s)
 {
     if (n == 0) return cudaSuccess;
+    const int mode = (src_valid ? 1 : 0) | (dst_valid ? 2 : 0);
     int grid = 0;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src);
+    if (n % 4 != 0 || (al & 15) != 0) {  // rows of an unaligned width
+        cudaError_t e = persistent_grid(reinterpret_cast<const void *>(&grad_fold_scalar_kernel),
+                                        256, 0, &grid);
+        if (e != cudaSuccess) return e;
+        const int64_t need = (n + 255) / 256;
+        if (need < grid) grid = (int)need;
+        grad_fold_scalar_kernel<<<grid, 256, 0, s>>>(dst, src, n, mode);
+        return cudaGetLastError();
+    }
     cudaError_t e = persistent_grid(reinterpret_cast<const void *>(&grad_fold_kernel), 256, 0, &grid);
     if (e != cudaSuccess) return e;
     const int64_t n4 = n / 4;
     const int64_t need = (n4 + 255) / 256;
     if (need < grid) grid = (int)need;
-    grad_fold_kernel<<<grid, 256, 0, s>>>(dst, src, n4, (src_valid ? 1 : 0) | (dst_valid ? 2 : 0));
+    grad_fold_kernel<<<grid, 256, 0, s>>>(dst, src, n4, mode);
     return cudaGetLastError();
 }
 
@@ -193,7 +236,9 @@ cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cu
 //   out = (e^(lse_A - lse) out_A + e^(lse_B - lse) out_B)   on each head's slice
 // ("Low-Rank Attention Residuals", Sec. 3.4: inter-block and intra-block
 // results merge with an online-softmax update). One warp per token.
-template <typename T>
+// VEC: 8-column chunks (d and d/H multiples of 8, aligned rows); otherwise
+// one column at a time, with the same arithmetic per element.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) merge_kernel(const T *oa, const float *la, const T *ob,
                                                     const float *lb, T *out, float *lse,
                                                     int64_t TT, int d, int H)
@@ -201,20 +246,25 @@ __global__ void __launch_bounds__(256) merge_kernel(const T *oa, const float *la
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int K = d / H, nch = d / 8;
+    const int K = d / H, nch = VEC ? d / 8 : d;
     for (int64_t t = w0; t < TT; t += nw) {
         for (int c = lane; c < nch; c += 32) {
-            const int h = (c * 8) / K;
+            const int h = (VEC ? c * 8 : c) / K;
             const float a = la[t * H + h], b = lb[t * H + h];
             const float m = fmaxf(a, b);
             const float ea = exp2f((a - m) * kLog2e), eb = exp2f((b - m) * kLog2e);
             const float inv = 1.f / (ea + eb);
-            float x[8], y[8], z[8];
-            ld_chunk_g(oa + t * d + c * 8, x);
-            ld_chunk_g(ob + t * d + c * 8, y);
+            if constexpr (VEC) {
+                float x[8], y[8], z[8];
+                ld_chunk_g(oa + t * d + c * 8, x);
+                ld_chunk_g(ob + t * d + c * 8, y);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) z[e] = fmaf(ea * inv, x[e], eb * inv * y[e]);
-            st_chunk_g(out + t * d + c * 8, z);
+                for (int e = 0; e < 8; ++e) z[e] = fmaf(ea * inv, x[e], eb * inv * y[e]);
+                st_chunk_g(out + t * d + c * 8, z);
+            } else {
+                const float x = to_f32(oa[t * d + c]), y = to_f32(ob[t * d + c]);
+                st_elem(out + t * d + c, fmaf(ea * inv, x, eb * inv * y));
+            }
         }
         for (int h = lane; h < H; h += 32) {
             const float a = la[t * H + h], b = lb[t * H + h];
@@ -224,26 +274,35 @@ __global__ void __launch_bounds__(256) merge_kernel(const T *oa, const float *la
     }
 }
 
-cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const float *lb,
-                         void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s)
+template <typename E>
+static cudaError_t merge_t(const void *oa, const float *la, const void *ob, const float *lb,
+                           void *out, float *lse, int64_t T, int d, int H, cudaStream_t s)
 {
-    if (T == 0) return cudaSuccess;
-    const void *k = dt == AR_BF16 ? reinterpret_cast<const void *>(&merge_kernel<__nv_bfloat16>)
-                                  : reinterpret_cast<const void *>(&merge_kernel<float>);
+    const uintptr_t al = reinterpret_cast<uintptr_t>(oa) | reinterpret_cast<uintptr_t>(ob) |
+                         reinterpret_cast<uintptr_t>(out);
+    const bool vec = d % 8 == 0 && (d / H) % 8 == 0 && (al & 15) == 0;
+    const void *k = vec ? reinterpret_cast<const void *>(&merge_kernel<E, true>)
+                        : reinterpret_cast<const void *>(&merge_kernel<E, false>);
     int grid = 0;
     cudaError_t e = persistent_grid(k, 256, 0, &grid);
     if (e != cudaSuccess) return e;
     const int64_t need = (T + 7) / 8;
     if (need < grid) grid = (int)need;
-    if (dt == AR_BF16)
-        merge_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(oa), la, static_cast<const __nv_bfloat16 *>(ob), lb,
-            static_cast<__nv_bfloat16 *>(out), lse, T, d, H);
+    const E *a = static_cast<const E *>(oa), *b = static_cast<const E *>(ob);
+    E *o = static_cast<E *>(out);
+    if (vec)
+        merge_kernel<E, true><<<grid, 256, 0, s>>>(a, la, b, lb, o, lse, T, d, H);
     else
-        merge_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(oa), la,
-                                                 static_cast<const float *>(ob), lb,
-                                                 static_cast<float *>(out), lse, T, d, H);
+        merge_kernel<E, false><<<grid, 256, 0, s>>>(a, la, b, lb, o, lse, T, d, H);
     return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const float *lb,
+                         void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s)
+{
+    if (T == 0) return cudaSuccess;
+    return dt == AR_BF16 ? merge_t<__nv_bfloat16>(oa, la, ob, lb, out, lse, T, d, H, s)
+                         : merge_t<float>(oa, la, ob, lb, out, lse, T, d, H, s);
 }
 
 // ---- dq / dg -----------------------------------------------------------------
@@ -251,7 +310,8 @@ cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const 
 // backward's warps runs in a fixed order (8 strided groups, then the groups
 // in order), so repeated runs give identical bits.
 __global__ void __launch_bounds__(256) dqdg_reduce_kernel(const float *ws, int rows, int r,
-                                                          const float *q, const float *g,
+                                                          const float *q, int64_t qs,
+                                                          const float *g, int64_t gs,
                                                           float *dq, float *dg, float *dalpha)
 {
     __shared__ float part[8][33];
@@ -281,45 +341,32 @@ __global__ void __launch_bounds__(256) dqdg_reduce_kernel(const float *ws, int r
         float t = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) t += part[k][lane];
-        dq[c] = (g ? g[c] : 1.0f) * t;
-        if (dg) dg[c] = q[c] * t;
+        dq[c * qs] = (g ? g[c * gs] : 1.0f) * t;
+        if (dg) dg[c * gs] = q[c * qs] * t;
     }
 }
 
-cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, const float *g,
-                               float *dq, float *dg, float *dalpha, cudaStream_t s)
+cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, int64_t q_stride,
+                               const float *g, int64_t g_stride, float *dq, float *dg,
+                               float *dalpha, cudaStream_t s)
 {
-    dqdg_reduce_kernel<<<(r + 31) / 32, 256, 0, s>>>(ws, rows, r, q, g, dq, dg, dalpha);
+    dqdg_reduce_kernel<<<(r + 31) / 32, 256, 0, s>>>(ws, rows, r, q, q_stride, g, g_stride, dq,
+                                                     dg, dalpha);
     return cudaGetLastError();
 }
 
-// ---- dtype / shape dispatch ----------------------------------------------------
-// r = d, d <= 2048: one warp per token (online softmax, register-resident).
-// d > 2048, or r < d with d a multiple of 1024: four warps share each row.
-// Other sliced-key shapes (d <= 4096): one warp per token, two-sweep forward.
-enum class Family { kFull, kCoop, kSliced, kNone };
-
-static Family family_of(int d, int r, int H)
-{
-    if (H < 1 || d <= 0 || r <= 0 || r > d || d % 256 != 0 || r % 8 != 0) return Family::kNone;
-    const bool pow2_h = H <= 32 && (32 % H) == 0;
-    if (r == d && d <= 2048 && pow2_h) return Family::kFull;
-    if (r % 256 == 0 && coop_supported(d, r, H)) return Family::kCoop;
-    // one warp per token, two sweeps: any key width with whole 8-column chunks
-    // per head (r = d included, for widths the other families leave out)
-    if (d <= 4096 && pow2_h && (r / H) % 8 == 0 && (r + 255) / 256 <= 16) return Family::kSliced;
-    return Family::kNone;
-}
-
+// ---- dtype / shape dispatch (family rules in shapes.h) ---------------------------
 cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 {
     const bool bf = dt == AR_BF16;
-    switch (family_of(a.d, a.r, a.H)) {
+    switch (family_of(a.d, a.r, a.H, a.n_src, bf ? 2 : 4)) {
     case Family::kFull: return bf ? dispatch_fwd<__nv_bfloat16>(a, s) : dispatch_fwd<float>(a, s);
     case Family::kCoop:
         return bf ? dispatch_coop_fwd<__nv_bfloat16>(a, s) : dispatch_coop_fwd<float>(a, s);
     case Family::kSliced:
         return bf ? dispatch_lr_fwd<__nv_bfloat16>(a, s) : dispatch_lr_fwd<float>(a, s);
+    case Family::kGeneric:
+        return bf ? dispatch_generic_fwd<__nv_bfloat16>(a, s) : dispatch_generic_fwd<float>(a, s);
     default: return cudaErrorNotSupported;
     }
 }
@@ -327,7 +374,7 @@ cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 static cudaError_t bwd_any(const RouteArgs &a, ar_dtype dt, cudaStream_t s, int *rows)
 {
     const bool bf = dt == AR_BF16;
-    switch (family_of(a.d, a.r, a.H)) {
+    switch (family_of(a.d, a.r, a.H, a.n_src, bf ? 2 : 4)) {
     case Family::kFull:
         return bf ? dispatch_bwd<__nv_bfloat16>(&a, s, rows) : dispatch_bwd<float>(&a, s, rows);
     case Family::kCoop:
@@ -335,6 +382,9 @@ static cudaError_t bwd_any(const RouteArgs &a, ar_dtype dt, cudaStream_t s, int 
                   : dispatch_coop_bwd<float>(&a, s, rows);
     case Family::kSliced:
         return bf ? dispatch_lr_bwd<__nv_bfloat16>(&a, s, rows) : dispatch_lr_bwd<float>(&a, s, rows);
+    case Family::kGeneric:
+        return bf ? dispatch_generic_bwd<__nv_bfloat16>(&a, s, rows)
+                  : dispatch_generic_bwd<float>(&a, s, rows);
     default: return cudaErrorNotSupported;
     }
 }
@@ -349,12 +399,24 @@ cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_rows)
     return bwd_any(a, dt, nullptr, grid_rows);
 }
 
-bool fused_shape_supported(int d, int r, int H) { return family_of(d, r, H) != Family::kNone; }
-
-bool delta_supported(int d, int r, int H)
+bool route_supported(int d, int r, int H, int n_src, ar_dtype dt)
 {
-    const Family f = family_of(d, r, H);
-    return f == Family::kFull || f == Family::kCoop;
+    return family_of(d, r, H, n_src, dt == AR_BF16 ? 2 : 4) != Family::kNone;
+}
+
+bool may_fall_back_to_generic(int d, int r, int H, ar_dtype dt)
+{
+    return family_of(d, r, H, 1, dt == AR_BF16 ? 2 : 4) == Family::kSliced;
+}
+
+cudaError_t generic_bwd_rows(int *rows)
+{
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    *rows = sms * kGenWarpsPerSm;
+    return cudaSuccess;
 }
 
 }  // namespace ar

@@ -38,17 +38,23 @@
  * - Banks are not thread-safe; distinct banks may be used from distinct
  *   threads.
  *
- * Shapes the fused routing kernels cover (1 <= n_src <= AR_MAX_SOURCES,
- * row/output pointers 16-byte aligned, d and r multiples of 256):
+ * Shapes: every d >= 1, 1 <= r <= d and H dividing both d and r are served.
+ * The tiled kernels (bulk copies into shared memory, 16-byte accesses) take
+ * d a multiple of 256 with r a multiple of 8 and:
  *   - r = d <= 2048, H in {1,2,4,8,16,32};
  *   - d a multiple of 1024 up to 8192, H a multiple of 4 with H/4 in
  *     {1,2,4,8,16,32}, and r = d or r = k*d/4 (k = 1, 2) with H/k a power of
  *     two <= 32;
- *   - other r < d with d <= 4096, H in {1,...,32} a power of two and
- *     r in {256, 512, 1024, 2048} (the forward's key cache,
- *     2*n_src*r*sizeof(dtype) bytes, within 200 KB). Other shapes return AR_ERR_UNSUPPORTED (or
- * AR_ERR_ALIGN for a misaligned pointer). Appends accept any d, r that are
- * multiples of 8.
+ *   - other r <= d with d <= 4096, H in {1,...,32} a power of two, r/H a
+ *     multiple of 8 and r <= 4096 (the forward's key cache,
+ *     2*n_src*r*sizeof(dtype) bytes, within 200 KB).
+ * Every other shape runs on the scalar-access kernels ("Low-Rank Attention
+ * Residuals", Appendix I: unaligned widths such as d = 513), which hold the
+ * site's [n_src, H] scores per warp in shared memory and return
+ * AR_ERR_UNSUPPORTED only when even one warp's arrays exceed 200 KB
+ * (about n_src*H > 20000). Row/output pointers must be 16-byte aligned
+ * (AR_ERR_ALIGN otherwise); the delta form is served by every family except
+ * the one-warp sliced-key kernels of the third item.
  */
 #ifndef ATTNRES_H
 #define ATTNRES_H
@@ -64,7 +70,7 @@ extern "C" {
 
 typedef enum {
     AR_OK = 0,
-    AR_ERR_INVALID_ARG = 1, /* null/duplicate/out-of-range argument        */
+    AR_ERR_INVALID_ARG = 1, /* null or out-of-range argument               */
     AR_ERR_SHAPE = 2,       /* inconsistent sizes (d % H, r > d, ...)       */
     AR_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned      */
     AR_ERR_CAPACITY = 4,    /* bank full, or workspace too small            */
@@ -153,6 +159,22 @@ ar_status ar_bank_row_ptr(const ar_bank *bank, int32_t row, void **ptr);
 ar_status ar_bank_append(ar_bank *bank, const void *src, int32_t accumulate_from,
                          int32_t *out_row, void *stream);
 
+/*
+ * ar_bank_append for a strided source: element (t, c) of the [T, d] source
+ * is src[t * token_stride + c * elem_stride] ("Low-Rank Attention
+ * Residuals", Appendix I: the operator is checked on strided sources). The
+ * stored row, its inverse RMS and everything downstream are bit for bit those
+ * of ar_bank_append on a contiguous copy of the same values.
+ *   token_stride : elements between tokens (>= 0; 0 repeats one row)
+ *   elem_stride  : elements between coordinates (>= 1)
+ * src needs only the alignment of one element; a contiguous source with
+ * 16-byte aligned token rows takes 16-byte accesses, any other one element at
+ * a time. Errors: as ar_bank_append; AR_ERR_INVALID_ARG for negative strides.
+ */
+ar_status ar_bank_append_strided(ar_bank *bank, const void *src, int64_t token_stride,
+                                 int64_t elem_stride, int32_t accumulate_from, int32_t *out_row,
+                                 void *stream);
+
 /* Start a new backward pass: mark every gradient row untouched, so that the
  * first backward that reaches a row stores into it and later ones accumulate
  * (MHAR Appendix E, FIRST_CALL). No memset is issued. */
@@ -165,7 +187,12 @@ ar_status ar_bank_reset(ar_bank *bank);
  * Forward of one routing site: online softmax over the listed sources with
  * the RMSNorm key fused in (MHAR Appendix E, "Forward: online softmax over
  * depth with the norm fused in", Figure 9), each source row read once.
- *   rows, n_src : host int32 list of distinct appended rows, 1..AR_MAX_SOURCES
+ *   rows, n_src : host int32 list of appended rows, 1..AR_MAX_SOURCES entries.
+ *                 A row may be listed more than once: the softmax runs over
+ *                 the list, so a row listed k times carries k times the
+ *                 weight of one listed once. It is still read once per token
+ *                 (log k is added to its score) and its gradient is the sum
+ *                 over its k entries.
  *   H           : routing heads
  *   q           : device float [r], the site's query
  *   g           : device float [r] RMSNorm weight, or NULL for ones
@@ -173,8 +200,8 @@ ar_status ar_bank_reset(ar_bank *bank);
  *   lse         : device float [T, H], per-head log-sum-exp (natural log)
  *   site_id     : caller's id of this site; pushed on the bank's call record
  *                 so that the backward can check reverse order.
- * Errors: AR_ERR_INVALID_ARG (row not appended, duplicate row, n_src out of
- * range, null pointers), AR_ERR_SHAPE (d % H or r % H nonzero),
+ * Errors: AR_ERR_INVALID_ARG (row not appended, n_src out of range, null
+ * pointers), AR_ERR_SHAPE (d % H or r % H nonzero),
  * AR_ERR_UNSUPPORTED, AR_ERR_ALIGN, AR_ERR_CUDA.
  */
 ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
@@ -204,6 +231,35 @@ ar_status ar_route_fwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, 
                              const float *q, const float *g, const void *partial,
                              const float *alpha, void *out, void *routed, float *lse,
                              int32_t site_id, void *stream);
+
+/*
+ * A routing site with its query and norm weight given as strided vectors
+ * ("Low-Rank Attention Residuals", Appendix I: the operator is checked on
+ * strided queries), e.g. one column of a [r, sites] parameter matrix.
+ *   rows, n_src, H, site_id : as in ar_route_fwd
+ *   q, q_stride : device float, entry c at q[c * q_stride] (q_stride >= 1)
+ *   g, g_stride : the same for g, or g = NULL for ones
+ * In the backward, dq is written with q's stride and dg with g's stride (the
+ * gradient laid out like its parameter).
+ */
+typedef struct ar_site {
+    const int32_t *rows;
+    int32_t n_src;
+    int32_t H;
+    const float *q;
+    int64_t q_stride;
+    const float *g;
+    int64_t g_stride;
+    int32_t site_id;
+} ar_site;
+
+/* Forward of one site described by an ar_site. partial, alpha and routed are
+ * all NULL (plain read, as ar_route_fwd) or all non-NULL (delta form, as
+ * ar_route_fwd_delta). Errors: as those calls; AR_ERR_INVALID_ARG for a
+ * NULL site, a stride < 1, or a partial set of the delta pointers. */
+ar_status ar_route_fwd_site(ar_bank *bank, const ar_site *site, const void *partial,
+                            const float *alpha, void *out, void *routed, float *lse,
+                            void *stream);
 
 /* Bytes of device workspace ar_route_bwd (and ar_route_bwd_delta) needs for
  * this bank and H: per-warp (or per-block) partial sums of dq/dg and of
@@ -301,6 +357,16 @@ ar_status ar_route_bwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, 
                              const void *dout, const float *lse, const float *alpha, float *dq,
                              float *dg, float *dalpha, void *ws, size_t ws_bytes, int32_t site_id,
                              void *stream);
+
+/* Backward of one site described by an ar_site. alpha and dalpha are both
+ * NULL (as ar_route_bwd; `out` is the forward output) or both non-NULL (as
+ * ar_route_bwd_delta; `out` is the routed mix). dq is written with the
+ * site's q_stride, dg with its g_stride. Errors: as those calls;
+ * AR_ERR_INVALID_ARG for a NULL site, a stride < 1, or only one of
+ * alpha/dalpha. */
+ar_status ar_route_bwd_site(ar_bank *bank, const ar_site *site, const void *out,
+                            const void *dout, const float *lse, const float *alpha, float *dq,
+                            float *dg, float *dalpha, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Append a row that holds the same vector for every token (the learnable null

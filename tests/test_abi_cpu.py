@@ -80,7 +80,7 @@ def test_bank_create_checks(B):
     assert code(16, 512, 512, 4, 1, 0, 1e-6, None, FAKE, FAKE) == "AR_ERR_INVALID_ARG"
     assert code(16, 512, 512, 0, 1, 0, 1e-6, FAKE, FAKE, FAKE) == "AR_ERR_INVALID_ARG"
     assert code(16, 512, 1024, 4, 1, 0, 1e-6, FAKE, FAKE, FAKE) == "AR_ERR_SHAPE"
-    assert code(16, 500, 500, 4, 1, 0, 1e-6, FAKE, FAKE, FAKE) == "AR_ERR_SHAPE"
+    assert code(16, 0, 0, 4, 1, 0, 1e-6, FAKE, FAKE, FAKE) == "AR_ERR_SHAPE"
     assert code(16, 512, 512, 4, 1, 0, 1e-6, FAKE + 8, FAKE, FAKE) == "AR_ERR_ALIGN"
     assert code(16, 512, 512, 4, 7, 0, 1e-6, FAKE, FAKE, FAKE) == "AR_ERR_INVALID_ARG"
     h = _bank(B)
@@ -106,15 +106,25 @@ def test_route_argument_checks_precede_launch(B):
     assert _err(B.ar_route_fwd, h, [], 4, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_INVALID_ARG"
     assert _err(B.ar_route_fwd, h, list(range(257)), 4, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_INVALID_ARG"
     assert _err(B.ar_route_fwd, h, [0], 3, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_SHAPE"
-    assert _err(B.ar_route_fwd, h, [0], 64, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
+    # H = 64 over d = 512 is served (by the scalar-access kernels): the row check fails
+    assert _err(B.ar_route_fwd, h, [0], 64, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_INVALID_ARG"
     assert _err(B.ar_route_fwd, h, [0], 4, None, None, FAKE, FAKE, 1, 0) == "AR_ERR_INVALID_ARG"
     B.ar_bank_destroy(h)
-    for d, r, H in ((8192, 8192, 2), (1024, 760, 8), (8192, 1024, 8), (1000, 1000, 8),
-                    (16384, 16384, 8), (512, 256, 64)):
+    # every shape has a kernel family unless the scalar-access kernels' per-warp
+    # [n_src, H] arrays outgrow shared memory
+    for d, r, H, n in ((8192, 8192, 8192, 4), (4096, 4096, 1024, 32), (2048, 2048, 2048, 16)):
         h = _bank(B, d=d, r=r)
-        assert _err(B.ar_route_fwd, h, [0], H, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_UNSUPPORTED"
+        assert _err(B.ar_route_fwd, h, list(range(n)), H, q, None, FAKE, FAKE, 1,
+                    0) == "AR_ERR_UNSUPPORTED"
+        # a repeated row counts once
+        assert _err(B.ar_route_fwd, h, [0] * n, H, q, None, FAKE, FAKE, 1,
+                    0) == "AR_ERR_INVALID_ARG"
         B.ar_bank_destroy(h)
-    # the delta form is served by the full-key and four-warp kernels only
+    for d, r, H in ((8192, 8192, 2), (1024, 760, 8), (8192, 1024, 8), (1000, 1000, 8),
+                    (513, 513, 1), (513, 128, 1), (520, 260, 5)):
+        h = _bank(B, d=d, r=r)
+        assert _err(B.ar_route_fwd, h, [0], H, q, None, FAKE, FAKE, 1, 0) == "AR_ERR_INVALID_ARG"
+        B.ar_bank_destroy(h)
     h = _bank(B, d=1280, r=256)
     assert _err(B.ar_route_fwd_delta, h, [0], 8, q, None, FAKE, FAKE, FAKE, FAKE, FAKE, 1,
                 0) == "AR_ERR_INVALID_ARG"   # nothing appended yet
@@ -129,7 +139,7 @@ def test_failed_append_leaves_bank_unchanged_without_gpu(B):
     assert _err(B.ar_bank_append, h, FAKE, -1, 0) == "AR_ERR_CUDA"
     assert B.ar_bank_row_count(h) == 0
     assert _err(B.ar_bank_append, h, FAKE, 0, 0) == "AR_ERR_INVALID_ARG"   # row 0 not appended
-    assert _err(B.ar_bank_append, h, FAKE + 4, -1, 0) == "AR_ERR_ALIGN"
+    assert _err(B.ar_bank_append, h, FAKE + 1, -1, 0) == "AR_ERR_ALIGN"
     B.ar_bank_destroy(h)
 
 
@@ -138,3 +148,42 @@ def test_backward_without_gradient_rows_is_rejected(B):
     assert _err(B.ar_route_bwd, h, [0], 4, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
                 0, 0) == "AR_ERR_INVALID_ARG"
     B.ar_bank_destroy(h)
+
+
+def test_site_descriptor_and_strided_append_checks(B):
+    h = _bank(B)
+    site = B.make_site([0], 4, FAKE, None, 1, q_stride=1, g_stride=1)
+    assert _err(B.ar_route_fwd_site, h, site, None, None, FAKE, None, FAKE, 0) == "AR_ERR_INVALID_ARG"
+    bad = B.make_site([0], 4, FAKE, None, 1, q_stride=0, g_stride=1)
+    assert _err(B.ar_route_fwd_site, h, bad, None, None, FAKE, None, FAKE, 0) == "AR_ERR_INVALID_ARG"
+    # the delta pointers come all together or not at all
+    assert _err(B.ar_route_fwd_site, h, site, FAKE, None, FAKE, None, FAKE,
+                0) == "AR_ERR_INVALID_ARG"
+    assert _err(B.ar_route_bwd_site, h, site, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE,
+                1 << 20, 0) == "AR_ERR_INVALID_ARG"
+    assert _err(B.ar_bank_append_strided, h, FAKE, -1, 1, -1, 0) == "AR_ERR_INVALID_ARG"
+    assert _err(B.ar_bank_append_strided, h, FAKE, 512, 0, -1, 0) == "AR_ERR_INVALID_ARG"
+    assert _err(B.ar_bank_append_strided, h, FAKE + 1, 512, 1, -1, 0) == "AR_ERR_ALIGN"
+    B.ar_bank_destroy(h)
+
+
+def test_site_struct_layout_matches_the_header(B, tmp_path):
+    """ctypes' ArSite has the field offsets and size gcc gives struct ar_site."""
+    import ctypes
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "attnres.h"\n'
+        'int main(void) { printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(ar_site),'
+        ' offsetof(ar_site, rows), offsetof(ar_site, n_src), offsetof(ar_site, H),'
+        ' offsetof(ar_site, q), offsetof(ar_site, q_stride), offsetof(ar_site, g),'
+        ' offsetof(ar_site, g_stride), offsetof(ar_site, site_id)); return 0; }\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(root, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    S = B.ArSite
+    want = [ctypes.sizeof(S)] + [getattr(S, f).offset for f, _ in S._fields_]
+    assert got == want

@@ -34,20 +34,25 @@ def _t64(t):
     return t.detach().to(torch.float64).cpu().numpy()
 
 
-@pytest.mark.parametrize("d,H,dtype", [(512, 4, "f32"), (512, 4, "bf16"), (1280, 8, "bf16"),
-                                       (4096, 8, "bf16"), (4096, 8, "f32")])
+@pytest.mark.parametrize("d,r,H,dtype", [(512, 512, 4, "f32"), (512, 512, 4, "bf16"),
+                                         (1280, 1280, 8, "bf16"), (4096, 4096, 8, "bf16"),
+                                         (4096, 4096, 8, "f32"), (1280, 256, 8, "bf16"),
+                                         (1536, 384, 1, "f32"), (513, 513, 1, "f32"),
+                                         (520, 130, 5, "bf16")])
 @pytest.mark.parametrize("alpha", [0.0, 0.7])
-def test_per_call_delta_stack(B, orc, d, H, dtype, alpha):
+def test_per_call_delta_stack(B, orc, d, r, H, dtype, alpha):
+    """Every kernel family: one warp per token (512, 1280), four warps per row
+    (4096), sliced keys (1280/256, 1536/384), scalar access (513, 520/130/5)."""
     import torch
     T, k = 173, 5                                   # null source + 5 block deltas
     inp = synth.HostInputs(seed=9, q_std=0.5, g_kind="random")
-    bank = B.Bank(T, d, d, k + 1, dtype)
+    bank = B.Bank(T, d, r, k + 1, dtype)
     null = inp.output(0, 1, d, dtype).reshape(d).contiguous()
     bank.append_broadcast(null)
     for j in range(1, k + 1):
         bank.append(inp.output(j, T, d, dtype))
     rows = list(range(k + 1))
-    q, g = inp.query(7, d), inp.norm_weight(7, d)
+    q, g = inp.query(7, r), inp.norm_weight(7, r)
     partial = inp.output(50, T, d, dtype)
     a_t = torch.tensor([alpha], device="cuda")
     out, routed, lse = bank.route_fwd_delta(rows, H, q, g, partial, a_t, site_id=1)
@@ -61,14 +66,14 @@ def test_per_call_delta_stack(B, orc, d, H, dtype, alpha):
         assert torch.equal(out, partial)             # closed gate: exactly the residual stream
     srcs = [np.broadcast_to(_t64(null), (T, d)).copy()] + \
            [inp.host_output(j, T, d, dtype) for j in range(1, k + 1)]
-    qh, gh = inp.host_query(7, d), inp.host_norm_weight(7, d)
-    h_ref, routed_ref, lse_ref = orc.route_fwd_delta(srcs, qh, gh, H, _t64(partial), alpha)
+    qh, gh = inp.host_query(7, r), inp.host_norm_weight(7, r)
+    h_ref, routed_ref, lse_ref = orc.route_fwd_delta(srcs, qh, gh, H, _t64(partial), alpha, r=r)
     tol = TOL[dtype]
     assert _nmax(_t64(out), h_ref) < tol
     assert _nmax(_t64(routed), routed_ref) < tol
     assert _nmax(_t64(lse), lse_ref) < tol
     ds, dq_r, dg_r, dal_r, _ = orc.route_bwd_delta(srcs, qh, gh, inp.host_dout(7, T, d, dtype), H,
-                                                   alpha)
+                                                   alpha, r=r)
     if alpha == 0.0:
         assert torch.all(bank.grad == 0) and torch.all(dq == 0) and torch.all(dg == 0)
     else:
@@ -77,19 +82,6 @@ def test_per_call_delta_stack(B, orc, d, H, dtype, alpha):
         assert _nmax(_t64(dnull), ds[0].sum(0)) < tol
         assert _nmax(_t64(dq), dq_r) < tol and _nmax(_t64(dg), dg_r) < tol
     assert abs(dal.item() - dal_r) <= tol * max(1.0, abs(dal_r))
-
-
-def test_delta_form_is_rejected_where_unsupported(B):
-    import torch
-    T, d, r = 16, 1280, 256                          # served by the one-warp sliced-key kernels
-    bank = B.Bank(T, d, r, 2, "bf16")
-    x = torch.zeros((T, d), dtype=torch.bfloat16, device="cuda")
-    bank.append(x)
-    bank.append(x)
-    q = torch.zeros(r, device="cuda")
-    with pytest.raises(B.ARError) as e:
-        bank.route_fwd_delta([0, 1], 8, q, None, x, torch.zeros(1, device="cuda"))
-    assert e.value.name == "AR_ERR_UNSUPPORTED"
 
 
 def test_full_size_delta_8b_sampled_tokens(B, orc):

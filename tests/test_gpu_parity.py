@@ -170,6 +170,69 @@ def test_low_rank_page_shapes(W, orc, d, r, H, dtype):
     run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
 
 
+@pytest.mark.parametrize("d,r,H,dtype,M", [(513, 513, 1, "bf16", 6), (513, 171, 3, "f32", 6),
+                                           (520, 130, 5, "bf16", 6), (1000, 1000, 8, "f32", 5),
+                                           (768, 768, 3, "bf16", 5), (2048, 2048, 64, "f32", 4),
+                                           (4096, 4096, 2, "bf16", 16), (100, 20, 4, "f32", 5)])
+def test_scalar_access_shapes(W, orc, d, r, H, dtype, M):
+    """Shapes outside the tiled kernels ("Low-Rank Attention Residuals",
+    Appendix I: unaligned width d = 513): widths that are not multiples of 8
+    or 256, head counts that are not powers of two, 64 heads. With d = 4096,
+    H = 2 the sites with more than 12 sources outgrow the sliced-key kernels'
+    key cache and move to the scalar-access kernels within one chain."""
+    _, wl = W
+    cfg = small(wl, "gen", T=67, d=d, H=H, dtype=dtype, M=M, r=r)
+    run_and_compare(W, orc, cfg, H, q_std=0.5, g_kind="random")
+
+
+@pytest.mark.parametrize("d,r,H,dtype", [(1280, 1280, 8, "f32"), (1280, 1280, 8, "bf16"),
+                                         (2048, 512, 4, "f32"), (1536, 384, 1, "f32"),
+                                         (4096, 4096, 8, "bf16"), (513, 513, 1, "f32")])
+def test_repeated_sources(W, orc, d, r, H, dtype):
+    """A row listed k times in one site: the softmax runs over the list, so the
+    read equals the oracle's over the literal list, and the row's gradient is
+    the sum of the oracle's gradients of its k entries. One shape per kernel
+    family (one warp per token, four warps per row, sliced keys, scalar
+    access)."""
+    import torch
+    B, _ = W
+    T, nrows = 211, 4
+    sites = {1: [0, 2, 2, 1, 2, 0], 2: [3, 3], 3: [1, 0, 3, 2, 1]}
+    inputs = synth.HostInputs(seed=17, q_std=0.5, g_kind="random")
+    bank = B.Bank(T, d, r, nrows, dtype)
+    for j in range(nrows):
+        o = inputs.output(j, T, d, dtype)
+        bank.rows[j].copy_(o)
+        bank.append(bank.rows[j])
+    host = [inputs.host_output(j, T, d, dtype) for j in range(nrows)]
+    fw = {s: bank.route_fwd(lst, H, inputs.query(s, r), inputs.norm_weight(s, r), site_id=s)
+          for s, lst in sites.items()}
+    bank.zero_grad()
+    got = {}
+    for s in reversed(list(sites)):
+        out, lse = fw[s]
+        got[s] = bank.route_bwd(sites[s], H, inputs.query(s, r), inputs.norm_weight(s, r), out,
+                                inputs.dout(s, T, d, dtype), lse, site_id=s)
+    torch.cuda.synchronize()
+    assert B.ar_device_error() == 0
+    tol = TOL[dtype]
+    dsrc = [np.zeros((T, d)) for _ in range(nrows)]
+    for s in reversed(list(sites)):
+        lst = sites[s]
+        qh, gh = inputs.host_query(s, r), inputs.host_norm_weight(s, r)
+        out, lse = orc.route_fwd([host[j] for j in lst], qh, gh, H, r=r)
+        assert nmax(to64(fw[s][0]), out) <= tol, f"out{s}"
+        assert nmax(to64(fw[s][1]), lse) <= tol, f"lse{s}"
+        per_entry, dq, dg = orc.route_bwd([host[j] for j in lst], qh, gh,
+                                          inputs.host_dout(s, T, d, dtype), H, r=r)
+        for j, g in zip(lst, per_entry):
+            dsrc[j] += g
+        assert nmax(to64(got[s][0]), dq) <= tol, f"dq{s}"
+        assert nmax(to64(got[s][1]), dg) <= tol, f"dg{s}"
+    for j in range(nrows):
+        assert nmax(to64(bank.grad[j]), dsrc[j]) <= tol, f"dV{j}"
+
+
 def test_single_source_site_is_identity(W, orc):
     import torch
     B, wl = W
@@ -271,8 +334,8 @@ def test_error_paths_on_device(W):
     assert e.value.name == "AR_ERR_CAPACITY"
     q = torch.zeros(512, device="cuda")
     with pytest.raises(B.ARError) as e:
-        bank.route_fwd([0, 0], 4, q)
-    assert e.value.name == "AR_ERR_INVALID_ARG"                   # duplicate source
+        bank.route_fwd([0, 3], 4, q)
+    assert e.value.name == "AR_ERR_INVALID_ARG"                   # row not appended
     out1, lse1 = bank.route_fwd([0, 1], 4, q, site_id=1)
     out2, lse2 = bank.route_fwd([0, 1, 2], 4, q, site_id=2)
     bank.zero_grad()
