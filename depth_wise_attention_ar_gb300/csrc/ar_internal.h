@@ -58,12 +58,12 @@ cudaError_t launch_append(const void *src, const void *prev, void *dst, float *i
 cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
                              bool dst_valid, cudaStream_t s);
 unsigned int *device_error_word();
-// Some kernel family serves n_src distinct rows at this shape.
-bool route_supported(int d, int r, int H, int n_src, ar_dtype dt);
-// The family serving one source may hand sites with many sources to the
-// scalar-access kernels (whose workspace differs).
-bool may_fall_back_to_generic(int d, int r, int H, ar_dtype dt);
-// Workspace rows (warps) of the scalar-access backward on the current device.
+// Some kernel family serves n_src distinct rows at this shape (`repeats`: the
+// site lists a row more than once).
+bool route_supported(int d, int r, int H, int n_src, ar_dtype dt, bool repeats);
+// Workspace rows of the scalar-access backward on the current device; any
+// site may run there (repeated rows, or a key cache too large for the
+// sliced-key kernels), so every workspace holds at least this many rows.
 cudaError_t generic_bwd_rows(int *rows);
 
 // Shapes of the four-warp kernels: d = 1024 * CPL (CPL in 1..8), H a multiple

@@ -57,7 +57,8 @@ ar_status check_site(const ar_bank *b, const int32_t *rows, int32_t n_src, int32
         while (k < i && rows[k] != rows[i]) ++k;
         distinct += k == i;
     }
-    if (!ar::route_supported(b->d, b->r, H, distinct, b->dtype)) return AR_ERR_UNSUPPORTED;
+    if (!ar::route_supported(b->d, b->r, H, distinct, b->dtype, distinct < n_src))
+        return AR_ERR_UNSUPPORTED;
     for (int i = 0; i < n_src; ++i)
         if (rows[i] < 0 || rows[i] >= b->count) return AR_ERR_INVALID_ARG;
     if (!aligned4(q) || (g && !aligned4(g))) return AR_ERR_ALIGN;
@@ -325,7 +326,7 @@ ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
 {
     if (!bank || !bytes) return AR_ERR_INVALID_ARG;
     if (H < 1 || bank->d % H != 0 || bank->r % H != 0) return AR_ERR_SHAPE;
-    if (!ar::route_supported(bank->d, bank->r, H, 1, bank->dtype)) return AR_ERR_UNSUPPORTED;
+    if (!ar::route_supported(bank->d, bank->r, H, 1, bank->dtype, false)) return AR_ERR_UNSUPPORTED;
     ar::RouteArgs a;
     std::memset(&a, 0, sizeof(a));
     a.d = bank->d;
@@ -335,13 +336,12 @@ ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
     int warps = 0;
     cudaError_t e = ar::route_bwd_grid(a, bank->dtype, &warps);
     if (e != cudaSuccess) return from_cuda(e);
-    if (ar::may_fall_back_to_generic(bank->d, bank->r, H, bank->dtype)) {
-        // sites with many sources may run on the scalar-access kernels
-        int gw = 0;
-        e = ar::generic_bwd_rows(&gw);
-        if (e != cudaSuccess) return from_cuda(e);
-        warps = std::max(warps, gw);
-    }
+    // any site may run on the scalar-access kernels (repeated rows, or more
+    // sources than the sliced-key kernels' key cache holds)
+    int gw = 0;
+    e = ar::generic_bwd_rows(&gw);
+    if (e != cudaSuccess) return from_cuda(e);
+    warps = std::max(warps, gw);
     // [rows, r] partial sums of dq/dg, then a [rows, 4] tail for dL/dalpha
     *bytes = (size_t)warps * ((size_t)bank->r + 4) * sizeof(float);
     return AR_OK;

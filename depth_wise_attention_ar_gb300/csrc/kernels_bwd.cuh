@@ -184,9 +184,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         P = group_sum(P, LPH);
         zr = group_sum(zr, LPH);
         const float iv = cur_inv[n];
-        float z = __fmul_rn(iv, zr);
-        if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
-        const float w = exp2f((z - lse_h) * kLog2e);
+        const float w = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
         const float dz = w * (P - S_h);
         const float C = (H == 1) ? dz * zr : warp_sum(sub == 0 ? dz * zr : 0.f);
         const float coef = iv * iv * iv * C * inv_d;

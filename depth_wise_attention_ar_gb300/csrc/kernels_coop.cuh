@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             for (int j = 0; j < CPL; ++j) zr = __fadd_rn(zr, dot8(qg[j], v[j]));
             zr = group_sum(zr, mp.LPH);
             z = __fmul_rn(zr, iv);
-            if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
         } else {
             if (mp.key_warp) {
                 float zr = 0.f;
@@ -162,11 +161,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                     zr = __fadd_rn(zr, dot8(qg[j], kv));
                 }
                 zr = group_sum(zr, mp.LPHk);
-                if (mp.ksub == 0) {
-                    float zz = __fmul_rn(zr, iv);
-                    if (a.has_bias) zz = __fadd_rn(zz, a.bias[n]);
-                    zs[par * 32 + mp.hk] = zz;
-                }
+                if (mp.ksub == 0) zs[par * 32 + mp.hk] = __fmul_rn(zr, iv);
             }
             __syncthreads();
             z = zs[par * 32 + mp.h];
@@ -372,9 +367,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             __syncthreads();
             zr = zsm[par * 32 + mp.h];
         }
-        float zb = __fmul_rn(iv, zr);
-        if (a.has_bias) zb = __fadd_rn(zb, a.bias[n]);
-        const float wgt = exp2f((zb - lse_h) * kLog2e);
+        const float wgt = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
         const float dz = wgt * (P - S_h);
         const float cpart = warp_sum(mp.sub == 0 ? dz * zr : 0.f);
         if (lane == 0) cws[par * 32 + w] = cpart;

@@ -152,8 +152,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
         zr = group_sum(zr, LPH);
         // __fmul_rn keeps the product uncontracted: the backward recomputes
         // the same bits
-        float z = __fmul_rn(zr, cur_inv[n]);
-        if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
+        const float z = __fmul_rn(zr, cur_inv[n]);
         if (n == 0) {  // first source of the token: weight exp(0) = 1 below
             m = z;
             l = 0.f;

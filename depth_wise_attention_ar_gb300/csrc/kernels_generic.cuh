@@ -14,8 +14,11 @@
 // inner, so that every load instruction reads 32 consecutive elements of one
 // row. Per-warp shared memory holds the site's scores or weights [N, H]; the
 // block shares q*g over the key coordinates. The backward also keeps its
-// warp's dq/dg partial sums (one per key coordinate) in shared memory and
-// writes them to the workspace at the end.
+// warp's dq/dg partial sums (one per key coordinate) in shared memory; at the
+// end each block adds its warps' sums, in order, into one workspace row.
+// Sites that list a row k > 1 times also run here: the row enters once with
+// log k added to its score (the softmax over the list), a term the tiled
+// kernels leave out of their inner loops.
 #pragma once
 
 #include "common.cuh"
@@ -204,12 +207,27 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
         }
         __syncwarp();
     }
-    // this warp's dq/dg partial sums -> workspace row gw; dL/dalpha -> tail
-    for (int c = lane; c < r; c += 32) a.ws[gw * r + c] = U[c];
-    if (a.dalpha && lane == 0) {
-        float *tail = a.ws + GW * r + gw * 4;
-        tail[0] = dal;
-        tail[1] = tail[2] = tail[3] = 0.f;
+    // the block's dq/dg partial sums (its warps in order) -> workspace row
+    // blockIdx.x; dL/dalpha -> tail
+    __syncthreads();
+    const size_t wf = gen_bwd_warp_floats(N, H, r);
+    const float *U0 = gsm + r + (U - W);                        // warp 0's U
+    for (int c = threadIdx.x; c < r; c += blockDim.x) {
+        float s = 0.f;
+        for (int w = 0; w < wpb; ++w) s += U0[(size_t)w * wf + c];
+        a.ws[(int64_t)blockIdx.x * r + c] = s;
+    }
+    if (a.dalpha) {
+        __shared__ float s_dal[4];
+        if (lane == 0) s_dal[warp] = dal;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float s = 0.f;
+            for (int w = 0; w < wpb; ++w) s += s_dal[w];
+            float *tail = a.ws + (int64_t)gridDim.x * r + (int64_t)blockIdx.x * 4;
+            tail[0] = s;
+            tail[1] = tail[2] = tail[3] = 0.f;
+        }
     }
 }
 
@@ -229,16 +247,16 @@ cudaError_t dispatch_generic_fwd(const RouteArgs &a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-// The grid is SMs x kGenWarpsPerSm warps whatever the block shape, so the
-// workspace (one row per warp) does not depend on the source count.
+// The grid is SMs x kGenBlocksPerSm blocks whatever their warp count, so the
+// workspace (one row per block) does not depend on the source count.
 template <typename T>
-cudaError_t dispatch_generic_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps)
+cudaError_t dispatch_generic_bwd(const RouteArgs *a, cudaStream_t s, int *grid_rows)
 {
-    int GW = 0;
-    cudaError_t e = generic_bwd_rows(&GW);
+    int blocks = 0;
+    cudaError_t e = generic_bwd_rows(&blocks);
     if (e != cudaSuccess) return e;
-    if (grid_warps) {
-        *grid_warps = GW;
+    if (grid_rows) {
+        *grid_rows = blocks;
         return cudaSuccess;
     }
     const int wpb = gen_block_warps(gen_bwd_warp_floats(a->n_src, a->H, a->r), a->r);
@@ -248,7 +266,7 @@ cudaError_t dispatch_generic_bwd(const RouteArgs *a, cudaStream_t s, int *grid_w
     int unused = 0;
     e = persistent_grid(k, wpb * 32, smem, &unused);  // shared-memory opt-in
     if (e != cudaSuccess) return e;
-    route_bwd_generic_kernel<T><<<GW / wpb, wpb * 32, smem, s>>>(*a, wpb);
+    route_bwd_generic_kernel<T><<<blocks, wpb * 32, smem, s>>>(*a, wpb);
     return cudaGetLastError();
 }
 

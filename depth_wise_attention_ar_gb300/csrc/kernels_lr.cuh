@@ -158,11 +158,7 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
                 }
             }
             zr = group_sum(zr, LPH);
-            if (sub == 0) {
-                float zz = __fmul_rn(zr, cinv[n]);
-                if (a.has_bias) zz = __fadd_rn(zz, a.bias[n]);
-                zs[n * H + h] = zz;
-            }
+            if (sub == 0) zs[n * H + h] = __fmul_rn(zr, cinv[n]);
         }
         __syncwarp();
         if (sub == 0) {  // exact softmax over the N sources of head h
@@ -389,9 +385,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
         P = alpha * group_sum(P, LPH);
         zr = group_sum(zr, LPH);
         const float iv = cur_inv[n];
-        float z = __fmul_rn(iv, zr);
-        if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
-        const float w = exp2f((z - lse_h) * kLog2e);
+        const float w = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
         const float dz = w * (P - S_h);
         const float C = (H == 1) ? dz * zr : warp_sum(sub == 0 ? dz * zr : 0.f);
         const float coef = iv * iv * iv * C * inv_width;

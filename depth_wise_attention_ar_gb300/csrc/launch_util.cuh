@@ -8,6 +8,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <utility>
 
 namespace ar {
 
@@ -15,6 +16,9 @@ inline cudaError_t persistent_grid(const void *kern, int threads, size_t smem, i
 {
     static std::mutex mu;
     static std::map<std::tuple<const void *, size_t, int>, int> cache;
+    // the dynamic shared-memory opt-in of each kernel only grows: a kernel
+    // launched with several sizes keeps the largest, so every cached size fits
+    static std::map<std::pair<const void *, int>, size_t> opt_in;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -25,10 +29,12 @@ inline cudaError_t persistent_grid(const void *kern, int threads, size_t smem, i
         *grid = it->second;
         return cudaSuccess;
     }
-    if (smem > 48 * 1024) {
+    size_t &cap = opt_in[std::make_pair(kern, dev)];
+    if (smem > 48 * 1024 && smem > cap) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
+        cap = smem;
     }
     int per_sm = 0, sms = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);

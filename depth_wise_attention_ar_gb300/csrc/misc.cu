@@ -40,16 +40,23 @@ unsigned int *device_error_word()
 // coordinates: the last r ("Low-Rank Attention Residuals" Eq. 11/13), or all
 // d for the full-width norm ("Multi-Head Attention Residuals" Appendix E).
 // The source is a strided [T, d] view: element (t, c) at src[t * ld + c * es]
-// (ld = 0 broadcasts one vector to every token). VEC: 16-byte accesses
-// (d a multiple of 8, es = 1, aligned rows); otherwise one element at a time.
-// Both walk the row in the same 8-column chunks (lane-strided, columns in
-// order within a chunk), so they give the same bits.
+// (ld = 0 broadcasts one vector to every token).
+//   kInPlace: the row already sits in its slot; 16-byte reads of its RMS
+//             chunks only.
+//   kCopy   : 16-byte reads of src (and prev), 16-byte stores (d and the
+//             first RMS column multiples of 8, es = 1, aligned rows).
+//   kScalar : anything else, one element at a time.
+// kScalar walks the row in the same 8-column chunks and lane order as the
+// 16-byte mode it stands in for, so a strided source gives the same bits as
+// a contiguous one.
+enum AppendMode { kInPlace = 0, kCopy = 1, kScalar = 2 };
+
 __device__ __forceinline__ float round_bf16(float x)
 {
     return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-template <typename T, bool VEC>
+template <typename T, int MODE>
 __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev, T *dst, float *inv,
                                                      int64_t TT, int d, int r, int inv_ld,
                                                      int norm_full, float eps, int64_t ld,
@@ -65,38 +72,55 @@ __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev
         const T *s = src + t * ld;
         T *o = dst + t * d;
         float ss = 0.f;
-        // a row already in its slot is only read for its RMS coordinates
-        for (int c = (in_place ? col0 / 8 : 0) + lane; c < nch; c += 32) {
-            float x[8];
-            if constexpr (VEC) {
-                ld_chunk_g(in_place ? o + c * 8 : s + c * 8, x);
+        if constexpr (MODE == kInPlace) {
+            for (int c = col0 / 8 + lane; c < nch; c += 32) {
+                float x[8];
+                ld_chunk_g(o + c * 8, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+            }
+        } else if constexpr (MODE == kCopy) {
+            for (int c = lane; c < nch; c += 32) {
+                float x[8];
+                ld_chunk_g(s + c * 8, x);
                 if (prev) {
                     float p[8];
                     ld_chunk_g(prev + t * d + c * 8, p);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] += p[e];
                 }
-                if (!in_place) st_chunk_g(o + c * 8, x);
-            } else {
+                st_chunk_g(o + c * 8, x);
+                if (c * 8 >= col0) {
+                    if constexpr (sizeof(T) == 2) {
+                        // square the stored (rounded) value
+                        float xr[8];
+                        uint4 u;
+                        u.x = pack_bf16x2(x[0], x[1]);
+                        u.y = pack_bf16x2(x[2], x[3]);
+                        u.z = pack_bf16x2(x[4], x[5]);
+                        u.w = pack_bf16x2(x[6], x[7]);
+                        unpack_bf16x8(u, xr);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(xr[e], xr[e], ss);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                    }
+                }
+            }
+        } else {
+            for (int c = (in_place ? col0 / 8 : 0) + lane; c < nch; c += 32) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int col = c * 8 + e;
-                    x[e] = 0.f;
                     if (col < d) {
                         float v = to_f32(in_place ? o[col] : s[col * es]);
                         if (prev) v += to_f32(prev[t * d + col]);
                         if (!in_place) st_elem(o + col, v);
-                        x[e] = v;
+                        // square the stored (rounded) value
+                        const float vr = sizeof(T) == 2 ? round_bf16(v) : v;
+                        if (col >= col0) ss = fmaf(vr, vr, ss);
                     }
-                }
-            }
-            if (c * 8 + 8 > col0) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int col = c * 8 + e;
-                    // square the stored (rounded) value
-                    const float xr = sizeof(T) == 2 ? round_bf16(x[e]) : x[e];
-                    if (col >= col0 && col < d) ss = fmaf(xr, xr, ss);
                 }
             }
         }
@@ -113,9 +137,13 @@ static cudaError_t append_t(const void *src, const void *prev, void *dst, float 
     const bool in_place = src == dst && prev == nullptr && ld == d && es == 1;
     const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
                          reinterpret_cast<uintptr_t>(prev);
-    const bool vec = d % 8 == 0 && es == 1 && (ld * (int64_t)sizeof(E)) % 16 == 0 && (al & 15) == 0;
-    const void *k = vec ? reinterpret_cast<const void *>(&append_kernel<E, true>)
-                        : reinterpret_cast<const void *>(&append_kernel<E, false>);
+    const int col0 = norm_full ? 0 : d - r;
+    const bool vec = d % 8 == 0 && col0 % 8 == 0 && es == 1 &&
+                     (ld * (int64_t)sizeof(E)) % 16 == 0 && (al & 15) == 0;
+    const int mode = !vec ? kScalar : in_place ? kInPlace : kCopy;
+    const void *k = mode == kInPlace ? reinterpret_cast<const void *>(&append_kernel<E, kInPlace>)
+                    : mode == kCopy  ? reinterpret_cast<const void *>(&append_kernel<E, kCopy>)
+                                     : reinterpret_cast<const void *>(&append_kernel<E, kScalar>);
     int grid = 0;
     cudaError_t e = persistent_grid(k, 256, 0, &grid);
     if (e != cudaSuccess) return e;
@@ -123,12 +151,15 @@ static cudaError_t append_t(const void *src, const void *prev, void *dst, float 
     if (need < grid) grid = (int)need;
     const E *sp = static_cast<const E *>(src), *pp = static_cast<const E *>(prev);
     E *dp = static_cast<E *>(dst);
-    if (vec)
-        append_kernel<E, true><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld, norm_full,
-                                                    eps, ld, es, in_place);
-    else
-        append_kernel<E, false><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld,
+    if (mode == kInPlace)
+        append_kernel<E, kInPlace><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld,
+                                                        norm_full, eps, ld, es, in_place);
+    else if (mode == kCopy)
+        append_kernel<E, kCopy><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld,
                                                      norm_full, eps, ld, es, in_place);
+    else
+        append_kernel<E, kScalar><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld,
+                                                       norm_full, eps, ld, es, in_place);
     return cudaGetLastError();
 }
 
@@ -359,7 +390,7 @@ cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q,
 cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 {
     const bool bf = dt == AR_BF16;
-    switch (family_of(a.d, a.r, a.H, a.n_src, bf ? 2 : 4)) {
+    switch (family_of(a.d, a.r, a.H, a.n_src, bf ? 2 : 4, a.has_bias != 0)) {
     case Family::kFull: return bf ? dispatch_fwd<__nv_bfloat16>(a, s) : dispatch_fwd<float>(a, s);
     case Family::kCoop:
         return bf ? dispatch_coop_fwd<__nv_bfloat16>(a, s) : dispatch_coop_fwd<float>(a, s);
@@ -374,7 +405,7 @@ cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 static cudaError_t bwd_any(const RouteArgs &a, ar_dtype dt, cudaStream_t s, int *rows)
 {
     const bool bf = dt == AR_BF16;
-    switch (family_of(a.d, a.r, a.H, a.n_src, bf ? 2 : 4)) {
+    switch (family_of(a.d, a.r, a.H, a.n_src, bf ? 2 : 4, a.has_bias != 0)) {
     case Family::kFull:
         return bf ? dispatch_bwd<__nv_bfloat16>(&a, s, rows) : dispatch_bwd<float>(&a, s, rows);
     case Family::kCoop:
@@ -399,14 +430,9 @@ cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_rows)
     return bwd_any(a, dt, nullptr, grid_rows);
 }
 
-bool route_supported(int d, int r, int H, int n_src, ar_dtype dt)
+bool route_supported(int d, int r, int H, int n_src, ar_dtype dt, bool repeats)
 {
-    return family_of(d, r, H, n_src, dt == AR_BF16 ? 2 : 4) != Family::kNone;
-}
-
-bool may_fall_back_to_generic(int d, int r, int H, ar_dtype dt)
-{
-    return family_of(d, r, H, 1, dt == AR_BF16 ? 2 : 4) == Family::kSliced;
+    return family_of(d, r, H, n_src, dt == AR_BF16 ? 2 : 4, repeats) != Family::kNone;
 }
 
 cudaError_t generic_bwd_rows(int *rows)
@@ -415,7 +441,7 @@ cudaError_t generic_bwd_rows(int *rows)
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    *rows = sms * kGenWarpsPerSm;
+    *rows = sms * kGenBlocksPerSm;
     return cudaSuccess;
 }
 

@@ -41,9 +41,10 @@ inline size_t lr_fwd_smem_bytes(int d, int r, int N, int H, size_t esize)
 __host__ __device__ inline int lr_kmax(int r) { return (r + 255) / 256; }
 
 // ---- scalar-access family ----------------------------------------------------------
-// Warps the backward's workspace is sized for (fixed, so that it does not
-// depend on the site's source count): SMs x this.
-constexpr int kGenWarpsPerSm = 8;
+// Blocks of the backward per SM. Each block reduces its warps' dq/dg partial
+// sums into one workspace row, so the workspace (SMs x this rows) does not
+// depend on the source count, which sets the warps per block.
+constexpr int kGenBlocksPerSm = 2;
 constexpr size_t kGenSmemLimit = 200 * 1024;
 
 // Per-warp shared floats of the forward: weights [N, H], lse [H], inverse RMS [N].
@@ -70,14 +71,16 @@ inline int gen_block_warps(size_t warp_floats, int r)
 // Other d <= 4096 with whole 8-column key chunks per head and the key cache
 // within its limit: one warp per token, two sweeps (kSliced).
 // Everything else: one warp per token with scalar accesses (kGeneric), as long
-// as its per-warp arrays fit.
+// as its per-warp arrays fit. So do sites that list a row more than once
+// (`repeats`): only these kernels add the log-multiplicity to a score, which
+// keeps that term out of the tiled kernels' inner loops.
 enum class Family { kFull, kCoop, kSliced, kGeneric, kNone };
 
-inline Family family_of(int d, int r, int H, int N, size_t esize)
+inline Family family_of(int d, int r, int H, int N, size_t esize, bool repeats)
 {
     if (H < 1 || d <= 0 || r <= 0 || r > d || d % H != 0 || r % H != 0) return Family::kNone;
     if (N < 1 || N > AR_MAX_SOURCES) return Family::kNone;
-    if (d % 256 == 0 && r % 8 == 0) {
+    if (!repeats && d % 256 == 0 && r % 8 == 0) {
         const bool pow2_h = H <= 32 && (32 % H) == 0;
         if (r == d && d <= 2048 && pow2_h) return Family::kFull;
         if (r % 256 == 0 && coop_supported(d, r, H)) return Family::kCoop;

@@ -48,8 +48,9 @@
  *   - other r <= d with d <= 4096, H in {1,...,32} a power of two, r/H a
  *     multiple of 8 and r <= 4096 (the forward's key cache,
  *     2*n_src*r*sizeof(dtype) bytes, within 200 KB).
- * Every other shape runs on the scalar-access kernels ("Low-Rank Attention
- * Residuals", Appendix I: unaligned widths such as d = 513), which hold the
+ * Every other shape, and every site that lists a row twice, runs on the
+ * scalar-access kernels ("Low-Rank Attention Residuals", Appendix I:
+ * unaligned widths such as d = 513, repeated sources), which hold the
  * site's [n_src, H] scores per warp in shared memory and return
  * AR_ERR_UNSUPPORTED only when even one warp's arrays exceed 200 KB
  * (about n_src*H > 20000). Row/output pointers must be 16-byte aligned
@@ -192,7 +193,8 @@ ar_status ar_bank_reset(ar_bank *bank);
  *                 the list, so a row listed k times carries k times the
  *                 weight of one listed once. It is still read once per token
  *                 (log k is added to its score) and its gradient is the sum
- *                 over its k entries.
+ *                 over its k entries. Such sites run on the scalar-access
+ *                 kernels (see "Shapes" above).
  *   H           : routing heads
  *   q           : device float [r], the site's query
  *   g           : device float [r] RMSNorm weight, or NULL for ones

@@ -233,6 +233,38 @@ def test_repeated_sources(W, orc, d, r, H, dtype):
         assert nmax(to64(bank.grad[j]), dsrc[j]) <= tol, f"dV{j}"
 
 
+@pytest.mark.parametrize("d,r,H", [(2560, 2048, 8), (513, 513, 1)])
+def test_source_counts_down_then_up(W, orc, d, r, H):
+    """Sites whose shared-memory need depends on the source count (the sliced
+    keys' cache, the scalar-access kernels' score arrays), in the order 12, 8,
+    12 sources: the launch for 12 after one for 8 still has its shared memory."""
+    import torch
+    B, _ = W
+    T, n, dtype = 64, 12, "bf16"
+    inputs = synth.HostInputs(seed=29, q_std=0.5, g_kind="random")
+    bank = B.Bank(T, d, r, n, dtype)
+    for j in range(n):
+        bank.append(inputs.output(j, T, d, dtype))
+    host = [inputs.host_output(j, T, d, dtype) for j in range(n)]
+    sites = {1: list(range(12)), 2: list(range(8)), 3: list(range(12))}
+    fw = {s: bank.route_fwd(lst, H, inputs.query(s, r), inputs.norm_weight(s, r), site_id=s)
+          for s, lst in sites.items()}
+    bank.zero_grad()
+    dq = {}
+    for s in (3, 2, 1):
+        dq[s] = bank.route_bwd(sites[s], H, inputs.query(s, r), inputs.norm_weight(s, r),
+                               fw[s][0], inputs.dout(s, T, d, dtype), fw[s][1], site_id=s)[0]
+    torch.cuda.synchronize()
+    assert B.ar_device_error() == 0
+    for s, lst in sites.items():
+        qh, gh = inputs.host_query(s, r), inputs.host_norm_weight(s, r)
+        out, lse = orc.route_fwd([host[j] for j in lst], qh, gh, H, r=r)
+        assert nmax(to64(fw[s][0]), out) <= TOL[dtype]
+        _, dq_r, _ = orc.route_bwd([host[j] for j in lst], qh, gh,
+                                   inputs.host_dout(s, T, d, dtype), H, r=r)
+        assert nmax(to64(dq[s]), dq_r) <= TOL[dtype]
+
+
 def test_single_source_site_is_identity(W, orc):
     import torch
     B, wl = W
