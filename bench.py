@@ -71,7 +71,7 @@ def peaks():
 def kernel_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "depth_wise_attention_ar_gb300", "csrc")
-    for name in ("kernels_bwd.cuh", "common.cuh"):
+    for name in ("kernels_bwd.cuh", "common.cuh", "ar_internal.h", "launch_util.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
