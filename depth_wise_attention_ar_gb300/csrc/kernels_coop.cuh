@@ -26,7 +26,11 @@ namespace ar {
 
 constexpr int kCoopWarps = 4;
 constexpr int kCoopFwdStages = 4;
-constexpr int kCoopBwdStages = 3;
+// Backward stages of (row + fp32 gradient row). Sliced keys use more
+// registers (two blocks per SM at most), so with bf16 rows they take 4 stages
+// and two blocks of d = 4096 still fit; full keys keep 3, which leaves room
+// for three blocks.
+constexpr int coop_bwd_stages(size_t esize, bool lr) { return esize == 2 && lr ? 4 : 3; }
 
 struct CoopMap {
     int Hw, LPH, hl, sub, h;      // value heads per warp, lanes per head, local head, lane in head, head
@@ -220,10 +224,10 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     }
 }
 
-inline size_t coop_bwd_smem_bytes(int d, size_t esize)
+inline size_t coop_bwd_smem_bytes(int d, size_t esize, bool lr)
 {
-    return (size_t)kCoopBwdStages * ((size_t)d * esize + (size_t)d * 4) + kCoopBwdStages * 8 +
-           3 * 2 * 32 * 4 + AR_MAX_SOURCES * 4;
+    const size_t S = (size_t)coop_bwd_stages(esize, lr);
+    return S * ((size_t)d * esize + (size_t)d * 4) + S * 8 + 3 * 2 * 32 * 4;
 }
 
 template <typename T, int CPL, bool LR>
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     __shared__ uint32_t s_first[AR_MAX_SOURCES / 32];
-    constexpr int S = kCoopBwdStages;
+    constexpr int S = coop_bwd_stages(sizeof(T), LR);
     constexpr int CB = ChunkBytes<T>::value;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = a.d, r = a.r, N = a.n_src, H = a.H;
@@ -248,7 +252,6 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     float *zsm = reinterpret_cast<float *>(bars + S);  // [2][32] raw scores (sliced keys)
     float *dzs = zsm + 64;                              // [2][32] dz per head (sliced keys)
     float *cws = dzs + 64;                              // [2][32] per-warp coupling sums
-    float *cur_inv = cws + 64;                          // [AR_MAX_SOURCES]
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
@@ -312,6 +315,10 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         if (i == lo || n == 0) {
             const T *grow = static_cast<const T *>(a.dout) + tok * d;
             const T *orow = static_cast<const T *>(a.fout) + tok * d;
+            if (threadIdx.x == 0 && (tok + 1) * N < hi) {  // the next token's rows, into L2
+                prefetch_l2(grow + d, vbytes);
+                prefetch_l2(orow + d, vbytes);
+            }
             float sp = 0.f, raw = 0.f;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
@@ -328,17 +335,18 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             S_h = group_sum(sp, mp.LPH);
             if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted once
             lse_h = __ldg(a.lse + tok * H + mp.h);
-            for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
-                cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
-            __syncthreads();
         }
+        // the source's inverse RMS (a small, cache-resident table), requested
+        // before the wait for the staged row so that its latency hides there
+        const float iv = __ldg(a.inv + tok * a.inv_ld + s_rows[n]);
+        // The first block barrier of an item also carries the wait's outcome
+        // (all threads leave together on a timeout); with sliced keys it also
+        // frees the stage of the previous item, which every warp has finished
+        // by then.
         const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
-        if (__syncthreads_or(!got)) { ok = false; break; }
-        phase ^= 1u << slot;
         unsigned char *vb = ring + (size_t)slot * slot_bytes;
         float *gb_s = reinterpret_cast<float *>(vb + vbytes);
         const bool first = (s_first[n >> 5] >> (n & 31)) & 1u;
-        const float iv = cur_inv[n];
 
         // pass A: value dots, raw scores
         float v[CPL][8];
@@ -364,7 +372,9 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                 zk = group_sum(zk, mp.LPHk);
                 if (mp.ksub == 0) zsm[par * 32 + mp.hk] = zk;
             }
-            __syncthreads();
+            if (__syncthreads_or(!got)) { ok = false; break; }
+            phase ^= 1u << slot;
+            if (i > lo && issued < hi) issue_next();
             zr = zsm[par * 32 + mp.h];
         }
         const float wgt = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
@@ -372,7 +382,12 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         const float cpart = warp_sum(mp.sub == 0 ? dz * zr : 0.f);
         if (lane == 0) cws[par * 32 + w] = cpart;
         if (LR && mp.sub == 0) dzs[par * 32 + mp.h] = dz;
-        __syncthreads();
+        if constexpr (LR) {
+            __syncthreads();
+        } else {
+            if (__syncthreads_or(!got)) { ok = false; break; }
+            phase ^= 1u << slot;
+        }
         float C = 0.f;
 #pragma unroll
         for (int k = 0; k < kCoopWarps; ++k) C += cws[par * 32 + k];
@@ -446,8 +461,12 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                 st_f32x8_g_sw(grad_row + cidx[j] * 8, sw, nv);
             }
         }
-        __syncthreads();  // every warp is past this stage
-        if (issued < hi) issue_next();
+        if constexpr (!LR) {
+            // full keys: free this stage at once (three blocks per SM want
+            // the earliest refill)
+            __syncthreads();
+            if (issued < hi) issue_next();
+        }
         par ^= 1;
         if (++n == N) { n = 0; ++tok; }
         if (++slot == S) slot = 0;
@@ -489,7 +508,7 @@ template <typename T, int CPL, bool LR>
 cudaError_t coop_bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_rows)
 {
     const void *k = reinterpret_cast<const void *>(&route_bwd_coop_kernel<T, CPL, LR>);
-    const size_t smem = coop_bwd_smem_bytes(a->d, sizeof(T));
+    const size_t smem = coop_bwd_smem_bytes(a->d, sizeof(T), LR);
     int grid = 0;
     cudaError_t e = persistent_grid(k, kCoopWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
