@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     bool ok = true;
     for (; i < total; ++i) {
         if (n == 0) {
+            // delta form: the residual-stream row this token's epilogue reads, into L2
+            if (a.partial && threadIdx.x == 0)
+                prefetch_l2(static_cast<const T *>(a.partial) + tok * d, row_bytes);
             for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
                 cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
             __syncthreads();
