@@ -190,6 +190,8 @@ class Microbatch:
         last = max(plan.run_sites)
         delta = self.cfg.delta
         for t in range(last + 1):
+            if on_site:
+                on_site("fwd_begin", t)
             if t < self.n_rows:
                 if t == 0 and delta:
                     bank.append_broadcast(self.null, stream)
