@@ -3,7 +3,7 @@
 // For one routing site, given dL/dout, emits dL/ds_n for every listed source
 // into the shared fp32 gradient rows (store on a row's first touch, in-place
 // accumulation afterwards: "Multi-Head Attention Residuals", Appendix E,
-// Figure 10) and per-warp partial sums for dL/dq and dL/dg.
+// Figure 10) and per-block partial sums for dL/dq and dL/dg.
 //
 // Per token t, source n, head h (w = softmax weight, recomputed from the
 // saved log-sum-exp; G = dL/dout):
@@ -49,7 +49,7 @@ inline size_t bwd_smem_bytes(int d, size_t esize)
 }
 
 template <typename T, int CPL>
-__global__ void __launch_bounds__(kBwdWarps * 32)
+__global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     route_bwd_kernel(const __grid_constant__ RouteArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -225,45 +225,64 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
         }
     }
 
-    // per-warp partial sums U -> workspace row gw; dL/dalpha partial -> tail
-    float *wrow = a.ws + gw * d;
+    // The block's partial sums: each warp puts U in its own (now idle) part of
+    // the ring, then the block adds the warps in order into workspace row
+    // blockIdx.x (a quarter of the rows a per-warp layout would leave for
+    // the reduction to read); dL/dalpha partials -> tail.
+    __syncthreads();
+    float *uw = reinterpret_cast<float *>(ring);
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) st_f32x8_g_sw(wrow + cidx[j] * 8, sw, U[j]);
-    if (a.dalpha && lane == 0)
-        *reinterpret_cast<float4 *>(a.ws + GW * d + gw * 4) = make_float4(dal, 0.f, 0.f, 0.f);
+    for (int j = 0; j < CPL; ++j) st_f32x8_g_sw(uw + cidx[j] * 8, sw, U[j]);
+    __shared__ float s_dal[kBwdWarps];
+    if (lane == 0) s_dal[warp] = dal;
+    __syncthreads();
+    const int64_t GB = gridDim.x, gb = blockIdx.x;
+    const size_t wstride = (size_t)S * slot_bytes / sizeof(float);
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < kBwdWarps; ++k) t += reinterpret_cast<const float *>(rings)[k * wstride + c];
+        a.ws[gb * d + c] = t;
+    }
+    if (a.dalpha && threadIdx.x == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < kBwdWarps; ++k) t += s_dal[k];
+        *reinterpret_cast<float4 *>(a.ws + GB * d + gb * 4) = make_float4(t, 0.f, 0.f, 0.f);
+    }
 }
 
 template <typename T, int CPL>
-cudaError_t bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_warps)
+cudaError_t bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_rows)
 {
     const void *k = reinterpret_cast<const void *>(&route_bwd_kernel<T, CPL>);
     const size_t smem = bwd_smem_bytes(a->d, sizeof(T));
     int grid = 0;
     cudaError_t e = persistent_grid(k, kBwdWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
-    if (grid_warps) {
-        *grid_warps = grid * kBwdWarps;
+    if (grid_rows) {
+        *grid_rows = grid;  // workspace rows: one per block
         return cudaSuccess;
     }
     route_bwd_kernel<T, CPL><<<grid, kBwdWarps * 32, smem, s>>>(*a);
     return cudaGetLastError();
 }
 
-// Same shapes as the forward. With grid_warps != nullptr only the grid (in
-// warps = workspace rows) is computed and nothing is launched.
+// Same shapes as the forward. With grid_rows != nullptr only the grid (in
+// blocks = workspace rows) is computed and nothing is launched.
 template <typename T>
-cudaError_t dispatch_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps)
+cudaError_t dispatch_bwd(const RouteArgs *a, cudaStream_t s, int *grid_rows)
 {
     if (a->r != a->d) return cudaErrorNotSupported;
     switch (a->d / 256) {
-    case 1: return bwd_inst<T, 1>(a, s, grid_warps);
-    case 2: return bwd_inst<T, 2>(a, s, grid_warps);
-    case 3: return bwd_inst<T, 3>(a, s, grid_warps);
-    case 4: return bwd_inst<T, 4>(a, s, grid_warps);
-    case 5: return bwd_inst<T, 5>(a, s, grid_warps);
-    case 6: return bwd_inst<T, 6>(a, s, grid_warps);
-    case 7: return bwd_inst<T, 7>(a, s, grid_warps);
-    case 8: return bwd_inst<T, 8>(a, s, grid_warps);
+    case 1: return bwd_inst<T, 1>(a, s, grid_rows);
+    case 2: return bwd_inst<T, 2>(a, s, grid_rows);
+    case 3: return bwd_inst<T, 3>(a, s, grid_rows);
+    case 4: return bwd_inst<T, 4>(a, s, grid_rows);
+    case 5: return bwd_inst<T, 5>(a, s, grid_rows);
+    case 6: return bwd_inst<T, 6>(a, s, grid_rows);
+    case 7: return bwd_inst<T, 7>(a, s, grid_rows);
+    case 8: return bwd_inst<T, 8>(a, s, grid_rows);
     default: return cudaErrorNotSupported;
     }
 }

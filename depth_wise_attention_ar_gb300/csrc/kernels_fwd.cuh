@@ -128,9 +128,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     bool ok = true;
     for (; i < total; ++i) {
         if (n == 0) {
-            // delta form: the residual-stream row this token's epilogue reads, into L2
-            if (a.partial && lane == 0)
-                prefetch_l2(static_cast<const T *>(a.partial) + tok * d, row_bytes);
 #pragma unroll
             for (int u = 0; u < AR_MAX_SOURCES / 32; ++u) {
                 const int nn = lane + 32 * u;
