@@ -24,6 +24,15 @@
 //   stay in natural units (exp2 only inside the exponent) so that the
 //   backward's recomputed score matches bit for bit.
 // - Grid: persistent, SM count x resident blocks; tokens strided over warps.
+//
+// Sliced keys (SK = true, r < d or any r with whole 8-column key chunks per
+// head): the same single pass, with head h's score taken from key slice h,
+// the h-th r/H block of the last r columns ("Low-Rank Attention Residuals",
+// Eq. 11-12). Lane l of head h also holds key chunks key0 + h*ckh + sub +
+// LPH*j (ckh = r/(8H) chunks per key slice), in the order and with the sums
+// of the sliced-key backward, so both compute the same score bits; the value
+// chunks are read after the weight is known, so only the accumulator and q*g
+// stay in registers.
 #pragma once
 
 #include "common.cuh"
@@ -40,7 +49,7 @@ inline size_t fwd_smem_bytes(int d, size_t esize)
            (size_t)kFwdWarps * AR_MAX_SOURCES * 4;
 }
 
-template <typename T, int CPL>
+template <typename T, int CPL, bool SK>
 __global__ void __launch_bounds__(kFwdWarps * 32)
     route_fwd_kernel(const __grid_constant__ RouteArgs a)
 {
@@ -75,14 +84,26 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     int cidx[CPL];
 #pragma unroll
     for (int j = 0; j < CPL; ++j) cidx[j] = chunk_of<CPL>(h, sub, LPH, j);
-    // query times norm weight over this lane's coordinates
+    // key chunks: the value chunks themselves for full keys; for sliced keys
+    // chunks of key slice h (at most CPL of them per lane since r <= d)
+    const int key0 = SK ? (d - a.r) / 8 : 0, ckh = SK ? a.r / 8 / H : 0;
+    int kidx[CPL];
+    bool kval[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        kval[j] = !SK || sub + LPH * j < ckh;
+        kidx[j] = SK ? key0 + h * ckh + sub + LPH * j : cidx[j];
+    }
+    // query times norm weight over this lane's key coordinates
     float qg[CPL][8];
 #pragma unroll
     for (int j = 0; j < CPL; ++j)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const int c = cidx[j] * 8 + e;
-            qg[j][e] = __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f);
+            const int c = kidx[j] * 8 + e - key0 * 8;
+            qg[j][e] = kval[j] ? __ldg(a.q + c * a.q_stride) *
+                                     (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f)
+                               : 0.f;
         }
 
     // ---- work: tokens gw, gw + GW, ...
@@ -142,12 +163,23 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
         const unsigned char *buf = ring + (size_t)slot * row_bytes;
 
         // score of this lane's head: q_h . (g * s_n)_[h], times inv_n
-        float v[CPL][8];
+        float v[SK ? 1 : CPL][8];
         float zr = 0.f;
+        if constexpr (SK) {
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
-            zr = __fadd_rn(zr, dot8(qg[j], v[j]));
+            for (int j = 0; j < CPL; ++j) {
+                if (kval[j]) {
+                    float kv[8];
+                    ld_chunk_s(reinterpret_cast<const T *>(buf + kidx[j] * CB), kv);
+                    zr = __fadd_rn(zr, dot8(qg[j], kv));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
+                zr = __fadd_rn(zr, dot8(qg[j], v[j]));
+            }
         }
         zr = group_sum(zr, LPH);
         // __fmul_rn keeps the product uncontracted: the backward recomputes
@@ -174,9 +206,17 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
         const float p = exp2f((z - m) * kLog2e);
         l += p;
 #pragma unroll
-        for (int j = 0; j < CPL; ++j)
+        for (int j = 0; j < CPL; ++j) {
+            if constexpr (SK) {
+                float vv[8];
+                ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), vv);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, v[j][e], acc[j][e]);
+                for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, vv[e], acc[j][e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, v[j][e], acc[j][e]);
+            }
+        }
         __syncwarp();
         if (issued < total) issue_next();  // refill the stage just consumed
 
@@ -206,15 +246,15 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     }
 }
 
-template <typename T, int CPL>
+template <typename T, int CPL, bool SK>
 cudaError_t launch_fwd_inst(const RouteArgs &a, cudaStream_t s)
 {
-    const void *k = reinterpret_cast<const void *>(&route_fwd_kernel<T, CPL>);
+    const void *k = reinterpret_cast<const void *>(&route_fwd_kernel<T, CPL, SK>);
     const size_t smem = fwd_smem_bytes(a.d, sizeof(T));
     int grid = 0;
     cudaError_t e = persistent_grid(k, kFwdWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
-    route_fwd_kernel<T, CPL><<<grid, kFwdWarps * 32, smem, s>>>(a);
+    route_fwd_kernel<T, CPL, SK><<<grid, kFwdWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -224,14 +264,34 @@ cudaError_t dispatch_fwd(const RouteArgs &a, cudaStream_t s)
 {
     if (a.r != a.d) return cudaErrorNotSupported;
     switch (a.d / 256) {
-    case 1: return launch_fwd_inst<T, 1>(a, s);
-    case 2: return launch_fwd_inst<T, 2>(a, s);
-    case 3: return launch_fwd_inst<T, 3>(a, s);
-    case 4: return launch_fwd_inst<T, 4>(a, s);
-    case 5: return launch_fwd_inst<T, 5>(a, s);
-    case 6: return launch_fwd_inst<T, 6>(a, s);
-    case 7: return launch_fwd_inst<T, 7>(a, s);
-    case 8: return launch_fwd_inst<T, 8>(a, s);
+    case 1: return launch_fwd_inst<T, 1, false>(a, s);
+    case 2: return launch_fwd_inst<T, 2, false>(a, s);
+    case 3: return launch_fwd_inst<T, 3, false>(a, s);
+    case 4: return launch_fwd_inst<T, 4, false>(a, s);
+    case 5: return launch_fwd_inst<T, 5, false>(a, s);
+    case 6: return launch_fwd_inst<T, 6, false>(a, s);
+    case 7: return launch_fwd_inst<T, 7, false>(a, s);
+    case 8: return launch_fwd_inst<T, 8, false>(a, s);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+// Sliced keys, single pass, d = 256 * CPL with CPL in 1..10 (the
+// sliced-key family's shapes; wider rows use its two-sweep forward).
+template <typename T>
+cudaError_t dispatch_fwd_sk(const RouteArgs &a, cudaStream_t s)
+{
+    switch (a.d / 256) {
+    case 1: return launch_fwd_inst<T, 1, true>(a, s);
+    case 2: return launch_fwd_inst<T, 2, true>(a, s);
+    case 3: return launch_fwd_inst<T, 3, true>(a, s);
+    case 4: return launch_fwd_inst<T, 4, true>(a, s);
+    case 5: return launch_fwd_inst<T, 5, true>(a, s);
+    case 6: return launch_fwd_inst<T, 6, true>(a, s);
+    case 7: return launch_fwd_inst<T, 7, true>(a, s);
+    case 8: return launch_fwd_inst<T, 8, true>(a, s);
+    case 9: return launch_fwd_inst<T, 9, true>(a, s);
+    case 10: return launch_fwd_inst<T, 10, true>(a, s);
     default: return cudaErrorNotSupported;
     }
 }

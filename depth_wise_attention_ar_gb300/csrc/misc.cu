@@ -9,6 +9,7 @@ namespace ar {
 template <typename T> cudaError_t dispatch_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
 template <typename T> cudaError_t dispatch_lr_fwd(const RouteArgs &a, cudaStream_t s);
+template <typename T> cudaError_t dispatch_fwd_sk(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_lr_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
 template <typename T> cudaError_t dispatch_coop_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_coop_bwd(const RouteArgs *a, cudaStream_t s, int *grid_rows);
@@ -395,6 +396,10 @@ cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
     case Family::kCoop:
         return bf ? dispatch_coop_fwd<__nv_bfloat16>(a, s) : dispatch_coop_fwd<float>(a, s);
     case Family::kSliced:
+        // rows up to 2560 wide: one pass with the accumulator in registers;
+        // wider rows: two sweeps with the key tails cached in shared memory
+        if (a.d / 256 <= 10)
+            return bf ? dispatch_fwd_sk<__nv_bfloat16>(a, s) : dispatch_fwd_sk<float>(a, s);
         return bf ? dispatch_lr_fwd<__nv_bfloat16>(a, s) : dispatch_lr_fwd<float>(a, s);
     case Family::kGeneric:
         return bf ? dispatch_generic_fwd<__nv_bfloat16>(a, s) : dispatch_generic_fwd<float>(a, s);
