@@ -24,6 +24,7 @@ STATUS = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_SHAPE", 3: "AR_ERR_ALI
 AR_F32, AR_BF16 = 0, 1
 AR_NORM_KEY, AR_NORM_FULL = 0, 1
 AR_MAX_SOURCES = 256
+AR_MAX_QUERIES = 8
 AR_DEVERR_WAIT_TIMEOUT = 1
 
 # Every function the header declares, with its ctypes signature.
@@ -67,6 +68,7 @@ SIGNATURES = {
                              ctypes.c_int),
     "ar_bank_grad_fold": ([_P, _I32, _I32, _P], ctypes.c_int),
     "ar_route_merge": ([_P, _I32, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "ar_route_fwd_multi": ([_P, _I32P, _I32, _I32, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
     "ar_block_schedule": ([_I32, _I32, _I32P, _I32P, _I32P, _I64, _I64P], ctypes.c_int),
     "ar_device_error": ([_U32P], ctypes.c_int),
 }
@@ -274,6 +276,21 @@ def ar_route_merge(bank, H, out_a, lse_a, out_b, lse_b, out, lse, stream=None):
                                                  _stream(stream)))
 
 
+def _ptr_array(xs):
+    arr = (ctypes.c_void_p * max(1, len(xs)))(*[_ptr(x) for x in xs])
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def ar_route_fwd_multi(bank, rows, H, qs, gs, outs, lses, stream=None):
+    arr, n = _rows(rows)
+    qa, qp = _ptr_array(qs)
+    ga, gp = _ptr_array(gs) if gs is not None else (None, None)
+    oa, op = _ptr_array(outs)
+    la, lp = _ptr_array(lses)
+    _check("ar_route_fwd_multi", _lib.ar_route_fwd_multi(bank, arr, n, H, len(qs), qp, gp, op, lp,
+                                                         _stream(stream)))
+
+
 def ar_block_schedule(M: int, NB: int | None):
     """Returns (acc_from [M+1], sites: list of M+1 row lists)."""
     acc = (ctypes.c_int32 * (M + 1))()
@@ -407,6 +424,23 @@ class Bank:
         ar_route_bwd_delta(self.handle, rows, H, q, g, routed, dout, lse, alpha, dq, dg, dalpha,
                            ws, ws.numel() * 4, site_id, stream)
         return dq, dg, dalpha
+
+    def route_fwd_multi(self, rows, H, qs, gs=None, outs=None, lses=None, stream=None):
+        """Reads of several sites over one row list in one pass (see
+        ar_route_fwd_multi); returns (outs, lses)."""
+        dev = self.rows.device
+        if outs is None:
+            outs = [torch.empty((self.T, self.d), dtype=self.torch_dtype, device=dev) for _ in qs]
+        if lses is None:
+            lses = [torch.empty((self.T, H), dtype=torch.float32, device=dev) for _ in qs]
+        for i, q in enumerate(qs):
+            self._check_tensor(q, (self.r,), torch.float32, f"q[{i}]")
+            if gs is not None and gs[i] is not None:
+                self._check_tensor(gs[i], (self.r,), torch.float32, f"g[{i}]")
+            self._check_tensor(outs[i], (self.T, self.d), self.torch_dtype, f"out[{i}]")
+            self._check_tensor(lses[i], (self.T, H), torch.float32, f"lse[{i}]")
+        ar_route_fwd_multi(self.handle, rows, H, qs, gs, outs, lses, stream)
+        return outs, lses
 
     def append_broadcast(self, vec, stream=None) -> int:
         self._check_tensor(vec, (self.d,), self.torch_dtype, "vec")

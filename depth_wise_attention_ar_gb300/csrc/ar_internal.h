@@ -38,10 +38,23 @@ struct RouteArgs {
     uint32_t first_mask[AR_MAX_SOURCES / 32];  // backward: bit n set = store (first touch)
 };
 
+// The multi-query forward's arguments: the shared fields plus one query,
+// norm weight, output and lse per site.
+struct MultiArgs {
+    RouteArgs base;
+    int nq;
+    const float *q[AR_MAX_QUERIES];
+    const float *g[AR_MAX_QUERIES];
+    void *out[AR_MAX_QUERIES];
+    float *lse[AR_MAX_QUERIES];
+};
+
 // ---- host-side launch entry points (one per kernel family) -----------------
 // Each returns cudaErrorNotSupported when no instantiation covers the shape.
 cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
 cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
+cudaError_t launch_route_fwd_multi(const MultiArgs &m, ar_dtype dt, cudaStream_t s);
+cudaError_t dispatch_fwd_multi_mma(const MultiArgs &m, cudaStream_t s);  // bf16 rows
 cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps);
 // dq and dg are written with the strides of q and g respectively.
 cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, int64_t q_stride,

@@ -322,6 +322,39 @@ ar_status ar_route_fwd_site(ar_bank *bank, const ar_site *site, const void *part
     return route_fwd_impl(bank, *site, partial, alpha, out, routed, lse, stream);
 }
 
+ar_status ar_route_fwd_multi(const ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                             int32_t n_q, const float *const *q, const float *const *g,
+                             void *const *out, float *const *lse, void *stream)
+{
+    if (!bank || !rows || !q) return AR_ERR_INVALID_ARG;
+    if (n_src < 1 || n_src > AR_MAX_SOURCES) return AR_ERR_INVALID_ARG;
+    if (n_q < 1 || n_q > AR_MAX_QUERIES) return AR_ERR_INVALID_ARG;
+    if (H < 1 || bank->d % H != 0 || bank->r % H != 0) return AR_ERR_SHAPE;
+    for (int i = 0; i < n_src; ++i)
+        if (rows[i] < 0 || rows[i] >= bank->count) return AR_ERR_INVALID_ARG;
+    for (int i = 0; i < n_q; ++i) {
+        if (!q[i]) return AR_ERR_INVALID_ARG;
+        if (!aligned4(q[i]) || (g && g[i] && !aligned4(g[i]))) return AR_ERR_ALIGN;
+        if (bank->T > 0) {
+            if (!out || !lse || !out[i] || !lse[i]) return AR_ERR_INVALID_ARG;
+            if (!aligned16(out[i]) || !aligned4(lse[i])) return AR_ERR_ALIGN;
+        }
+    }
+    if (bank->T == 0) return AR_OK;
+    ar::MultiArgs m;
+    std::memset(&m, 0, sizeof(m));
+    fill_common(m.base, bank, rows, n_src, H, q[0], g ? g[0] : nullptr);
+    m.nq = n_q;
+    for (int i = 0; i < n_q; ++i) {
+        m.q[i] = q[i];
+        m.g[i] = g ? g[i] : nullptr;
+        m.out[i] = out[i];
+        m.lse[i] = lse[i];
+    }
+    const cudaError_t e = ar::launch_route_fwd_multi(m, bank->dtype, static_cast<cudaStream_t>(stream));
+    return from_cuda(e);
+}
+
 ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
 {
     if (!bank || !bytes) return AR_ERR_INVALID_ARG;

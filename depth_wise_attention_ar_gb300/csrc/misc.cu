@@ -10,6 +10,7 @@ template <typename T> cudaError_t dispatch_fwd(const RouteArgs &a, cudaStream_t 
 template <typename T> cudaError_t dispatch_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
 template <typename T> cudaError_t dispatch_lr_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_fwd_sk(const RouteArgs &a, cudaStream_t s);
+template <typename T> cudaError_t dispatch_fwd_multi(const MultiArgs &m, cudaStream_t s);
 template <typename T> cudaError_t dispatch_lr_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
 template <typename T> cudaError_t dispatch_coop_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_coop_bwd(const RouteArgs *a, cudaStream_t s, int *grid_rows);
@@ -433,6 +434,22 @@ cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)
 cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_rows)
 {
     return bwd_any(a, dt, nullptr, grid_rows);
+}
+
+// One block per token with one lane per 8-column chunk: d a multiple of 256
+// up to 4096, whole chunks per value and key head.
+cudaError_t launch_route_fwd_multi(const MultiArgs &m, ar_dtype dt, cudaStream_t s)
+{
+    const RouteArgs &a = m.base;
+    if (a.d % 256 != 0 || a.d > 4096 || (a.d / a.H) % 8 != 0 || (a.r / a.H) % 8 != 0)
+        return cudaErrorNotSupported;
+    if (dt == AR_BF16) {
+        // tensor cores where the shape fits them, else the CUDA-core kernel
+        const cudaError_t e = dispatch_fwd_multi_mma(m, s);
+        if (e != cudaErrorNotSupported) return e;
+        return dispatch_fwd_multi<__nv_bfloat16>(m, s);
+    }
+    return dispatch_fwd_multi<float>(m, s);
 }
 
 bool route_supported(int d, int r, int H, int n_src, ar_dtype dt, bool repeats)

@@ -68,6 +68,7 @@ extern "C" {
 #endif
 
 #define AR_MAX_SOURCES 256
+#define AR_MAX_QUERIES 8
 
 typedef enum {
     AR_OK = 0,
@@ -307,6 +308,36 @@ ar_status ar_route_bwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
  * gradient rows), AR_ERR_CUDA.
  */
 ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, void *stream);
+
+/*
+ * Reads of up to AR_MAX_QUERIES sites over one source list, in one pass over
+ * the sources: phase 1 of two-phase block inference ("Low-Rank Attention
+ * Residuals", Sec. 3.4: the queries are input-independent, so the inter-block
+ * reads of all sites of a block can be done first, together; each site's
+ * intra-block read is merged in later with ar_route_merge). Output i is
+ * what ar_route_fwd would give with query q[i] and norm weight g[i], while
+ * every row is read once per token instead of n_q times.
+ *   rows, n_src, H : as ar_route_fwd (a row listed twice enters once with
+ *                    log 2 added to its score)
+ *   n_q            : number of queries, 1..AR_MAX_QUERIES
+ *   q, g           : host arrays of n_q device pointers to float [r]
+ *                    (contiguous); g may be NULL (ones everywhere), and so may
+ *                    any g[i]
+ *   out, lse       : host arrays of n_q device pointers: out[i] [T, d] of the
+ *                    bank dtype (16-byte aligned), lse[i] float [T, H]
+ * Forward only: nothing enters the bank's call record, and there is no
+ * backward (inference). Shapes: d a multiple of 256 up to 4096, d/H and r/H
+ * multiples of 8, r <= 2048, and a token's n_src rows (n_src * d * dtype
+ * bytes) within about 200 KB of shared memory; others get
+ * AR_ERR_UNSUPPORTED (the per-site ar_route_fwd serves every shape). Each
+ * block stages all rows of a token at once, computes every query's scores
+ * and weights, then sums the rows per column for every query.
+ * Errors: AR_ERR_INVALID_ARG (rows, n_q out of range, null pointers),
+ * AR_ERR_SHAPE, AR_ERR_UNSUPPORTED, AR_ERR_ALIGN, AR_ERR_CUDA.
+ */
+ar_status ar_route_fwd_multi(const ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,
+                             int32_t n_q, const float *const *q, const float *const *g,
+                             void *const *out, float *const *lse, void *stream);
 
 /*
  * Merge two partial reads of one site over disjoint source sets A and B into

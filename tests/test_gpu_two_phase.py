@@ -71,3 +71,81 @@ def test_two_phase_block_read_equals_single_read(B, orc, d, r, H, dtype):
         assert _nmax(_t64(lse), ref_lse) < tol, t
         checked += 1
     assert checked >= 6
+
+
+@pytest.mark.parametrize("d,r,H,dtype,nq,N", [(4096, 1024, 8, "bf16", 8, 9), (1280, 1280, 8, "bf16", 3, 5),
+                                               (512, 512, 4, "f32", 1, 4), (1536, 384, 1, "f32", 8, 9),
+                                               (2048, 512, 4, "f32", 5, 7), (768, 768, 3, "bf16", 2, 3)])
+def test_multi_query_read_equals_per_query_reads(B, orc, d, r, H, dtype, nq, N):
+    """ar_route_fwd_multi: output i and lse i match the oracle's read with
+    query i, for full and sliced keys and 1 to 8 queries."""
+    import torch
+    T = 157
+    inp = synth.HostInputs(seed=31, q_std=0.8, g_kind="random")
+    bank = B.Bank(T, d, r, N, dtype)
+    for j in range(N):
+        bank.append(inp.output(j, T, d, dtype))
+    rows = list(range(N))
+    qs = [inp.query(100 + i, r) for i in range(nq)]
+    gs = [inp.norm_weight(100 + i, r) if i % 2 == 0 else None for i in range(nq)]
+    outs, lses = bank.route_fwd_multi(rows, H, qs, gs)
+    torch.cuda.synchronize()
+    assert B.ar_device_error() == 0
+    srcs = [inp.host_output(j, T, d, dtype) for j in range(N)]
+    tol = 1e-5 if dtype == "f32" else 2e-2
+    for i in range(nq):
+        gh = inp.host_norm_weight(100 + i, r) if gs[i] is not None else None
+        ref_out, ref_lse = orc.route_fwd(srcs, inp.host_query(100 + i, r), gh, H, r=r)
+        assert _nmax(_t64(outs[i]), ref_out) < tol, i
+        assert _nmax(_t64(lses[i]), ref_lse) < tol, i
+
+
+@pytest.mark.parametrize("d,r,H,dtype", [(4096, 1024, 8, "bf16"), (1024, 256, 4, "f32")])
+def test_two_phase_with_batched_phase_one(B, orc, d, r, H, dtype):
+    """Phase 1 reads the inter-block rows once for all the sites of a block
+    (ar_route_fwd_multi, the block's input-independent queries); phase 2 reads
+    each site's partial sum and merges. Every merged read equals the oracle's
+    read over all of the site's sources."""
+    import torch
+    from oracle import schedule, storage
+    T, M, NB = 131, 12, 3
+    acc, sites = B.ar_block_schedule(M, NB)
+    inp = synth.HostInputs(seed=37, q_std=0.8, g_kind="random")
+    bank = B.Bank(T, d, r, M + 1, dtype)
+    for t in range(M + 1):
+        o = inp.output(t, T, d, dtype)
+        if acc[t] < 0:
+            bank.rows[t].copy_(o)
+            bank.append(bank.rows[t])
+        else:
+            bank.append(o, acc[t])
+    ref_rows = storage.block_bank([inp.host_output(t, T, d, dtype) for t in range(M + 1)],
+                                  schedule.block_plan(M, NB), dtype)
+    ends = set(schedule.block_ends(M, NB))
+    # group the sites that read a partial sum by their inter-block rows
+    groups = {}
+    for t in range(1, M + 1):
+        if t in ends:
+            continue
+        groups.setdefault(tuple(sites[t][:-1]), []).append(t)
+    tol = 1e-5 if dtype == "f32" else 2e-2
+    checked = 0
+    for inter, members in groups.items():
+        for k in range(0, len(members), B.AR_MAX_QUERIES):
+            batch = members[k:k + B.AR_MAX_QUERIES]
+            qs = [inp.query(t, r) for t in batch]
+            gs = [inp.norm_weight(t, r) for t in batch]
+            outs_a, lses_a = bank.route_fwd_multi(list(inter), H, qs, gs)
+            for t, q, g, out_a, lse_a in zip(batch, qs, gs, outs_a, lses_a):
+                out_b, lse_b = bank.route_fwd([sites[t][-1]], H, q, g, site_id=t)
+                out = torch.empty_like(out_a)
+                lse = torch.empty_like(lse_a)
+                B.ar_route_merge(bank.handle, H, out_a, lse_a, out_b, lse_b, out, lse)
+                torch.cuda.synchronize()
+                ref_out, ref_lse = orc.route_fwd([ref_rows[j] for j in sites[t]],
+                                                 inp.host_query(t, r), inp.host_norm_weight(t, r),
+                                                 H, r=r)
+                assert _nmax(_t64(out), ref_out) < tol, t
+                assert _nmax(_t64(lse), ref_lse) < tol, t
+                checked += 1
+    assert checked >= 6
