@@ -68,10 +68,17 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash() -> str:
+# Sources of the backward kernel each workload's roofline entry measures.
+KERNEL_SOURCES = {
+    "full": ("kernels_bwd.cuh", "common.cuh", "ar_internal.h", "launch_util.cuh", "shapes.h"),
+    "coop": ("kernels_coop.cuh", "common.cuh", "ar_internal.h", "launch_util.cuh", "shapes.h"),
+}
+
+
+def kernel_hash(family: str = "full") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "depth_wise_attention_ar_gb300", "csrc")
-    for name in ("kernels_bwd.cuh", "common.cuh", "ar_internal.h", "launch_util.cuh"):
+    for name in KERNEL_SOURCES[family]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -83,7 +90,7 @@ def measured_traffic(config: str, H: int):
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
         e = rec.get(f"{config}/H{H}")
-        if e and e.get("kernel_hash") == kernel_hash():
+        if e and e.get("kernel_hash") == kernel_hash(e.get("family", "full")):
             return e["bytes_per_launch"]
     except Exception:
         pass
@@ -316,7 +323,7 @@ def main():
         "step_roofline": {"achieved": mbytes["total"] / (ms * 1e-3) / 1e9, "peak": hbm,
                           "unit": "GB/s", "frac": mbytes["total"] / (ms * 1e-3) / 1e9 / hbm,
                           "peak_source": peak_kind},
-        "roofline": {"kernel": "route_bwd_kernel (backward phase, incl. its dq/dg reduce)",
+        "roofline": {"kernel": "the backward kernel (route_bwd_*; backward phase, incl. its dq/dg reduce)",
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
                      "launches_per_step": n_bwd,
