@@ -35,6 +35,8 @@ if ROOT not in sys.path:
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "route_bwd_traffic.json")
+# GB300's nominal HBM3e bandwidth (~8 TB/s); fractions are also reported against it
+NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "routing ms per microbatch fwd+bwd (all sites), tokens/s, % of HBM roofline"
 
@@ -322,10 +324,12 @@ def main():
         "model_bytes": mbytes,
         "step_roofline": {"achieved": mbytes["total"] / (ms * 1e-3) / 1e9, "peak": hbm,
                           "unit": "GB/s", "frac": mbytes["total"] / (ms * 1e-3) / 1e9 / hbm,
+                          "frac_of_nominal": mbytes["total"] / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
                           "peak_source": peak_kind},
         "roofline": {"kernel": "the backward kernel (route_bwd_*; backward phase, incl. its dq/dg reduce)",
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic,
+                     "frac": achieved / hbm, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS, "traffic": traffic,
                      "launches_per_step": n_bwd,
                      "bytes_per_launch_avg": bwd_bytes / n_bwd,
                      "ms_per_launch_avg": bwd_ms / n_bwd,
