@@ -288,6 +288,7 @@ def main():
         total_ms, fwd_ms, bwd_ms = max_over_ranks([total_ms, fwd_ms, bwd_ms],
                                                   device=f"cuda:{local}")
     ms = total_ms / K
+    per_step = sorted(ev[k][0].elapsed_time(ev[k][2]) for k in range(K))
     if binding.ar_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
@@ -321,6 +322,7 @@ def main():
                    "cuda_graphs": use_graph, "l2": "inputs larger than L2 (bank "
                    f"{mb.bank.rows.numel() * mb.bank.rows.element_size() / 1e9:.2f} GB)"},
         "phases_ms": {"forward_and_appends": fwd_ms, "backward": bwd_ms},
+        "step_ms_spread": {"median": per_step[K // 2], "min": per_step[0], "max": per_step[-1]},
         "model_bytes": mbytes,
         "step_roofline": {"achieved": mbytes["total"] / (ms * 1e-3) / 1e9, "peak": hbm,
                           "unit": "GB/s", "frac": mbytes["total"] / (ms * 1e-3) / 1e9 / hbm,
