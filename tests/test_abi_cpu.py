@@ -187,3 +187,14 @@ def test_site_struct_layout_matches_the_header(B, tmp_path):
     S = B.ArSite
     want = [ctypes.sizeof(S)] + [getattr(S, f).offset for f, _ in S._fields_]
     assert got == want
+
+
+def test_multi_query_read_argument_checks(B):
+    h = _bank(B)
+    # nothing appended: a row out of range; query count out of range; null query
+    assert _err(B.ar_route_fwd_multi, h, [0], 4, [FAKE], None, [FAKE], [FAKE], 0) == "AR_ERR_INVALID_ARG"
+    assert _err(B.ar_route_fwd_multi, h, [0], 4, [], None, [], [], 0) == "AR_ERR_INVALID_ARG"
+    nine = [FAKE] * (B.AR_MAX_QUERIES + 1)
+    assert _err(B.ar_route_fwd_multi, h, [0], 4, nine, None, nine, nine, 0) == "AR_ERR_INVALID_ARG"
+    assert _err(B.ar_route_fwd_multi, h, [0], 3, [FAKE], None, [FAKE], [FAKE], 0) == "AR_ERR_SHAPE"
+    B.ar_bank_destroy(h)
