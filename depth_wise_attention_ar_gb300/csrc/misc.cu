@@ -4,7 +4,11 @@
 #include "launch_util.cuh"
 #include "shapes.h"
 
+#include <cooperative_groups.h>
+
 namespace ar {
+
+namespace cg = cooperative_groups;
 
 template <typename T> cudaError_t dispatch_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
@@ -339,52 +343,121 @@ cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const 
 }
 
 // ---- dq / dg -----------------------------------------------------------------
-// dq_c = g_c * sum_w ws[w, c], dg_c = q_c * sum_w ws[w, c]; the sum over the
-// backward's warps runs in a fixed order (8 strided groups, then the groups
-// in order), so repeated runs give identical bits.
-__global__ void __launch_bounds__(256) dqdg_reduce_kernel(const float *ws, int rows, int r,
-                                                          const float *q, int64_t qs,
-                                                          const float *g, int64_t gs,
-                                                          float *dq, float *dg, float *dalpha)
+// dq_c = g_c * sum_w ws[w, c], dg_c = q_c * sum_w ws[w, c] over the
+// backward's partial rows w (one per block of the backward grid).
+//
+// One cluster of kRedCtas CTAs per tile of 32 * V columns (V = 4: float4
+// columns when r is a multiple of 4). The cluster's 8 x 16 warps take the
+// rows round-robin, each with four independent running sums so that several
+// loads are in flight; a CTA adds its warps' sums in warp order in shared
+// memory, and CTA 0 adds the CTAs' sums in rank order through distributed
+// shared memory. Every sum has a fixed order, so repeated runs give identical
+// bits.
+constexpr int kRedCtas = 8;
+constexpr int kRedWarps = 16;
+
+template <int V>
+__device__ __forceinline__ void red_load_add(const float *p, float (&s)[V])
 {
-    __shared__ float part[8][33];
-    if (dalpha && blockIdx.x == 0) {
+    if constexpr (V == 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4 *>(p));
+        s[0] += x.x;
+        s[1] += x.y;
+        s[2] += x.z;
+        s[3] += x.w;
+    } else {
+        s[0] += __ldcg(p);
+    }
+}
+
+template <int V>
+__global__ void __cluster_dims__(kRedCtas, 1, 1) __launch_bounds__(kRedWarps * 32)
+    dqdg_reduce_kernel(const float *__restrict__ ws, int rows, int r, const float *q, int64_t qs,
+                       const float *g, int64_t gs, float *dq, float *dg, float *dalpha)
+{
+    __shared__ float part[kRedWarps][32 * V];
+    __shared__ float cta_sum[32 * V];
+    __shared__ float red[kRedWarps * 32];
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c0 = (blockIdx.y * 32 + lane) * V;   // this lane's first column
+    const bool valid = c0 < r;
+    constexpr int stride = kRedCtas * kRedWarps;
+
+    float s[4][V];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < V; ++e) s[u][e] = 0.f;
+    if (valid) {
+        int w = rank * kRedWarps + warp;
+        for (; w + 3 * stride < rows; w += 4 * stride) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) red_load_add<V>(ws + (int64_t)(w + u * stride) * r + c0, s[u]);
+        }
+        for (; w < rows; w += stride) red_load_add<V>(ws + (int64_t)w * r + c0, s[0]);
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) part[warp][lane * V + e] = (s[0][e] + s[1][e]) + (s[2][e] + s[3][e]);
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            float t = 0.f;
+#pragma unroll
+            for (int k = 0; k < kRedWarps; ++k) t += part[k][lane * V + e];
+            cta_sum[lane * V + e] = t;
+        }
+    }
+    cl.sync();
+    if (rank == 0 && warp == 0 && valid) {
+        float t[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) t[e] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kRedCtas; ++k) {
+            const float *rem = cl.map_shared_rank(cta_sum, k);
+#pragma unroll
+            for (int e = 0; e < V; ++e) t[e] += rem[lane * V + e];
+        }
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            const int c = c0 + e;
+            dq[c * qs] = (g ? g[c * gs] : 1.0f) * t[e];
+            if (dg) dg[c * gs] = q[c * qs] * t[e];
+        }
+    }
+    if (dalpha && blockIdx.y == 0 && rank == 1) {
         // dL/dalpha of the delta form: the rows * 4 tail partials, fixed order
-        __shared__ float red[256];
         const float *tail = ws + (int64_t)rows * r;
-        float s = 0.f;
-        for (int k = threadIdx.x; k < rows * 4; k += 256) s += tail[k];
-        red[threadIdx.x] = s;
+        float a = 0.f;
+        for (int k = threadIdx.x; k < rows * 4; k += kRedWarps * 32) a += tail[k];
+        red[threadIdx.x] = a;
         __syncthreads();
-        for (int o = 128; o > 0; o >>= 1) {
+        for (int o = kRedWarps * 16; o > 0; o >>= 1) {
             if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
             __syncthreads();
         }
         if (threadIdx.x == 0) *dalpha = red[0];
-        __syncthreads();
     }
-    const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
-    const int c = blockIdx.x * 32 + lane;
-    float s = 0.f;
-    if (c < r)
-        for (int w = grp; w < rows; w += 8) s += ws[(int64_t)w * r + c];
-    part[grp][lane] = s;
-    __syncthreads();
-    if (grp == 0 && c < r) {
-        float t = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) t += part[k][lane];
-        dq[c * qs] = (g ? g[c * gs] : 1.0f) * t;
-        if (dg) dg[c * gs] = q[c * qs] * t;
-    }
+    // no CTA leaves while CTA 0 may still read its shared memory
+    cl.sync();
 }
 
 cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, int64_t q_stride,
                                const float *g, int64_t g_stride, float *dq, float *dg,
                                float *dalpha, cudaStream_t s)
 {
-    dqdg_reduce_kernel<<<(r + 31) / 32, 256, 0, s>>>(ws, rows, r, q, q_stride, g, g_stride, dq,
-                                                     dg, dalpha);
+    if (r % 4 == 0) {
+        const dim3 grid(kRedCtas, (r / 4 + 31) / 32);
+        dqdg_reduce_kernel<4><<<grid, kRedWarps * 32, 0, s>>>(ws, rows, r, q, q_stride, g,
+                                                             g_stride, dq, dg, dalpha);
+    } else {
+        const dim3 grid(kRedCtas, (r + 31) / 32);
+        dqdg_reduce_kernel<1><<<grid, kRedWarps * 32, 0, s>>>(ws, rows, r, q, q_stride, g,
+                                                             g_stride, dq, dg, dalpha);
+    }
     return cudaGetLastError();
 }
 
