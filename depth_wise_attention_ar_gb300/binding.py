@@ -324,7 +324,9 @@ class Bank:
 
     def __init__(self, T: int, d: int, r: int | None = None, capacity: int = 1,
                  dtype: str = "bf16", norm: str = "key", eps: float = 1e-6,
-                 with_grad: bool = True, device=None):
+                 with_grad: bool = True, device=None, grad: torch.Tensor | None = None):
+        """grad: optional caller-owned [capacity, T, d] fp32 gradient rows
+        (16-byte aligned; any view of that shape with unit inner strides)."""
         r = d if r is None else r
         dev = torch.device("cuda" if device is None else device)
         self.T, self.d, self.r, self.capacity, self.dtype = T, d, r, capacity, dtype
@@ -333,8 +335,14 @@ class Bank:
         self.inv_ld = (capacity + 3) // 4 * 4
         self.inv = torch.empty(max(1, ar_inv_rms_floats(T, capacity)), dtype=torch.float32,
                                device=dev)
-        self.grad = (torch.empty((capacity, T, d), dtype=torch.float32, device=dev)
-                     if with_grad else None)
+        if grad is not None:
+            if (tuple(grad.shape) != (capacity, T, d) or grad.dtype != torch.float32
+                    or not grad.is_contiguous()):
+                raise ValueError("grad must be a contiguous fp32 [capacity, T, d] tensor")
+            self.grad = grad
+        else:
+            self.grad = (torch.empty((capacity, T, d), dtype=torch.float32, device=dev)
+                         if with_grad else None)
         self.handle = ar_bank_create(T, d, r, capacity, _AR_DT[dtype],
                                      AR_NORM_FULL if norm == "full" else AR_NORM_KEY, eps,
                                      self.rows, self.inv, self.grad)

@@ -30,6 +30,7 @@ struct RouteArgs {
     int64_t T;
     int64_t q_stride, g_stride;  // elements between consecutive entries of q, g
     int d, r, H, n_src, inv_ld, norm_full;
+    int grad_v8;           // gradient rows' base is 32-byte aligned: 256-bit stores
     int rows[AR_MAX_SOURCES];
     // a row listed k > 1 times in a site enters once with log k added to its
     // score (softmax over the list = softmax over distinct rows with weights k)

@@ -107,6 +107,7 @@ void fill_common(ar::RouteArgs &a, const ar_bank *b, const int32_t *rows_in, int
     a.n_src = n_src;
     a.inv_ld = b->inv_ld;
     a.norm_full = b->norm_full;
+    a.grad_v8 = b->grad && (reinterpret_cast<uintptr_t>(b->grad) & 31u) == 0;
     a.err = ar::device_error_word();
     for (int i = 0; i < n_src; ++i) {
         a.rows[i] = rows[i];

@@ -245,6 +245,28 @@ __device__ __forceinline__ void st_f32x8_g_sw(float *p, int sw, const float v[8]
     *reinterpret_cast<float4 *>(p + (sw ^ 4)) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// One fp32 chunk of a gradient row in global memory: a single 256-bit store
+// (one whole 32-byte sector) when the rows' base is 32-byte aligned (v8),
+// else two 16-byte stores. Lanes holding swapped halves (sw = 4) put them
+// back in order.
+__device__ __forceinline__ void st_grad8(float *p, int sw, const float v[8], bool v8)
+{
+    if (v8) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[e] = sw ? v[e + 4] : v[e];
+            x[e + 4] = sw ? v[e] : v[e + 4];
+        }
+        asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                         __cvta_generic_to_global(p)),
+                     "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+                     "f"(x[7]));
+    } else {
+        st_f32x8_g_sw(p, sw, v);
+    }
+}
+
 // Chunk order of a lane inside its head: rotating by the head index keeps the
 // head groups that share a quarter-warp on different banks when d/256 (CPL)
 // is even; for odd CPL the plain order already does.

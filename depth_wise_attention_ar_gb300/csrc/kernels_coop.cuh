@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                     nv[e] = fmaf(-coef, v[j][e], nv[e]);
                     U[j][e] = fmaf(ak, v[j][e], U[j][e]);
                 }
-                st_f32x8_g_sw(grad_row + cidx[j] * 8, sw, nv);
+                st_grad8(grad_row + cidx[j] * 8, sw, nv, a.grad_v8);
             }
         } else {
             // key-path terms on the tail, staged in the shared gradient row
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                     nv[e] = fmaf(wgt, G[j][e], nv[e]);
                     nv[e] = fmaf(-c2, v[j][e], nv[e]);
                 }
-                st_f32x8_g_sw(grad_row + cidx[j] * 8, sw, nv);
+                st_grad8(grad_row + cidx[j] * 8, sw, nv, a.grad_v8);
             }
         }
         if constexpr (!LR) {

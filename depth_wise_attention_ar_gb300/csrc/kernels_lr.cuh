@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) nv[e] = fmaf(wa, gv[e], nv[e]);
-            st_f32x8_g(grad_row + c * 8, nv);
+            st_grad8(grad_row + c * 8, 0, nv, a.grad_v8);
         }
         __syncwarp();
         if (issued < hi) issue_next();

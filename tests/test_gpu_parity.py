@@ -320,6 +320,41 @@ def test_repeatable_bits(W):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("d,r,H", [(1280, 1280, 8), (1280, 1280, 16), (4096, 1024, 8),
+                                   (3072, 3072, 8), (1536, 384, 1)])
+def test_gradient_rows_not_32_byte_aligned(W, d, r, H):
+    """Gradient rows whose base is 16- but not 32-byte aligned are written with
+    two 16-byte stores per chunk instead of one 256-bit store: the results are
+    the same bits as with an aligned base (one-warp, four-warp and sliced-key
+    backward kernels; stores on first touch and accumulation)."""
+    import torch
+    B, _ = W
+    T, N = 300, 4
+    inp = synth.HostInputs(seed=41, q_std=0.5, g_kind="random")
+    res = []
+    for off in (0, 4):
+        buf = torch.empty(N * T * d + 8, dtype=torch.float32, device="cuda")
+        grad = buf[off: off + N * T * d].view(N, T, d)
+        assert (grad.data_ptr() % 32 == 0) == (off == 0)
+        bank = B.Bank(T, d, r, N, "bf16", grad=grad)
+        for j in range(N):
+            bank.append(inp.output(j, T, d, "bf16"))
+        q, g = inp.query(7, r), inp.norm_weight(7, r)
+        rows = list(range(N))
+        out0, lse0 = bank.route_fwd(rows, H, q, g, site_id=0)
+        out1, lse1 = bank.route_fwd(rows[:2], H, q, g, site_id=1)
+        bank.zero_grad()
+        dq1, dg1 = bank.route_bwd(rows[:2], H, q, g, out1, inp.dout(1, T, d, "bf16"), lse1,
+                                  site_id=1)
+        dq0, dg0 = bank.route_bwd(rows, H, q, g, out0, inp.dout(0, T, d, "bf16"), lse0,
+                                  site_id=0)
+        torch.cuda.synchronize()
+        assert B.ar_device_error() == 0
+        res.append([grad.clone(), dq0, dg0, dq1, dg1])
+    for x, y in zip(*res):
+        assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("r", [512, 256])
 def test_block_bank_rows_and_inverse_rms(W, orc, dtype, r):
