@@ -246,6 +246,216 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     }
 }
 
+// Two tokens per warp, full keys, rows of 256 or 512 columns, H <= 4.
+//
+// On short rows the per-row cost of the stage wait, the refill and the loop
+// bounds the one-token kernel above by instruction issue. Here a warp serves
+// two adjacent tokens at once, one per half-warp: a stage is one bulk copy of
+// both tokens' rows of a source (adjacent in the bank). CPL = d / 256 is the
+// chunk count of one lane of the one-warp backward; a lane here holds the
+// chunks of two backward lanes of its head (sub and sub + LPH, LPH = lanes
+// per head here, half the backward's) and keeps their two partial scores
+// apart through the in-group butterfly, adding them last: that is the
+// backward's reduction tree, so the recomputed score keeps the forward's
+// bits. Odd heads take their two backward lanes' chunks in the other order,
+// so that the two head groups of a quarter-warp read different bank groups.
+template <typename T, int CPL>
+__global__ void __launch_bounds__(kFwdWarps * 32)
+    route_fwd_pair_kernel(const __grid_constant__ RouteArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_rows[AR_MAX_SOURCES];
+    constexpr int S = kFwdStages;
+    constexpr int CB = ChunkBytes<T>::value;
+    constexpr int NC = 2 * CPL;         // chunks held by one lane
+    constexpr unsigned FULL = 0xffffffffu;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = a.d, N = a.n_src, H = a.H;
+    const int64_t TT = a.T;
+    const uint32_t row_bytes = (uint32_t)d * (uint32_t)sizeof(T);
+    const uint32_t stage_bytes = 2 * row_bytes;
+
+    for (int i = threadIdx.x; i < N; i += blockDim.x) s_rows[i] = a.rows[i];
+    unsigned char *ring = smem + (size_t)warp * S * stage_bytes;
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + (size_t)kFwdWarps * S * stage_bytes) + warp * S;
+    float *inv_warp = reinterpret_cast<float *>(smem + (size_t)kFwdWarps * S * stage_bytes +
+                                                (size_t)kFwdWarps * S * 8) +
+                      warp * 2 * AR_MAX_SOURCES;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ---- lane -> token of the pair, head and chunks
+    const int tt = lane >> 4, fl = lane & 15;
+    const int LPHb = 32 / H, LPH = 16 / H;
+    const int h = fl / LPH, sub = fl - h * LPH;
+    int cidx[NC];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int kk = (k ^ h) & 1;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) cidx[k * CPL + j] = chunk_of<CPL>(h, sub + kk * LPH, LPHb, j);
+    }
+    float qg[NC][8];
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = cidx[j] * 8 + e;
+            qg[j][e] = __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f);
+        }
+
+    // ---- work: token pairs gw, gw + GW, ...
+    const int64_t UT = (TT + 1) / 2;
+    const int64_t GW = (int64_t)gridDim.x * kFwdWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kFwdWarps + warp;
+    const int64_t npair = gw < UT ? (UT - 1 - gw) / GW + 1 : 0;
+    const int64_t total = npair * N;
+    const uint64_t pol = l2_policy_evict_first();
+
+    int64_t issued = 0, u_p = gw;
+    int n_p = 0, slot_p = 0;
+    auto issue_next = [&]() {
+        if (lane == 0) {
+            const int64_t t0 = u_p * 2;
+            const uint32_t bytes = t0 + 1 < TT ? stage_bytes : row_bytes;  // ragged last pair
+            const unsigned char *src = static_cast<const unsigned char *>(a.bank) +
+                                       ((int64_t)s_rows[n_p] * TT + t0) * row_bytes;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[slot_p], bytes);
+            bulk_g2s(ring + (size_t)slot_p * stage_bytes, src, bytes, &bars[slot_p], pol);
+        }
+        ++issued;
+        if (++n_p == N) { n_p = 0; u_p += GW; }
+        if (++slot_p == S) slot_p = 0;
+    };
+    for (int s = 0; s < S && issued < total; ++s) issue_next();
+
+    // inverse RMS of the next pair's sources, prefetched into registers
+    float pre_inv[2][AR_MAX_SOURCES / 32];
+    auto prefetch_inv = [&](int64_t u) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int64_t t = u * 2 + k;
+#pragma unroll
+            for (int v = 0; v < AR_MAX_SOURCES / 32; ++v) {
+                const int nn = lane + 32 * v;
+                if (nn < N && t < TT) pre_inv[k][v] = __ldg(a.inv + t * a.inv_ld + s_rows[nn]);
+            }
+        }
+    };
+    if (npair > 0) prefetch_inv(gw);
+
+    int n = 0, slot = 0;
+    uint32_t phase = 0;
+    int64_t u = gw, i = 0;
+    float m = 0.f, l = 0.f;
+    float acc[NC][8];
+    const float *cur_inv = inv_warp + tt * AR_MAX_SOURCES;
+    bool ok = true;
+    for (; i < total; ++i) {
+        if (n == 0) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int v = 0; v < AR_MAX_SOURCES / 32; ++v) {
+                    const int nn = lane + 32 * v;
+                    if (nn < N) inv_warp[k * AR_MAX_SOURCES + nn] = pre_inv[k][v];
+                }
+            __syncwarp();
+            if (u + GW < UT) prefetch_inv(u + GW);
+        }
+        const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
+        if (!__all_sync(FULL, got)) { ok = false; break; }
+        phase ^= 1u << slot;
+        // this half-warp's token row (the second row of a ragged last pair is
+        // stale data: computed on, never stored)
+        const unsigned char *buf = ring + (size_t)slot * stage_bytes + (size_t)tt * row_bytes;
+
+        float v[NC][8];
+        float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+            ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
+            if (j < CPL) z0 = __fadd_rn(z0, dot8(qg[j], v[j]));
+            else z1 = __fadd_rn(z1, dot8(qg[j], v[j]));
+        }
+        const float zr = __fadd_rn(group_sum(z0, LPH), group_sum(z1, LPH));
+        const float z = __fmul_rn(zr, cur_inv[n]);
+        if (n == 0) {
+            m = z;
+            l = 0.f;
+#pragma unroll
+            for (int j = 0; j < NC; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+        }
+        const bool need = z > m + kRescaleTau;
+        if (__any_sync(FULL, need)) {
+            const float sc = need ? exp2f((m - z) * kLog2e) : 1.f;
+            m = need ? z : m;
+            l *= sc;
+#pragma unroll
+            for (int j = 0; j < NC; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[j][e] *= sc;
+        }
+        const float p = exp2f((z - m) * kLog2e);
+        l += p;
+#pragma unroll
+        for (int j = 0; j < NC; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, v[j][e], acc[j][e]);
+        __syncwarp();
+        if (issued < total) issue_next();
+
+        if (n == N - 1) {
+            const int64_t tok = u * 2 + tt;
+            if (tok < TT) {
+                const float rl = 1.f / l;
+#pragma unroll
+                for (int j = 0; j < NC; ++j) {
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
+                    store_output<T>(a, tok * d + cidx[j] * 8, o);
+                }
+                if (sub == 0) a.lse[tok * H + h] = m + log2f(l) * kLn2;
+            }
+        }
+        if (++n == N) { n = 0; u += GW; }
+        if (++slot == S) slot = 0;
+    }
+
+    if (!ok) {
+        if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
+        for (int64_t j = i; j < issued; ++j) {
+            mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+            phase ^= 1u << slot;
+            if (++slot == S) slot = 0;
+        }
+    }
+}
+
+template <typename T, int CPL>
+cudaError_t launch_fwd_pair(const RouteArgs &a, cudaStream_t s)
+{
+    const void *k = reinterpret_cast<const void *>(&route_fwd_pair_kernel<T, CPL>);
+    const size_t smem = (size_t)kFwdWarps * kFwdStages * 2 * a.d * sizeof(T) +
+                        (size_t)kFwdWarps * kFwdStages * 8 +
+                        (size_t)kFwdWarps * 2 * AR_MAX_SOURCES * 4;
+    int grid = 0;
+    cudaError_t e = persistent_grid(k, kFwdWarps * 32, smem, &grid);
+    if (e != cudaSuccess) return e;
+    route_fwd_pair_kernel<T, CPL><<<grid, kFwdWarps * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename T, int CPL, bool SK>
 cudaError_t launch_fwd_inst(const RouteArgs &a, cudaStream_t s)
 {
@@ -258,14 +468,16 @@ cudaError_t launch_fwd_inst(const RouteArgs &a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-// Full-width keys with d = 256 * CPL, CPL in 1..8.
+// Full-width keys with d = 256 * CPL, CPL in 1..8 (rows of 256 or 512
+// columns with at most 4 heads: two tokens per warp).
 template <typename T>
 cudaError_t dispatch_fwd(const RouteArgs &a, cudaStream_t s)
 {
     if (a.r != a.d) return cudaErrorNotSupported;
+    const bool pair = a.H <= 4;  // two tokens per warp on rows of 256 or 512
     switch (a.d / 256) {
-    case 1: return launch_fwd_inst<T, 1, false>(a, s);
-    case 2: return launch_fwd_inst<T, 2, false>(a, s);
+    case 1: return pair ? launch_fwd_pair<T, 1>(a, s) : launch_fwd_inst<T, 1, false>(a, s);
+    case 2: return pair ? launch_fwd_pair<T, 2>(a, s) : launch_fwd_inst<T, 2, false>(a, s);
     case 3: return launch_fwd_inst<T, 3, false>(a, s);
     case 4: return launch_fwd_inst<T, 4, false>(a, s);
     case 5: return launch_fwd_inst<T, 5, false>(a, s);
