@@ -163,24 +163,48 @@ class Microbatch:
             else:
                 self.bank.rows[j].copy_(x)
             del x
-        self.q = {s: src.query(s, cfg.r) for s in self.plan.run_sites}
-        self.g = {s: src.norm_weight(s, cfg.r) for s in self.plan.run_sites}
+        run = self.plan.run_sites
+        # per-site queries, norm weights (and gates) live in one buffer, and
+        # their gradients in another, so that a host pipeline moves each set
+        # with one copy
+        q = {s: src.query(s, cfg.r) for s in run}
+        g = {s: src.norm_weight(s, cfg.r) for s in run}
+        alpha = {s: src.query(2000 + s, 1) for s in run} if cfg.delta else {}
+        parts = [*q.values(), *(x for x in g.values() if x is not None), *alpha.values()]
+        self.small_in = torch.cat([x.reshape(-1).float() for x in parts])
+        off = 0
+
+        def view(x):
+            nonlocal off
+            v = self.small_in[off:off + x.numel()].view(x.shape)
+            off += x.numel()
+            return v
+
+        self.q = {s: view(q[s]) for s in run}
+        self.g = {s: view(g[s]) if g[s] is not None else None for s in run}
+        if cfg.delta:
+            self.alpha = {s: view(alpha[s]) for s in run}
+        del q, g, alpha, parts
         self.dout = {s: src.dout(s, cfg.T, cfg.d, cfg.dtype) for s in self.plan.run_sites}
         self.out = {s: torch.empty((cfg.T, cfg.d), dtype=tdt, device=dev)
                     for s in self.plan.run_sites}
         self.lse = {s: torch.empty((cfg.T, self.H), dtype=torch.float32, device=dev)
                     for s in self.plan.run_sites}
-        self.dq = {s: torch.empty(cfg.r, device=dev) for s in self.plan.run_sites}
-        self.dg = {s: torch.empty(cfg.r, device=dev) for s in self.plan.run_sites}
+        ns = len(run)
+        n_out = 2 * ns * cfg.r + ((ns + cfg.d) if cfg.delta else 0)
+        self.small_out = torch.empty(n_out, device=dev)
+        so = self.small_out
+        self.dq = {s: so[i * cfg.r:(i + 1) * cfg.r] for i, s in enumerate(run)}
+        self.dg = {s: so[(ns + i) * cfg.r:(ns + i + 1) * cfg.r] for i, s in enumerate(run)}
         self.ws = self.bank.workspace(self.H)
         if cfg.delta:
             self.partial = {s: src.output(1000 + s, cfg.T, cfg.d, cfg.dtype)
                             for s in self.plan.run_sites}
-            self.alpha = {s: src.query(2000 + s, 1) for s in self.plan.run_sites}
             self.routed = {s: torch.empty((cfg.T, cfg.d), dtype=tdt, device=dev)
                            for s in self.plan.run_sites}
-            self.dalpha = {s: torch.empty(1, device=dev) for s in self.plan.run_sites}
-            self.dnull = torch.empty(cfg.d, device=dev)
+            base = 2 * ns * cfg.r
+            self.dalpha = {s: so[base + i:base + i + 1] for i, s in enumerate(run)}
+            self.dnull = so[base + ns:base + ns + cfg.d]
 
     def forward(self, stream=None, on_site=None):
         bank, plan = self.bank, self.plan
