@@ -322,7 +322,7 @@ constexpr int kMsZp = 20;   // score row pitch (floats): conflict-free softmax r
 struct MsLayout {
     int TC, tc_shift, ntiles, kt0, nk, S;   // tile width (2^tc_shift), tiles per row,
                                             // first key tile, key tiles, ring
-    uint32_t row_pitch, tile_pitch;
+    uint32_t row_pitch, tile_pitch, qg_pitch;
     size_t smem;
 };
 
@@ -337,15 +337,20 @@ inline bool ms_layout(int d, int r, int H, int N, MsLayout *L)
     L->nk = L->ntiles - L->kt0;
     L->row_pitch = (uint32_t)L->TC * 2u + 16u;   // 16-byte pad: conflict-free ldmatrix rows
     L->tile_pitch = (uint32_t)N * L->row_pitch;
+    L->qg_pitch = (uint32_t)r * 2u + 16u;
     const size_t fixed = 2 * (size_t)kMsMaxStages * 8 + 16 + (size_t)AR_MAX_QUERIES * H * kMsZp * 4 +
                          2 * (size_t)H * 256 * 2 + 2 * (size_t)kMmaMaxRows * 4 +
-                         (size_t)kMsWarps * 8 * kStgPitch;
-    int S = kMsMaxStages;
-    while (S > L->nk + 1 && (size_t)S * L->tile_pitch + fixed > 200 * 1024) --S;
-    if ((size_t)S * L->tile_pitch + fixed > 200 * 1024) return false;
-    L->S = S;
-    L->smem = (size_t)S * L->tile_pitch + fixed;
-    return true;
+                         (size_t)kMsWarps * 8 * kStgPitch + 2 * (size_t)AR_MAX_QUERIES * L->qg_pitch;
+    // two blocks per SM when a ring deeper than the key tiles fits in half
+    // the shared memory, else one
+    for (const size_t budget : {(size_t)112 * 1024, (size_t)200 * 1024})
+        for (int S = kMsMaxStages; S > L->nk; --S)
+            if ((size_t)S * L->tile_pitch + fixed <= budget) {
+                L->S = S;
+                L->smem = (size_t)S * L->tile_pitch + fixed;
+                return true;
+            }
+    return false;
 }
 
 __device__ __forceinline__ void ms_bar()
@@ -367,7 +372,7 @@ __device__ __forceinline__ bool ms_bar_or(bool v)
     return r != 0;
 }
 
-__global__ void __launch_bounds__(kMsThreads, 1)
+__global__ void __launch_bounds__(kMsThreads, 2)
     route_fwd_multi_stream_kernel(const __grid_constant__ MultiArgs m, const MsLayout L)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -400,6 +405,19 @@ __global__ void __launch_bounds__(kMsThreads, 1)
     float *invs = reinterpret_cast<float *>(p);                 // [2][16]
     p += 2 * (size_t)kMmaMaxRows * 4;
     unsigned char *stg = p + (size_t)(warp < kMsWarps ? warp : 0) * 8 * kStgPitch;
+    p += (size_t)kMsWarps * 8 * kStgPitch;
+    // q*g of every query over the key columns as bf16 hi and lo parts,
+    // [part][query][key column], rows padded: the scores' B operands
+    unsigned char *qgs = p;
+    const uint32_t qgp = L.qg_pitch;
+    for (int i = tid; i < QM * r; i += kMsThreads) {
+        const int qi = i / r, c = i - qi * r;
+        const float v = qi < nq ? __ldg(m.q[qi] + c) * (m.g[qi] ? __ldg(m.g[qi] + c) : 1.0f) : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        *reinterpret_cast<__nv_bfloat16 *>(qgs + (size_t)qi * qgp + c * 2) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(qgs + (size_t)(QM + qi) * qgp + c * 2) =
+            __float2bfloat16_rn(v - __bfloat162float(hi));
+    }
 
     for (int i = tid; i < 2 * H * 256; i += kMsThreads) pw[i] = __float2bfloat16_rn(0.f);
     if (tid < 4) reinterpret_cast<uint32_t *>(zline)[tid] = 0u;
@@ -473,28 +491,7 @@ __global__ void __launch_bounds__(kMsThreads, 1)
     }
 
     // ---- consumers
-    // B fragments of q*g for this warp's head (warp h < H), two bf16 parts,
-    // per 16-column step of the key slice; queries past nq are zero
     const int nks = Kr / 16;
-    uint32_t qh[kMmaMaxSteps][2], ql[kMmaMaxSteps][2];
-#pragma unroll
-    for (int ks = 0; ks < kMmaMaxSteps; ++ks)
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float v[2] = {0.f, 0.f};
-            if (warp < H && ks < nks && g8 < nq) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int c = warp * Kr + ks * 16 + half * 8 + 2 * t4 + e;
-                    v[e] = __ldg(m.q[g8] + c) * (m.g[g8] ? __ldg(m.g[g8] + c) : 1.0f);
-                }
-            }
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(v[0], v[1]);
-            const __nv_bfloat162 lo =
-                __floats2bfloat162_rn(v[0] - __low2float(hi), v[1] - __high2float(hi));
-            qh[ks][half] = *reinterpret_cast<const uint32_t *>(&hi);
-            ql[ks][half] = *reinterpret_cast<const uint32_t *>(&lo);
-        }
     // this lane's two output rows of the staged 64-column pieces
     const int orow0 = lane >> 3, oseg = lane & 7;
     __nv_bfloat16 *out0 = orow0 < nq ? static_cast<__nv_bfloat16 *>(m.out[orow0]) : nullptr;
@@ -505,7 +502,7 @@ __global__ void __launch_bounds__(kMsThreads, 1)
     const bool sact = spair < nq * H;
     float *lse_out = sact ? m.lse[sq] : nullptr;
 
-    const uint32_t zaddr = smem_u32(zline), ring_a = smem_u32(ring);
+    const uint32_t zaddr = smem_u32(zline), ring_a = smem_u32(ring), qg_a = smem_u32(qgs);
     const int ntl = TC / 8, ngr = ntl / 8;   // 8-column MMA tiles, groups of 8 per tile
     const bool one_head = K % 64 == 0;       // every 64-column group within one head
     int st0 = 0, rnd0 = 0;                   // ring slot and round of the token's first tile
@@ -541,15 +538,19 @@ __global__ void __launch_bounds__(kMsThreads, 1)
                 const int tile = col >> L.tc_shift;
                 int sk = st0 + (tile - kt0);
                 if (sk >= S) sk -= S;
-                uint32_t af[4];
+                uint32_t af[4], bh0, bh1, bl0, bl1;
                 ldsm_x4(rowA < N ? ring_a + sk * tp + rowA * rp + (col & (TC - 1)) * 2 : zaddr, af);
+                const uint32_t qa = qg_a + (lane & 7) * qgp +
+                                    (h * Kr + ks * 16 + ((lane >> 3) & 1) * 8) * 2;
+                ldsm_x2(qa, bh0, bh1);
+                ldsm_x2(qa + QM * qgp, bl0, bl1);
                 // four accumulation chains: q*g hi and lo parts, even and odd steps
                 if (ks & 1) {
-                    mma_16816(c2, af, qh[ks][0], qh[ks][1]);
-                    mma_16816(cl2, af, ql[ks][0], ql[ks][1]);
+                    mma_16816(c2, af, bh0, bh1);
+                    mma_16816(cl2, af, bl0, bl1);
                 } else {
-                    mma_16816(c, af, qh[ks][0], qh[ks][1]);
-                    mma_16816(cl, af, ql[ks][0], ql[ks][1]);
+                    mma_16816(c, af, bh0, bh1);
+                    mma_16816(cl, af, bl0, bl1);
                 }
             }
 #pragma unroll
