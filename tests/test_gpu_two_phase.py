@@ -100,6 +100,37 @@ def test_multi_query_read_equals_per_query_reads(B, orc, d, r, H, dtype, nq, N):
         assert _nmax(_t64(lses[i]), ref_lse) < tol, i
 
 
+@pytest.mark.parametrize("d,r,H,nq,rows,T", [
+    (4096, 2048, 8, 8, list(range(16)), 131),    # 16 rows: the ring only fits one block per SM
+    (4096, 1024, 8, 1, list(range(16)), 100),    # one query, fewer tokens than blocks
+    (4096, 1024, 8, 4, [0, 1, 2, 1, 3], 157),    # a row listed twice
+    (2304, 1152, 8, 8, list(range(9)), 157),     # 256-column tiles, heads across 64-column groups
+])
+def test_multi_query_read_streaming_shapes(B, orc, d, r, H, nq, rows, T):
+    """The tiled multi-query kernel at the edges of its layout: the most rows,
+    a single query, fewer tokens than blocks, a repeated row (its score gets
+    log 2 added), tiles of 256 columns with heads that change inside a 64-column
+    group; with 16 rows the ring wraps inside a token. Every output and lse against the
+    oracle's read over the listed sources."""
+    inp = synth.HostInputs(seed=43, q_std=0.8, g_kind="random")
+    nrow = max(rows) + 1
+    bank = B.Bank(T, d, r, nrow, "bf16")
+    for j in range(nrow):
+        bank.append(inp.output(j, T, d, "bf16"))
+    qs = [inp.query(200 + i, r) for i in range(nq)]
+    gs = [inp.norm_weight(200 + i, r) for i in range(nq)]
+    outs, lses = bank.route_fwd_multi(rows, H, qs, gs)
+    import torch
+    torch.cuda.synchronize()
+    assert B.ar_device_error() == 0
+    srcs = [inp.host_output(j, T, d, "bf16") for j in rows]
+    for i in range(nq):
+        ref_out, ref_lse = orc.route_fwd(srcs, inp.host_query(200 + i, r),
+                                         inp.host_norm_weight(200 + i, r), H, r=r)
+        assert _nmax(_t64(outs[i]), ref_out) < 2e-2, i
+        assert _nmax(_t64(lses[i]), ref_lse) < 2e-2, i
+
+
 @pytest.mark.parametrize("d,r,H,dtype", [(4096, 1024, 8, "bf16"), (1024, 256, 4, "f32")])
 def test_two_phase_with_batched_phase_one(B, orc, d, r, H, dtype):
     """Phase 1 reads the inter-block rows once for all the sites of a block
