@@ -59,6 +59,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--eager", action="store_true", help="no CUDA graphs")
+    p.add_argument("--report", metavar="DIR", default=None,
+                   help="run every workload (each in its own process) and write DIR/report.json "
+                        "and DIR/report.md")
     return p.parse_args()
 
 
@@ -210,8 +213,51 @@ def config_of(args, workload):
     return cfg
 
 
+# (config, heads or None) of the report: the shaped workloads, the 1B head
+# sweep, and the rows past the hot path
+REPORT_RUNS = [("1B", None), ("1B", 1), ("1B", 4), ("1B", 16), ("350M", None), ("100M", None),
+               ("lr_block", None), ("delta_8b", None), ("lr_page_1b", None), ("lr_page_4b", None)]
+
+
+def report(args):
+    """Every workload through this script, one process each; JSON + Markdown."""
+    os.makedirs(args.report, exist_ok=True)
+    lines = []
+    for cfg, heads in REPORT_RUNS:
+        cmd = [sys.executable, os.path.abspath(__file__), "--config", cfg, "--steps", str(args.steps),
+               "--warmup", str(args.warmup)]
+        if heads:
+            cmd += ["--heads", str(heads)]
+        if cfg != "1B" or heads:
+            cmd += ["--no-cpu-baseline"]
+        p = subprocess.run(cmd, capture_output=True, text=True)
+        if p.returncode != 0:
+            raise RuntimeError(f"{' '.join(cmd)} failed:\n{p.stderr[-2000:]}")
+        lines.append(json.loads(p.stdout.strip().splitlines()[-1]))
+    with open(os.path.join(args.report, "report.json"), "w") as f:
+        json.dump(lines, f, indent=1)
+    rows = ["| workload | H | ms / microbatch | tokens/s | of roofline | forward + appends (ms) | "
+            "backward (ms, of roofline) | end to end (ms) | SM MHz |",
+            "|---|---|---|---|---|---|---|---|---|"]
+    for L in lines:
+        c, ph, e = L["config"], L["phases_ms"], L.get("e2e") or {}
+        rows.append(f"| {c['workload']} | {c['H']} | {L['ms_per_step']:.2f} | {L['value']:,.0f} | "
+                    f"{100 * L['step_roofline']['frac']:.1f} % | {ph['forward_and_appends']:.2f} | "
+                    f"{ph['backward']:.2f} ({100 * L['roofline']['frac']:.1f} %) | "
+                    f"{e.get('ms_per_step', float('nan')):.1f} | {L['clocks'].get('sm_mhz')} |")
+    cb = next((L["cpu_baseline"] for L in lines if "cpu_baseline" in L), None)
+    if cb:
+        rows.append("")
+        rows.append(f"CPU oracle: {cb['value']:.1f} {cb['unit']} on {cb['cores']} cores ({cb['sample']}).")
+    with open(os.path.join(args.report, "report.md"), "w") as f:
+        f.write("\n".join(rows) + "\n")
+    print("\n".join(rows))
+
+
 def main():
     args = parse()
+    if args.report:
+        return report(args)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
