@@ -237,14 +237,15 @@ def report(args):
     with open(os.path.join(args.report, "report.json"), "w") as f:
         json.dump(lines, f, indent=1)
     rows = ["| workload | H | ms / microbatch | tokens/s | of roofline | forward + appends (ms) | "
-            "backward (ms, of roofline) | end to end (ms) | SM MHz |",
-            "|---|---|---|---|---|---|---|---|---|"]
+            "backward (ms, of roofline) | end to end (ms) | host link alone (GB/s) | SM MHz |",
+            "|---|---|---|---|---|---|---|---|---|---|"]
     for L in lines:
         c, ph, e = L["config"], L["phases_ms"], L.get("e2e") or {}
         rows.append(f"| {c['workload']} | {c['H']} | {L['ms_per_step']:.2f} | {L['value']:,.0f} | "
                     f"{100 * L['step_roofline']['frac']:.1f} % | {ph['forward_and_appends']:.2f} | "
                     f"{ph['backward']:.2f} ({100 * L['roofline']['frac']:.1f} %) | "
-                    f"{e.get('ms_per_step', float('nan')):.1f} | {L['clocks'].get('sm_mhz')} |")
+                    f"{e.get('ms_per_step', float('nan')):.1f} | {e.get('h2d_gbs_alone', float('nan')):.0f} | "
+                    f"{L['clocks'].get('sm_mhz')} |")
     cb = next((L["cpu_baseline"] for L in lines if "cpu_baseline" in L), None)
     if cb:
         rows.append("")
@@ -510,6 +511,17 @@ def end_to_end(args, mb, stream, run_fwd, run_bwd, world, local):
     with torch.cuda.stream(stream):
         run(2)                                   # warm-up: both buffer sets
     torch.cuda.synchronize()
+    # the host link alone: one step's input copies with nothing else running
+    # (the host's memory and links are shared with other jobs on the machine,
+    # so the end-to-end figure is read against this)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(h2d_stream):
+        c0.record(h2d_stream)
+    issue_copies(0)
+    with torch.cuda.stream(h2d_stream):
+        c1.record(h2d_stream)
+    torch.cuda.synchronize()
+    h2d_gbs_alone = h2d / (c0.elapsed_time(c1) * 1e-3) / 1e9
     if world > 1:
         dist.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -525,6 +537,8 @@ def end_to_end(args, mb, stream, run_fwd, run_bwd, world, local):
     del mbs[1]
     return {"value": world * mb.cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_gbs_alone": h2d_gbs_alone,
+            "copy_bound_ms": h2d / (h2d_gbs_alone * 1e9) * 1e3,
             "copies": "H2D on its own stream, double-buffered: the next step's inputs stream "
                       "in while the current step computes; D2H of each step's packed dq/dg "
                       "after the step"}
