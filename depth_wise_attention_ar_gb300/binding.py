@@ -55,6 +55,8 @@ SIGNATURES = {
     "ar_bank_zero_grad": ([_P], ctypes.c_int),
     "ar_bank_reset": ([_P], ctypes.c_int),
     "ar_route_fwd": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _I32, _P], ctypes.c_int),
+    "ar_route_fwd_append": ([_P, _P, _I32, _I32P, _I32P, _I32, _I32, _P, _P, _P, _P, _I32, _I32P,
+                             _P], ctypes.c_int),
     "ar_route_fwd_delta": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
                            ctypes.c_int),
     "ar_route_bwd_delta": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
@@ -208,6 +210,18 @@ def ar_route_fwd(bank, rows, H, q, g, out, lse, site_id, stream=None):
     arr, n = _rows(rows)
     _check("ar_route_fwd", _lib.ar_route_fwd(bank, arr, n, H, _ptr(q), _ptr(g), _ptr(out),
                                              _ptr(lse), site_id, _stream(stream)))
+
+
+def ar_route_fwd_append(bank, src, accumulate_from, rows, H, q, g, out, lse, site_id,
+                        stream=None):
+    """Append + forward in one call; returns (new row, fused)."""
+    arr, n = _rows(rows)
+    row, fused = ctypes.c_int32(-1), ctypes.c_int32(0)
+    _check("ar_route_fwd_append",
+           _lib.ar_route_fwd_append(bank, _ptr(src), accumulate_from, ctypes.byref(row), arr, n,
+                                    H, _ptr(q), _ptr(g), _ptr(out), _ptr(lse), site_id,
+                                    ctypes.byref(fused), _stream(stream)))
+    return row.value, bool(fused.value)
 
 
 def ar_route_fwd_delta(bank, rows, H, q, g, partial, alpha, out, routed, lse, site_id,
@@ -402,6 +416,25 @@ class Bank:
         else:
             ar_route_fwd(self.handle, rows, H, q, g, out, lse, site_id, stream)
         return out, lse
+
+    def route_fwd_append(self, src, accumulate_from, rows, H, q, g=None, out=None, lse=None,
+                         site_id=0, stream=None):
+        """Append src as the next row, then read the site (see ar_route_fwd_append);
+        returns (out, lse, row, fused)."""
+        dev = self.rows.device
+        if out is None:
+            out = torch.empty((self.T, self.d), dtype=self.torch_dtype, device=dev)
+        if lse is None:
+            lse = torch.empty((self.T, H), dtype=torch.float32, device=dev)
+        self._check_tensor(src, (self.T, self.d), self.torch_dtype, "src")
+        self._check_tensor(out, (self.T, self.d), self.torch_dtype, "out")
+        self._check_tensor(lse, (self.T, H), torch.float32, "lse")
+        self._check_tensor(q, (self.r,), torch.float32, "q")
+        if g is not None:
+            self._check_tensor(g, (self.r,), torch.float32, "g")
+        row, fused = ar_route_fwd_append(self.handle, src, accumulate_from, rows, H, q, g, out,
+                                         lse, site_id, stream)
+        return out, lse, row, fused
 
     def route_fwd_delta(self, rows, H, q, g, partial, alpha, out=None, routed=None, lse=None,
                         site_id=0, stream=None):

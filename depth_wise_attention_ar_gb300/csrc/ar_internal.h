@@ -31,6 +31,10 @@ struct RouteArgs {
     int64_t q_stride, g_stride;  // elements between consecutive entries of q, g
     int d, r, H, n_src, inv_ld, norm_full;
     int grad_v8;           // gradient rows' base is 32-byte aligned: 256-bit stores
+    // forward with the append fused in: 1 + the list index of the row appended
+    // in this call, whose inverse RMS the kernel computes and caches (0: none)
+    int fresh1;
+    float eps;             // the bank's RMSNorm epsilon
     int rows[AR_MAX_SOURCES];
     // a row listed k > 1 times in a site enters once with log k added to its
     // score (softmax over the list = softmax over distinct rows with weights k)
@@ -57,6 +61,9 @@ cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
 cudaError_t launch_route_fwd_multi(const MultiArgs &m, ar_dtype dt, cudaStream_t s);
 cudaError_t dispatch_fwd_multi_mma(const MultiArgs &m, cudaStream_t s);  // bf16 rows
 cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps);
+// The site runs on a forward kernel that can take the append of a listed row
+// (full-width keys on the one-warp kernels).
+bool fwd_fuses_append(const RouteArgs &a, ar_dtype dt);
 // dq and dg are written with the strides of q and g respectively.
 cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, int64_t q_stride,
                                const float *g, int64_t g_stride, float *dq, float *dg,

@@ -108,6 +108,7 @@ void fill_common(ar::RouteArgs &a, const ar_bank *b, const int32_t *rows_in, int
     a.inv_ld = b->inv_ld;
     a.norm_full = b->norm_full;
     a.grad_v8 = b->grad && (reinterpret_cast<uintptr_t>(b->grad) & 31u) == 0;
+    a.eps = b->eps;
     a.err = ar::device_error_word();
     for (int i = 0; i < n_src; ++i) {
         a.rows[i] = rows[i];
@@ -304,6 +305,57 @@ ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
 {
     return route_fwd_impl(bank, make_site(rows, n_src, H, q, g, site_id), nullptr, nullptr, out,
                           nullptr, lse, stream);
+}
+
+ar_status ar_route_fwd_append(ar_bank *bank, const void *src, int32_t accumulate_from,
+                              int32_t *out_row, const int32_t *rows, int32_t n_src, int32_t H,
+                              const float *q, const float *g, void *out, float *lse,
+                              int32_t site_id, int32_t *fused, void *stream)
+{
+    if (fused) *fused = 0;
+    if (!bank || (!src && bank->T > 0)) return AR_ERR_INVALID_ARG;
+    if (bank->count >= bank->cap) return AR_ERR_CAPACITY;
+    if (accumulate_from < -1 || accumulate_from >= bank->count) return AR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(src) % bank->esize) != 0) return AR_ERR_ALIGN;
+    // the site's checks, with the new row counted, before anything happens
+    const int32_t new_row = bank->count;
+    ++bank->count;
+    ar_status st = check_site(bank, rows, n_src, H, q, g);
+    if (st == AR_OK && bank->T > 0 && (!out || !lse)) st = AR_ERR_INVALID_ARG;
+    if (st == AR_OK && (!aligned16(out) || !aligned4(lse))) st = AR_ERR_ALIGN;
+    --bank->count;
+    if (st != AR_OK) return st;
+
+    void *slot = nullptr;
+    ar_bank_row_ptr(bank, new_row, &slot);
+    if (src == slot && accumulate_from < 0 && bank->T > 0) {
+        // the row already sits in its slot: the forward computes its inverse RMS
+        ++bank->count;
+        ar::RouteArgs a;
+        fill_common(a, bank, rows, n_src, H, q, g);
+        int idx = -1;
+        for (int i = 0; i < a.n_src; ++i)
+            if (a.rows[i] == new_row) idx = i;
+        if (idx >= 0 && ar::fwd_fuses_append(a, bank->dtype)) {
+            a.fresh1 = idx + 1;
+            a.out = out;
+            a.lse = lse;
+            const cudaError_t e =
+                ar::launch_route_fwd(a, bank->dtype, static_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess) {
+                --bank->count;
+                return from_cuda(e);
+            }
+            bank->fwd_record.push_back(site_id);
+            if (out_row) *out_row = new_row;
+            if (fused) *fused = 1;
+            return AR_OK;
+        }
+        --bank->count;
+    }
+    st = ar_bank_append(bank, src, accumulate_from, out_row, stream);
+    if (st != AR_OK) return st;
+    return ar_route_fwd(bank, rows, n_src, H, q, g, out, lse, site_id, stream);
 }
 
 ar_status ar_route_fwd_delta(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_t H,

@@ -49,7 +49,7 @@ inline size_t fwd_smem_bytes(int d, size_t esize)
            (size_t)kFwdWarps * AR_MAX_SOURCES * 4;
 }
 
-template <typename T, int CPL, bool SK>
+template <typename T, int CPL, bool SK, bool FRESH = false>
 __global__ void __launch_bounds__(kFwdWarps * 32)
     route_fwd_kernel(const __grid_constant__ RouteArgs a)
 {
@@ -182,9 +182,24 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
             }
         }
         zr = group_sum(zr, LPH);
+        float ivn = cur_inv[n];
+        if constexpr (FRESH && !SK) {
+            if (n + 1 == a.fresh1) {
+                // the row appended with this read: its inverse RMS from the
+                // staged (stored) values, over all d columns, into the cache
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(v[j][e], v[j][e], ss);
+                ss = warp_sum(ss);
+                ivn = rsqrtf(fmaf(ss, 1.0f / (float)d, a.eps));
+                if (lane == 0) const_cast<float *>(a.inv)[tok * a.inv_ld + s_rows[n]] = ivn;
+            }
+        }
         // __fmul_rn keeps the product uncontracted: the backward recomputes
         // the same bits
-        const float z = __fmul_rn(zr, cur_inv[n]);
+        const float z = __fmul_rn(zr, ivn);
         if (n == 0) {  // first source of the token: weight exp(0) = 1 below
             m = z;
             l = 0.f;
@@ -259,7 +274,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
 // backward's reduction tree, so the recomputed score keeps the forward's
 // bits. Odd heads take their two backward lanes' chunks in the other order,
 // so that the two head groups of a quarter-warp read different bank groups.
-template <typename T, int CPL>
+template <typename T, int CPL, bool FRESH = false>
 __global__ void __launch_bounds__(kFwdWarps * 32)
     route_fwd_pair_kernel(const __grid_constant__ RouteArgs a)
 {
@@ -386,7 +401,22 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
             else z1 = __fadd_rn(z1, dot8(qg[j], v[j]));
         }
         const float zr = __fadd_rn(group_sum(z0, LPH), group_sum(z1, LPH));
-        const float z = __fmul_rn(zr, cur_inv[n]);
+        float ivn = cur_inv[n];
+        if (FRESH && n + 1 == a.fresh1) {
+            // the row appended with this read: its inverse RMS (half-warp sum)
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < NC; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(v[j][e], v[j][e], ss);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+            ivn = rsqrtf(fmaf(ss, 1.0f / (float)d, a.eps));
+            const int64_t tk = u * 2 + tt;
+            if (fl == 0 && tk < TT)
+                const_cast<float *>(a.inv)[tk * a.inv_ld + s_rows[n]] = ivn;
+        }
+        const float z = __fmul_rn(zr, ivn);
         if (n == 0) {
             m = z;
             l = 0.f;
@@ -442,30 +472,48 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     }
 }
 
-template <typename T, int CPL>
-cudaError_t launch_fwd_pair(const RouteArgs &a, cudaStream_t s)
+template <typename T, int CPL, bool FRESH>
+cudaError_t launch_fwd_pair_inst(const RouteArgs &a, cudaStream_t s)
 {
-    const void *k = reinterpret_cast<const void *>(&route_fwd_pair_kernel<T, CPL>);
+    const void *k = reinterpret_cast<const void *>(&route_fwd_pair_kernel<T, CPL, FRESH>);
     const size_t smem = (size_t)kFwdWarps * kFwdStages * 2 * a.d * sizeof(T) +
                         (size_t)kFwdWarps * kFwdStages * 8 +
                         (size_t)kFwdWarps * 2 * AR_MAX_SOURCES * 4;
     int grid = 0;
     cudaError_t e = persistent_grid(k, kFwdWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
-    route_fwd_pair_kernel<T, CPL><<<grid, kFwdWarps * 32, smem, s>>>(a);
+    route_fwd_pair_kernel<T, CPL, FRESH><<<grid, kFwdWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-template <typename T, int CPL, bool SK>
-cudaError_t launch_fwd_inst(const RouteArgs &a, cudaStream_t s)
+template <typename T, int CPL>
+cudaError_t launch_fwd_pair(const RouteArgs &a, cudaStream_t s)
 {
-    const void *k = reinterpret_cast<const void *>(&route_fwd_kernel<T, CPL, SK>);
+    return a.fresh1 ? launch_fwd_pair_inst<T, CPL, true>(a, s) : launch_fwd_pair_inst<T, CPL, false>(a, s);
+}
+
+template <typename T, int CPL, bool SK, bool FRESH>
+cudaError_t launch_fwd_inst2(const RouteArgs &a, cudaStream_t s)
+{
+    const void *k = reinterpret_cast<const void *>(&route_fwd_kernel<T, CPL, SK, FRESH>);
     const size_t smem = fwd_smem_bytes(a.d, sizeof(T));
     int grid = 0;
     cudaError_t e = persistent_grid(k, kFwdWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
-    route_fwd_kernel<T, CPL, SK><<<grid, kFwdWarps * 32, smem, s>>>(a);
+    route_fwd_kernel<T, CPL, SK, FRESH><<<grid, kFwdWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+// The fresh-row variant only for full keys on rows up to 1024 wide (the host
+// sets fresh1 only there: on 1280-wide rows the variant measured slower than
+// a separate append).
+template <typename T, int CPL, bool SK>
+cudaError_t launch_fwd_inst(const RouteArgs &a, cudaStream_t s)
+{
+    if constexpr (!SK && CPL <= 4) {
+        if (a.fresh1) return launch_fwd_inst2<T, CPL, SK, true>(a, s);
+    }
+    return launch_fwd_inst2<T, CPL, SK, false>(a, s);
 }
 
 // Full-width keys with d = 256 * CPL, CPL in 1..8 (rows of 256 or 512

@@ -213,9 +213,22 @@ class Microbatch:
         run = set(plan.run_sites)
         last = max(plan.run_sites)
         delta = self.cfg.delta
+        self.fused_appends = 0
         for t in range(last + 1):
             if on_site:
                 on_site("fwd_begin", t)
+            if t < self.n_rows and not delta and t in run:
+                # append and read in one call: fused into one launch when the
+                # row sits in its slot and the site runs on the one-warp kernels
+                src = self.outputs.get(t, bank.rows[t])
+                _, _, _, fused = bank.route_fwd_append(src, plan.acc_from[t], plan.sites[t], self.H,
+                                                       self.q[t], self.g[t], self.out[t],
+                                                       self.lse[t], site_id=t, stream=stream)
+                self.fused_appends += int(fused)
+                appended += 1
+                if on_site:
+                    on_site("fwd", t)
+                continue
             if t < self.n_rows:
                 if t == 0 and delta:
                     bank.append_broadcast(self.null, stream)
@@ -260,5 +273,8 @@ class Microbatch:
         self.backward(stream)
 
     def kernel_launches(self) -> int:
-        """Kernels one step launches: appends, forwards, backward + reduce per site."""
-        return self.n_rows + 3 * len(self.plan.run_sites) + (1 if self.cfg.delta else 0)
+        """Kernels one step launches: appends (those fused into their site's forward
+        excepted, as counted by the last forward), forwards, backward + reduce per site."""
+        fused = getattr(self, "fused_appends", 0)
+        return (self.n_rows - fused + 3 * len(self.plan.run_sites) +
+                (1 if self.cfg.delta else 0))

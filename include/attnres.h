@@ -212,6 +212,30 @@ ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
                        int32_t site_id, void *stream);
 
 /*
+ * ar_bank_append followed by ar_route_fwd, in one call: append src as the
+ * next row (rows[accumulate_from] + src when accumulate_from >= 0), then read
+ * the site over `rows`, which may list the new row (its index is the bank's
+ * row count before the call; it is also returned in *out_row when out_row is
+ * not NULL). When the source already sits in its slot (src is the slot
+ * ar_bank_row_ptr gives for the new row, accumulate_from = -1), the site has
+ * full-width keys (r = d) on the one-warp kernels with rows up to 1024 wide
+ * (d = 256, 512, 768 or 1024, H a power of two up to 32, no row listed
+ * twice), the new row's
+ * inverse RMS ("Low-Rank Attention Residuals" Eq. 11, over all d columns) is
+ * computed inside the forward from the staged row and written to the cache:
+ * one launch instead of two, and the rows' key columns are not read a second
+ * time. Otherwise the two calls run one after the other. *fused (when not
+ * NULL) is set to 1 in the first case and to 0 in the second.
+ * Arguments as ar_bank_append and ar_route_fwd; the site's checks run before
+ * anything is appended, so on an argument error the bank is unchanged.
+ * Errors: those of ar_bank_append and ar_route_fwd.
+ */
+ar_status ar_route_fwd_append(ar_bank *bank, const void *src, int32_t accumulate_from,
+                              int32_t *out_row, const int32_t *rows, int32_t n_src, int32_t H,
+                              const float *q, const float *g, void *out, float *lse,
+                              int32_t site_id, int32_t *fused, void *stream);
+
+/*
  * Forward of one routing site in the delta form of attention residuals:
  *   out = partial + alpha * routed,   routed = the read of ar_route_fwd
  * ("Multi-Head Attention Residuals", Sec. 3.3 "Identity-preserving

@@ -325,6 +325,61 @@ def test_repeatable_bits(W):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("d,r,H,dtype,fuses", [(1024, 1024, 8, "bf16", True),
+                                                (1280, 1280, 8, "bf16", False),  # kept apart
+                                                (512, 512, 4, "bf16", True),    # two tokens per warp
+                                                (512, 512, 2, "f32", True),
+                                                (1536, 384, 1, "bf16", False),  # sliced keys
+                                                (4096, 4096, 8, "bf16", False)])  # four-warp kernels
+def test_route_fwd_append(W, orc, d, r, H, dtype, fuses):
+    """ar_route_fwd_append: the append and the read of a site that lists the
+    new row, in one call. Where the kernel family allows, the new row's inverse
+    RMS is computed inside the forward; either way the cached inverse RMS, the
+    output and the lse match the oracle, and a later site reads the cache."""
+    import torch
+    B, _ = W
+    from oracle import inv_rms
+    T, N = 301, 4
+    inp = synth.HostInputs(seed=47, q_std=0.6, g_kind="random")
+    bank = B.Bank(T, d, r, N + 1, dtype)
+    for j in range(N - 1):
+        bank.rows[j].copy_(inp.output(j, T, d, dtype))
+        bank.append(bank.rows[j])
+    bank.rows[N - 1].copy_(inp.output(N - 1, T, d, dtype))
+    q, g = inp.query(5, r), inp.norm_weight(5, r)
+    rows = [0, 2, N - 1, 1]                     # the new row inside the list
+    out, lse, row, fused = bank.route_fwd_append(bank.rows[N - 1], -1, rows, H, q, g, site_id=0)
+    # a second site over the same rows reads the cached inverse RMS
+    out2, lse2 = bank.route_fwd([N - 1, 0], H, q, g, site_id=1)
+    torch.cuda.synchronize()
+    assert B.ar_device_error() == 0
+    assert row == N - 1 and bank.count == N and fused == fuses
+    srcs = [inp.host_output(j, T, d, dtype) for j in range(N)]
+    tol = 1e-5 if dtype == "f32" else 2e-2
+    ref_inv = inv_rms(srcs[N - 1], r=r)
+    got_inv = to64(bank.inv_rms()[:, N - 1])
+    assert np.max(np.abs(got_inv - ref_inv) / ref_inv) < 1e-5
+    ref_out, ref_lse = orc.route_fwd([srcs[j] for j in rows], inp.host_query(5, r),
+                                     inp.host_norm_weight(5, r), H, r=r)
+    assert nmax(to64(out), ref_out) < tol and nmax(to64(lse), ref_lse) < tol
+    ref_out2, ref_lse2 = orc.route_fwd([srcs[N - 1], srcs[0]], inp.host_query(5, r),
+                                       inp.host_norm_weight(5, r), H, r=r)
+    assert nmax(to64(out2), ref_out2) < tol and nmax(to64(lse2), ref_lse2) < tol
+
+
+def test_route_fwd_append_checks_before_appending(W):
+    """A site that lists a row past the new one is refused and nothing is appended."""
+    B, _ = W
+    import torch
+    bank = B.Bank(64, 256, 256, 4, "bf16")
+    bank.append(torch.randn(64, 256, device="cuda").bfloat16())
+    q = 0.1 * torch.randn(256, device="cuda")
+    with pytest.raises(B.ARError) as e:
+        bank.route_fwd_append(bank.rows[1], -1, [0, 2], 4, q)
+    assert e.value.name == "AR_ERR_INVALID_ARG"
+    assert bank.count == 1
+
+
 @pytest.mark.parametrize("d,r,H", [(1280, 1280, 8), (1280, 1280, 16), (4096, 1024, 8),
                                    (3072, 3072, 8), (1536, 384, 1)])
 def test_gradient_rows_not_32_byte_aligned(W, d, r, H):
