@@ -198,3 +198,26 @@ def test_multi_query_read_argument_checks(B):
     assert _err(B.ar_route_fwd_multi, h, [0], 4, nine, None, nine, nine, 0) == "AR_ERR_INVALID_ARG"
     assert _err(B.ar_route_fwd_multi, h, [0], 3, [FAKE], None, [FAKE], [FAKE], 0) == "AR_ERR_SHAPE"
     B.ar_bank_destroy(h)
+
+
+def test_route_fwd_append_checks_precede_launch(B):
+    """ar_route_fwd_append runs the append's and the site's checks before it
+    appends or launches anything: on each refusal the bank is unchanged."""
+    import torch
+    h = _bank(B, cap=2)
+    fa = B.ar_route_fwd_append
+    # the site lists a row past the new one (the new row is 0)
+    assert _err(fa, h, FAKE, -1, [0, 1], 4, FAKE, None, FAKE, FAKE, 0, 0) == "AR_ERR_INVALID_ARG"
+    # accumulation onto a row that does not exist
+    assert _err(fa, h, FAKE, 0, [0], 4, FAKE, None, FAKE, FAKE, 0, 0) == "AR_ERR_INVALID_ARG"
+    assert _err(fa, h, FAKE + 1, -1, [0], 4, FAKE, None, FAKE, FAKE, 0, 0) == "AR_ERR_ALIGN"
+    assert _err(fa, h, FAKE, -1, [0], 3, FAKE, None, FAKE, FAKE, 0, 0) == "AR_ERR_SHAPE"
+    assert _err(fa, h, FAKE, -1, [0], 4, FAKE, None, None, FAKE, 0, 0) == "AR_ERR_INVALID_ARG"
+    assert _err(fa, h, FAKE, -1, [0], 4, None, None, FAKE, FAKE, 0, 0) == "AR_ERR_INVALID_ARG"
+    assert _err(fa, h, FAKE, -1, [], 4, FAKE, None, FAKE, FAKE, 0, 0) == "AR_ERR_INVALID_ARG"
+    assert B.ar_bank_row_count(h) == 0
+    if not torch.cuda.is_available():
+        # a valid call reaches the launch, which fails without a GPU
+        assert _err(fa, h, FAKE, -1, [0], 4, FAKE, None, FAKE, FAKE, 0, 0) == "AR_ERR_CUDA"
+        assert B.ar_bank_row_count(h) == 0
+    B.ar_bank_destroy(h)
