@@ -284,12 +284,14 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     const float inv_width = 1.0f / (float)(a.norm_full ? d : r);
 
     const int64_t GB = gridDim.x, gb = blockIdx.x;
-    const int64_t total = TT * N;
-    const int64_t lo = total * gb / GB, hi = total * (gb + 1) / GB;
+    // tokens gb, gb + GB, ..., every source of each in list order: at any
+    // time the blocks read neighbouring tokens of the same row
+    const int64_t ntok = gb < TT ? (TT - 1 - gb) / GB + 1 : 0;
+    const int64_t lo = 0, hi = ntok * N;
     const uint64_t pol = l2_policy_evict_first();
 
-    int64_t issued = lo, tok_p = lo / N;
-    int n_p = (int)(lo - tok_p * N), slot_p = 0;
+    int64_t issued = lo, tok_p = gb;
+    int n_p = 0, slot_p = 0;
     auto issue_next = [&]() {
         if (threadIdx.x == 0) {
             const bool first = (s_first[n_p >> 5] >> (n_p & 31)) & 1u;
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             if (!first) bulk_g2s(dst + vbytes, a.grad + off * d, gbytes, &bars[slot_p], pol);
         }
         ++issued;
-        if (++n_p == N) { n_p = 0; ++tok_p; }
+        if (++n_p == N) { n_p = 0; tok_p += GB; }
         if (++slot_p == S) slot_p = 0;
     };
     for (int s = 0; s < S && issued < hi; ++s) issue_next();
@@ -310,17 +312,17 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     float G[CPL][8];
     float S_h = 0.f, lse_h = 0.f, dal = 0.f;
     const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
-    int64_t tok = lo / N, i = lo;
-    int n = (int)(lo - tok * N), slot = 0, par = 0;
+    int64_t tok = gb, i = lo;
+    int n = 0, slot = 0, par = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (; i < hi; ++i) {
         if (i == lo || n == 0) {
             const T *grow = static_cast<const T *>(a.dout) + tok * d;
             const T *orow = static_cast<const T *>(a.fout) + tok * d;
-            if (threadIdx.x == 0 && (tok + 1) * N < hi) {  // the next token's rows, into L2
-                prefetch_l2(grow + d, vbytes);
-                prefetch_l2(orow + d, vbytes);
+            if (threadIdx.x == 0 && tok + GB < TT) {  // this block's next token's rows, into L2
+                prefetch_l2(grow + GB * d, vbytes);
+                prefetch_l2(orow + GB * d, vbytes);
             }
             float sp = 0.f, raw = 0.f;
 #pragma unroll
@@ -471,7 +473,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             if (issued < hi) issue_next();
         }
         par ^= 1;
-        if (++n == N) { n = 0; ++tok; }
+        if (++n == N) { n = 0; tok += GB; }
         if (++slot == S) slot = 0;
     }
     if (!ok) {
