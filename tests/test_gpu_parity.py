@@ -479,14 +479,18 @@ def test_error_paths_on_device(W):
     assert B.ar_device_error() == 0
 
 
-def test_full_size_1b_sampled_tokens(W, orc):
-    """The 1B-shaped microbatch at full size (T=16384, d=1280, H=8, 73 sites), in
-    the launch configuration the benchmark times: outputs, lse and source
-    gradients of 48 sampled tokens against the oracle, dq/dg of the last site
-    (all 73 sources, all tokens) against the oracle in token chunks."""
+@pytest.mark.parametrize("name", ["1B", "350M", "100M"])
+def test_full_size_sampled_tokens(W, orc, name):
+    """The 1B / 350M / 100M-shaped microbatches at full size (T=16384; d=1280 /
+    1024 / 512; 73 / 49 / 25 sites), in the launch configuration the benchmark
+    times (appends fused into the forward where the kernels allow): the cached
+    inverse RMS, outputs, lse and source gradients of 48 sampled tokens
+    against the oracle, dq/dg of the last site (every source, all tokens)
+    against the oracle in token chunks."""
     import torch
+    from oracle import inv_rms
     _, wl = W
-    cfg = wl.CONFIGS["1B"]
+    cfg = wl.CONFIGS[name]
     inputs = synth.DeviceInputs(seed=11, q_std=0.3, g_kind="random")
     mb = wl.Microbatch(cfg, cfg.H, inputs)
     mb.step()
@@ -497,6 +501,10 @@ def test_full_size_1b_sampled_tokens(W, orc):
     toks[0], toks[-1] = 0, T - 1
     ti = torch.as_tensor(toks, device="cuda")
     rows = [to64(mb.bank.rows[j][ti]) for j in range(mb.n_rows)]
+    inv = to64(mb.bank.inv_rms()[ti])
+    for j in range(mb.n_rows):
+        ref = inv_rms(rows[j])
+        assert np.max(np.abs(inv[:, j] - ref) / ref) < 1e-5, j
     dsrc = {j: np.zeros((len(toks), d)) for j in range(mb.n_rows)}
     tol = TOL["bf16"]
     for s in mb.plan.run_sites:
