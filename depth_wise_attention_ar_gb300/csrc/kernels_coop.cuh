@@ -60,7 +60,7 @@ __device__ __forceinline__ CoopMap coop_map(int w, int lane, int H, int d, int r
 inline size_t coop_fwd_smem_bytes(int d, size_t esize)
 {
     return (size_t)kCoopFwdStages * d * esize + kCoopFwdStages * 8 + 2 * 32 * 4 +
-           AR_MAX_SOURCES * 4;
+           2 * AR_MAX_SOURCES * 4;
 }
 
 template <typename T, int CPL, bool LR>
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     unsigned char *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)S * row_bytes);
     float *zs = reinterpret_cast<float *>(bars + S);   // [2][32] scores per head
-    float *cur_inv = zs + 64;                           // [AR_MAX_SOURCES]
+    float *cur_inv = zs + 64;                           // [2][AR_MAX_SOURCES]
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
@@ -127,28 +127,47 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     };
     for (int s = 0; s < S && issued < total; ++s) issue_next();
 
-    int n = 0, slot = 0, par = 0;
+    // One block barrier per item: it carries the stage wait's outcome, the
+    // key warp's scores (sliced keys) and the token's inverse RMS, and shows
+    // that every warp is past the previous item, whose stage thread 0 then
+    // refills. Scores and inverse RMS are double-buffered for that.
+    int n = 0, slot = 0, par = 0, tpar = 0;
     uint32_t phase = 0;
     int64_t tok = gb, i = 0;
     float m = 0.f, l = 0.f;
     float acc[CPL][8];
     bool ok = true;
     for (; i < total; ++i) {
+        float *inv_t = cur_inv + tpar * AR_MAX_SOURCES;
         if (n == 0) {
             // delta form: the residual-stream row this token's epilogue reads, into L2
             if (a.partial && threadIdx.x == 0)
                 prefetch_l2(static_cast<const T *>(a.partial) + tok * d, row_bytes);
             for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
-                cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
-            __syncthreads();
+                inv_t[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
         }
         const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
+        const unsigned char *buf = ring + (size_t)slot * row_bytes;
+        float v[CPL][8];
+        if constexpr (LR) {
+            if (mp.key_warp && got) {
+                float zr = 0.f;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    float kv[8];
+                    ld_chunk_s(reinterpret_cast<const T *>(buf + kidx[j] * CB), kv);
+                    zr = __fadd_rn(zr, dot8(qg[j], kv));
+                }
+                zr = group_sum(zr, mp.LPHk);
+                // the raw score: the inverse RMS is applied after the barrier
+                if (mp.ksub == 0) zs[par * 32 + mp.hk] = zr;
+            }
+        }
         if (__syncthreads_or(!got)) { ok = false; break; }
         phase ^= 1u << slot;
-        const unsigned char *buf = ring + (size_t)slot * row_bytes;
-        const float iv = cur_inv[n];
+        if (i > 0 && issued < total) issue_next();  // the previous item's stage is free
+        const float iv = inv_t[n];
 
-        float v[CPL][8];
 #pragma unroll
         for (int j = 0; j < CPL; ++j) ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
         float z;
@@ -159,19 +178,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             zr = group_sum(zr, mp.LPH);
             z = __fmul_rn(zr, iv);
         } else {
-            if (mp.key_warp) {
-                float zr = 0.f;
-#pragma unroll
-                for (int j = 0; j < CPL; ++j) {
-                    float kv[8];
-                    ld_chunk_s(reinterpret_cast<const T *>(buf + kidx[j] * CB), kv);
-                    zr = __fadd_rn(zr, dot8(qg[j], kv));
-                }
-                zr = group_sum(zr, mp.LPHk);
-                if (mp.ksub == 0) zs[par * 32 + mp.hk] = __fmul_rn(zr, iv);
-            }
-            __syncthreads();
-            z = zs[par * 32 + mp.h];
+            z = __fmul_rn(zs[par * 32 + mp.h], iv);
         }
         if (n == 0) {
             m = z;
@@ -197,8 +204,6 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         for (int j = 0; j < CPL; ++j)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, v[j][e], acc[j][e]);
-        __syncthreads();  // every warp is past this stage
-        if (issued < total) issue_next();
 
         if (n == N - 1) {
             const float rl = 1.f / l;
@@ -212,7 +217,11 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             if (mp.sub == 0) a.lse[tok * H + mp.h] = m + log2f(l) * kLn2;
         }
         par ^= 1;
-        if (++n == N) { n = 0; tok += GB; }
+        if (++n == N) {
+            n = 0;
+            tok += GB;
+            tpar ^= 1;
+        }
         if (++slot == S) slot = 0;
     }
     if (!ok) {
