@@ -57,10 +57,12 @@ __device__ __forceinline__ CoopMap coop_map(int w, int lane, int H, int d, int r
     return m;
 }
 
-inline size_t coop_fwd_smem_bytes(int d, size_t esize)
+// Stages, barriers, scores, inverse RMS; with the delta form also two
+// buffers of the residual-stream row and their barriers.
+inline size_t coop_fwd_smem_bytes(int d, size_t esize, bool delta)
 {
     return (size_t)kCoopFwdStages * d * esize + kCoopFwdStages * 8 + 2 * 32 * 4 +
-           2 * AR_MAX_SOURCES * 4;
+           2 * AR_MAX_SOURCES * 4 + (delta ? 16 + 2 * (size_t)d * esize : 0);
 }
 
 template <typename T, int CPL, bool LR>
@@ -81,8 +83,17 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)S * row_bytes);
     float *zs = reinterpret_cast<float *>(bars + S);   // [2][32] scores per head
     float *cur_inv = zs + 64;                           // [2][AR_MAX_SOURCES]
+    // delta form: the token's residual-stream row, staged by a bulk copy at
+    // the token's first item (two buffers, by token parity)
+    const bool delta = a.partial != nullptr;
+    uint64_t *pbars = reinterpret_cast<uint64_t *>(cur_inv + 2 * AR_MAX_SOURCES);
+    unsigned char *pbuf = reinterpret_cast<unsigned char *>(pbars + 2);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        if (delta) {
+            mbar_init(&pbars[0], 1);
+            mbar_init(&pbars[1], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
@@ -132,17 +143,23 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     // that every warp is past the previous item, whose stage thread 0 then
     // refills. Scores and inverse RMS are double-buffered for that.
     int n = 0, slot = 0, par = 0, tpar = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, pphase = 0;
     int64_t tok = gb, i = 0;
     float m = 0.f, l = 0.f;
     float acc[CPL][8];
-    bool ok = true;
+    const float alpha = delta && a.alpha ? __ldg(a.alpha) : 1.0f;
+    bool ok = true, bad = false;
     for (; i < total; ++i) {
         float *inv_t = cur_inv + tpar * AR_MAX_SOURCES;
         if (n == 0) {
-            // delta form: the residual-stream row this token's epilogue reads, into L2
-            if (a.partial && threadIdx.x == 0)
-                prefetch_l2(static_cast<const T *>(a.partial) + tok * d, row_bytes);
+            // every warp is past token tok - 2 GB, whose residual row used this buffer
+            if (delta && threadIdx.x == 0) {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&pbars[tpar], row_bytes);
+                bulk_g2s(pbuf + (size_t)tpar * row_bytes,
+                         static_cast<const unsigned char *>(a.partial) + tok * row_bytes, row_bytes,
+                         &pbars[tpar], pol);
+            }
             for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
                 inv_t[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
         }
@@ -163,7 +180,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                 if (mp.ksub == 0) zs[par * 32 + mp.hk] = zr;
             }
         }
-        if (__syncthreads_or(!got)) { ok = false; break; }
+        if (__syncthreads_or(!got || bad)) { ok = false; break; }
         phase ^= 1u << slot;
         if (i > 0 && issued < total) issue_next();  // the previous item's stage is free
         const float iv = inv_t[n];
@@ -207,14 +224,35 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
 
         if (n == N - 1) {
             const float rl = 1.f / l;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                float o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
-                store_output<T>(a, tok * d + cidx[j] * 8, o);
+            bool pg = true;
+            if (delta) {
+                pg = mbar_wait(&pbars[tpar], (pphase >> tpar) & 1u, kWaitLimit);
+                pphase ^= 1u << tpar;
+                bad = bad || !pg;
             }
-            if (mp.sub == 0) a.lse[tok * H + mp.h] = m + log2f(l) * kLn2;
+            if (pg) {
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
+                    const int64_t off = tok * d + cidx[j] * 8;
+                    if (delta) {
+                        // out = partial + alpha * routed, routed kept for the backward
+                        float pv[8], y[8];
+                        ld_chunk_s(reinterpret_cast<const T *>(pbuf + (size_t)tpar * row_bytes +
+                                                               cidx[j] * CB),
+                                   pv);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) y[e] = fmaf(alpha, o[e], pv[e]);
+                        if (a.routed) st_chunk_g(static_cast<T *>(a.routed) + off, o);
+                        st_chunk_g(static_cast<T *>(a.out) + off, y);
+                    } else {
+                        store_output<T>(a, off, o);
+                    }
+                }
+                if (mp.sub == 0) a.lse[tok * H + mp.h] = m + log2f(l) * kLn2;
+            }
         }
         par ^= 1;
         if (++n == N) {
@@ -224,7 +262,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         }
         if (++slot == S) slot = 0;
     }
-    if (!ok) {
+    if (!ok || bad) {
         if (threadIdx.x == 0) {
             report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
             for (int64_t j = i; j < issued; ++j) {
@@ -232,6 +270,8 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                 phase ^= 1u << slot;
                 if (++slot == S) slot = 0;
             }
+            // a residual row still in flight (the current token's)
+            if (delta) mbar_wait(&pbars[tpar], (pphase >> tpar) & 1u, 1u << 16);
         }
     }
 }
@@ -510,7 +550,7 @@ template <typename T, int CPL, bool LR>
 cudaError_t coop_fwd_inst(const RouteArgs &a, cudaStream_t s)
 {
     const void *k = reinterpret_cast<const void *>(&route_fwd_coop_kernel<T, CPL, LR>);
-    const size_t smem = coop_fwd_smem_bytes(a.d, sizeof(T));
+    const size_t smem = coop_fwd_smem_bytes(a.d, sizeof(T), a.partial != nullptr);
     int grid = 0;
     cudaError_t e = persistent_grid(k, kCoopWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
