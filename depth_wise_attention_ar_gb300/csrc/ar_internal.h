@@ -35,6 +35,11 @@ struct RouteArgs {
     // in this call, whose inverse RMS the kernel computes and caches (0: none)
     int fresh1;
     float eps;             // the bank's RMSNorm epsilon
+    // the fused append's source when the new row is not already in its slot:
+    // new = fresh_src (copy) or row acc_row + fresh_src (block partial sum),
+    // written to its slot by the forward; acc_row = -1 for a copy
+    const void *fresh_src;
+    int acc_row;
     int rows[AR_MAX_SOURCES];
     // a row listed k > 1 times in a site enters once with log k added to its
     // score (softmax over the list = softmax over distinct rows with weights k)
@@ -61,9 +66,11 @@ cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
 cudaError_t launch_route_fwd_multi(const MultiArgs &m, ar_dtype dt, cudaStream_t s);
 cudaError_t dispatch_fwd_multi_mma(const MultiArgs &m, cudaStream_t s);  // bf16 rows
 cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps);
-// The site runs on a forward kernel that can take the append of a listed row
-// (full-width keys on the one-warp kernels).
-bool fwd_fuses_append(const RouteArgs &a, ar_dtype dt);
+// The site runs on a forward kernel that can take the append of a listed row:
+// with the row in its slot (in_place) the one-warp full-key kernels on rows up
+// to 1024 wide and the four-warp kernels; with a copy or a partial sum to
+// form, the four-warp kernels.
+bool fwd_fuses_append(const RouteArgs &a, ar_dtype dt, bool in_place);
 // dq and dg are written with the strides of q and g respectively.
 cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, int64_t q_stride,
                                const float *g, int64_t g_stride, float *dq, float *dg,

@@ -328,16 +328,20 @@ ar_status ar_route_fwd_append(ar_bank *bank, const void *src, int32_t accumulate
 
     void *slot = nullptr;
     ar_bank_row_ptr(bank, new_row, &slot);
-    if (src == slot && accumulate_from < 0 && bank->T > 0) {
-        // the row already sits in its slot: the forward computes its inverse RMS
+    const bool in_place = src == slot && accumulate_from < 0;
+    if (bank->T > 0 && (in_place || aligned16(src))) {
+        // the forward forms the row (copy or partial sum) where needed and
+        // computes its inverse RMS
         ++bank->count;
         ar::RouteArgs a;
         fill_common(a, bank, rows, n_src, H, q, g);
         int idx = -1;
         for (int i = 0; i < a.n_src; ++i)
             if (a.rows[i] == new_row) idx = i;
-        if (idx >= 0 && ar::fwd_fuses_append(a, bank->dtype)) {
+        if (idx >= 0 && ar::fwd_fuses_append(a, bank->dtype, in_place)) {
             a.fresh1 = idx + 1;
+            a.fresh_src = in_place ? nullptr : src;
+            a.acc_row = accumulate_from;
             a.out = out;
             a.lse = lse;
             const cudaError_t e =

@@ -59,13 +59,16 @@ __device__ __forceinline__ CoopMap coop_map(int w, int lane, int H, int d, int r
 
 // Stages, barriers, scores, inverse RMS; with the delta form also two
 // buffers of the residual-stream row and their barriers.
-inline size_t coop_fwd_smem_bytes(int d, size_t esize, bool delta)
+// Stages, barriers, scores, inverse RMS, the fused append's squares; with
+// the delta form or a fused partial sum also two buffers of a per-token row
+// (the residual stream, or the sublayer output to add) and their barriers.
+inline size_t coop_fwd_smem_bytes(int d, size_t esize, bool tok_row)
 {
     return (size_t)kCoopFwdStages * d * esize + kCoopFwdStages * 8 + 2 * 32 * 4 +
-           2 * AR_MAX_SOURCES * 4 + (delta ? 16 + 2 * (size_t)d * esize : 0);
+           2 * AR_MAX_SOURCES * 4 + 8 * 4 + (tok_row ? 16 + 2 * (size_t)d * esize : 0);
 }
 
-template <typename T, int CPL, bool LR>
+template <typename T, int CPL, bool LR, bool FRESH = false>
 __global__ void __launch_bounds__(kCoopWarps * 32)
     route_fwd_coop_kernel(const __grid_constant__ RouteArgs a)
 {
@@ -83,14 +86,19 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)S * row_bytes);
     float *zs = reinterpret_cast<float *>(bars + S);   // [2][32] scores per head
     float *cur_inv = zs + 64;                           // [2][AR_MAX_SOURCES]
-    // delta form: the token's residual-stream row, staged by a bulk copy at
-    // the token's first item (two buffers, by token parity)
+    float *ssq = cur_inv + 2 * AR_MAX_SOURCES;           // [2][4] fused append: squares
+    // a per-token row staged by a bulk copy at the token's first item (two
+    // buffers, by token parity): the delta form's residual stream, or the
+    // sublayer output a fused partial sum adds
     const bool delta = a.partial != nullptr;
-    uint64_t *pbars = reinterpret_cast<uint64_t *>(cur_inv + 2 * AR_MAX_SOURCES);
+    const bool fresh_acc = FRESH && a.acc_row >= 0;
+    const bool tok_row = delta || fresh_acc;
+    const unsigned char *tok_src = static_cast<const unsigned char *>(delta ? a.partial : a.fresh_src);
+    uint64_t *pbars = reinterpret_cast<uint64_t *>(ssq + 8);
     unsigned char *pbuf = reinterpret_cast<unsigned char *>(pbars + 2);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-        if (delta) {
+        if (tok_row) {
             mbar_init(&pbars[0], 1);
             mbar_init(&pbars[1], 1);
         }
@@ -126,8 +134,15 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     int n_p = 0, slot_p = 0;
     auto issue_next = [&]() {
         if (threadIdx.x == 0) {
+            // the fused append's item stages the row the new one is formed
+            // from: the previous partial sum, or the source to copy
             const unsigned char *src = static_cast<const unsigned char *>(a.bank) +
                                        ((int64_t)s_rows[n_p] * TT + tok_p) * row_bytes;
+            if (FRESH && n_p + 1 == a.fresh1 && a.fresh_src)
+                src = a.acc_row >= 0
+                          ? static_cast<const unsigned char *>(a.bank) +
+                                ((int64_t)a.acc_row * TT + tok_p) * row_bytes
+                          : static_cast<const unsigned char *>(a.fresh_src) + tok_p * row_bytes;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bars[slot_p], row_bytes);
             bulk_g2s(ring + (size_t)slot_p * row_bytes, src, row_bytes, &bars[slot_p], pol);
@@ -152,12 +167,11 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     for (; i < total; ++i) {
         float *inv_t = cur_inv + tpar * AR_MAX_SOURCES;
         if (n == 0) {
-            // every warp is past token tok - 2 GB, whose residual row used this buffer
-            if (delta && threadIdx.x == 0) {
+            // every warp is past token tok - 2 GB, whose row used this buffer
+            if (tok_row && threadIdx.x == 0) {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(&pbars[tpar], row_bytes);
-                bulk_g2s(pbuf + (size_t)tpar * row_bytes,
-                         static_cast<const unsigned char *>(a.partial) + tok * row_bytes, row_bytes,
+                bulk_g2s(pbuf + (size_t)tpar * row_bytes, tok_src + tok * row_bytes, row_bytes,
                          &pbars[tpar], pol);
             }
             for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
@@ -166,6 +180,53 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
         const unsigned char *buf = ring + (size_t)slot * row_bytes;
         float v[CPL][8];
+        const bool fresh = FRESH && n + 1 == a.fresh1;
+        if constexpr (FRESH) {
+            if (fresh && got) {
+                // the fused append: form the new row where needed (in the stage
+                // and in its slot), then the squares of its stored values over
+                // the RMS columns of this warp's group
+                unsigned char *sb = ring + (size_t)slot * row_bytes;
+                bool pg = true;
+                if (fresh_acc) {
+                    pg = mbar_wait(&pbars[tpar], (pphase >> tpar) & 1u, kWaitLimit);
+                    pphase ^= 1u << tpar;
+                    bad = bad || !pg;
+                }
+                if (a.fresh_src && pg) {
+                    T *slot_row = static_cast<T *>(const_cast<void *>(a.bank)) +
+                                  ((int64_t)s_rows[n] * TT + tok) * d;
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) {
+                        float x[8];
+                        ld_chunk_s(reinterpret_cast<const T *>(sb + cidx[j] * CB), x);
+                        if (fresh_acc) {
+                            float y[8];
+                            ld_chunk_s(reinterpret_cast<const T *>(pbuf + (size_t)tpar * row_bytes +
+                                                                   cidx[j] * CB),
+                                       y);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) x[e] += y[e];
+                        }
+                        st_chunk_g(reinterpret_cast<T *>(sb + cidx[j] * CB), x);
+                        st_chunk_g(slot_row + cidx[j] * 8, x);
+                    }
+                    __syncwarp();
+                }
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    if (a.norm_full || cidx[j] >= key0) {
+                        float x[8];
+                        ld_chunk_s(reinterpret_cast<const T *>(sb + cidx[j] * CB), x);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                    }
+                }
+                ss = warp_sum(ss);
+                if (lane == 0) ssq[par * 4 + w] = ss;
+            }
+        }
         if constexpr (LR) {
             if (mp.key_warp && got) {
                 float zr = 0.f;
@@ -183,7 +244,12 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         if (__syncthreads_or(!got || bad)) { ok = false; break; }
         phase ^= 1u << slot;
         if (i > 0 && issued < total) issue_next();  // the previous item's stage is free
-        const float iv = inv_t[n];
+        float iv = inv_t[n];
+        if (FRESH && fresh) {
+            const float sum = ((ssq[par * 4 + 0] + ssq[par * 4 + 1]) + ssq[par * 4 + 2]) + ssq[par * 4 + 3];
+            iv = rsqrtf(fmaf(sum, 1.0f / (float)(a.norm_full ? d : r), a.eps));
+            if (threadIdx.x == 0) const_cast<float *>(a.inv)[tok * a.inv_ld + s_rows[n]] = iv;
+        }
 
 #pragma unroll
         for (int j = 0; j < CPL; ++j) ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
@@ -270,8 +336,8 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                 phase ^= 1u << slot;
                 if (++slot == S) slot = 0;
             }
-            // a residual row still in flight (the current token's)
-            if (delta) mbar_wait(&pbars[tpar], (pphase >> tpar) & 1u, 1u << 16);
+            // a per-token row still in flight (the current token's)
+            if (tok_row) mbar_wait(&pbars[tpar], (pphase >> tpar) & 1u, 1u << 16);
         }
     }
 }
@@ -546,16 +612,24 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     if (a.dalpha && lane == 0) a.ws[GB * r + gb * 4 + w] = dal;
 }
 
-template <typename T, int CPL, bool LR>
-cudaError_t coop_fwd_inst(const RouteArgs &a, cudaStream_t s)
+template <typename T, int CPL, bool LR, bool FRESH>
+cudaError_t coop_fwd_inst2(const RouteArgs &a, cudaStream_t s)
 {
-    const void *k = reinterpret_cast<const void *>(&route_fwd_coop_kernel<T, CPL, LR>);
-    const size_t smem = coop_fwd_smem_bytes(a.d, sizeof(T), a.partial != nullptr);
+    const void *k = reinterpret_cast<const void *>(&route_fwd_coop_kernel<T, CPL, LR, FRESH>);
+    const size_t smem = coop_fwd_smem_bytes(a.d, sizeof(T),
+                                            a.partial != nullptr || (a.fresh1 && a.acc_row >= 0));
     int grid = 0;
     cudaError_t e = persistent_grid(k, kCoopWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
-    route_fwd_coop_kernel<T, CPL, LR><<<grid, kCoopWarps * 32, smem, s>>>(a);
+    route_fwd_coop_kernel<T, CPL, LR, FRESH><<<grid, kCoopWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+// The fused-append variant when the host asks for it (fresh1).
+template <typename T, int CPL, bool LR>
+cudaError_t coop_fwd_inst(const RouteArgs &a, cudaStream_t s)
+{
+    return a.fresh1 ? coop_fwd_inst2<T, CPL, LR, true>(a, s) : coop_fwd_inst2<T, CPL, LR, false>(a, s);
 }
 
 template <typename T, int CPL, bool LR>

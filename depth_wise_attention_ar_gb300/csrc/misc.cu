@@ -509,12 +509,14 @@ cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_rows)
     return bwd_any(a, dt, nullptr, grid_rows);
 }
 
-bool fwd_fuses_append(const RouteArgs &a, ar_dtype dt)
+bool fwd_fuses_append(const RouteArgs &a, ar_dtype dt, bool in_place)
 {
-    // rows up to 1024 wide: at 1280 the fused forward measured slower than the
-    // separate append (1B forward phase 18.02 -> 18.46 ms)
-    return a.r == a.d && a.d <= 1024 && !a.has_bias && !a.partial &&
-           family_of(a.d, a.r, a.H, a.n_src, dt == AR_BF16 ? 2 : 4, false) == Family::kFull;
+    if (a.has_bias || a.partial) return false;
+    const Family f = family_of(a.d, a.r, a.H, a.n_src, dt == AR_BF16 ? 2 : 4, false);
+    if (f == Family::kCoop) return true;
+    // one-warp kernels, rows up to 1024 wide: at 1280 the fused forward measured
+    // slower than the separate append (1B forward phase 18.02 -> 18.46 ms)
+    return in_place && f == Family::kFull && a.r == a.d && a.d <= 1024;
 }
 
 // One block per token with one lane per 8-column chunk: d a multiple of 256

@@ -325,40 +325,57 @@ def test_repeatable_bits(W):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("d,r,H,dtype,fuses", [(1024, 1024, 8, "bf16", True),
-                                                (1280, 1280, 8, "bf16", False),  # kept apart
-                                                (512, 512, 4, "bf16", True),    # two tokens per warp
-                                                (512, 512, 2, "f32", True),
-                                                (1536, 384, 1, "bf16", False),  # sliced keys
-                                                (4096, 4096, 8, "bf16", False)])  # four-warp kernels
-def test_route_fwd_append(W, orc, d, r, H, dtype, fuses):
+@pytest.mark.parametrize("d,r,H,dtype,mode,fuses", [
+    (1024, 1024, 8, "bf16", "in_place", True),
+    (1280, 1280, 8, "bf16", "in_place", False),   # kept apart (measured slower fused)
+    (512, 512, 4, "bf16", "in_place", True),      # two tokens per warp
+    (512, 512, 2, "f32", "in_place", True),
+    (1536, 384, 1, "bf16", "in_place", False),    # sliced keys
+    (1024, 1024, 8, "bf16", "acc", False),        # one-warp kernels: row in place only
+    (4096, 4096, 8, "bf16", "in_place", True),    # four-warp kernels
+    (4096, 1024, 8, "bf16", "acc", True),         # block partial sum formed in the forward
+    (4096, 1024, 8, "bf16", "copy", True),
+    (3072, 3072, 8, "f32", "acc", True),
+    (2048, 512, 4, "bf16", "copy", True),
+])
+def test_route_fwd_append(W, orc, d, r, H, dtype, mode, fuses):
     """ar_route_fwd_append: the append and the read of a site that lists the
-    new row, in one call. Where the kernel family allows, the new row's inverse
-    RMS is computed inside the forward; either way the cached inverse RMS, the
-    output and the lse match the oracle, and a later site reads the cache."""
+    new row, in one call. Where the kernel family allows, the forward forms the
+    new row (a copy or a partial sum, rounded once) and computes its inverse
+    RMS. The bank row must equal what ar_bank_append writes, bit for bit, the
+    cached inverse RMS the oracle's, and the output, the lse and a later
+    site's read the oracle's."""
     import torch
     B, _ = W
     from oracle import inv_rms
     T, N = 301, 4
     inp = synth.HostInputs(seed=47, q_std=0.6, g_kind="random")
-    bank = B.Bank(T, d, r, N + 1, dtype)
-    for j in range(N - 1):
-        bank.rows[j].copy_(inp.output(j, T, d, dtype))
-        bank.append(bank.rows[j])
-    bank.rows[N - 1].copy_(inp.output(N - 1, T, d, dtype))
+    banks = [B.Bank(T, d, r, N + 1, dtype) for _ in range(2)]   # fused call, separate calls
+    src = inp.output(N - 1, T, d, dtype)
+    for bank in banks:
+        for j in range(N - 1):
+            bank.rows[j].copy_(inp.output(j, T, d, dtype))
+            bank.append(bank.rows[j])
+        if mode == "in_place":
+            bank.rows[N - 1].copy_(src)
+    acc = 0 if mode == "acc" else -1
     q, g = inp.query(5, r), inp.norm_weight(5, r)
     rows = [0, 2, N - 1, 1]                     # the new row inside the list
-    out, lse, row, fused = bank.route_fwd_append(bank.rows[N - 1], -1, rows, H, q, g, site_id=0)
-    # a second site over the same rows reads the cached inverse RMS
-    out2, lse2 = bank.route_fwd([N - 1, 0], H, q, g, site_id=1)
+    fb, sb = banks
+    f_src = fb.rows[N - 1] if mode == "in_place" else src
+    out, lse, row, fused = fb.route_fwd_append(f_src, acc, rows, H, q, g, site_id=0)
+    out2, lse2 = fb.route_fwd([N - 1, 0], H, q, g, site_id=1)   # reads the cached inverse RMS
+    sb.append(sb.rows[N - 1] if mode == "in_place" else src, acc)
     torch.cuda.synchronize()
     assert B.ar_device_error() == 0
-    assert row == N - 1 and bank.count == N and fused == fuses
-    srcs = [inp.host_output(j, T, d, dtype) for j in range(N)]
-    tol = 1e-5 if dtype == "f32" else 2e-2
-    ref_inv = inv_rms(srcs[N - 1], r=r)
-    got_inv = to64(bank.inv_rms()[:, N - 1])
+    assert row == N - 1 and fb.count == N and fused == fuses
+    assert torch.equal(fb.rows[N - 1], sb.rows[N - 1])
+    new = to64(sb.rows[N - 1])
+    got_inv = to64(fb.inv_rms()[:, N - 1])
+    ref_inv = inv_rms(new, r=r)
     assert np.max(np.abs(got_inv - ref_inv) / ref_inv) < 1e-5
+    srcs = [to64(sb.rows[j]) for j in range(N)]
+    tol = 1e-5 if dtype == "f32" else 2e-2
     ref_out, ref_lse = orc.route_fwd([srcs[j] for j in rows], inp.host_query(5, r),
                                      inp.host_norm_weight(5, r), H, r=r)
     assert nmax(to64(out), ref_out) < tol and nmax(to64(lse), ref_lse) < tol
