@@ -216,16 +216,19 @@ ar_status ar_route_fwd(ar_bank *bank, const int32_t *rows, int32_t n_src, int32_
  * next row (rows[accumulate_from] + src when accumulate_from >= 0), then read
  * the site over `rows`, which may list the new row (its index is the bank's
  * row count before the call; it is also returned in *out_row when out_row is
- * not NULL). When the source already sits in its slot (src is the slot
- * ar_bank_row_ptr gives for the new row, accumulate_from = -1), the site has
- * full-width keys (r = d) on the one-warp kernels with rows up to 1024 wide
- * (d = 256, 512, 768 or 1024, H a power of two up to 32, no row listed
- * twice), the new row's
- * inverse RMS ("Low-Rank Attention Residuals" Eq. 11, over all d columns) is
- * computed inside the forward from the staged row and written to the cache:
- * one launch instead of two, and the rows' key columns are not read a second
- * time. Otherwise the two calls run one after the other. *fused (when not
- * NULL) is set to 1 in the first case and to 0 in the second.
+ * not NULL). The forward itself forms the new row (a copy, or the partial sum
+ * rounded once, written to the row's slot) and computes its inverse RMS
+ * ("Low-Rank Attention Residuals" Eq. 11) from the staged values when the
+ * site lists the new row once and runs on
+ *   - the four-warp kernels (d a multiple of 1024; src 16-byte aligned
+ *     unless it is the slot itself), or
+ *   - the one-warp full-key kernels with rows up to 1024 wide (d = 256, 512,
+ *     768 or 1024, H a power of two up to 32), when src already sits in its
+ *     slot (the pointer ar_bank_row_ptr gives, accumulate_from = -1):
+ * one launch instead of two, and the new row is not read back. Otherwise the
+ * two calls run one after the other. *fused (when not NULL) is set to 1 in
+ * the first case and to 0 in the second. The bank row and its cached inverse
+ * RMS are those ar_bank_append gives (the row bit for bit).
  * Arguments as ar_bank_append and ar_route_fwd; the site's checks run before
  * anything is appended, so on an argument error the bank is unchanged.
  * Errors: those of ar_bank_append and ar_route_fwd.
