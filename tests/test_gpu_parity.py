@@ -330,7 +330,9 @@ def test_repeatable_bits(W):
     (1280, 1280, 8, "bf16", "in_place", False),   # kept apart (measured slower fused)
     (512, 512, 4, "bf16", "in_place", True),      # two tokens per warp
     (512, 512, 2, "f32", "in_place", True),
-    (1536, 384, 1, "bf16", "in_place", False),    # sliced keys
+    (1536, 384, 1, "bf16", "in_place", False),    # sliced keys: kept apart
+    (1536, 384, 1, "bf16", "acc", False),
+    (4096, 512, 8, "bf16", "acc", False),
     (1024, 1024, 8, "bf16", "acc", False),        # one-warp kernels: row in place only
     (4096, 4096, 8, "bf16", "in_place", True),    # four-warp kernels
     (4096, 1024, 8, "bf16", "acc", True),         # block partial sum formed in the forward
