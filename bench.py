@@ -81,12 +81,21 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank lines (comment edits keep the hash)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_hash(family: str = "full") -> str:
+    """Hash of the code (not the comments) of a kernel family's sources."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "depth_wise_attention_ar_gb300", "csrc")
     for name in KERNEL_SOURCES[family]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
