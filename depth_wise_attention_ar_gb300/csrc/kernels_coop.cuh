@@ -17,6 +17,14 @@
 //   backward also publishes dz per head, and the key-path terms on the tail
 //   are staged in the shared gradient row before the owning lanes write it.
 // Score bits match between the passes (same lanes, same order, dot8 sums).
+//
+// The forward takes one block barrier per item and can take the site's append
+// (FRESH): the new row's item stages the row it is formed from, each warp
+// forms its columns (a copy, or a block partial sum rounded once) into the
+// stage and the row's slot, and the item's barrier publishes the squares for
+// the new row's inverse RMS. In the delta form, and for a fused partial sum,
+// a per-token row (the residual stream, or the sublayer output to add) is
+// staged by a bulk copy at the token's first item.
 #pragma once
 
 #include "common.cuh"
