@@ -33,6 +33,11 @@
 // of the sliced-key backward, so both compute the same score bits; the value
 // chunks are read after the weight is known, so only the accumulator and q*g
 // stay in registers.
+//
+// FRESH (full keys, rows up to 1024 wide): the site's append is fused in. The
+// new row already sits in its slot; at its item the kernel squares the staged
+// values it holds, sums them over the token's lanes, and caches the inverse
+// RMS before scoring the row (one launch per site instead of two).
 #pragma once
 
 #include "common.cuh"
