@@ -48,19 +48,36 @@ namespace ar {
 constexpr int kFwdWarps = 4;
 constexpr int kFwdStages = 4;
 
-inline size_t fwd_smem_bytes(int d, size_t esize)
+// Sliced keys on rows of 2048 columns or more: three stages per warp, so that
+// three blocks fit in shared memory (more warps for the same token count).
+__host__ __device__ constexpr int fwd_stages(bool sk, int cpl)
 {
-    return (size_t)kFwdWarps * kFwdStages * d * esize + (size_t)kFwdWarps * kFwdStages * 8 +
+    return sk && cpl >= 8 ? 3 : kFwdStages;
+}
+
+// Resident blocks the sliced-key bf16 instantiations are compiled for: the
+// accumulator (8 CPL floats) and q*g of the key chunks (8 KM floats) set the
+// register need; four blocks where that stays within 128 registers without
+// spilling, else three, and two for the widest key slices. (fp32 rows fill
+// shared memory first: no bound.)
+constexpr int fwd_min_blocks(bool sk_bf16, int cpl, int km)
+{
+    return !sk_bf16 ? 1 : (cpl + km <= 8 ? 4 : (cpl + km <= 13 ? 3 : 2));
+}
+
+inline size_t fwd_smem_bytes(int d, size_t esize, int stages = kFwdStages)
+{
+    return (size_t)kFwdWarps * stages * d * esize + (size_t)kFwdWarps * stages * 8 +
            (size_t)kFwdWarps * AR_MAX_SOURCES * 4;
 }
 
-template <typename T, int CPL, bool SK, bool FRESH = false>
-__global__ void __launch_bounds__(kFwdWarps * 32)
-    route_fwd_kernel(const __grid_constant__ RouteArgs a)
+template <typename T, int CPL, bool SK, bool FRESH, int KM>
+__device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
 {
+    static_assert(SK || KM == CPL, "full keys: a lane's key chunks are its value chunks");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
-    constexpr int S = kFwdStages;
+    constexpr int S = fwd_stages(SK, CPL);
     constexpr int CB = ChunkBytes<T>::value;
     constexpr unsigned FULL = 0xffffffffu;
 
@@ -90,19 +107,19 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
 #pragma unroll
     for (int j = 0; j < CPL; ++j) cidx[j] = chunk_of<CPL>(h, sub, LPH, j);
     // key chunks: the value chunks themselves for full keys; for sliced keys
-    // chunks of key slice h (at most CPL of them per lane since r <= d)
+    // chunks of key slice h (ceil(r / 256) <= KM of them per lane)
     const int key0 = SK ? (d - a.r) / 8 : 0, ckh = SK ? a.r / 8 / H : 0;
-    int kidx[CPL];
-    bool kval[CPL];
+    int kidx[KM];
+    bool kval[KM];
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
+    for (int j = 0; j < KM; ++j) {
         kval[j] = !SK || sub + LPH * j < ckh;
         kidx[j] = SK ? key0 + h * ckh + sub + LPH * j : cidx[j];
     }
     // query times norm weight over this lane's key coordinates
-    float qg[CPL][8];
+    float qg[KM][8];
 #pragma unroll
-    for (int j = 0; j < CPL; ++j)
+    for (int j = 0; j < KM; ++j)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = kidx[j] * 8 + e - key0 * 8;
@@ -172,7 +189,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
         float zr = 0.f;
         if constexpr (SK) {
 #pragma unroll
-            for (int j = 0; j < CPL; ++j) {
+            for (int j = 0; j < KM; ++j) {
                 if (kval[j]) {
                     float kv[8];
                     ld_chunk_s(reinterpret_cast<const T *>(buf + kidx[j] * CB), kv);
@@ -264,6 +281,23 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
             if (++slot == S) slot = 0;
         }
     }
+}
+
+// Full keys: the register count is left to the compiler (one block per SM
+// minimum), which keeps three blocks resident on 1280-column rows.
+template <typename T, int CPL, bool FRESH = false>
+__global__ void __launch_bounds__(kFwdWarps * 32)
+    route_fwd_kernel(const __grid_constant__ RouteArgs a)
+{
+    route_fwd_body<T, CPL, false, FRESH, CPL>(a);
+}
+
+// Sliced keys: compiled for fwd_min_blocks resident blocks.
+template <typename T, int CPL, int KM>
+__global__ void __launch_bounds__(kFwdWarps * 32, fwd_min_blocks(sizeof(T) == 2, CPL, KM))
+    route_fwd_sk_kernel(const __grid_constant__ RouteArgs a)
+{
+    route_fwd_body<T, CPL, true, false, KM>(a);
 }
 
 // Two tokens per warp, full keys, rows of 256 or 512 columns, H <= 4.
@@ -497,15 +531,22 @@ cudaError_t launch_fwd_pair(const RouteArgs &a, cudaStream_t s)
     return a.fresh1 ? launch_fwd_pair_inst<T, CPL, true>(a, s) : launch_fwd_pair_inst<T, CPL, false>(a, s);
 }
 
-template <typename T, int CPL, bool SK, bool FRESH>
+template <typename T, int CPL, bool SK, bool FRESH, int KM = CPL>
 cudaError_t launch_fwd_inst2(const RouteArgs &a, cudaStream_t s)
 {
-    const void *k = reinterpret_cast<const void *>(&route_fwd_kernel<T, CPL, SK, FRESH>);
-    const size_t smem = fwd_smem_bytes(a.d, sizeof(T));
+    const void *k;
+    if constexpr (SK)
+        k = reinterpret_cast<const void *>(&route_fwd_sk_kernel<T, CPL, KM>);
+    else
+        k = reinterpret_cast<const void *>(&route_fwd_kernel<T, CPL, FRESH>);
+    const size_t smem = fwd_smem_bytes(a.d, sizeof(T), fwd_stages(SK, CPL));
     int grid = 0;
     cudaError_t e = persistent_grid(k, kFwdWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
-    route_fwd_kernel<T, CPL, SK, FRESH><<<grid, kFwdWarps * 32, smem, s>>>(a);
+    if constexpr (SK)
+        route_fwd_sk_kernel<T, CPL, KM><<<grid, kFwdWarps * 32, smem, s>>>(a);
+    else
+        route_fwd_kernel<T, CPL, FRESH><<<grid, kFwdWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -515,10 +556,21 @@ cudaError_t launch_fwd_inst2(const RouteArgs &a, cudaStream_t s)
 template <typename T, int CPL, bool SK>
 cudaError_t launch_fwd_inst(const RouteArgs &a, cudaStream_t s)
 {
-    if constexpr (!SK && CPL <= 4) {
-        if (a.fresh1) return launch_fwd_inst2<T, CPL, SK, true>(a, s);
+    if constexpr (SK) {
+        // key chunks per lane: ceil(r / 256), held in the smallest of a
+        // quarter, a half or all of the lane's CPL value-chunk slots that fits
+        // (q*g of unused slots would otherwise occupy registers)
+        constexpr int kQuarter = (CPL + 3) / 4, kHalf = (CPL + 1) / 2;
+        const int km = (a.r + 255) / 256;
+        if (km <= kQuarter) return launch_fwd_inst2<T, CPL, true, false, kQuarter>(a, s);
+        if (km <= kHalf) return launch_fwd_inst2<T, CPL, true, false, kHalf>(a, s);
+        return launch_fwd_inst2<T, CPL, true, false, CPL>(a, s);
+    } else {
+        if constexpr (CPL <= 4) {
+            if (a.fresh1) return launch_fwd_inst2<T, CPL, false, true>(a, s);
+        }
+        return launch_fwd_inst2<T, CPL, false, false>(a, s);
     }
-    return launch_fwd_inst2<T, CPL, SK, false>(a, s);
 }
 
 // Full-width keys with d = 256 * CPL, CPL in 1..8 (rows of 256 or 512

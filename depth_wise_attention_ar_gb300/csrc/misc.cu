@@ -348,25 +348,29 @@ cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const 
 //
 // One cluster of kRedCtas CTAs per tile of 32 * V columns (V = 4: float4
 // columns when r is a multiple of 4). The cluster's 8 x 16 warps take the
-// rows round-robin, each with four independent running sums so that several
-// loads are in flight; a CTA adds its warps' sums in warp order in shared
+// rows round-robin, each with eight running sums: a warp's rows (about ten
+// for a persistent backward grid) arrive in two rounds of eight loads in
+// flight. A CTA adds its warps' sums in warp order in shared
 // memory, and CTA 0 adds the CTAs' sums in rank order through distributed
 // shared memory. Every sum has a fixed order, so repeated runs give identical
 // bits.
 constexpr int kRedCtas = 8;
 constexpr int kRedWarps = 16;
 
+constexpr int kRedSums = 8;   // running sums (and loads in flight) per lane
+static_assert(kRedSums == 8, "the sums are combined as a fixed tree of eight");
+
 template <int V>
-__device__ __forceinline__ void red_load_add(const float *p, float (&s)[V])
+__device__ __forceinline__ void red_load(const float *p, float (&x)[V])
 {
     if constexpr (V == 4) {
-        const float4 x = __ldcg(reinterpret_cast<const float4 *>(p));
-        s[0] += x.x;
-        s[1] += x.y;
-        s[2] += x.z;
-        s[3] += x.w;
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p));
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
     } else {
-        s[0] += __ldcg(p);
+        x[0] = __ldcg(p);
     }
 }
 
@@ -385,21 +389,33 @@ __global__ void __cluster_dims__(kRedCtas, 1, 1) __launch_bounds__(kRedWarps * 3
     const bool valid = c0 < r;
     constexpr int stride = kRedCtas * kRedWarps;
 
-    float s[4][V];
+    float s[kRedSums][V];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kRedSums; ++u)
 #pragma unroll
         for (int e = 0; e < V; ++e) s[u][e] = 0.f;
     if (valid) {
-        int w = rank * kRedWarps + warp;
-        for (; w + 3 * stride < rows; w += 4 * stride) {
+        // rounds of kRedSums rows (w + u * stride, u = 0 .. kRedSums - 1), all
+        // loads of a round issued before the first add; rows past the end
+        // add zero
+        for (int w = rank * kRedWarps + warp; w < rows; w += kRedSums * stride) {
+            float x[kRedSums][V];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) red_load_add<V>(ws + (int64_t)(w + u * stride) * r + c0, s[u]);
+            for (int u = 0; u < kRedSums; ++u) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) x[u][e] = 0.f;
+                if (w + u * stride < rows) red_load<V>(ws + (int64_t)(w + u * stride) * r + c0, x[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kRedSums; ++u)
+#pragma unroll
+                for (int e = 0; e < V; ++e) s[u][e] += x[u][e];
         }
-        for (; w < rows; w += stride) red_load_add<V>(ws + (int64_t)w * r + c0, s[0]);
     }
 #pragma unroll
-    for (int e = 0; e < V; ++e) part[warp][lane * V + e] = (s[0][e] + s[1][e]) + (s[2][e] + s[3][e]);
+    for (int e = 0; e < V; ++e)
+        part[warp][lane * V + e] = ((s[0][e] + s[1][e]) + (s[2][e] + s[3][e])) +
+                                   ((s[4][e] + s[5][e]) + (s[6][e] + s[7][e]));
     __syncthreads();
     if (warp == 0) {
 #pragma unroll
