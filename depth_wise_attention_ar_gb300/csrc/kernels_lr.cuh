@@ -232,14 +232,14 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
     }
 }
 
-inline size_t lr_bwd_smem_bytes(int d, size_t esize)
+inline size_t lr_bwd_smem_bytes(int d, size_t esize, bool g_in_registers)
 {
     return (size_t)kLrBwdStages * ((size_t)d * esize + (size_t)d * 4)  // ring
-           + (size_t)d * esize                                          // G of the token
+           + (g_in_registers ? 0 : (size_t)d * esize)                   // G of the token
            + (size_t)kLrBwdStages * 8 + (size_t)AR_MAX_SOURCES * 4;
 }
 
-template <typename T, int KMAX>
+template <typename T, int KMAX, int CPLT = 0>
 __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant__ RouteArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -257,7 +257,8 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
     if (lane < AR_MAX_SOURCES / 32) s_first[lane] = a.first_mask[lane];
     unsigned char *ring = smem;
     T *Gs = reinterpret_cast<T *>(ring + (size_t)S * slot_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<unsigned char *>(Gs) + vbytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<unsigned char *>(Gs) +
+                                                  (CPLT > 0 ? 0u : vbytes));
     float *cur_inv = reinterpret_cast<float *>(bars + S);
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -267,8 +268,20 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 
     const int LPH = 32 / H;
     const int h = lane / LPH, sub = lane - h * LPH;
-    const int cpl = d / 256;                        // value chunks per lane
+    const int cpl = CPLT > 0 ? CPLT : d / 256;      // value chunks per lane
     const int key0 = (d - r) / 8;                   // first key chunk
+    // With the chunk count a template constant (CPLT > 0) the chunk loops
+    // unroll and the token's G stays in registers (Gr) instead of shared
+    // memory; the arithmetic and its order are the same either way.
+    float Gr[CPLT > 0 ? CPLT : 1][8];
+    auto for_chunks = [&](auto &&f) {
+        if constexpr (CPLT > 0) {
+#pragma unroll
+            for (int j = 0; j < CPLT; ++j) f(j);
+        } else {
+            for (int j = 0; j < cpl; ++j) f(j);
+        }
+    };
     const int ckh = r / 8 / H;                      // key chunks per head
     int kidx[KMAX];
     bool kval[KMAX];
@@ -326,28 +339,34 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
             const T *grow = static_cast<const T *>(a.dout) + tok * d;
             const T *orow = static_cast<const T *>(a.fout) + tok * d;
             float sp = 0.f;
-            for (int j = 0; j < cpl; ++j) {
+            for_chunks([&](int j) {
                 const int c = vbase + LPH * j;
                 const uint4 graw = __ldg(reinterpret_cast<const uint4 *>(
                     reinterpret_cast<const unsigned char *>(grow) + (size_t)c * ChunkBytes<T>::value));
                 float gv[8], o[8];
                 if constexpr (sizeof(T) == 2) {
-                    *reinterpret_cast<uint4 *>(Gs + c * 8) = graw;
+                    if constexpr (CPLT == 0) *reinterpret_cast<uint4 *>(Gs + c * 8) = graw;
                     unpack_bf16x8(graw, gv);
                 } else {
                     const uint4 g2 = __ldg(reinterpret_cast<const uint4 *>(
                         reinterpret_cast<const unsigned char *>(grow) + (size_t)c * 32 + 16));
-                    reinterpret_cast<uint4 *>(Gs + c * 8)[0] = graw;
-                    reinterpret_cast<uint4 *>(Gs + c * 8)[1] = g2;
+                    if constexpr (CPLT == 0) {
+                        reinterpret_cast<uint4 *>(Gs + c * 8)[0] = graw;
+                        reinterpret_cast<uint4 *>(Gs + c * 8)[1] = g2;
+                    }
                     gv[0] = __uint_as_float(graw.x); gv[1] = __uint_as_float(graw.y);
                     gv[2] = __uint_as_float(graw.z); gv[3] = __uint_as_float(graw.w);
                     gv[4] = __uint_as_float(g2.x); gv[5] = __uint_as_float(g2.y);
                     gv[6] = __uint_as_float(g2.z); gv[7] = __uint_as_float(g2.w);
                 }
+                if constexpr (CPLT > 0) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) Gr[j][e] = gv[e];
+                }
                 ld_chunk_g(orow + c * 8, o);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) sp = fmaf(gv[e], o[e], sp);
-            }
+            });
             // each token's <dL/dh, routed> counted by the warp owning (t, 0)
             if (a.dalpha && n == 0) dal += warp_sum(sp);
             S_h = alpha * group_sum(sp, LPH);
@@ -366,14 +385,20 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 
         // pass A: value dot and raw score
         float P = 0.f, zr = 0.f;
-        for (int j = 0; j < cpl; ++j) {
+        for_chunks([&](int j) {
             const int c = vbase + LPH * j;
-            float v[8], gv[8];
+            float v[8];
             ld_chunk_s(V + c * 8, v);
-            ld_chunk_s(Gs + c * 8, gv);
+            if constexpr (CPLT > 0) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) P = fmaf(gv[e], v[e], P);
-        }
+                for (int e = 0; e < 8; ++e) P = fmaf(Gr[j][e], v[e], P);
+            } else {
+                float gv[8];
+                ld_chunk_s(Gs + c * 8, gv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) P = fmaf(gv[e], v[e], P);
+            }
+        });
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             if (kval[j]) {
@@ -416,7 +441,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
         // pass C: w G everywhere (+ radial term off the slice for the full norm)
         float *grad_row = a.grad + ((int64_t)s_rows[n] * TT + tok) * d;
         const float cv = a.norm_full ? coef : 0.f;
-        for (int j = 0; j < cpl; ++j) {
+        for_chunks([&](int j) {
             const int c = vbase + LPH * j;
             const bool tail = c >= key0;
             float nv[8], gv[8];
@@ -426,7 +451,12 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 #pragma unroll
                 for (int e = 0; e < 8; ++e) nv[e] = 0.f;
             }
-            ld_chunk_s(Gs + c * 8, gv);
+            if constexpr (CPLT > 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gv[e] = Gr[j][e];
+            } else {
+                ld_chunk_s(Gs + c * 8, gv);
+            }
             if (!tail && cv != 0.f) {
                 float v[8];
                 ld_chunk_s(V + c * 8, v);
@@ -436,7 +466,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 8; ++e) nv[e] = fmaf(wa, gv[e], nv[e]);
             st_grad8(grad_row + c * 8, 0, nv, a.grad_v8);
-        }
+        });
         __syncwarp();
         if (issued < hi) issue_next();
         if (++n == N) { n = 0; ++tok; }
@@ -471,11 +501,11 @@ cudaError_t launch_lr_fwd_inst(const RouteArgs &a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-template <typename T, int KMAX>
+template <typename T, int KMAX, int CPLT = 0>
 cudaError_t lr_bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_warps)
 {
-    const void *k = reinterpret_cast<const void *>(&route_bwd_lr_kernel<T, KMAX>);
-    const size_t smem = lr_bwd_smem_bytes(a->d, sizeof(T));
+    const void *k = reinterpret_cast<const void *>(&route_bwd_lr_kernel<T, KMAX, CPLT>);
+    const size_t smem = lr_bwd_smem_bytes(a->d, sizeof(T), CPLT > 0);
     int grid = 0;
     cudaError_t e = persistent_grid(k, 32, smem, &grid);
     if (e != cudaSuccess) return e;
@@ -483,7 +513,7 @@ cudaError_t lr_bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_warps)
         *grid_warps = grid;
         return cudaSuccess;
     }
-    route_bwd_lr_kernel<T, KMAX><<<grid, 32, smem, s>>>(*a);
+    route_bwd_lr_kernel<T, KMAX, CPLT><<<grid, 32, smem, s>>>(*a);
     return cudaGetLastError();
 }
 
@@ -502,9 +532,46 @@ cudaError_t dispatch_lr_fwd(const RouteArgs &a, cudaStream_t s)
     return cudaErrorNotSupported;
 }
 
+// Rows up to 2560 wide: the chunk count d / 256 as a template constant, with
+// the key chunks per lane held in the smallest of a quarter, a half or all of
+// it that fits ceil(r / 256). Instantiated in its own translation units.
+template <typename T, int CPL>
+cudaError_t lr_bwd_fixed(const RouteArgs *a, cudaStream_t s, int *grid_warps)
+{
+    constexpr int kQuarter = (CPL + 3) / 4, kHalf = (CPL + 1) / 2;
+    const int km = lr_kmax(a->r);
+    if (km <= kQuarter) return lr_bwd_inst<T, kQuarter, CPL>(a, s, grid_warps);
+    if (km <= kHalf) return lr_bwd_inst<T, kHalf, CPL>(a, s, grid_warps);
+    // key tails over half of rows 2304 or 2560 wide: G and the key chunks
+    // together would spill, so the chunk loop stays a runtime loop there
+    if constexpr (CPL >= 9)
+        return lr_bwd_inst<T, 10, 0>(a, s, grid_warps);
+    else
+        return lr_bwd_inst<T, CPL, CPL>(a, s, grid_warps);
+}
+
+template <typename T>
+cudaError_t dispatch_lr_bwd_fixed(const RouteArgs *a, cudaStream_t s, int *grid_warps)
+{
+    switch (a->d / 256) {
+    case 1: return lr_bwd_fixed<T, 1>(a, s, grid_warps);
+    case 2: return lr_bwd_fixed<T, 2>(a, s, grid_warps);
+    case 3: return lr_bwd_fixed<T, 3>(a, s, grid_warps);
+    case 4: return lr_bwd_fixed<T, 4>(a, s, grid_warps);
+    case 5: return lr_bwd_fixed<T, 5>(a, s, grid_warps);
+    case 6: return lr_bwd_fixed<T, 6>(a, s, grid_warps);
+    case 7: return lr_bwd_fixed<T, 7>(a, s, grid_warps);
+    case 8: return lr_bwd_fixed<T, 8>(a, s, grid_warps);
+    case 9: return lr_bwd_fixed<T, 9>(a, s, grid_warps);
+    case 10: return lr_bwd_fixed<T, 10>(a, s, grid_warps);
+    default: return cudaErrorNotSupported;
+    }
+}
+
 template <typename T>
 cudaError_t dispatch_lr_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps)
 {
+    if (a->d / 256 <= 10) return dispatch_lr_bwd_fixed<T>(a, s, grid_warps);
     const int km = lr_kmax(a->r);
 #define AR_CASE(K) if (km <= K) return lr_bwd_inst<T, K>(a, s, grid_warps);
     AR_LR_KMAX_CASES(AR_CASE)
