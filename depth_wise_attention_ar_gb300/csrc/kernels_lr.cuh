@@ -333,6 +333,34 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
     int n = (int)(lo - tok * N), slot = 0;
     uint32_t phase = 0;
     bool ok = true;
+
+    // bf16 rows of up to 2048 columns with a constant chunk count: the next
+    // token's G and forward output chunks, lse and (first 32 sources) inverse
+    // RMS are loaded into registers while this token's items run, so a token
+    // start does not wait on DRAM. (GB300, 49 sites, T = 4096: backward
+    // 3.24 -> 3.18 ms at d = 1536; at d = 2560 the longer items hide the wait
+    // already and the extra registers cost 9.41 -> 9.53 ms, so not there;
+    // nor with key tails over half the row, where the registers would spill.)
+    constexpr bool kPre = CPLT > 0 && CPLT <= 8 && 2 * KMAX <= CPLT + 1 && sizeof(T) == 2;
+    uint4 preG[kPre ? CPLT : 1], preO[kPre ? CPLT : 1];
+    float pre_lse = 0.f, pre_inv = 0.f;
+    const int64_t last_tok = hi > lo ? (hi - 1) / N : -1;
+    auto prefetch_tok = [&](int64_t t) {
+        if constexpr (kPre) {
+            const uint4 *g4 = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dout) + t * d);
+            const uint4 *o4 = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.fout) + t * d);
+#pragma unroll
+            for (int j = 0; j < CPLT; ++j) {
+                const int c = vbase + LPH * j;
+                preG[j] = __ldg(g4 + c);
+                preO[j] = __ldg(o4 + c);
+            }
+            pre_lse = __ldg(a.lse + t * H + h);
+            if (lane < N) pre_inv = __ldg(a.inv + t * a.inv_ld + s_rows[lane]);
+        }
+    };
+    if (tok <= last_tok) prefetch_tok(tok);
+
     for (; i < hi; ++i) {
         if (i == lo || n == 0) {
             __syncwarp();
@@ -341,38 +369,51 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
             float sp = 0.f;
             for_chunks([&](int j) {
                 const int c = vbase + LPH * j;
-                const uint4 graw = __ldg(reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const unsigned char *>(grow) + (size_t)c * ChunkBytes<T>::value));
                 float gv[8], o[8];
-                if constexpr (sizeof(T) == 2) {
-                    if constexpr (CPLT == 0) *reinterpret_cast<uint4 *>(Gs + c * 8) = graw;
-                    unpack_bf16x8(graw, gv);
+                if constexpr (kPre) {
+                    unpack_bf16x8(preG[j], gv);
+                    unpack_bf16x8(preO[j], o);
                 } else {
-                    const uint4 g2 = __ldg(reinterpret_cast<const uint4 *>(
-                        reinterpret_cast<const unsigned char *>(grow) + (size_t)c * 32 + 16));
-                    if constexpr (CPLT == 0) {
-                        reinterpret_cast<uint4 *>(Gs + c * 8)[0] = graw;
-                        reinterpret_cast<uint4 *>(Gs + c * 8)[1] = g2;
+                    const uint4 graw = __ldg(reinterpret_cast<const uint4 *>(
+                        reinterpret_cast<const unsigned char *>(grow) + (size_t)c * ChunkBytes<T>::value));
+                    if constexpr (sizeof(T) == 2) {
+                        if constexpr (CPLT == 0) *reinterpret_cast<uint4 *>(Gs + c * 8) = graw;
+                        unpack_bf16x8(graw, gv);
+                    } else {
+                        const uint4 g2 = __ldg(reinterpret_cast<const uint4 *>(
+                            reinterpret_cast<const unsigned char *>(grow) + (size_t)c * 32 + 16));
+                        if constexpr (CPLT == 0) {
+                            reinterpret_cast<uint4 *>(Gs + c * 8)[0] = graw;
+                            reinterpret_cast<uint4 *>(Gs + c * 8)[1] = g2;
+                        }
+                        gv[0] = __uint_as_float(graw.x); gv[1] = __uint_as_float(graw.y);
+                        gv[2] = __uint_as_float(graw.z); gv[3] = __uint_as_float(graw.w);
+                        gv[4] = __uint_as_float(g2.x); gv[5] = __uint_as_float(g2.y);
+                        gv[6] = __uint_as_float(g2.z); gv[7] = __uint_as_float(g2.w);
                     }
-                    gv[0] = __uint_as_float(graw.x); gv[1] = __uint_as_float(graw.y);
-                    gv[2] = __uint_as_float(graw.z); gv[3] = __uint_as_float(graw.w);
-                    gv[4] = __uint_as_float(g2.x); gv[5] = __uint_as_float(g2.y);
-                    gv[6] = __uint_as_float(g2.z); gv[7] = __uint_as_float(g2.w);
+                    ld_chunk_g(orow + c * 8, o);
                 }
                 if constexpr (CPLT > 0) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) Gr[j][e] = gv[e];
                 }
-                ld_chunk_g(orow + c * 8, o);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) sp = fmaf(gv[e], o[e], sp);
             });
             // each token's <dL/dh, routed> counted by the warp owning (t, 0)
             if (a.dalpha && n == 0) dal += warp_sum(sp);
             S_h = alpha * group_sum(sp, LPH);
-            lse_h = __ldg(a.lse + tok * H + h);
-            for (int nn = lane; nn < N; nn += 32)
-                cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+            if constexpr (kPre) {
+                lse_h = pre_lse;
+                if (lane < N) cur_inv[lane] = pre_inv;
+                for (int nn = lane + 32; nn < N; nn += 32)
+                    cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+                if (tok < last_tok) prefetch_tok(tok + 1);
+            } else {
+                lse_h = __ldg(a.lse + tok * H + h);
+                for (int nn = lane; nn < N; nn += 32)
+                    cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+            }
             __syncwarp();
         }
         const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
