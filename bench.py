@@ -78,6 +78,7 @@ def peaks():
 KERNEL_SOURCES = {
     "full": ("kernels_bwd.cuh", "common.cuh", "ar_internal.h", "launch_util.cuh", "shapes.h"),
     "coop": ("kernels_coop.cuh", "common.cuh", "ar_internal.h", "launch_util.cuh", "shapes.h"),
+    "lr": ("kernels_lr.cuh", "common.cuh", "ar_internal.h", "launch_util.cuh", "shapes.h"),
 }
 
 
