@@ -359,7 +359,10 @@ def main():
     n_bwd = len(mb.plan.run_sites)
     bwd_bytes = mbytes["bwd"]
     achieved = bwd_bytes / (bwd_ms * 1e-3) / 1e9
-    traffic = measured_traffic(args.config, H)
+    # the record holds the mean over every site of the full workload: another
+    # token count or site selection is a different launch mix
+    traffic = (measured_traffic(args.config, H)
+               if args.sites == "all" and not args.tokens else None)
     line = {
         "metric": METRIC,
         "value": world * cfg.T / (ms * 1e-3),
