@@ -7,6 +7,8 @@
   (oracle/torch_route.py), for every gradient the oracle's closed form gives
   (this also pins that restatement, which the model-chain tests use);
 * central finite differences of the oracle's own forward;
+* a second backward formulation (the per-head score form of the MHAR page's
+  Appendix E) against the oracle's source-gradient form;
 * the invariants the pages state (H=1 is single-head AttnRes, heads are
   independent slices, weights sum to one, one-hot read, zero query gives the
   mean, one source is the identity, permutation, scale invariance, gradient
@@ -93,6 +95,47 @@ def test_backward_matches_torch_autograd(orc, N, T, d, H, r, fw):
     assert _nmax(np.stack(dsrc), V.grad.numpy()) < 1e-11
     assert _nmax(dq, tq.grad.numpy()) < 1e-10
     assert _nmax(dg, tg.grad.numpy()) < 1e-10
+
+
+def _score_coupling_backward(V, q, g, G, H, r, eps, full_width):
+    """The backward in the per-head score form of "Multi-Head Attention
+    Residuals" Appendix E (Figure 10), written out in numpy: weights recomputed
+    from the log-sum-exp, the value dot products P[n,h] = <G_h, V_{n,h}> and their
+    weighted sum per head, the score gradient dz = w (P - S), then the value
+    path, the key path and the radial term of the key norm. The oracle instead
+    follows the source-gradient form of "Low-Rank Attention Residuals" Eq. 15 /
+    Eq. 21 / Eq. 22."""
+    N, T, d = V.shape
+    K, Kr = d // H, r // H
+    tail = V[..., d - r:]
+    width = d if full_width else r
+    inv = 1.0 / np.sqrt(((V * V).mean(-1) if full_width else (tail * tail).mean(-1)) + eps)
+    qg = q * g
+    zr = np.einsum("he,nthe->nth", qg.reshape(H, Kr), tail.reshape(N, T, H, Kr))
+    z = inv[..., None] * zr
+    w = np.exp(z - sps.logsumexp(z, axis=0)[None])
+    P = np.einsum("the,nthe->nth", G.reshape(T, H, K), V.reshape(N, T, H, K))
+    dz = w * (P - (w * P).sum(0)[None])
+    dV = np.repeat(w, K, axis=2) * G[None]                       # value path
+    kz = inv[..., None] * dz
+    dV[..., d - r:] += np.repeat(kz, Kr, axis=2) * qg[None, None]  # key path
+    radial = (inv ** 3 / width * (dz * zr).sum(-1))[..., None]   # norm of the key
+    if full_width:
+        dV -= radial * V
+    else:
+        dV[..., d - r:] -= radial * tail
+    U = np.einsum("nth,nthe->he", kz, tail.reshape(N, T, H, Kr)).reshape(r)
+    return dV, g * U, q * U
+
+
+@pytest.mark.parametrize("N,T,d,H,r,fw", SHAPES)
+def test_backward_matches_score_coupling_form(orc, N, T, d, H, r, fw):
+    srcs, q, g, G = _case(14, N, T, d, H, r)
+    dsrc, dq, dg = orc.route_bwd(srcs, q, g, G, H, r=r, eps=1e-6, full_width=fw)
+    dV, dq2, dg2 = _score_coupling_backward(np.stack(srcs), q, g, G, H, r, 1e-6, fw)
+    assert _nmax(np.stack(dsrc), dV) < 1e-11
+    assert _nmax(dq, dq2) < 1e-10
+    assert _nmax(dg, dg2) < 1e-10
 
 
 @pytest.mark.parametrize("fw,r", [(False, 16), (False, 32), (True, 16)])
