@@ -593,21 +593,22 @@ ar_status ar_block_schedule(int32_t M, int32_t NB, int32_t *acc_from, int32_t *s
     const int64_t nb = (NB <= 0 || NB >= M) ? M : NB;
     std::vector<uint8_t> is_end(static_cast<size_t>(M) + 1, 0);
     for (int64_t j = 1; j <= nb; ++j) is_end[(M * j + nb - 1) / nb] = 1;  // ceil(M j / NB)
-    std::vector<int32_t> blocks{0};
-    int32_t partial = -1;
+    // Row t holds its block's running sum up to sublayer t: a copy of o_t when
+    // t opens a block (t = 1, or t - 1 closed one), else row t - 1 plus o_t.
+    // The read after sublayer t lists row 0, the last row of every block
+    // closed before t, and row t.
+    std::vector<int32_t> closed;  // last rows of the blocks closed so far
     std::vector<int32_t> flat{0};
     std::vector<int32_t> ptr{0, 1};
     acc_from[0] = -1;
     for (int32_t t = 1; t <= M; ++t) {
-        acc_from[t] = partial;  // -1 at a block start
-        partial = t;
-        if (is_end[t]) {
-            blocks.push_back(partial);
-            partial = -1;
-        }
-        flat.insert(flat.end(), blocks.begin(), blocks.end());
-        if (partial >= 0) flat.push_back(partial);
+        const bool opens = t == 1 || is_end[t - 1];
+        acc_from[t] = opens ? -1 : t - 1;
+        flat.push_back(0);
+        flat.insert(flat.end(), closed.begin(), closed.end());
+        flat.push_back(t);
         ptr.push_back(static_cast<int32_t>(flat.size()));
+        if (is_end[t]) closed.push_back(t);
     }
     *site_rows_len = static_cast<int64_t>(flat.size());
     for (int32_t t = 0; t <= M + 1; ++t) site_ptr[t] = ptr[t];

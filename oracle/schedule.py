@@ -3,15 +3,15 @@
 Full routing ("Multi-Head Attention Residuals", Sec. 2.2 and Figure 3;
 "Low-Rank Attention Residuals", Eq. 4): the sources are the token embedding
 plus every sublayer output, N = 2L+1 in all; routing site i (1-based) reads
-the first i sources ("replacement routing": each sublayer appends its raw
-output as a new source).
+the first i sources, since each sublayer's output joins the bank unchanged.
 
-Block routing ("Low-Rank Attention Residuals", Eq. 5-6 and the Figure 11
-pseudocode): M = 2L sublayers are grouped into NB blocks whose last sublayers
-are ceil(M*j/NB), j = 1..NB. After sublayer t the running partial sum takes
-o_t; at a block end the partial sum becomes a completed block source and the
-partial accumulator empties. The read after sublayer t sees the embedding,
-the completed block sums and, if nonempty, the current partial sum.
+Block routing ("Low-Rank Attention Residuals", Eq. 5-6 and Figure 11): the
+M = 2L sublayers fall into NB consecutive blocks, block k ending at sublayer
+ceil(M*(k+1)/NB). A block's source is the sum of its sublayers' outputs. The
+read after sublayer t, which lies in block k, sees the embedding and the sums
+of blocks 0..k, block k's sum taken only up to sublayer t (the partial sum;
+when t ends the block it is the whole block sum). So the source list grows
+by one entry at each block start and otherwise has its last entry replaced.
 
 Bank layout used by both sides of the parity checks: row 0 holds the
 embedding; in full routing row j holds sublayer output j; in block routing
@@ -21,6 +21,8 @@ forward read (a completed block is the last version of its block).
 """
 
 from __future__ import annotations
+
+import bisect
 
 __all__ = ["full_sites", "block_ends", "block_plan"]
 
@@ -54,16 +56,13 @@ def block_plan(M: int, NB: int | None = None) -> dict:
                     ``sites[t]`` = completed block rows + [current partial row]
                     for the read after sublayer t.
     """
-    ends = set(block_ends(M, NB))
-    blocks = [0]
-    partial = None
+    ends = block_ends(M, NB)
     row_ops: list[tuple] = [("emb",)]
     sites = [[0]]
     for t in range(1, M + 1):
-        row_ops.append(("copy", t) if partial is None else ("acc", partial, t))
-        partial = t
-        if t in ends:
-            blocks.append(partial)
-            partial = None
-        sites.append(blocks + ([] if partial is None else [partial]))
-    return {"ends": sorted(ends), "row_ops": row_ops, "sites": sites}
+        k = bisect.bisect_left(ends, t)            # the block holding sublayer t
+        start = ends[k - 1] + 1 if k else 1        # its first sublayer
+        row_ops.append(("copy", t) if t == start else ("acc", t - 1, t))
+        # blocks before k end at ends[:k]; row t is block k's sum up to t
+        sites.append([0] + ends[:k] + [t])
+    return {"ends": ends, "row_ops": row_ops, "sites": sites}

@@ -44,17 +44,19 @@ def chain(x, sublayers, queries, norm_weights, H: int, r: int | None = None, NB:
     (full routing, MHAR Figure 3). ``queries``/``norm_weights`` hold one entry
     per read (len(sublayers) + 1, the first for the read that feeds sublayer
     1). Returns the final read."""
+    import bisect
+
     from .schedule import block_ends
-    M = len(sublayers)
-    ends = set(block_ends(M, NB))
-    blocks, partial = [x], None
+    ends = block_ends(len(sublayers), NB)
+    sums = []    # sums[k]: block k's outputs added up so far
     h = route([x], queries[0], norm_weights[0], H, r, eps, full_width)
     for t, f in enumerate(sublayers, start=1):
-        y = f(h)
-        partial = y if partial is None else partial + y
-        if t in ends:
-            blocks.append(partial)
-            partial = None
-        srcs = blocks + ([] if partial is None else [partial])
-        h = route(srcs, queries[t], norm_weights[t], H, r, eps, full_width)
+        k = bisect.bisect_left(ends, t)    # the block holding sublayer t
+        o = f(h)
+        if k == len(sums):
+            sums.append(o)                 # first sublayer of block k
+        else:
+            sums[k] = sums[k] + o
+        # the embedding, the finished blocks and block k up to sublayer t
+        h = route([x] + sums, queries[t], norm_weights[t], H, r, eps, full_width)
     return h
