@@ -294,8 +294,9 @@ __device__ __forceinline__ void st_f32x8_g(float *p, const float v[8]) { st_chun
 
 // Forward epilogue of one 8-element chunk of the routed mix o at element
 // offset off: out = o, or out = partial + alpha * o in the delta form
-// ("Multi-Head Attention Residuals", Appendix E, Figure 9: the kernel adds
-// the residual stream in delta modes); the plain mix also goes to routed when
+// ("Multi-Head Attention Residuals", Appendix E, Figure 9: in the delta form
+// the forward's epilogue sums the partial and the gated mix); the plain mix
+// also goes to routed when
 // asked for (the delta backward needs it).
 template <typename T>
 __device__ __forceinline__ void store_output(const RouteArgs &a, int64_t off, const float o[8])

@@ -271,8 +271,10 @@ cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cu
 // (out_A, lse_A) and (out_B, lse_B), the read over A u B is
 //   lse = m + log(e^(lse_A - m) + e^(lse_B - m)),  m = max(lse_A, lse_B)
 //   out = (e^(lse_A - lse) out_A + e^(lse_B - lse) out_B)   on each head's slice
-// ("Low-Rank Attention Residuals", Sec. 3.4: inter-block and intra-block
-// results merge with an online-softmax update). One warp per token.
+// ("Low-Rank Attention Residuals", Sec. 3.4: two-phase block inference
+// combines the read over the finished blocks with the read over the partial
+// sum by their log-sum-exp, as one step of an online softmax). One warp per
+// token.
 // VEC: 8-column chunks (d and d/H multiples of 8, aligned rows); otherwise
 // one column at a time, with the same arithmetic per element.
 template <typename T, bool VEC>

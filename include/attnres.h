@@ -104,10 +104,11 @@ const char *ar_status_string(ar_status s);
 ar_status ar_inv_rms_floats(int64_t T, int32_t capacity, int64_t *floats);
 
 /*
- * Create a bank: the shared source buffer of MHAR Appendix E ("Shared source
- * buffer": one [2L+1, B, T, d] buffer written once per source) plus the
- * per-row inverse-RMS cache and the shared fp32 gradient accumulator
- * (Appendix E, backward: "one shared fp32 buffer, in place").
+ * Create a bank: the single source store of MHAR Appendix E (every source row
+ * lives in one preallocated tensor with a slot per sublayer output plus the
+ * embedding, each slot filled once), the per-row inverse-RMS cache, and the
+ * fp32 gradient rows that every site's backward adds into (Appendix E,
+ * backward).
  *   T        : tokens (batch x sequence), T >= 0. T = 0 makes every compute
  *              call a no-op (the backward still zeroes dq/dg), and then every
  *              per-token pointer (rows, inv_rms, src, out, lse, dout, ws) may
@@ -142,9 +143,9 @@ ar_status ar_bank_row_count(const ar_bank *bank, int32_t *count);
 ar_status ar_bank_row_ptr(const ar_bank *bank, int32_t row, void **ptr);
 
 /*
- * Append one source row (MHAR Sec. 2.2: "each later source is the raw output
- * of one attention or MLP sublayer"; LR-AttnRes Eq. 5-6 and Figure 11 for
- * the block variant) and cache its per-token inverse RMS once, for reuse by
+ * Append one source row (MHAR Sec. 2.2: after the embedding, every attention
+ * and every MLP sublayer contributes its output, unnormalised, as one source;
+ * LR-AttnRes Eq. 5-6 and Figure 11 for the block variant) and cache its per-token inverse RMS once, for reuse by
  * every later site.
  *   src             : device [T, d] of the bank dtype. It may be the address
  *                     of the slot being filled (ar_bank_row_ptr), then
@@ -152,8 +153,9 @@ ar_status ar_bank_row_ptr(const ar_bank *bank, int32_t row, void **ptr);
  *   accumulate_from : -1 to store src as is; otherwise a row index p already
  *                     appended: the new row is rows[p] + src computed in fp32
  *                     and rounded once to the storage dtype (a new immutable
- *                     partial-sum version; "accumulation precedes slicing and
- *                     normalization", LR-AttnRes Sec. 3.3).
+ *                     partial-sum version; LR-AttnRes Sec. 3.3: the block
+ *                     sum is formed at full width before any key is sliced
+ *                     out of it or normalised).
  *   out_row         : receives the new row's index (may be NULL).
  * Errors: AR_ERR_CAPACITY (bank full), AR_ERR_INVALID_ARG (bad p, null src),
  * AR_ERR_ALIGN, AR_ERR_CUDA.
@@ -187,8 +189,8 @@ ar_status ar_bank_reset(ar_bank *bank);
 
 /*
  * Forward of one routing site: online softmax over the listed sources with
- * the RMSNorm key fused in (MHAR Appendix E, "Forward: online softmax over
- * depth with the norm fused in", Figure 9), each source row read once.
+ * the RMSNorm key computed in the same pass (MHAR Appendix E, forward kernel,
+ * Figure 9), each source row read once.
  *   rows, n_src : host int32 list of appended rows, 1..AR_MAX_SOURCES entries.
  *                 A row may be listed more than once: the softmax runs over
  *                 the list, so a row listed k times carries k times the
@@ -244,7 +246,8 @@ ar_status ar_route_fwd_append(ar_bank *bank, const void *src, int32_t accumulate
  * ("Multi-Head Attention Residuals", Sec. 3.3 "Identity-preserving
  * conversion": h = partial + alpha * routed with a zero-initialised gate, so
  * that alpha = 0 leaves the residual stream untouched; Appendix E, Figure 9:
- * the fused kernel adds the residual stream in delta modes).
+ * in the delta form the forward's epilogue sums the partial and the gated
+ * mix).
  *   partial : device [T, d] of the bank dtype, the intact residual stream
  *   alpha   : device float, the site's gate
  *   out     : device [T, d] of the bank dtype (may not alias partial)
@@ -297,10 +300,10 @@ ar_status ar_route_fwd_site(ar_bank *bank, const ar_site *site, const void *part
 ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes);
 
 /*
- * Backward of one routing site (MHAR Appendix E, "Backward: one kernel,
- * norms recomputed, gradients accumulated in place", Figure 10; the
- * value/routing split of LR-AttnRes Eq. 15 with the score gradient of
- * Eq. 21/22). Given dL/dout it emits dL/ds_n for every listed source into the
+ * Backward of one routing site (MHAR Appendix E, backward kernel: a single
+ * launch that recomputes the key norms and adds into the gradient rows,
+ * Figure 10; the value/routing split of LR-AttnRes Eq. 15 with the score
+ * gradient of Eq. 21/22). Given dL/dout it emits dL/ds_n for every listed source into the
  * bank's fp32 gradient rows — a store on a row's first touch since
  * ar_bank_zero_grad, an in-place accumulation afterwards — and dL/dq, dL/dg.
  *   rows, n_src, H, q, g : exactly as in the forward of this site

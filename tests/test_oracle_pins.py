@@ -171,7 +171,7 @@ def test_backward_finite_differences(orc, fw, r):
 
 
 def test_single_head_is_attention_residuals(orc):
-    """H=1 is Eq. 2 of the MHAR page: one softmax over depth read by all d coordinates."""
+    """H=1 is Eq. 2 of the MHAR page: a single weight per source, shared by every coordinate."""
     N, T, d = 5, 6, 16
     srcs, q, g, _ = _case(14, N, T, d, 1, d)
     out, lse = orc.route_fwd(srcs, q, g, 1)
@@ -185,7 +185,7 @@ def test_single_head_is_attention_residuals(orc):
 @pytest.mark.parametrize("d,H,r", [(16, 4, 16), (32, 2, 16), (24, 3, 12)])
 def test_heads_are_independent_single_head_reads(orc, d, H, r):
     """Head h of MHAR equals a single-head read whose query is zero outside key slice h
-    (Eq. 3: each head scores only its own slice and mixes only its own slice)."""
+    (Eq. 3: a head's logits come from its key slice alone, and its weights mix its value slice alone)."""
     N, T = 4, 5
     srcs, q, g, G = _case(15, N, T, d, H, r)
     out, lse = orc.route_fwd(srcs, q, g, H, r=r)
