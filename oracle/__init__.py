@@ -10,7 +10,7 @@ holds the source-schedule bookkeeping (``schedule.py``) and the storage
 rounding of accumulated block sums (``storage.py``).
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against brute
-force (an einsum restatement of the pages' pseudocode), torch autograd,
+force (the routing equations term by term in numpy), torch autograd,
 finite differences and the invariants the pages state.
 """
 

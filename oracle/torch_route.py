@@ -1,10 +1,10 @@
 """Plain PyTorch (float64, CPU) restatement of one routing site and of a whole
 routed model chain — test infrastructure only.
 
-``route`` restates the route pseudocode of "Multi-Head Attention Residuals"
-(Figure 3; Figure 7 at H = 1) and of "Low-Rank Attention Residuals"
-(Figure 11, sliced keys): stack the sources, normalise the keys, one logit per
-(source, head), softmax over depth, mix each head's value slice. Being plain
+``route`` restates one routing read of "Multi-Head Attention Residuals"
+(Eq. 3; Eq. 2 at H = 1) with the sliced keys of "Low-Rank Attention
+Residuals" (Eq. 11): normalised keys, one logit per (source, head), softmax
+over the sources, each head's weights on its own value slice. Being plain
 torch ops, it is differentiable by autograd, so a routed model chain built
 from it gives reference gradients for every parameter.
 
@@ -25,15 +25,14 @@ def route(sources, q, g, H: int, r: int | None = None, eps: float = 1e-6,
     V = torch.stack(list(sources))
     N, T, d = V.shape
     r = d if r is None else r
-    K = V[..., d - r:]
-    ms = (V * V).mean(-1, keepdim=True) if full_width else (K * K).mean(-1, keepdim=True)
-    khat = K * torch.rsqrt(ms + eps)
+    keys = V[..., d - r:]
+    sq = V * V if full_width else keys * keys
+    khat = keys * torch.rsqrt(sq.mean(-1, keepdim=True) + eps)
     if g is not None:
         khat = khat * g
-    logits = torch.einsum("he,nthe->nth", q.view(H, r // H), khat.view(N, T, H, r // H))
-    alpha = torch.softmax(logits, dim=0)
-    mixed = torch.einsum("nth,nthe->the", alpha, V.view(N, T, H, d // H))
-    return mixed.reshape(T, d)
+    logits = (khat * q).reshape(N, T, H, r // H).sum(-1)     # one per (source, head)
+    alpha = torch.softmax(logits, dim=0)                     # over the sources
+    return (alpha.repeat_interleave(d // H, dim=-1) * V).sum(0)
 
 
 def chain(x, sublayers, queries, norm_weights, H: int, r: int | None = None, NB: int | None = None,

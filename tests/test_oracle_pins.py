@@ -1,8 +1,8 @@
 """Pins for the CPU oracle, against things other than the oracle itself.
 
-* brute force: an einsum restatement of the pages' route pseudocode
-  ("Multi-Head Attention Residuals" Figure 3 / Figure 7, "Low-Rank Attention
-  Residuals" Figure 11), softmax/logsumexp from scipy;
+* brute force: Eq. 3 of "Multi-Head Attention Residuals" (Eq. 2 at H = 1;
+  the sliced keys of "Low-Rank Attention Residuals" Eq. 11) term by term in
+  numpy, softmax/logsumexp from scipy;
 * torch autograd (float64, CPU) on the torch restatement of the forward
   (oracle/torch_route.py), for every gradient the oracle's closed form gives
   (this also pins that restatement, which the model-chain tests use);
@@ -37,16 +37,22 @@ def _case(seed, N, T, d, H, r, qstd=0.7, gkind="random"):
     return srcs, q, g, G
 
 
-def _einsum_route(V, q, g, H, r, eps, full_width):
-    """Brute force: stack, normalise keys, per-head logits, softmax over depth, mix."""
+def _per_head_sum(Y, H):
+    """Sums of the last axis over each of its H equal contiguous slices."""
+    return Y.reshape(*Y.shape[:-1], H, Y.shape[-1] // H).sum(-1)
+
+
+def _brute_route(V, q, g, H, r, eps, full_width):
+    """Brute force: normalised keys, per-head logits, softmax over sources, and
+    each head's weights applied to its own value slice."""
     N, T, d = V.shape
-    K = V[..., d - r:]
-    ms = (V * V).mean(-1, keepdims=True) if full_width else (K * K).mean(-1, keepdims=True)
-    khat = K / np.sqrt(ms + eps) * g
-    logits = np.einsum("he,nthe->nth", q.reshape(H, r // H), khat.reshape(N, T, H, r // H))
+    keys = V[..., d - r:]
+    sq = V * V if full_width else keys * keys
+    khat = keys / np.sqrt(sq.mean(-1, keepdims=True) + eps) * g
+    logits = _per_head_sum(khat * q, H)                       # [N, T, H]
     alpha = sps.softmax(logits, axis=0)
-    mixed = np.einsum("nth,nthe->the", alpha, V.reshape(N, T, H, d // H))
-    return mixed.reshape(T, d), sps.logsumexp(logits, axis=0), alpha
+    mixed = (np.repeat(alpha, d // H, axis=-1) * V).sum(0)    # [T, d]
+    return mixed, sps.logsumexp(logits, axis=0), alpha
 
 
 def _torch_route(V, q, g, H, r, eps, full_width):
@@ -73,10 +79,10 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("N,T,d,H,r,fw", SHAPES)
-def test_forward_matches_einsum_brute_force(orc, N, T, d, H, r, fw):
+def test_forward_matches_brute_force(orc, N, T, d, H, r, fw):
     srcs, q, g, _ = _case(11, N, T, d, H, r)
     out, lse, alpha = orc.route_fwd(srcs, q, g, H, r=r, eps=1e-6, full_width=fw, want_alpha=True)
-    ref_out, ref_lse, ref_alpha = _einsum_route(np.stack(srcs), q, g, H, r, 1e-6, fw)
+    ref_out, ref_lse, ref_alpha = _brute_route(np.stack(srcs), q, g, H, r, 1e-6, fw)
     assert _nmax(out, ref_out) < 1e-12
     assert _nmax(lse, ref_lse) < 1e-12
     assert _nmax(alpha, ref_alpha.transpose(1, 0, 2)) < 1e-12
@@ -111,10 +117,10 @@ def _score_coupling_backward(V, q, g, G, H, r, eps, full_width):
     width = d if full_width else r
     inv = 1.0 / np.sqrt(((V * V).mean(-1) if full_width else (tail * tail).mean(-1)) + eps)
     qg = q * g
-    zr = np.einsum("he,nthe->nth", qg.reshape(H, Kr), tail.reshape(N, T, H, Kr))
+    zr = _per_head_sum(tail * qg, H)
     z = inv[..., None] * zr
     w = np.exp(z - sps.logsumexp(z, axis=0)[None])
-    P = np.einsum("the,nthe->nth", G.reshape(T, H, K), V.reshape(N, T, H, K))
+    P = _per_head_sum(V * G[None], H)
     dz = w * (P - (w * P).sum(0)[None])
     dV = np.repeat(w, K, axis=2) * G[None]                       # value path
     kz = inv[..., None] * dz
@@ -124,7 +130,7 @@ def _score_coupling_backward(V, q, g, G, H, r, eps, full_width):
         dV -= radial * V
     else:
         dV[..., d - r:] -= radial * tail
-    U = np.einsum("nth,nthe->he", kz, tail.reshape(N, T, H, Kr)).reshape(r)
+    U = (np.repeat(kz, Kr, axis=-1) * tail).sum((0, 1))
     return dV, g * U, q * U
 
 
@@ -177,9 +183,9 @@ def test_single_head_is_attention_residuals(orc):
     out, lse = orc.route_fwd(srcs, q, g, 1)
     V = np.stack(srcs)
     rms = np.sqrt((V * V).mean(-1) + 1e-6)                  # [N, T]
-    logits = np.einsum("d,ntd->nt", q * g, V) / rms         # q^T RMSNorm(s_i)
+    logits = (V * (q * g)).sum(-1) / rms                    # q^T RMSNorm(s_i)
     w = np.exp(logits - logits.max(0)) / np.exp(logits - logits.max(0)).sum(0)
-    assert _nmax(out, np.einsum("nt,ntd->td", w, V)) < 1e-13
+    assert _nmax(out, (w[..., None] * V).sum(0)) < 1e-13
 
 
 @pytest.mark.parametrize("d,H,r", [(16, 4, 16), (32, 2, 16), (24, 3, 12)])
@@ -218,7 +224,7 @@ def test_one_hot_read_when_query_scaled_up(orc):
     srcs, q, g, G = _case(17, N, T, d, H, d, gkind="ones")
     V = np.stack(srcs)
     rms = np.sqrt((V * V).mean(-1) + 1e-6)
-    z = np.einsum("he,nthe->nth", q.reshape(H, d // H), V.reshape(N, T, H, d // H)) / rms[..., None]
+    z = _per_head_sum(V * q, H) / rms[..., None]
     zs = np.sort(z, axis=0)
     gap = float(np.min(zs[-1] - zs[-2]))
     assert gap > 0
@@ -254,8 +260,7 @@ def test_single_source_is_identity(orc):
     ds, dq, dg = orc.route_bwd(srcs, q, g, G, H)
     assert np.array_equal(ds[0], G)
     assert np.all(dq == 0.0) and np.all(dg == 0.0)
-    z = orc.inv_rms(srcs[0])[:, None] * np.einsum("he,the->th", (q * g).reshape(H, 4),
-                                                 srcs[0].reshape(T, H, 4))
+    z = orc.inv_rms(srcs[0])[:, None] * _per_head_sum(srcs[0] * (q * g), H)
     assert _nmax(lse, z) < 1e-14
 
 
