@@ -58,6 +58,16 @@ def test_block_schedule_matches_oracle(B, M, NB):
     assert acc == exp_acc
 
 
+def test_block_schedule_matches_oracle_sweep(B):
+    from oracle import schedule
+    for M in range(1, 41):
+        for NB in list(range(1, M + 1)) + [None]:
+            acc, sites = B.ar_block_schedule(M, NB)
+            plan = schedule.block_plan(M, NB)
+            assert sites == plan["sites"], (M, NB)
+            assert acc == [-1 if op[0] in ("emb", "copy") else op[1] for op in plan["row_ops"]]
+
+
 def test_block_schedule_errors(B):
     with pytest.raises(B.ARError) as e:
         B.ar_block_schedule(0, 1)
