@@ -231,3 +231,24 @@ def test_route_fwd_append_checks_precede_launch(B):
         assert _err(fa, h, FAKE, -1, [0], 4, FAKE, None, FAKE, FAKE, 0, 0) == "AR_ERR_CUDA"
         assert B.ar_bank_row_count(h) == 0
     B.ar_bank_destroy(h)
+
+
+def test_binding_refuses_to_import_without_the_library(tmp_path):
+    """No fallback: the package's Python, copied without the compiled library,
+    raises on import of the binding and on any package name it provides."""
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "depth_wise_attention_ar_gb300")
+    dst = tmp_path / "depth_wise_attention_ar_gb300"
+    dst.mkdir()
+    for name in os.listdir(src):
+        if name.endswith(".py"):
+            shutil.copy(os.path.join(src, name), dst / name)
+    for stmt in ("import depth_wise_attention_ar_gb300.binding",
+                 "import depth_wise_attention_ar_gb300 as p; p.Bank"):
+        p = subprocess.run([sys.executable, "-c", stmt],
+                           cwd=tmp_path, capture_output=True, text=True,
+                           env={**os.environ, "PYTHONPATH": str(tmp_path)})
+        assert p.returncode != 0
+        assert "ImportError" in p.stderr and "is not built" in p.stderr
