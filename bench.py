@@ -161,8 +161,9 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(cfg, H, seconds: float, steps: int = 1):
-    """The oracle (float64 C, OpenMP over tokens) on a token sample of the workload."""
+def cpu_baseline(cfg, H, seconds: float, steps: int = 1, warmup: int = 0):
+    """The oracle (float64 C, OpenMP over tokens) on a token sample of the workload:
+    `warmup` untimed runs, then the mean of `steps` timed runs."""
     import numpy as np
 
     import oracle
@@ -194,6 +195,8 @@ def cpu_baseline(cfg, H, seconds: float, steps: int = 1):
     tp = one(probe)
     Ts = int(max(probe, min(cfg.T, probe * seconds / max(tp, 1e-6))))
     Ts = max(threads, (Ts // threads) * threads)
+    for _ in range(warmup):
+        one(Ts)
     times = [one(Ts) for _ in range(steps)]
     dt = sum(times) / len(times)
     return {"value": Ts / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -565,9 +568,10 @@ def reference_arm(args, rank, world):
     from depth_wise_attention_ar_gb300 import workload
     cfg = config_of(args, workload)
     H = args.heads or cfg.H
-    for _ in range(args.warmup):
-        pass
-    cb, dt, Ts = cpu_baseline(cfg, H, args.cpu_seconds, steps=max(1, args.steps))
+    # each of the W + K runs is one token sample, sized so that the whole run
+    # stays within a few minutes
+    per_run = min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))
+    cb, dt, Ts = cpu_baseline(cfg, H, per_run, steps=max(1, args.steps), warmup=args.warmup)
     line = {
         "metric": METRIC,
         "value": cb["value"],
