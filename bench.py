@@ -108,7 +108,7 @@ def measured_traffic(config: str, H: int):
         e = rec.get(f"{config}/H{H}")
         if e and e.get("kernel_hash") == kernel_hash(e.get("family", "full")):
             return e["bytes_per_launch"]
-    except Exception:
+    except (OSError, ValueError, KeyError):   # no record, or an unreadable one
         pass
     return None
 
