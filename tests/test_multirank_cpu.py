@@ -84,3 +84,15 @@ def test_token_sharded_routing_matches_unsharded():
             assert np.array_equal(o, out[lo:hi]) and np.array_equal(l, lse[lo:hi])
             for n in range(N):
                 assert np.array_equal(dsh[n], ds[n][lo:hi])
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the oracle's benchmark runs on rank 0 alone: another rank
+    exits 0 at once and prints nothing."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], cwd=root, capture_output=True, text=True,
+                       timeout=120, env={**os.environ, "RANK": "1", "WORLD_SIZE": "2"})
+    assert p.returncode == 0 and p.stdout == ""
