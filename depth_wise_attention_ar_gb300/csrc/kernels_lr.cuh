@@ -3,25 +3,30 @@
 // full width), with MHAR heads laid over the key slice (head h scores with
 // the h-th r/H block of the key and mixes the h-th d/H block of the value).
 //
-// Forward, per warp and token (two sweeps, exact softmax):
+// Forward, per warp and token (two sweeps, exact softmax), for rows wider
+// than 2560 (narrower rows take the single-pass sliced-key forward of
+// kernels_fwd.cuh):
 //   sweep 1: the key tails of the N listed rows (r coordinates each) land in a
 //            per-warp shared-memory cache by 1-D bulk copies; every head's
 //            scores, softmax weights and lse follow from the cache;
 //   sweep 2: the value rows are mixed in column blocks of CW columns (at most
 //            1024; CW divides both d - r and r) with those weights: blocks left
-//            of the tail stream through
-//            a ring of shared-memory stages, tail blocks come from the cache,
-//            so every source coordinate is read from HBM once.
+//            of the tail stream through a ring of shared-memory stages, tail
+//            blocks come from the cache, so every source coordinate is read
+//            from HBM once.
 //   The cache is double-buffered: the next token's key tails are requested as
 //   soon as this token's weights are known, and arrive during sweep 2.
 // Backward, per warp, over an even contiguous share of the (token, source)
-// items (token-major), as for full keys: G = dL/dout of the current token
-// sits in shared memory; a stage holds the source row and (unless first
+// items (token-major): G = dL/dout of the current token sits in registers
+// when the chunk count d/256 is a template constant (rows up to 2560 wide),
+// else in shared memory; a stage holds the source row and (unless first
 // touch) its fp32 gradient row. Pass A: value dot P (head's value slice) and
 // raw score zr (head's key slice). Pass B: the key-path terms are added into
 // the staged gradient row on the tail. Pass C: w*G is added on every
 // coordinate (and the radial term outside the slice for the full-width
-// norm) and the row is written out.
+// norm) and the row is written out. On bf16 rows up to 2048 wide with key
+// tails up to half the row, the next token's G, output chunks, lse and first
+// inverse RMS values are loaded into registers while this token's items run.
 #pragma once
 
 #include "common.cuh"
