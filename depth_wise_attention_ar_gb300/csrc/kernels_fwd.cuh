@@ -32,7 +32,10 @@
 // LPH*j (ckh = r/(8H) chunks per key slice), in the order and with the sums
 // of the sliced-key backward, so both compute the same score bits; the value
 // chunks are read after the weight is known, so only the accumulator and q*g
-// stay in registers.
+// stay in registers. q*g is held for KM key-chunk slots per lane (a quarter,
+// a half or all of CPL, whichever first covers the key tail), and these
+// instantiations have their own entry, route_fwd_sk_kernel, compiled for the
+// resident blocks fwd_min_blocks gives.
 //
 // FRESH (full keys, rows up to 1024 wide): the site's append is fused in. The
 // new row already sits in its slot; at its item the kernel squares the staged
