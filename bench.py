@@ -378,6 +378,7 @@ def main():
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": cfg.dtype,
+        "compute": f"fp32 arithmetic on {cfg.dtype} rows; fp32 gradient rows, lse, dq, dg",
         "data": "synthetic (seeded torch Philox on device; recipe of the 1B/100M/350M/LR models)",
         "config": {"workload": f"{cfg.name}-shaped routing microbatch", "T": cfg.T, "d": cfg.d,
                    "H": H, "r": cfg.r, "sites": n_bwd,
