@@ -94,7 +94,7 @@ __device__ __forceinline__ void mix_pair(int tile, int slot, bool two, int K, in
             __floats2bfloat162_rn(c1[0] + d1[0], c1[1] + d1[1]);
 }
 
-inline size_t multi_mma_fixed_bytes(int r, int H)
+inline size_t multi_mma_fixed_bytes(int H)
 {
     return 2 * 8                                   // mbarriers
            + 16                                    // a zero line
@@ -109,7 +109,7 @@ inline size_t multi_mma_fixed_bytes(int r, int H)
 // else one; 0 when none fits.
 inline int multi_mma_buffers(int d, int r, int H, int N, size_t *smem)
 {
-    const size_t fixed = multi_mma_fixed_bytes(r, H);
+    const size_t fixed = multi_mma_fixed_bytes(H);
     const size_t tok = (size_t)N * (d * 2 + 16);
     if (2 * (tok + fixed + 1024) <= 228 * 1024) {
         *smem = tok + fixed;
