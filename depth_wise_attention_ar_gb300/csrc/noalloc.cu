@@ -12,7 +12,9 @@
 // The array is a file-scope __device__ object: every GPU that loads this
 // library holds it (kNoAllocScratchBytes) until the process exits. Its device
 // address is looked up once per device, on the first call made with that
-// device current; make that first call before any stream capture. Every call
+// device current; make that first call before any stream capture. The
+// address is kept for the life of the process, so a cudaDeviceReset between
+// uses (which unloads this code and its array) is not supported. Every call
 // shares the one array: calls whose kernels may overlap on the GPU (different
 // streams without ordering between them) race on it and must be serialised by
 // the caller. Nothing in it has to start at zero: the backward writes every

@@ -464,7 +464,10 @@ ar_status ar_bank_grad_token_sum(const ar_bank *bank, int32_t row, float *out, v
  *     nothing; use ar_route_bwd with a workspace instead.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture. The address is kept for the life of the process: do not
+ *     call cudaDeviceReset on a device between uses of this entry point (the
+ *     reset unloads the library's device code, and the kept address would no
+ *     longer be valid).
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero). Calls whose kernels can overlap
  *     on the GPU (unordered streams) race on it: serialise them.
