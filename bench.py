@@ -15,8 +15,8 @@ parameter gradients copied back, inside the timed region.
 Multi-GPU (torchrun): every rank routes its own microbatch (tokens shard with
 no exchange in the routing path), weak scaling; time = max over ranks.
 
-``--impl reference`` times the CPU oracle on the host cores instead (a bounded
-token sample of the same workload per step).
+``--impl reference`` times the CPU oracle (its float32 build) on the host
+cores instead: each step is one bounded token sample of the same workload.
 """
 
 from __future__ import annotations
@@ -162,8 +162,10 @@ class ClockSampler:
 
 
 def cpu_baseline(cfg, H, seconds: float, steps: int = 1, warmup: int = 0):
-    """The oracle (float64 C, OpenMP over tokens) on a token sample of the workload:
-    `warmup` untimed runs, then the mean of `steps` timed runs."""
+    """The oracle's float32 build (C, OpenMP over tokens, all host cores) on a
+    token sample of the workload: every site's forward in order and every
+    site's backward in reverse; `warmup` untimed runs, then the mean of
+    `steps` timed runs."""
     import numpy as np
 
     import oracle
@@ -173,27 +175,35 @@ def cpu_baseline(cfg, H, seconds: float, steps: int = 1, warmup: int = 0):
     oplan = schedule.block_plan(cfg.M, cfg.NB)
     run = list(cfg.sites) if cfg.sites is not None else list(range(len(oplan["sites"])))
     nrows = max(max(oplan["sites"][s]) for s in run) + 1
+    f32 = np.float32
 
     def one(Ts):
         outs = [synth.storage_to_f64(synth.sublayer_output(1, j, Ts, cfg.d, cfg.dtype), cfg.dtype)
                 for j in range(nrows)]
-        rows = storage.block_bank(outs, {"row_ops": oplan["row_ops"][:nrows]}, cfg.dtype)
-        qs = {s: synth.site_query(1, s, cfg.r).astype(np.float64) for s in run}
-        gouts = {s: synth.storage_to_f64(synth.site_dout(1, s, Ts, cfg.d, cfg.dtype), cfg.dtype)
+        rows = [x.astype(f32) for x in
+                storage.block_bank(outs, {"row_ops": oplan["row_ops"][:nrows]}, cfg.dtype)]
+        qs = {s: synth.site_query(1, s, cfg.r) for s in run}
+        gouts = {s: synth.storage_to_f32(synth.site_dout(1, s, Ts, cfg.d, cfg.dtype), cfg.dtype)
                  for s in run}
+        dsrc = {j: np.zeros((Ts, cfg.d), dtype=f32) for j in range(nrows)}
         t0 = time.perf_counter()
         for s in run:
-            oracle.route_fwd([rows[j] for j in oplan["sites"][s]], qs[s], None, H, r=cfg.r)
-        dsrc = {j: np.zeros((Ts, cfg.d)) for j in range(nrows)}
+            oracle.route_fwd([rows[j] for j in oplan["sites"][s]], qs[s], None, H, r=cfg.r,
+                             precision="f32")
         for s in reversed(run):
             oracle.route_bwd([rows[j] for j in oplan["sites"][s]], qs[s], None, gouts[s], H,
-                             r=cfg.r, dsrc=[dsrc[j] for j in oplan["sites"][s]])
+                             r=cfg.r, dsrc=[dsrc[j] for j in oplan["sites"][s]],
+                             precision="f32")
         return time.perf_counter() - t0
 
     threads = oracle.threads()
-    probe = max(threads, 8)
-    tp = one(probe)
-    Ts = int(max(probe, min(cfg.T, probe * seconds / max(tp, 1e-6))))
+    # size the sample from two small probes: a run costs a + b * tokens (a:
+    # per-call overheads, which dominate small runs)
+    t1, t2 = 8 * threads, 32 * threads
+    p1, p2 = one(t1), one(t2)
+    b = max((p2 - p1) / (t2 - t1), 1e-9)
+    a = max(p1 - b * t1, 0.0)
+    Ts = int(min(cfg.T, max(t2, (seconds - a) / b)))
     Ts = max(threads, (Ts // threads) * threads)
     for _ in range(warmup):
         one(Ts)
@@ -201,7 +211,18 @@ def cpu_baseline(cfg, H, seconds: float, steps: int = 1, warmup: int = 0):
     dt = sum(times) / len(times)
     return {"value": Ts / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{Ts} of {cfg.T} tokens, every site forward + backward in reverse, "
-                      f"float64 oracle, {dt:.1f} s per sample"}, dt, Ts
+                      f"float32 build of the oracle, {dt:.1f} s per sample"}, dt, Ts
+
+
+def line_config(cfg, H, world, sites, run):
+    """The `config` object of the JSON line, the same for both arms (`sites`:
+    every site's row list; `run`: the sites that run)."""
+    nrows = max(max(sites[s]) for s in run) + 1
+    b = 2 if cfg.dtype == "bf16" else 4
+    return {"workload": f"{cfg.name}-shaped routing microbatch", "T": cfg.T, "d": cfg.d, "H": H,
+            "r": cfg.r, "sites": len(run), "sources_read": sum(len(sites[s]) for s in run),
+            "global_batch_tokens": world * cfg.T, "parallelism": f"dp{world} (token shards)",
+            "l2": f"inputs larger than L2 (bank {nrows * cfg.T * cfg.d * b / 1e9:.2f} GB)"}
 
 
 def max_over_ranks(values, device="cpu"):
@@ -238,11 +259,9 @@ def report(args):
     lines = []
     for cfg, heads in REPORT_RUNS:
         cmd = [sys.executable, os.path.abspath(__file__), "--config", cfg, "--steps", str(args.steps),
-               "--warmup", str(args.warmup)]
+               "--warmup", str(args.warmup), "--cpu-seconds", str(args.cpu_seconds)]
         if heads:
             cmd += ["--heads", str(heads)]
-        if cfg != "1B" or heads:
-            cmd += ["--no-cpu-baseline"]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
             raise RuntimeError(f"{' '.join(cmd)} failed:\n{p.stderr[-2000:]}")
@@ -259,10 +278,17 @@ def report(args):
                     f"{ph['backward']:.2f} ({100 * L['roofline']['frac']:.1f} %) | "
                     f"{e.get('ms_per_step', float('nan')):.1f} | {e.get('h2d_gbs_alone', float('nan')):.0f} | "
                     f"{L['clocks'].get('sm_mhz')} |")
-    cb = next((L["cpu_baseline"] for L in lines if "cpu_baseline" in L), None)
-    if cb:
-        rows.append("")
-        rows.append(f"CPU oracle: {cb['value']:.1f} {cb['unit']} on {cb['cores']} cores ({cb['sample']}).")
+    rows.append("")
+    rows.append("CPU oracle (float32 build, all host cores) on a token sample of each workload:")
+    rows.append("")
+    rows.append("| workload | H | oracle tokens/s | cores | GPU / oracle | sample |")
+    rows.append("|---|---|---|---|---|---|")
+    for L in lines:
+        cb = L.get("cpu_baseline")
+        if cb:
+            c = L["config"]
+            rows.append(f"| {c['workload']} | {c['H']} | {cb['value']:,.1f} | {cb['cores']} | "
+                        f"{L['value'] / cb['value']:,.0f} | {cb['sample']} |")
     with open(os.path.join(args.report, "report.md"), "w") as f:
         f.write("\n".join(rows) + "\n")
     print("\n".join(rows))
@@ -380,12 +406,8 @@ def main():
         "dtype": cfg.dtype,
         "compute": f"fp32 arithmetic on {cfg.dtype} rows; fp32 gradient rows, lse, dq, dg",
         "data": "synthetic (seeded torch Philox on device; recipe of the 1B/100M/350M/LR models)",
-        "config": {"workload": f"{cfg.name}-shaped routing microbatch", "T": cfg.T, "d": cfg.d,
-                   "H": H, "r": cfg.r, "sites": n_bwd,
-                   "sources_read": sum(len(mb.plan.sites[s]) for s in mb.plan.run_sites),
-                   "global_batch_tokens": world * cfg.T, "parallelism": f"dp{world} (token shards)",
-                   "cuda_graphs": use_graph, "l2": "inputs larger than L2 (bank "
-                   f"{mb.bank.rows.numel() * mb.bank.rows.element_size() / 1e9:.2f} GB)"},
+        "config": line_config(cfg, H, world, mb.plan.sites, mb.plan.run_sites),
+        "cuda_graphs": use_graph,
         "phases_ms": {"forward_and_appends": fwd_ms, "backward": bwd_ms},
         "step_ms_spread": {"median": per_step[K // 2], "min": per_step[0], "max": per_step[-1]},
         "model_bytes": mbytes,
@@ -528,17 +550,21 @@ def end_to_end(args, mb, stream, run_fwd, run_bwd, world, local):
     with torch.cuda.stream(stream):
         run(2)                                   # warm-up: both buffer sets
     torch.cuda.synchronize()
-    # the host link alone: one step's input copies with nothing else running
-    # (the host's memory and links are shared with other jobs on the machine,
-    # so the end-to-end figure is read against this)
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(h2d_stream):
-        c0.record(h2d_stream)
-    issue_copies(0)
-    with torch.cuda.stream(h2d_stream):
-        c1.record(h2d_stream)
-    torch.cuda.synchronize()
-    h2d_gbs_alone = h2d / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    # the host link alone: one step's input copies with nothing else running,
+    # three times, the median kept (the host's memory and links are shared
+    # with other jobs on the machine, so the end-to-end figure is read
+    # against this)
+    probes = []
+    for _ in range(3):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(h2d_stream):
+            c0.record(h2d_stream)
+        issue_copies(0)
+        with torch.cuda.stream(h2d_stream):
+            c1.record(h2d_stream)
+        torch.cuda.synchronize()
+        probes.append(h2d / (c0.elapsed_time(c1) * 1e-3) / 1e9)
+    h2d_gbs_alone = sorted(probes)[1]
     if world > 1:
         dist.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -552,10 +578,13 @@ def end_to_end(args, mb, stream, run_fwd, run_bwd, world, local):
     if world > 1:
         (ms,) = max_over_ranks([ms], device=f"cuda:{local}")
     del mbs[1]
+    # the copies alone at the probed rate; a probe slower than the loop itself
+    # saw (the step moved the same bytes faster) is no bound, so none is given
+    copy_ms = h2d / (h2d_gbs_alone * 1e9) * 1e3
     return {"value": world * mb.cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "h2d_gbs_alone": h2d_gbs_alone,
-            "copy_bound_ms": h2d / (h2d_gbs_alone * 1e9) * 1e3,
+            "h2d_gbs_alone": h2d_gbs_alone, "h2d_gbs_probes": probes,
+            "copy_bound_ms": copy_ms if copy_ms <= ms else None,
             "copies": "H2D on its own stream, double-buffered: the next step's inputs stream "
                       "in while the current step computes; D2H of each step's packed dq/dg "
                       "after the step"}
@@ -573,6 +602,9 @@ def reference_arm(args, rank, world):
     # stays within a few minutes
     per_run = min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))
     cb, dt, Ts = cpu_baseline(cfg, H, per_run, steps=max(1, args.steps), warmup=args.warmup)
+    from oracle import schedule
+    oplan = schedule.block_plan(cfg.M, cfg.NB)
+    run = list(cfg.sites) if cfg.sites is not None else list(range(len(oplan["sites"])))
     line = {
         "metric": METRIC,
         "value": cb["value"],
@@ -580,14 +612,14 @@ def reference_arm(args, rank, world):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": dt * 1e3 * cfg.T / Ts,
+        "ms_per_step": dt * 1e3,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f64",
+        "dtype": "f32",
         "data": "synthetic (seeded numpy Philox)",
-        "config": {"workload": f"{cfg.name}-shaped routing microbatch", "T": cfg.T, "d": cfg.d,
-                   "H": H, "r": cfg.r},
+        "config": line_config(cfg, H, world, oplan["sites"], run),
+        "tokens_per_step": Ts,
         "impl": "reference",
         "cpu_baseline": cb,
         "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -68,11 +68,15 @@ SIGNATURES = {
                      ctypes.c_int),
     "ar_route_bwd_noalloc": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P],
                              ctypes.c_int),
+    "ar_noalloc_scratch_bytes": ([_SZP], ctypes.c_int),
     "ar_bank_grad_fold": ([_P, _I32, _I32, _P], ctypes.c_int),
     "ar_route_merge": ([_P, _I32, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "ar_route_fwd_multi": ([_P, _I32P, _I32, _I32, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
     "ar_block_schedule": ([_I32, _I32, _I32P, _I32P, _I32P, _I64, _I64P], ctypes.c_int),
     "ar_device_error": ([_U32P], ctypes.c_int),
+    "ar_device_status": ([], ctypes.c_int),
+    "ar_route_fwd_lost_copies": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, ctypes.c_uint32, _P],
+                                 ctypes.c_int),
 }
 
 if not os.path.exists(LIBPATH):
@@ -277,7 +281,10 @@ def ar_route_bwd_noalloc(bank, rows, H, q, g, out, dout, lse, dq, dg, site_id, s
                                                              _stream(stream)))
 
 
-AR_NOALLOC_SCRATCH_BYTES = 8 << 20
+def ar_noalloc_scratch_bytes() -> int:
+    b = ctypes.c_size_t()
+    _check("ar_noalloc_scratch_bytes", _lib.ar_noalloc_scratch_bytes(ctypes.byref(b)))
+    return b.value
 
 
 def ar_bank_grad_fold(bank, dst_row: int, src_row: int, stream=None):
@@ -325,6 +332,19 @@ def ar_device_error() -> int:
     bits = ctypes.c_uint32()
     _check("ar_device_error", _lib.ar_device_error(ctypes.byref(bits)))
     return bits.value
+
+
+def ar_device_status():
+    """Raises ARError (AR_ERR_TIMEOUT) if a device-side wait ran out since the
+    last read of the device error word; clears the word."""
+    _check("ar_device_status", _lib.ar_device_status())
+
+
+def ar_route_fwd_lost_copies(bank, rows, H, q, g, out, lse, poll_limit: int, stream=None):
+    arr, n = _rows(rows)
+    _check("ar_route_fwd_lost_copies",
+           _lib.ar_route_fwd_lost_copies(bank, arr, n, H, _ptr(q), _ptr(g), _ptr(out), _ptr(lse),
+                                         poll_limit, _stream(stream)))
 
 
 # ---- convenience owner of a bank's buffers -------------------------------------

@@ -40,6 +40,12 @@ struct RouteArgs {
     // written to its slot by the forward; acc_row = -1 for a copy
     const void *fresh_src;
     int acc_row;
+    // polls of an mbarrier wait before it is declared lost (0: kWaitLimit);
+    // with lost_copies set (a test of the failure path, one-warp full-key
+    // forward only) every stage is armed for its bytes but no copy is issued,
+    // so the first wait of every warp runs out with nothing in flight
+    uint32_t wait_limit;
+    int lost_copies;
     int rows[AR_MAX_SOURCES];
     // a row listed k > 1 times in a site enters once with log k added to its
     // score (softmax over the list = softmax over distinct rows with weights k)
@@ -86,6 +92,10 @@ cudaError_t launch_append(const void *src, const void *prev, void *dst, float *i
 cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
                              bool dst_valid, cudaStream_t s);
 unsigned int *device_error_word();
+// AR_OK when the current device is the one the bank was created on (or the
+// bank's device is unknown), else AR_ERR_INVALID_ARG: every launch runs on the
+// current device, and the bank's buffers belong to its own.
+ar_status bank_device_check(const ar_bank *b);
 // Some kernel family serves n_src distinct rows at this shape (`repeats`: the
 // site lists a row more than once).
 bool route_supported(int d, int r, int H, int n_src, ar_dtype dt, bool repeats);

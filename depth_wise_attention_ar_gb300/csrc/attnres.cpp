@@ -14,6 +14,7 @@
 
 #include "attnres.h"
 #include "ar_internal.h"
+#include "shapes.h"
 
 struct ar_bank {
     int64_t T = 0;
@@ -31,6 +32,21 @@ struct ar_bank {
     size_t esize = 2;
 };
 
+namespace ar {
+
+ar_status bank_device_check(const ar_bank *b)
+{
+    if (!b || b->device < 0) return AR_OK;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return AR_OK;  // no usable device: the launch itself reports the failure
+    }
+    return dev == b->device ? AR_OK : AR_ERR_INVALID_ARG;
+}
+
+}  // namespace ar
+
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -43,6 +59,8 @@ ar_status from_cuda(cudaError_t e)
     cudaGetLastError();  // clear a sticky-free launch error so the caller may retry
     return AR_ERR_CUDA;
 }
+
+ar_status on_bank_device(const ar_bank *b) { return ar::bank_device_check(b); }
 
 // Checks shared by the forward and the backward of a site.
 ar_status check_site(const ar_bank *b, const int32_t *rows, int32_t n_src, int32_t H,
@@ -158,7 +176,7 @@ ar_status ar_bank_create(ar_bank **out, int64_t T, int32_t d, int32_t r, int32_t
     if (norm != AR_NORM_KEY && norm != AR_NORM_FULL) return AR_ERR_INVALID_ARG;
     if (d < 1 || r < 1 || r > d) return AR_ERR_SHAPE;
     if (!aligned16(rows) || !aligned16(inv_rms) || (grad && !aligned16(grad))) return AR_ERR_ALIGN;
-    int dev = -1;  // recorded for information; launches use the current device
+    int dev = -1;  // launches use the current device; every call checks it is this one
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         dev = -1;
@@ -210,6 +228,7 @@ ar_status ar_bank_append_strided(ar_bank *bank, const void *src, int64_t token_s
 {
     if (!bank || (!src && bank->T > 0)) return AR_ERR_INVALID_ARG;
     if (token_stride < 0 || elem_stride < 1) return AR_ERR_INVALID_ARG;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (bank->count >= bank->cap) return AR_ERR_CAPACITY;
     if (accumulate_from < -1 || accumulate_from >= bank->count) return AR_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(src) % bank->esize) != 0) return AR_ERR_ALIGN;
@@ -263,6 +282,7 @@ ar_status route_fwd_impl(ar_bank *bank, const ar_site &st_, const void *partial,
     ar_status st = check_site(bank, rows, n_src, H, q, g);
     if (st != AR_OK) return st;
     if (bank->T > 0 && (!out || !lse)) return AR_ERR_INVALID_ARG;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned4(lse) || !aligned16(partial) || !aligned16(routed) ||
         !aligned4(alpha))
         return AR_ERR_ALIGN;
@@ -314,6 +334,7 @@ ar_status ar_route_fwd_append(ar_bank *bank, const void *src, int32_t accumulate
 {
     if (fused) *fused = 0;
     if (!bank || (!src && bank->T > 0)) return AR_ERR_INVALID_ARG;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (bank->count >= bank->cap) return AR_ERR_CAPACITY;
     if (accumulate_from < -1 || accumulate_from >= bank->count) return AR_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(src) % bank->esize) != 0) return AR_ERR_ALIGN;
@@ -386,6 +407,7 @@ ar_status ar_route_fwd_multi(const ar_bank *bank, const int32_t *rows, int32_t n
     if (!bank || !rows || !q) return AR_ERR_INVALID_ARG;
     if (n_src < 1 || n_src > AR_MAX_SOURCES) return AR_ERR_INVALID_ARG;
     if (n_q < 1 || n_q > AR_MAX_QUERIES) return AR_ERR_INVALID_ARG;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (H < 1 || bank->d % H != 0 || bank->r % H != 0) return AR_ERR_SHAPE;
     for (int i = 0; i < n_src; ++i)
         if (rows[i] < 0 || rows[i] >= bank->count) return AR_ERR_INVALID_ARG;
@@ -450,6 +472,7 @@ ar_status route_bwd_impl(ar_bank *bank, const ar_site &st_, const void *out, con
     if (bank && !bank->grad && bank->T > 0) return AR_ERR_INVALID_ARG;
     ar_status st = check_site(bank, rows, n_src, H, q, g);
     if (st != AR_OK) return st;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (!dq || (bank->T > 0 && (!out || !dout || !lse || !ws))) return AR_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(dout) || !aligned4(lse) || !aligned4(dq) ||
         (dg && !aligned4(dg)) || !aligned16(ws) || !aligned4(alpha) || !aligned4(dalpha))
@@ -525,6 +548,7 @@ ar_status ar_route_bwd_site(ar_bank *bank, const ar_site *site, const void *out,
 ar_status ar_bank_append_broadcast(ar_bank *bank, const void *vec, int32_t *out_row, void *stream)
 {
     if (!bank || !vec) return AR_ERR_INVALID_ARG;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (bank->count >= bank->cap) return AR_ERR_CAPACITY;
     if ((reinterpret_cast<uintptr_t>(vec) % bank->esize) != 0) return AR_ERR_ALIGN;
     void *dst = nullptr;
@@ -542,6 +566,7 @@ ar_status ar_bank_append_broadcast(ar_bank *bank, const void *vec, int32_t *out_
 ar_status ar_bank_grad_token_sum(const ar_bank *bank, int32_t row, float *out, void *stream)
 {
     if (!bank || !out || row < 0 || row >= bank->count) return AR_ERR_INVALID_ARG;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (!bank->grad && bank->T > 0) return AR_ERR_INVALID_ARG;
     if (!aligned4(out)) return AR_ERR_ALIGN;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -559,6 +584,7 @@ ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, voi
     if (!bank || dst_row < 0 || src_row < 0 || dst_row >= bank->count ||
         src_row >= bank->count || dst_row == src_row)
         return AR_ERR_INVALID_ARG;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (!bank->grad) return bank->T == 0 ? AR_OK : AR_ERR_INVALID_ARG;
     const int64_t n = bank->T * (int64_t)bank->d;
     float *dst = bank->grad + (int64_t)dst_row * n;
@@ -575,6 +601,7 @@ ar_status ar_route_merge(const ar_bank *bank, int32_t H, const void *out_a, cons
                          const void *out_b, const float *lse_b, void *out, float *lse, void *stream)
 {
     if (!bank) return AR_ERR_INVALID_ARG;
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
     if (H < 1 || bank->d % H != 0) return AR_ERR_SHAPE;
     if (bank->T > 0 && (!out_a || !lse_a || !out_b || !lse_b || !out || !lse))
         return AR_ERR_INVALID_ARG;
@@ -615,6 +642,39 @@ ar_status ar_block_schedule(int32_t M, int32_t NB, int32_t *acc_from, int32_t *s
     if (!site_rows || site_rows_cap < (int64_t)flat.size()) return AR_ERR_CAPACITY;
     std::memcpy(site_rows, flat.data(), flat.size() * sizeof(int32_t));
     return AR_OK;
+}
+
+ar_status ar_route_fwd_lost_copies(ar_bank *bank, const int32_t *rows, int32_t n_src,
+                                   int32_t H, const float *q, const float *g, void *out,
+                                   float *lse, uint32_t poll_limit, void *stream)
+{
+    if (on_bank_device(bank) != AR_OK) return AR_ERR_INVALID_ARG;
+    ar_status st = check_site(bank, rows, n_src, H, q, g);
+    if (st != AR_OK) return st;
+    if (poll_limit < 1 || bank->T < 1 || !out || !lse) return AR_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned4(lse)) return AR_ERR_ALIGN;
+    // the one-warp full-key forward: full keys, rows of 768 to 2048 columns
+    // (narrower rows with at most 4 heads take the two-tokens-per-warp kernel)
+    const size_t es = bank->dtype == AR_BF16 ? 2 : 4;
+    if (ar::family_of(bank->d, bank->r, H, n_src, es, false) != ar::Family::kFull ||
+        (bank->d <= 512 && H <= 4))
+        return AR_ERR_UNSUPPORTED;
+    ar::RouteArgs a;
+    fill_common(a, bank, rows, n_src, H, q, g);
+    if (a.has_bias) return AR_ERR_UNSUPPORTED;
+    a.out = out;
+    a.lse = lse;
+    a.wait_limit = poll_limit;
+    a.lost_copies = 1;
+    return from_cuda(ar::launch_route_fwd(a, bank->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+ar_status ar_device_status(void)
+{
+    uint32_t bits = 0;
+    const ar_status st = ar_device_error(&bits);
+    if (st != AR_OK) return st;
+    return (bits & AR_DEVERR_WAIT_TIMEOUT) ? AR_ERR_TIMEOUT : AR_OK;
 }
 
 ar_status ar_device_error(uint32_t *bits)

@@ -147,13 +147,15 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
                                        ((int64_t)s_rows[n_p] * TT + tok_p) * row_bytes;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bars[slot_p], row_bytes);
-            bulk_g2s(ring + (size_t)slot_p * row_bytes, src, row_bytes, &bars[slot_p], pol);
+            if (!a.lost_copies)
+                bulk_g2s(ring + (size_t)slot_p * row_bytes, src, row_bytes, &bars[slot_p], pol);
         }
         ++issued;
         if (++n_p == N) { n_p = 0; tok_p += GW; }
         if (++slot_p == S) slot_p = 0;
     };
     for (int s = 0; s < S && issued < total; ++s) issue_next();
+    const uint32_t wait_limit = a.wait_limit ? a.wait_limit : kWaitLimit;
 
     // inverse RMS of the next token's sources, prefetched into registers
     float pre_inv[AR_MAX_SOURCES / 32];
@@ -182,7 +184,7 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
             __syncwarp();
             if (tok + GW < TT) prefetch_inv(tok + GW);
         }
-        const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
+        const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, wait_limit);
         if (!__all_sync(FULL, got)) { ok = false; break; }
         phase ^= 1u << slot;
         const unsigned char *buf = ring + (size_t)slot * row_bytes;
@@ -278,8 +280,9 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
     if (!ok) {
         if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
         // wait briefly for this warp's copies still in flight, then leave
+        const uint32_t drain = a.wait_limit ? a.wait_limit : 1u << 16;
         for (int64_t j = i; j < issued; ++j) {
-            mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+            mbar_wait(&bars[slot], (phase >> slot) & 1u, drain);
             phase ^= 1u << slot;
             if (++slot == S) slot = 0;
         }

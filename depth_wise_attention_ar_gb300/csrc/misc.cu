@@ -6,6 +6,8 @@
 
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 namespace ar {
 
 namespace cg = cooperative_groups;
@@ -26,10 +28,14 @@ __device__ unsigned int g_device_error = 0;
 
 unsigned int *device_error_word()
 {
-    // cached per device: the symbol lookup is done once, outside any capture
+    // cached per device (devices 0..63): the symbol lookup is done once,
+    // outside any capture; the lock keeps first calls from several host
+    // threads off each other's entries
+    static std::mutex mu;
     static unsigned int *cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
     if (!cache[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;

@@ -37,6 +37,10 @@
  *   ar_device_error().
  * - Banks are not thread-safe; distinct banks may be used from distinct
  *   threads.
+ * - A bank belongs to the device that was current when it was created.
+ *   Every call that launches work on a bank's buffers runs on the current
+ *   device and returns AR_ERR_INVALID_ARG, launching nothing, when that is
+ *   not the bank's device.
  *
  * Shapes: every d >= 1, 1 <= r <= d and H dividing both d and r are served.
  * The tiled kernels (bulk copies into shared memory, 16-byte accesses) take
@@ -455,15 +459,20 @@ ar_status ar_bank_grad_token_sum(const ar_bank *bank, int32_t row, float *out, v
  * not call cudaMalloc, or code embedded in a process whose device memory
  * belongs to another framework's pool).
  *   Arguments, results and checks are those of ar_route_bwd, minus ws and
- *   ws_bytes: the backward's scratch (its per-warp dq/dg partial sums) lives
+ *   ws_bytes: the backward's scratch (its per-block dq/dg partial sums) lives
  *   in a fixed device array inside this library, AR_NOALLOC_SCRATCH_BYTES
- *   large, which every GPU that loads the library holds until the process
- *   exits. The call allocates nothing.
+ *   large (ar_noalloc_scratch_bytes() reports it), which every GPU on which
+ *   the library's device code is loaded holds until the process exits. Under
+ *   CUDA's lazy module loading (the default) that happens when the library is
+ *   first used on the device, which may be this entry point's first call:
+ *   count the array against a fixed memory budget from that call on. The
+ *   call allocates nothing.
  *   - If ar_route_bwd_workspace() for this bank and H exceeds
  *     AR_NOALLOC_SCRATCH_BYTES, the call returns AR_ERR_CAPACITY and runs
  *     nothing; use ar_route_bwd with a workspace instead.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
+ *     per device, with that device current, for devices 0..63; a higher
+ *     device number gets AR_ERR_CUDA); make that first call before any
  *     stream capture. The address is kept for the life of the process: do not
  *     call cudaDeviceReset on a device between uses of this entry point (the
  *     reset unloads the library's device code, and the kept address would no
@@ -478,9 +487,37 @@ ar_status ar_route_bwd_noalloc(ar_bank *bank, const int32_t *rows, int32_t n_src
                                const float *lse, float *dq, float *dg, int32_t site_id,
                                void *stream);
 
+/* The size of ar_route_bwd_noalloc's fixed scratch array in bytes
+ * (AR_NOALLOC_SCRATCH_BYTES, as this build of the library has it). */
+ar_status ar_noalloc_scratch_bytes(size_t *bytes);
+
 /* Read and clear the device error word of the current device (bit mask of
  * AR_DEVERR_*; 0 = none). This call synchronises the device. */
 ar_status ar_device_error(uint32_t *bits);
+
+/* The device error word as a status: synchronises the device, reads and
+ * clears the word, and returns AR_ERR_TIMEOUT if a device-side wait ran out
+ * since the last read (AR_DEVERR_WAIT_TIMEOUT), AR_OK if none did, AR_ERR_CUDA
+ * if the device could not be read. */
+ar_status ar_device_status(void);
+
+/*
+ * Test of the failure path (no counterpart in the papers): the forward of a
+ * site, as ar_route_fwd, except that every shared-memory stage is armed for
+ * its row's bytes and no copy is ever issued. Each warp's first wait then
+ * runs out after poll_limit polls with nothing in flight; the kernel sets
+ * AR_DEVERR_WAIT_TIMEOUT in the device error word, waits at most poll_limit
+ * polls per armed stage, and returns without writing out or lse. The host
+ * sees it through ar_device_status() (AR_ERR_TIMEOUT); the context stays
+ * usable. Nothing is recorded in the bank (no backward may follow).
+ *   Served on the one-warp full-key forward only: r = d, d a multiple of 256
+ *   from 768 to 2048 (or 256 and 512 with H > 4), H a power of two <= 32,
+ *   distinct rows; other shapes get AR_ERR_UNSUPPORTED. poll_limit >= 1 and
+ *   T >= 1 (else AR_ERR_INVALID_ARG). Other checks as ar_route_fwd.
+ */
+ar_status ar_route_fwd_lost_copies(ar_bank *bank, const int32_t *rows, int32_t n_src,
+                                   int32_t H, const float *q, const float *g, void *out,
+                                   float *lse, uint32_t poll_limit, void *stream);
 
 #ifdef __cplusplus
 }

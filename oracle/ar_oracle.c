@@ -5,9 +5,12 @@
  * smoke check and the benchmark's CPU-baseline leg call it. It shares no
  * code, header or constant with the CUDA path.
  *
- * Everything is float64 and written as the definitions read, one token at a
- * time (tokens are independent: the attention runs over depth, not over
- * tokens). OpenMP, when available, only splits the token loop.
+ * Everything is written as the definitions read, one token at a time (tokens
+ * are independent: the attention runs over depth, not over tokens), in one
+ * arithmetic type `real`: float64 for the parity reference (the default
+ * build), float32 for the timed CPU baseline (built with -DORC_FLOAT; the
+ * same source, so the two builds differ only in precision). OpenMP, when
+ * available, only splits the token loop.
  *
  * Notation (per token; N sources s_0..s_{N-1} in R^d; H heads):
  *   key coordinates   : the last r of the d coordinates (r = d is the plain
@@ -26,17 +29,26 @@
  *   out_c             : sum_n alpha_{n,h(c)} s_{n,c}                   (Eq. 3)
  *   lse_h             : max_n z + log sum_n exp(z - max)
  */
-#include <math.h>
 #include <stdint.h>
+#include <tgmath.h> /* exp, log, sqrt follow the type of their argument */
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
 
+#ifdef ORC_FLOAT
+typedef float real;
+#else
+typedef double real;
+#endif
+
 #define ORC_OK 0
 #define ORC_BAD_ARG 1
 #define ORC_NO_MEMORY 2
+
+/* Bytes of the arithmetic type of this build (8: float64, 4: float32). */
+int orc_real_bytes(void) { return (int)sizeof(real); }
 
 int orc_max_threads(void)
 {
@@ -57,21 +69,21 @@ static int check_shape(int N, int64_t T, int d, int r, int H)
 /* Inverse RMS of one token's vector over the RMS coordinates.
  * "Multi-Head Attention Residuals", Appendix E: r = (||s||^2/d + eps)^(-1/2);
  * "Low-Rank Attention Residuals", Eq. 13 (slice: over the last r coordinates). */
-static double inv_rms_one(const double *x, int d, int r, int full_width, double eps)
+static real inv_rms_one(const real *x, int d, int r, int full_width, real eps)
 {
     int c0 = full_width ? 0 : d - r;
     int w = d - c0;
-    double ss = 0.0;
+    real ss = (real)0;
     for (int c = c0; c < d; ++c) ss += x[c] * x[c];
-    return 1.0 / sqrt(ss / (double)w + eps);
+    return (real)1 / sqrt(ss / (real)w + eps);
 }
 
 /* inv[t] for every token of one [T,d] source. */
-int orc_inv_rms(const double *x, int64_t T, int d, int r, int full_width, double eps, double *inv)
+int orc_inv_rms(const real *x, int64_t T, int d, int r, int full_width, double eps, real *inv)
 {
     if (check_shape(1, T, d, r, 1)) return ORC_BAD_ARG;
 #pragma omp parallel for schedule(static)
-    for (int64_t t = 0; t < T; ++t) inv[t] = inv_rms_one(x + t * d, d, r, full_width, eps);
+    for (int64_t t = 0; t < T; ++t) inv[t] = inv_rms_one(x + t * d, d, r, full_width, (real)eps);
     return ORC_OK;
 }
 
@@ -82,17 +94,17 @@ int orc_inv_rms(const double *x, int64_t T, int d, int r, int full_width, double
  *   out     : [T,d]   lse : [T,H]       alpha: [T,N,H] or NULL
  * Softmax is the explicit two-pass form: max, then normalised exponentials.
  */
-int orc_route_fwd(const double *const *src, int N, int64_t T, int d, int r, int H,
-                  int full_width, double eps, const double *q, const double *g,
-                  double *out, double *lse, double *alpha)
+int orc_route_fwd(const real *const *src, int N, int64_t T, int d, int r, int H,
+                  int full_width, double eps, const real *q, const real *g,
+                  real *out, real *lse, real *alpha)
 {
     if (check_shape(N, T, d, r, H)) return ORC_BAD_ARG;
     const int K = d / H, Kr = r / H, c_key = d - r;
     int bad = 0;
 #pragma omp parallel
     {
-        double *z = (double *)malloc(sizeof(double) * (size_t)N * H);
-        double *a = (double *)malloc(sizeof(double) * (size_t)N * H);
+        real *z = (real *)malloc(sizeof(real) * (size_t)N * H);
+        real *a = (real *)malloc(sizeof(real) * (size_t)N * H);
         if (!z || !a) {
 #pragma omp atomic write
             bad = 1;
@@ -102,23 +114,23 @@ int orc_route_fwd(const double *const *src, int N, int64_t T, int d, int r, int 
             if (!z || !a) continue;
             /* scores z_{n,h} = q_h . RMSNorm(s_n)_[h] (g folded into the key) */
             for (int n = 0; n < N; ++n) {
-                const double *s = src[n] + t * d;
-                double inv = inv_rms_one(s, d, r, full_width, eps);
+                const real *s = src[n] + t * d;
+                real inv = inv_rms_one(s, d, r, full_width, (real)eps);
                 for (int h = 0; h < H; ++h) {
-                    double dot = 0.0;
+                    real dot = (real)0;
                     for (int k = 0; k < Kr; ++k) {
                         int j = h * Kr + k; /* index into q, g */
-                        dot += q[j] * (g ? g[j] : 1.0) * s[c_key + j];
+                        dot += q[j] * (g ? g[j] : (real)1) * s[c_key + j];
                     }
                     z[n * H + h] = inv * dot;
                 }
             }
             /* softmax over sources, per head */
             for (int h = 0; h < H; ++h) {
-                double m = z[h];
+                real m = z[h];
                 for (int n = 1; n < N; ++n)
                     if (z[n * H + h] > m) m = z[n * H + h];
-                double sum = 0.0;
+                real sum = (real)0;
                 for (int n = 0; n < N; ++n) sum += exp(z[n * H + h] - m);
                 for (int n = 0; n < N; ++n) a[n * H + h] = exp(z[n * H + h] - m) / sum;
                 lse[t * H + h] = m + log(sum);
@@ -126,11 +138,11 @@ int orc_route_fwd(const double *const *src, int N, int64_t T, int d, int r, int 
             /* mix: each head mixes only its own value slice */
             for (int c = 0; c < d; ++c) {
                 int h = c / K;
-                double acc = 0.0;
+                real acc = (real)0;
                 for (int n = 0; n < N; ++n) acc += a[n * H + h] * src[n][t * d + c];
                 out[t * d + c] = acc;
             }
-            if (alpha) memcpy(alpha + t * (int64_t)N * H, a, sizeof(double) * (size_t)N * H);
+            if (alpha) memcpy(alpha + t * (int64_t)N * H, a, sizeof(real) * (size_t)N * H);
         }
         free(z);
         free(a);
@@ -155,28 +167,28 @@ int orc_route_fwd(const double *const *src, int N, int64_t T, int d, int r, int 
  *             sites sums their contributions)
  *   dq, dg  : [r], overwritten; dg may be NULL. g may be NULL (= ones).
  */
-int orc_route_bwd(const double *const *src, int N, int64_t T, int d, int r, int H,
-                  int full_width, double eps, const double *q, const double *g,
-                  const double *dout, double *const *dsrc, double *dq, double *dg)
+int orc_route_bwd(const real *const *src, int N, int64_t T, int d, int r, int H,
+                  int full_width, double eps, const real *q, const real *g,
+                  const real *dout, real *const *dsrc, real *dq, real *dg)
 {
     if (check_shape(N, T, d, r, H)) return ORC_BAD_ARG;
     const int K = d / H, Kr = r / H, c_key = d - r;
     const int c_rms = full_width ? 0 : d - r, w_rms = d - c_rms;
     for (int j = 0; j < r; ++j) {
-        dq[j] = 0.0;
-        if (dg) dg[j] = 0.0;
+        dq[j] = (real)0;
+        if (dg) dg[j] = (real)0;
     }
     int bad = 0;
 #pragma omp parallel
     {
         size_t nh = (size_t)N * H;
-        double *inv = (double *)malloc(sizeof(double) * N);
-        double *zraw = (double *)malloc(sizeof(double) * nh);
-        double *a = (double *)malloc(sizeof(double) * nh);
-        double *fb = (double *)malloc(sizeof(double) * nh);
-        double *o = (double *)malloc(sizeof(double) * d);
-        double *dq_p = (double *)calloc((size_t)r, sizeof(double));
-        double *dg_p = (double *)calloc((size_t)r, sizeof(double));
+        real *inv = (real *)malloc(sizeof(real) * N);
+        real *zraw = (real *)malloc(sizeof(real) * nh);
+        real *a = (real *)malloc(sizeof(real) * nh);
+        real *fb = (real *)malloc(sizeof(real) * nh);
+        real *o = (real *)malloc(sizeof(real) * d);
+        real *dq_p = (real *)calloc((size_t)r, sizeof(real));
+        real *dg_p = (real *)calloc((size_t)r, sizeof(real));
         int ok = inv && zraw && a && fb && o && dq_p && dg_p;
         if (!ok) {
 #pragma omp atomic write
@@ -185,61 +197,61 @@ int orc_route_bwd(const double *const *src, int N, int64_t T, int d, int r, int 
 #pragma omp for schedule(static)
         for (int64_t t = 0; t < T; ++t) {
             if (!ok) continue;
-            const double *G = dout + t * d;
+            const real *G = dout + t * d;
             /* recompute the forward of this token: inv, raw scores, alpha, out */
             for (int n = 0; n < N; ++n) {
-                const double *s = src[n] + t * d;
-                inv[n] = inv_rms_one(s, d, r, full_width, eps);
+                const real *s = src[n] + t * d;
+                inv[n] = inv_rms_one(s, d, r, full_width, (real)eps);
                 for (int h = 0; h < H; ++h) {
-                    double dot = 0.0;
+                    real dot = (real)0;
                     for (int k = 0; k < Kr; ++k) {
                         int j = h * Kr + k;
-                        dot += q[j] * (g ? g[j] : 1.0) * s[c_key + j];
+                        dot += q[j] * (g ? g[j] : (real)1) * s[c_key + j];
                     }
                     zraw[n * H + h] = dot;
                 }
             }
             for (int h = 0; h < H; ++h) {
-                double m = inv[0] * zraw[h];
+                real m = inv[0] * zraw[h];
                 for (int n = 1; n < N; ++n) {
-                    double zz = inv[n] * zraw[n * H + h];
+                    real zz = inv[n] * zraw[n * H + h];
                     if (zz > m) m = zz;
                 }
-                double sum = 0.0;
+                real sum = (real)0;
                 for (int n = 0; n < N; ++n) sum += exp(inv[n] * zraw[n * H + h] - m);
                 for (int n = 0; n < N; ++n) a[n * H + h] = exp(inv[n] * zraw[n * H + h] - m) / sum;
             }
             for (int c = 0; c < d; ++c) {
                 int h = c / K;
-                double acc = 0.0;
+                real acc = (real)0;
                 for (int n = 0; n < N; ++n) acc += a[n * H + h] * src[n][t * d + c];
                 o[c] = acc;
             }
             /* routing feedback fb_{n,h} = alpha <G_[h], s_[h] - out_[h]>  (Eq. 15, 20) */
             for (int n = 0; n < N; ++n) {
-                const double *s = src[n] + t * d;
+                const real *s = src[n] + t * d;
                 for (int h = 0; h < H; ++h) {
-                    double dot = 0.0;
+                    real dot = (real)0;
                     for (int c = h * K; c < (h + 1) * K; ++c) dot += G[c] * (s[c] - o[c]);
                     fb[n * H + h] = a[n * H + h] * dot;
                 }
             }
             for (int n = 0; n < N; ++n) {
-                const double *s = src[n] + t * d;
-                double *ds = dsrc[n] + t * d;
+                const real *s = src[n] + t * d;
+                real *ds = dsrc[n] + t * d;
                 /* direct value gradient alpha_{n,h(c)} G_c */
                 for (int c = 0; c < d; ++c) ds[c] += a[n * H + c / K] * G[c];
                 /* routing feedback times the score gradient (Eq. 21 / 22) */
-                double iv = inv[n], iv3 = iv * iv * iv;
+                real iv = inv[n], iv3 = iv * iv * iv;
                 for (int h = 0; h < H; ++h) {
-                    double f = fb[n * H + h];
+                    real f = fb[n * H + h];
                     for (int k = 0; k < Kr; ++k) {
                         int j = h * Kr + k, c = c_key + j;
-                        ds[c] += f * iv * q[j] * (g ? g[j] : 1.0);
-                        dq_p[j] += f * iv * (g ? g[j] : 1.0) * s[c];
+                        ds[c] += f * iv * q[j] * (g ? g[j] : (real)1);
+                        dq_p[j] += f * iv * (g ? g[j] : (real)1) * s[c];
                         dg_p[j] += f * iv * q[j] * s[c];
                     }
-                    double coef = f * iv3 * zraw[n * H + h] / (double)w_rms;
+                    real coef = f * iv3 * zraw[n * H + h] / (real)w_rms;
                     for (int c = c_rms; c < d; ++c) ds[c] -= coef * s[c];
                 }
             }

@@ -498,28 +498,58 @@ def test_error_paths_on_device(W):
     assert B.ar_device_error() == 0
 
 
-@pytest.mark.parametrize("name", ["1B", "350M", "100M"])
-def test_full_size_sampled_tokens(W, orc, name):
+@pytest.mark.parametrize("H", [1, 4, 8, 16])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_many_tokens_per_warp_1280_columns(W, orc, H, dtype):
+    """One site over 41 sources at d = 1280 with T = 7919 tokens: more than four
+    tokens per warp of the persistent forward and backward grids (at most 1824
+    resident warps), so each warp's source ring and inverse-RMS prefetch run
+    across several tokens, and T is prime (a ragged last round). Every head
+    width of the 1B head sweep ("Multi-Head Attention Residuals", routing-head
+    sweep): one lane group of 32 lanes per head at H = 1, two lanes per head
+    at H = 16. Every output, lse, source gradient, dq and dg against the
+    oracle."""
+    _, wl = W
+    cfg = small(wl, "ring", T=7919, d=1280, H=H, dtype=dtype, M=40, sites=(40,))
+    run_and_compare(W, orc, cfg, H, q_std=0.3, g_kind="random")
+
+
+FULL_SIZE = [("1B", 8), ("1B", 1), ("1B", 4), ("1B", 16), ("350M", None), ("100M", None)]
+
+
+@pytest.mark.parametrize("name,heads", FULL_SIZE,
+                         ids=[f"{n}-H{h}" if h else n for n, h in FULL_SIZE])
+def test_full_size_sampled_tokens(W, orc, name, heads):
     """The 1B / 350M / 100M-shaped microbatches at full size (T=16384; d=1280 /
-    1024 / 512; 73 / 49 / 25 sites), in the launch configuration the benchmark
-    times (appends fused into the forward where the kernels allow): the cached
-    inverse RMS, outputs, lse and source gradients of 48 sampled tokens
-    against the oracle, dq/dg of the last site (every source, all tokens)
-    against the oracle in token chunks."""
+    1024 / 512; 73 / 49 / 25 sites), the 1B shape at every head count of its
+    sweep (H = 1, 4, 8, 16 on the same bank), in the launch configuration the
+    benchmark times (appends fused into the forward where the kernels allow):
+    the cached inverse RMS, outputs, lse and source gradients of 48 sampled
+    tokens against the oracle, dq/dg of the last site (every source, all
+    tokens) against the oracle in token chunks. The oracle's source rows are
+    drawn again from the seeded generator, not read back from the bank."""
     import torch
     from oracle import inv_rms
     _, wl = W
     cfg = wl.CONFIGS[name]
+    H = heads or cfg.H
     inputs = synth.DeviceInputs(seed=11, q_std=0.3, g_kind="random")
-    mb = wl.Microbatch(cfg, cfg.H, inputs)
+    mb = wl.Microbatch(cfg, H, inputs)
     mb.step()
     torch.cuda.synchronize()
-    T, d, H = cfg.T, cfg.d, cfg.H
+    assert mb.plan.acc_from == [-1] * len(mb.plan.acc_from)      # full routing: rows as drawn
+    T, d = cfg.T, cfg.d
     rng = np.random.default_rng(0)
     toks = np.sort(rng.choice(T, size=48, replace=False))
     toks[0], toks[-1] = 0, T - 1
     ti = torch.as_tensor(toks, device="cuda")
-    rows = [to64(mb.bank.rows[j][ti]) for j in range(mb.n_rows)]
+
+    def drawn(j, sl):
+        return to64(inputs.output(j, T, d, cfg.dtype)[sl])
+
+    rows = [drawn(j, ti) for j in range(mb.n_rows)]
+    for j in range(mb.n_rows):                                   # the bank keeps them unchanged
+        assert np.array_equal(to64(mb.bank.rows[j][ti]), rows[j]), j
     inv = to64(mb.bank.inv_rms()[ti])
     for j in range(mb.n_rows):
         ref = inv_rms(rows[j])
@@ -544,7 +574,7 @@ def test_full_size_sampled_tokens(W, orc, name):
     dg = np.zeros(d)
     for t0 in range(0, T, 2048):
         sl = slice(t0, min(T, t0 + 2048))
-        src = [to64(mb.bank.rows[j][sl]) for j in mb.plan.sites[s]]
+        src = [drawn(j, sl) for j in mb.plan.sites[s]]
         _, a, b = orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][sl]), H)
         dq += a
         dg += b
@@ -572,13 +602,10 @@ def test_full_size_lr_block_sampled_tokens(W, orc):
     toks[0], toks[-1] = 0, T - 1
     ti = torch.as_tensor(toks, device="cuda")
     oplan = schedule.block_plan(cfg.M, cfg.NB)
-    outs = [to64((mb.outputs[j] if j in mb.outputs else mb.bank.rows[j])[ti])
-            for j in range(mb.n_rows)]
-    # rows stored as is are the producer's outputs; partial sums are recomputed
-    outs_raw = []
-    for j in range(mb.n_rows):
-        outs_raw.append(outs[j])
-    rows = storage.block_bank(outs_raw, oplan, "bf16")
+    # the sublayer outputs drawn again from the seeded generator (not read
+    # back from the bank); the oracle forms the partial sums itself
+    outs = [to64(inputs.output(j, T, d, "bf16")[ti]) for j in range(mb.n_rows)]
+    rows = storage.block_bank(outs, oplan, "bf16")
     for j in range(mb.n_rows):
         assert np.array_equal(to64(mb.bank.rows[j][ti]), rows[j]), j
     tol = TOL["bf16"]
@@ -599,7 +626,9 @@ def test_full_size_lr_block_sampled_tokens(W, orc):
     dg = np.zeros(r)
     for t0 in range(0, T, 1024):
         sl = slice(t0, min(T, t0 + 1024))
-        src = [to64(mb.bank.rows[j][sl]) for j in mb.plan.sites[s]]
+        outs_sl = [to64(inputs.output(j, T, d, "bf16")[sl]) for j in range(mb.n_rows)]
+        rows_sl = storage.block_bank(outs_sl, oplan, "bf16")
+        src = [rows_sl[j] for j in mb.plan.sites[s]]
         _, a, b = orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][sl]), H, r=r)
         dq += a
         dg += b

@@ -427,3 +427,37 @@ def test_lse_merge_of_disjoint_source_sets(orc):
     wb = np.repeat(np.exp(lb - lse), K, axis=1)
     assert _nmax(lse, l) < 1e-14
     assert _nmax(wa * oa + wb * ob, o) < 1e-13
+
+
+@pytest.mark.parametrize("N,T,d,H,r,fw", [(5, 17, 64, 4, 64, False), (9, 11, 96, 2, 32, False),
+                                          (4, 13, 64, 8, 32, True), (1, 7, 32, 1, 32, False)])
+def test_float32_build_agrees_with_float64(orc, N, T, d, H, r, fw):
+    """The float32 build (the same C source compiled with -DORC_FLOAT, which
+    the benchmark times as the CPU baseline) against the float64 reference
+    pinned above: forward, lse, every source gradient, dq and dg within the
+    fp32 bound of the parity suite. The float32 library really computes in
+    float32 (its type size is checked on load), so its results differ from
+    the float64 ones, but only by rounding."""
+    srcs, q, g, G = _case(13, N, T, d, H, r)
+    srcs32 = [s.astype(np.float32) for s in srcs]
+    out64, lse64 = orc.route_fwd(srcs32, q.astype(np.float32), g.astype(np.float32), H, r=r,
+                                 full_width=fw)
+    out32, lse32 = orc.route_fwd(srcs32, q, g, H, r=r, full_width=fw, precision="f32")
+    assert out32.dtype == np.float32 and lse32.dtype == np.float32
+
+    def nmax(x, ref):
+        return float(np.max(np.abs(x.astype(np.float64) - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+    assert nmax(out32, out64) < 1e-5 and nmax(lse32, lse64) < 1e-5
+    assert 0 < nmax(out32, out64) or N == 1        # rounding differs: a real float32 build
+    ds64, dq64, dg64 = orc.route_bwd(srcs32, q.astype(np.float32), g.astype(np.float32),
+                                     G.astype(np.float32), H, r=r, full_width=fw)
+    ds32, dq32, dg32 = orc.route_bwd(srcs32, q, g, G, H, r=r, full_width=fw, precision="f32")
+    for a, b in zip(ds32, ds64):
+        assert nmax(a, b) < 1e-5
+    if N > 1:
+        assert nmax(dq32, dq64) < 1e-5 and nmax(dg32, dg64) < 1e-5
+    else:
+        assert np.all(dq32 == 0) and np.all(dg32 == 0)
+    inv32 = orc.inv_rms(srcs32[0], r=r, full_width=fw, precision="f32")
+    assert nmax(inv32, orc.inv_rms(srcs32[0], r=r, full_width=fw)) < 1e-6
