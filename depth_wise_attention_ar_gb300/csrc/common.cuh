@@ -18,8 +18,17 @@ constexpr float kLn2 = 0.6931471805599453f;
 // moved when a score exceeds it by more than this, so the exponentials stay
 // below 2^8 and most sources skip the rescale of the accumulator.
 constexpr float kRescaleTau = 8.0f;
-// Bound on mbarrier polls before a wait is declared lost (no device trap).
-constexpr uint32_t kWaitLimit = 1u << 24;
+// Suspend-time hint of one mbarrier poll, in ns: a waiting thread sleeps until
+// the phase completes or this much time has passed, instead of coming back at
+// once and spinning on the poll (1B forward phase 18.57 -> 18.39 ms; the
+// length of the hint made no difference between 10 us and 1 ms).
+constexpr uint32_t kPollSuspendNs = 10000;
+// Bound on mbarrier polls before a wait is declared lost (no device trap):
+// about 1.3 s when every poll sleeps its whole hint.
+constexpr uint32_t kWaitLimit = 1u << 17;
+// Bound on the polls per stage when, after a lost wait, a warp waits for its
+// copies still in flight before it leaves.
+constexpr uint32_t kDrainLimit = 1u << 12;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -82,10 +91,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kPollSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -191,9 +200,47 @@ __device__ __forceinline__ void st_chunk_g(float *p, const float v[8])
     reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// ---- packed fp32 pairs ---------------------------------------------------------
+// sm_100-class GPUs execute two fp32 multiplies or FMAs as one f32x2
+// instruction; each lane is rounded exactly as __fmul_rn / fmaf round, so the
+// packed forms below give the bits of the scalar code they replace, with half
+// the instructions. Elements e and e + 4 of a chunk share a pair (the two
+// halves of the dot product below run side by side).
+__device__ __forceinline__ uint64_t pk2(float x, float y)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &x, float &y)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// y[e] = fmaf(a, x[e], y[e]) for the 8 elements of a chunk.
+__device__ __forceinline__ void axpy8(float a, const float x[8], float y[8])
+{
+    const uint64_t aa = pk2(a, a);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) upk2(fma2(aa, pk2(x[e], x[e + 4]), pk2(y[e], y[e + 4])), y[e], y[e + 4]);
+}
+
 // Dot product of two 8-element chunks as (low half) + (high half), each half
-// a fixed chain. Exchanging the halves (lane-swapped order below) gives the
-// same bits, because the final addition commutes exactly.
+// a fixed chain (a product, then three FMAs in element order). Exchanging the
+// halves (lane-swapped order below) gives the same bits, because the final
+// addition commutes exactly.
 __device__ __forceinline__ float dot8(const float a[8], const float b[8])
 {
     float lo = __fmul_rn(a[0], b[0]);
@@ -204,6 +251,19 @@ __device__ __forceinline__ float dot8(const float a[8], const float b[8])
     hi = fmaf(a[5], b[5], hi);
     hi = fmaf(a[6], b[6], hi);
     hi = fmaf(a[7], b[7], hi);
+    return __fadd_rn(lo, hi);
+}
+
+// dot8 with its two chains run as one packed chain: the same bits in half the
+// multiply-add instructions. (Used by the forwards; in the backward kernels
+// the packed forms measured slower: 1B backward 90.0 -> 91.2 ms.)
+__device__ __forceinline__ float dot8p(const float a[8], const float b[8])
+{
+    uint64_t s = mul2(pk2(a[0], a[4]), pk2(b[0], b[4]));
+#pragma unroll
+    for (int e = 1; e < 4; ++e) s = fma2(pk2(a[e], a[e + 4]), pk2(b[e], b[e + 4]), s);
+    float lo, hi;
+    upk2(s, lo, hi);
     return __fadd_rn(lo, hi);
 }
 

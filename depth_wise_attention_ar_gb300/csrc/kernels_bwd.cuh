@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     if (!ok) {
         if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
         for (int64_t j = i; j < issued; ++j) {
-            mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+            mbar_wait(&bars[slot], (phase >> slot) & 1u, kDrainLimit);
             phase ^= 1u << slot;
             if (++slot == S) slot = 0;
         }

@@ -340,12 +340,12 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         if (threadIdx.x == 0) {
             report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
             for (int64_t j = i; j < issued; ++j) {
-                mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+                mbar_wait(&bars[slot], (phase >> slot) & 1u, kDrainLimit);
                 phase ^= 1u << slot;
                 if (++slot == S) slot = 0;
             }
             // a per-token row still in flight (the current token's)
-            if (tok_row) mbar_wait(&pbars[tpar], (pphase >> tpar) & 1u, 1u << 16);
+            if (tok_row) mbar_wait(&pbars[tpar], (pphase >> tpar) & 1u, kDrainLimit);
         }
     }
 }
@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         if (threadIdx.x == 0) {
             report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
             for (int64_t j = i; j < issued; ++j) {
-                mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+                mbar_wait(&bars[slot], (phase >> slot) & 1u, kDrainLimit);
                 phase ^= 1u << slot;
                 if (++slot == S) slot = 0;
             }

@@ -51,6 +51,7 @@ namespace ar {
 constexpr int kFwdWarps = 4;
 constexpr int kFwdStages = 4;
 
+
 // Sliced keys on rows of 2048 columns or more: three stages per warp, so that
 // three blocks fit in shared memory (more warps for the same token count).
 __host__ __device__ constexpr int fwd_stages(bool sk, int cpl)
@@ -78,6 +79,10 @@ template <typename T, int CPL, bool SK, bool FRESH, int KM>
 __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
 {
     static_assert(SK || KM == CPL, "full keys: a lane's key chunks are its value chunks");
+    // packed fp32 pairs for the score and the mix (same bits): measured faster
+    // on full-key rows of 1280 columns and more (1B forward phase 18.54 ->
+    // 17.87 ms), slightly slower on 1024 (350M 7.41 -> 7.45 ms)
+    constexpr bool kPacked = !SK && CPL >= 5;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     constexpr int S = fwd_stages(SK, CPL);
@@ -205,7 +210,7 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
-                zr = __fadd_rn(zr, dot8(qg[j], v[j]));
+                zr = __fadd_rn(zr, kPacked ? dot8p(qg[j], v[j]) : dot8(qg[j], v[j]));
             }
         }
         zr = group_sum(zr, LPH);
@@ -254,6 +259,8 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
                 ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), vv);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, vv[e], acc[j][e]);
+            } else if constexpr (kPacked) {
+                axpy8(p, v[j], acc[j]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, v[j][e], acc[j][e]);
@@ -280,7 +287,7 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
     if (!ok) {
         if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
         // wait briefly for this warp's copies still in flight, then leave
-        const uint32_t drain = a.wait_limit ? a.wait_limit : 1u << 16;
+        const uint32_t drain = a.wait_limit ? a.wait_limit : kDrainLimit;
         for (int64_t j = i; j < issued; ++j) {
             mbar_wait(&bars[slot], (phase >> slot) & 1u, drain);
             phase ^= 1u << slot;
@@ -319,8 +326,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32, fwd_min_blocks(sizeof(T) == 2,
 // backward's reduction tree, so the recomputed score keeps the forward's
 // bits. Odd heads take their two backward lanes' chunks in the other order,
 // so that the two head groups of a quarter-warp read different bank groups.
-template <typename T, int CPL, bool FRESH = false>
-__global__ void __launch_bounds__(kFwdWarps * 32)
+template <typename T, int CPL, bool FRESH = false, int NG = AR_MAX_SOURCES / 32, int MINB = 1>
+__global__ void __launch_bounds__(kFwdWarps * 32, MINB)
     route_fwd_pair_kernel(const __grid_constant__ RouteArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -396,14 +403,15 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     };
     for (int s = 0; s < S && issued < total; ++s) issue_next();
 
-    // inverse RMS of the next pair's sources, prefetched into registers
-    float pre_inv[2][AR_MAX_SOURCES / 32];
+    // inverse RMS of the next pair's sources, prefetched into registers (NG
+    // groups of 32 sources: one group for sites of at most 32 sources)
+    float pre_inv[2][NG];
     auto prefetch_inv = [&](int64_t u) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int64_t t = u * 2 + k;
 #pragma unroll
-            for (int v = 0; v < AR_MAX_SOURCES / 32; ++v) {
+            for (int v = 0; v < NG; ++v) {
                 const int nn = lane + 32 * v;
                 if (nn < N && t < TT) pre_inv[k][v] = __ldg(a.inv + t * a.inv_ld + s_rows[nn]);
             }
@@ -423,7 +431,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
 #pragma unroll
             for (int k = 0; k < 2; ++k)
 #pragma unroll
-                for (int v = 0; v < AR_MAX_SOURCES / 32; ++v) {
+                for (int v = 0; v < NG; ++v) {
                     const int nn = lane + 32 * v;
                     if (nn < N) inv_warp[k * AR_MAX_SOURCES + nn] = pre_inv[k][v];
                 }
@@ -442,8 +450,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
 #pragma unroll
         for (int j = 0; j < NC; ++j) {
             ld_chunk_s(reinterpret_cast<const T *>(buf + cidx[j] * CB), v[j]);
-            if (j < CPL) z0 = __fadd_rn(z0, dot8(qg[j], v[j]));
-            else z1 = __fadd_rn(z1, dot8(qg[j], v[j]));
+            if (j < CPL) z0 = __fadd_rn(z0, dot8p(qg[j], v[j]));
+            else z1 = __fadd_rn(z1, dot8p(qg[j], v[j]));
         }
         const float zr = __fadd_rn(group_sum(z0, LPH), group_sum(z1, LPH));
         float ivn = cur_inv[n];
@@ -483,9 +491,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
         const float p = exp2f((z - m) * kLog2e);
         l += p;
 #pragma unroll
-        for (int j = 0; j < NC; ++j)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(p, v[j][e], acc[j][e]);
+        for (int j = 0; j < NC; ++j) axpy8(p, v[j], acc[j]);
         __syncwarp();
         if (issued < total) issue_next();
 
@@ -510,31 +516,42 @@ __global__ void __launch_bounds__(kFwdWarps * 32)
     if (!ok) {
         if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
         for (int64_t j = i; j < issued; ++j) {
-            mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+            mbar_wait(&bars[slot], (phase >> slot) & 1u, kDrainLimit);
             phase ^= 1u << slot;
             if (++slot == S) slot = 0;
         }
     }
 }
 
-template <typename T, int CPL, bool FRESH>
+template <typename T, int CPL, bool FRESH, int NG, int MINB>
 cudaError_t launch_fwd_pair_inst(const RouteArgs &a, cudaStream_t s)
 {
-    const void *k = reinterpret_cast<const void *>(&route_fwd_pair_kernel<T, CPL, FRESH>);
+    const void *k = reinterpret_cast<const void *>(&route_fwd_pair_kernel<T, CPL, FRESH, NG, MINB>);
     const size_t smem = (size_t)kFwdWarps * kFwdStages * 2 * a.d * sizeof(T) +
                         (size_t)kFwdWarps * kFwdStages * 8 +
                         (size_t)kFwdWarps * 2 * AR_MAX_SOURCES * 4;
     int grid = 0;
     cudaError_t e = persistent_grid(k, kFwdWarps * 32, smem, &grid);
     if (e != cudaSuccess) return e;
-    route_fwd_pair_kernel<T, CPL, FRESH><<<grid, kFwdWarps * 32, smem, s>>>(a);
+    route_fwd_pair_kernel<T, CPL, FRESH, NG, MINB><<<grid, kFwdWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+// Sites of at most 32 sources prefetch one inverse RMS per token and lane
+// (100M forward phase 1.31 -> 1.23 ms with the suspend hint of the waits; a
+// bound of four resident blocks, 128 registers with a small spill, measured
+// slower than three).
+template <typename T, int CPL, bool FRESH>
+cudaError_t launch_fwd_pair_n(const RouteArgs &a, cudaStream_t s)
+{
+    if (a.n_src <= 32) return launch_fwd_pair_inst<T, CPL, FRESH, 1, 1>(a, s);
+    return launch_fwd_pair_inst<T, CPL, FRESH, AR_MAX_SOURCES / 32, 1>(a, s);
 }
 
 template <typename T, int CPL>
 cudaError_t launch_fwd_pair(const RouteArgs &a, cudaStream_t s)
 {
-    return a.fresh1 ? launch_fwd_pair_inst<T, CPL, true>(a, s) : launch_fwd_pair_inst<T, CPL, false>(a, s);
+    return a.fresh1 ? launch_fwd_pair_n<T, CPL, true>(a, s) : launch_fwd_pair_n<T, CPL, false>(a, s);
 }
 
 template <typename T, int CPL, bool SK, bool FRESH, int KM = CPL>

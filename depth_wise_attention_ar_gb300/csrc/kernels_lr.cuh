@@ -228,12 +228,12 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
     if (!ok) {
         if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
         for (int64_t j = consumed; j < issued; ++j) {
-            mbar_wait(&rbar[slot], (rphase >> slot) & 1u, 1u << 16);
+            mbar_wait(&rbar[slot], (rphase >> slot) & 1u, kDrainLimit);
             rphase ^= 1u << slot;
             if (++slot == S) slot = 0;
         }
-        mbar_wait(&kbar[0], kphase & 1u, 1u << 16);
-        mbar_wait(&kbar[1], (kphase >> 1) & 1u, 1u << 16);
+        mbar_wait(&kbar[0], kphase & 1u, kDrainLimit);
+        mbar_wait(&kbar[1], (kphase >> 1) & 1u, kDrainLimit);
     }
 }
 
@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
     if (!ok) {
         if (lane == 0) report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
         for (int64_t j = i; j < issued; ++j) {
-            mbar_wait(&bars[slot], (phase >> slot) & 1u, 1u << 16);
+            mbar_wait(&bars[slot], (phase >> slot) & 1u, kDrainLimit);
             phase ^= 1u << slot;
             if (++slot == S) slot = 0;
         }

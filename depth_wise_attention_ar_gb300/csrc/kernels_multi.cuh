@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kMultiThreads)
         report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
         // wait briefly for the copies still in flight, then leave
         for (int k = 0; k < nbuf; ++k) {
-            mbar_wait(&bars[b], (phase >> b) & 1u, 1u << 16);
+            mbar_wait(&bars[b], (phase >> b) & 1u, kDrainLimit);
             phase ^= 1u << b;
             if (++b == nbuf) b = 0;
         }

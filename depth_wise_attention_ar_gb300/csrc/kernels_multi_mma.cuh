@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kMmaThreads)
     if (!ok && tid == 0) {
         report_error(a.err, AR_DEVERR_WAIT_TIMEOUT);
         for (int k = 0; k < nbuf; ++k) {
-            mbar_wait(&bars[b], (phase >> b) & 1u, 1u << 16);
+            mbar_wait(&bars[b], (phase >> b) & 1u, kDrainLimit);
             phase ^= 1u << b;
             if (++b == nbuf) b = 0;
         }
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kMsThreads, 2)
                     s2 = S - 1;
                     --r2;
                 }
-                mbar_wait(&full[s2], (uint32_t)(r2 & 1), 1u << 16);
+                mbar_wait(&full[s2], (uint32_t)(r2 & 1), kDrainLimit);
             }
         }
         return;

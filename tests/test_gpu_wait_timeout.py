@@ -46,7 +46,16 @@ def test_lost_copy_wait_runs_out_and_reports_timeout(B, orc):
     B.ar_device_status()                       # a clean error word to start from
     out = torch.full((T, d), 7.0, dtype=torch.bfloat16, device="cuda")
     lse = torch.full((T, H), 7.0, device="cuda")
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
     B.ar_route_fwd_lost_copies(bank.handle, rows, H, q, g, out, lse, 2000)
+    t1.record()
+    torch.cuda.synchronize()
+    # bounded: at most 2000 polls for the lost wait and per armed stage, each
+    # sleeping at most the kernels' suspend hint (10 us)
+    ms = t0.elapsed_time(t1)
+    print(f"lost-copy forward: {ms:.2f} ms")
+    assert ms < 1000.0
     with pytest.raises(B.ARError) as e:
         B.ar_device_status()
     assert e.value.name == "AR_ERR_TIMEOUT"
