@@ -51,8 +51,9 @@ def parse():
     p.add_argument("--config", default="1B")
     p.add_argument("--heads", type=int, default=None)
     p.add_argument("--tokens", type=int, default=None, help="override T (profiling cases)")
-    p.add_argument("--sites", choices=["all", "last"], default="all",
-                   help="run every routing site, or only the last one (profiling cases)")
+    p.add_argument("--sites", default="all",
+                   help="all: every routing site; last: only the last one; an integer k: "
+                        "only site k (profiling cases)")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target wall time of the CPU-oracle sample")
@@ -244,6 +245,11 @@ def config_of(args, workload):
         cfg = dataclasses.replace(cfg, T=args.tokens)
     if args.sites == "last":
         cfg = dataclasses.replace(cfg, sites=(cfg.M,))
+    elif args.sites != "all":
+        k = int(args.sites)
+        if not 0 <= k <= cfg.M:
+            raise SystemExit(f"--sites {k}: the workload has sites 0..{cfg.M}")
+        cfg = dataclasses.replace(cfg, sites=(k,))
     return cfg
 
 

@@ -118,6 +118,17 @@ __device__ __forceinline__ void report_error(unsigned int *err, unsigned int bit
     if (err) atomicOr(err, bits);
 }
 
+
+// 16-byte asynchronous copy global -> shared by one thread (completes at this
+// thread's next cp_async_wait_all); both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---- 8-element chunks ------------------------------------------------------
 // A chunk is 8 consecutive elements of a row: 16 bytes in bf16, 32 in fp32.
 

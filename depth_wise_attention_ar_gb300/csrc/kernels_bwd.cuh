@@ -47,10 +47,18 @@ namespace ar {
 constexpr int kBwdWarps = 4;
 constexpr int kBwdStages = 3;
 
+// Rows of 768 and 1024 columns fetch the next token's dL/dout and output rows
+// into shared memory (cp.async, each lane its own chunks) while the current
+// token runs: 350M backward phase 33.39 -> 33.17 ms. On rows of 512 columns
+// it measured slower (100M 4.63 -> 4.67 ms), and from 1280 columns on the
+// buffer would cost the second resident block.
+__host__ __device__ constexpr bool bwd_token_prefetch(int cpl) { return cpl == 3 || cpl == 4; }
+
 inline size_t bwd_smem_bytes(int d, size_t esize)
 {
     return (size_t)kBwdWarps * kBwdStages * ((size_t)d * esize + (size_t)d * 4) +
-           (size_t)kBwdWarps * kBwdStages * 8 + (size_t)kBwdWarps * AR_MAX_SOURCES * 4;
+           (size_t)kBwdWarps * kBwdStages * 8 + (size_t)kBwdWarps * AR_MAX_SOURCES * 4 +
+           (bwd_token_prefetch(d / 256) ? (size_t)kBwdWarps * 2 * d * esize : 0);
 }
 
 template <typename T, int CPL>
@@ -84,6 +92,10 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     unsigned char *ring = rings + (size_t)warp * S * slot_bytes;
     uint64_t *bars = bars_all + warp * S;
     float *cur_inv = inv_all + warp * AR_MAX_SOURCES;
+    // this warp's token buffer (rows of 768 or 1024 columns): the next token's
+    // dL/dout row, then its output row, fetched by each lane for its own
+    // chunks while the current token runs (unused, and not allocated, otherwise)
+    T *tbuf = reinterpret_cast<T *>(inv_all + kBwdWarps * AR_MAX_SOURCES) + (size_t)warp * 2 * d;
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -142,6 +154,24 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) U[j][e] = 0.f;
 
+    constexpr int kPieces = CB / 16;   // 16-byte pieces per chunk
+    constexpr bool kTokPf = bwd_token_prefetch(CPL);
+    auto fetch_token = [&](int64_t t) {
+        if constexpr (!kTokPf) return;
+        const T *grow = static_cast<const T *>(a.dout) + t * d;
+        const T *orow = static_cast<const T *>(a.fout) + t * d;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int k = 0; k < kPieces; ++k) {
+                const int off = cidx[j] * 8 + k * (16 / (int)sizeof(T));
+                cp_async16(tbuf + off, grow + off);
+                cp_async16(tbuf + d + off, orow + off);
+            }
+        cp_async_commit();
+    };
+    if (hi > lo) fetch_token(gw);
+
     float G[CPL][8];
     float S_h = 0.f, lse_h = 0.f, dal = 0.f;
     const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
@@ -154,12 +184,18 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
             // token-level data: dL/dout, the coupling term S, lse, inverse RMS
             const T *grow = static_cast<const T *>(a.dout) + tok * d;
             const T *orow = static_cast<const T *>(a.fout) + tok * d;
+            if constexpr (kTokPf) cp_async_wait_all();
             float sp = 0.f, raw = 0.f;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float o[8];
-                ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
-                ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
+                if constexpr (kTokPf) {
+                    ld_chunk_s_sw(tbuf + cidx[j] * 8, sw, G[j]);
+                    ld_chunk_s_sw(tbuf + d + cidx[j] * 8, sw, o);
+                } else {
+                    ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
+                    ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
+                }
                 if (a.dalpha) raw = __fadd_rn(raw, dot8(G[j], o));
                 if (a.alpha) {
 #pragma unroll
@@ -168,6 +204,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
                 sp = __fadd_rn(sp, dot8(G[j], o));
             }
             S_h = group_sum(sp, LPH);
+            if (tok + GW < TT) fetch_token(tok + GW);      // this lane's chunks are read
             if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted by the warp owning (t, 0)
             lse_h = __ldg(a.lse + tok * H + h);
             __syncwarp();
