@@ -60,6 +60,10 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--eager", action="store_true", help="no CUDA graphs")
+    p.add_argument("--multi-read", type=int, metavar="Q", default=None,
+                   help="time ar_route_fwd_multi instead: Q queries read the largest site's row "
+                        "list of the workload in one pass (two-phase block inference, phase 1), "
+                        "against Q single reads")
     p.add_argument("--report", metavar="DIR", default=None,
                    help="run every workload (each in its own process) and write DIR/report.json "
                         "and DIR/report.md")
@@ -101,14 +105,19 @@ def kernel_hash(family: str = "full") -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(config: str, H: int):
-    """ncu DRAM bytes per backward launch, if measured on the current kernel source."""
+def measured_traffic(config: str, H: int, bytes_per_launch: float, T: int):
+    """DRAM bytes per backward launch at full size, from the small-case ncu
+    captures recorded in profiles/route_bwd_traffic.json: the launch's
+    algorithmic bytes, plus the forward output it reads per token (outside
+    the byte model), less the write tail those captures found still dirty in
+    L2 at the end of each launch. None when there is no record for the
+    workload or the kernel's code changed since it was taken."""
     try:
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)
+            rec = json.load(f)["configs"]
         e = rec.get(f"{config}/H{H}")
         if e and e.get("kernel_hash") == kernel_hash(e.get("family", "full")):
-            return e["bytes_per_launch"]
+            return bytes_per_launch + T * e["output_bytes_per_token"] - e["tail_bytes"]
     except (OSError, ValueError, KeyError):   # no record, or an unreadable one
         pass
     return None
@@ -310,6 +319,8 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args, rank, world)
+    if args.multi_read:
+        return multi_read(args)
 
     import torch
     import torch.distributed as dist
@@ -396,7 +407,7 @@ def main():
     achieved = bwd_bytes / (bwd_ms * 1e-3) / 1e9
     # the record holds the mean over every site of the full workload: another
     # token count or site selection is a different launch mix
-    traffic = (measured_traffic(args.config, H)
+    traffic = (measured_traffic(args.config, H, bwd_bytes / n_bwd, cfg.T)
                if args.sites == "all" and not args.tokens else None)
     line = {
         "metric": METRIC,
@@ -425,6 +436,11 @@ def main():
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "nominal_peak": NOMINAL_HBM_GBS, "traffic": traffic,
+                     "traffic_source": "ncu DRAM bytes of small-case backward launches "
+                                       "(profiles/route_bwd_traffic.json): the algorithmic "
+                                       "bytes per launch plus the forward output read per "
+                                       "token, less the write tail still in L2 at each "
+                                       "launch's end; null if the kernel changed since",
                      "launches_per_step": n_bwd,
                      "bytes_per_launch_avg": bwd_bytes / n_bwd,
                      "ms_per_launch_avg": bwd_ms / n_bwd,
@@ -594,6 +610,66 @@ def end_to_end(args, mb, stream, run_fwd, run_bwd, world, local):
             "copies": "H2D on its own stream, double-buffered: the next step's inputs stream "
                       "in while the current step computes; D2H of each step's packed dq/dg "
                       "after the step"}
+
+
+def multi_read(args):
+    """One JSON line: Q queries over one row list (the workload's largest site)
+    in one ar_route_fwd_multi launch, timed with CUDA events on its stream
+    (inputs larger than L2), against the same Q reads one site at a time."""
+    import torch
+
+    import synth
+    from depth_wise_attention_ar_gb300 import binding, workload
+
+    torch.cuda.set_device(0)
+    cfg = config_of(args, workload)
+    H = args.heads or cfg.H
+    Q = args.multi_read
+    plan = workload.make_plan(cfg)
+    rows = max((plan.sites[s] for s in plan.run_sites), key=len)
+    inputs = synth.DeviceInputs(seed=3)
+    bank = binding.Bank(cfg.T, cfg.d, cfg.r, max(rows) + 1, cfg.dtype, device="cuda")
+    for j in range(max(rows) + 1):
+        bank.append(inputs.output(j, cfg.T, cfg.d, cfg.dtype))
+    qs = [inputs.query(k, cfg.r) for k in range(Q)]
+    outs = [torch.empty((cfg.T, cfg.d), dtype=bank.torch_dtype, device="cuda") for _ in range(Q)]
+    lses = [torch.empty((cfg.T, H), dtype=torch.float32, device="cuda") for _ in range(Q)]
+    stream = torch.cuda.Stream()
+
+    def multi():
+        bank.route_fwd_multi(rows, H, qs, None, outs, lses, stream=stream)
+
+    def singles():
+        for k in range(Q):
+            binding.ar_route_fwd(bank.handle, rows, H, qs[k], None, outs[k], lses[k], k, stream)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record(stream)
+            for _ in range(args.steps):
+                fn()
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / args.steps
+
+    ms_multi, ms_single = timed(multi), timed(singles)
+    if binding.ar_device_error() != 0:
+        raise RuntimeError("device error word set")
+    b = 2 if cfg.dtype == "bf16" else 4
+    nbytes = cfg.T * (len(rows) * (cfg.d * b + 4) + Q * (cfg.d * b + 4 * H))
+    hbm, kind = peaks()
+    gbs = nbytes / (ms_multi * 1e-3) / 1e9
+    print(json.dumps({"metric": "multi-query read (ar_route_fwd_multi), ms per launch",
+                      "value": ms_multi, "unit": "ms", "higher_is_better": False,
+                      "config": {"workload": f"{cfg.name}-shaped rows", "T": cfg.T, "d": cfg.d,
+                                 "r": cfg.r, "H": H, "rows": len(rows), "queries": Q},
+                      "single_reads_ms": ms_single,
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                   "frac": gbs / hbm, "bytes_per_launch": nbytes,
+                                   "peak_source": kind}}), flush=True)
 
 
 def reference_arm(args, rank, world):
