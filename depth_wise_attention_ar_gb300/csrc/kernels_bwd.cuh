@@ -45,20 +45,20 @@
 namespace ar {
 
 constexpr int kBwdWarps = 4;
-constexpr int kBwdStages = 3;
-
-// Rows of 768 and 1024 columns fetch the next token's dL/dout and output rows
-// into shared memory (cp.async, each lane its own chunks) while the current
-// token runs: 350M backward phase 33.39 -> 33.17 ms. On rows of 512 columns
-// it measured slower (100M 4.63 -> 4.67 ms), and from 1280 columns on the
-// buffer would cost the second resident block.
-__host__ __device__ constexpr bool bwd_token_prefetch(int cpl) { return cpl == 3 || cpl == 4; }
+// Two stages of (source row + fp32 gradient row) per warp, plus a per-warp
+// buffer into which each lane fetches its own chunks of the next token's
+// dL/dout and forward-output rows by cp.async while the current token's items
+// run, so a token's first item does not wait on DRAM for them. Against three
+// stages and plain loads of the token rows: 1B backward phase 90.54 -> 89.65
+// ms, 350M 33.13 -> 32.53 ms, 100M 4.63 -> 4.53 ms (three stages with the
+// buffer were slower on 512-wide rows).
+constexpr int kBwdStages = 2;
 
 inline size_t bwd_smem_bytes(int d, size_t esize)
 {
     return (size_t)kBwdWarps * kBwdStages * ((size_t)d * esize + (size_t)d * 4) +
            (size_t)kBwdWarps * kBwdStages * 8 + (size_t)kBwdWarps * AR_MAX_SOURCES * 4 +
-           (bwd_token_prefetch(d / 256) ? (size_t)kBwdWarps * 2 * d * esize : 0);
+           (size_t)kBwdWarps * 2 * d * esize;
 }
 
 template <typename T, int CPL>
@@ -92,9 +92,8 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     unsigned char *ring = rings + (size_t)warp * S * slot_bytes;
     uint64_t *bars = bars_all + warp * S;
     float *cur_inv = inv_all + warp * AR_MAX_SOURCES;
-    // this warp's token buffer (rows of 768 or 1024 columns): the next token's
-    // dL/dout row, then its output row, fetched by each lane for its own
-    // chunks while the current token runs (unused, and not allocated, otherwise)
+    // this warp's token buffer: the next token's dL/dout row, then its output
+    // row, fetched by each lane for its own chunks while the current token runs
     T *tbuf = reinterpret_cast<T *>(inv_all + kBwdWarps * AR_MAX_SOURCES) + (size_t)warp * 2 * d;
     if (lane == 0) {
 #pragma unroll
@@ -155,9 +154,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
         for (int e = 0; e < 8; ++e) U[j][e] = 0.f;
 
     constexpr int kPieces = CB / 16;   // 16-byte pieces per chunk
-    constexpr bool kTokPf = bwd_token_prefetch(CPL);
     auto fetch_token = [&](int64_t t) {
-        if constexpr (!kTokPf) return;
         const T *grow = static_cast<const T *>(a.dout) + t * d;
         const T *orow = static_cast<const T *>(a.fout) + t * d;
 #pragma unroll
@@ -182,20 +179,13 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     for (; i < hi; ++i) {
         if (i == lo || n == 0) {
             // token-level data: dL/dout, the coupling term S, lse, inverse RMS
-            const T *grow = static_cast<const T *>(a.dout) + tok * d;
-            const T *orow = static_cast<const T *>(a.fout) + tok * d;
-            if constexpr (kTokPf) cp_async_wait_all();
+            cp_async_wait_all();
             float sp = 0.f, raw = 0.f;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float o[8];
-                if constexpr (kTokPf) {
-                    ld_chunk_s_sw(tbuf + cidx[j] * 8, sw, G[j]);
-                    ld_chunk_s_sw(tbuf + d + cidx[j] * 8, sw, o);
-                } else {
-                    ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
-                    ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
-                }
+                ld_chunk_s_sw(tbuf + cidx[j] * 8, sw, G[j]);
+                ld_chunk_s_sw(tbuf + d + cidx[j] * 8, sw, o);
                 if (a.dalpha) raw = __fadd_rn(raw, dot8(G[j], o));
                 if (a.alpha) {
 #pragma unroll

@@ -34,11 +34,17 @@ namespace ar {
 
 constexpr int kCoopWarps = 4;
 constexpr int kCoopFwdStages = 4;
-// Backward stages of (row + fp32 gradient row). Sliced keys use more
-// registers (two blocks per SM at most), so with bf16 rows they take 4 stages
-// and two blocks of d = 4096 still fit; full keys keep 3, which leaves room
-// for three blocks.
-constexpr int coop_bwd_stages(size_t esize, bool lr) { return esize == 2 && lr ? 4 : 3; }
+// Backward stages of (row + fp32 gradient row), and with bf16 rows a block
+// buffer (2 d b bytes) into which each thread fetches its own chunks of the
+// next token's dL/dout and output rows by cp.async while the current token
+// runs. Sliced keys (two blocks per SM at most, by registers) take 3 stages
+// and the buffer; full keys take 2 and the buffer, which leaves room for three
+// blocks of d = 4096. Against 4 stages (sliced) and 3 stages (full) with an L2
+// prefetch of the next token's rows: low-rank block backward 19.00 -> 18.92
+// ms, delta 8B 20.47 -> 19.54 ms. (4 stages and the buffer left one block per
+// SM: 28.9 ms.)
+constexpr int coop_bwd_stages(size_t esize, bool lr) { return esize == 2 ? (lr ? 3 : 2) : 3; }
+constexpr bool coop_bwd_tokbuf(size_t esize) { return esize == 2; }
 
 struct CoopMap {
     int Hw, LPH, hl, sub, h;      // value heads per warp, lanes per head, local head, lane in head, head
@@ -353,7 +359,8 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
 inline size_t coop_bwd_smem_bytes(int d, size_t esize, bool lr)
 {
     const size_t S = (size_t)coop_bwd_stages(esize, lr);
-    return S * ((size_t)d * esize + (size_t)d * 4) + S * 8 + 3 * 2 * 32 * 4;
+    const size_t base = S * ((size_t)d * esize + (size_t)d * 4) + S * 8 + 3 * 2 * 32 * 4;
+    return coop_bwd_tokbuf(esize) ? (base + 15) / 16 * 16 + 2 * (size_t)d * esize : base;
 }
 
 template <typename T, int CPL, bool LR>
@@ -378,6 +385,8 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     float *zsm = reinterpret_cast<float *>(bars + S);  // [2][32] raw scores (sliced keys)
     float *dzs = zsm + 64;                              // [2][32] dz per head (sliced keys)
     float *cws = dzs + 64;                              // [2][32] per-warp coupling sums
+    constexpr bool kTok = coop_bwd_tokbuf(sizeof(T));
+    T *tbuf = reinterpret_cast<T *>(smem + ((size_t)S * slot_bytes + S * 8 + 3 * 2 * 32 * 4 + 15) / 16 * 16);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
@@ -432,6 +441,19 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     };
     for (int s = 0; s < S && issued < hi; ++s) issue_next();
 
+    auto fetch_token = [&](int64_t t) {
+        const T *grow = static_cast<const T *>(a.dout) + t * d;
+        const T *orow = static_cast<const T *>(a.fout) + t * d;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int off = cidx[j] * 8;
+            cp_async16(tbuf + off, grow + off);
+            cp_async16(tbuf + d + off, orow + off);
+        }
+        cp_async_commit();
+    };
+    if (kTok && hi > lo) fetch_token(gb);
+
     float G[CPL][8];
     float S_h = 0.f, lse_h = 0.f, dal = 0.f;
     const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
@@ -443,16 +465,22 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         if (i == lo || n == 0) {
             const T *grow = static_cast<const T *>(a.dout) + tok * d;
             const T *orow = static_cast<const T *>(a.fout) + tok * d;
-            if (threadIdx.x == 0 && tok + GB < TT) {  // this block's next token's rows, into L2
+            if (!kTok && threadIdx.x == 0 && tok + GB < TT) {  // next token's rows, into L2
                 prefetch_l2(grow + GB * d, vbytes);
                 prefetch_l2(orow + GB * d, vbytes);
             }
+            if (kTok) cp_async_wait_all();
             float sp = 0.f, raw = 0.f;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float o[8];
-                ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
-                ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
+                if (kTok) {
+                    ld_chunk_s_sw(tbuf + cidx[j] * 8, sw, G[j]);
+                    ld_chunk_s_sw(tbuf + d + cidx[j] * 8, sw, o);
+                } else {
+                    ld_chunk_g_sw(grow + cidx[j] * 8, sw, G[j]);
+                    ld_chunk_g_sw(orow + cidx[j] * 8, sw, o);
+                }
                 if (a.dalpha) raw = __fadd_rn(raw, dot8(G[j], o));
                 if (a.alpha) {
 #pragma unroll
@@ -461,6 +489,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                 sp = __fadd_rn(sp, dot8(G[j], o));
             }
             S_h = group_sum(sp, mp.LPH);
+            if (kTok && tok + GB < TT) fetch_token(tok + GB);   // this thread's chunks are read
             if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted once
             lse_h = __ldg(a.lse + tok * H + mp.h);
         }
