@@ -252,3 +252,30 @@ def test_binding_refuses_to_import_without_the_library(tmp_path):
                            env={**os.environ, "PYTHONPATH": str(tmp_path)})
         assert p.returncode != 0
         assert "ImportError" in p.stderr and "is not built" in p.stderr
+
+
+def test_noalloc_scratch_size_is_reported_by_the_library(B):
+    """The no-alloc backward's fixed scratch size comes from the library (the
+    header's AR_NOALLOC_SCRATCH_BYTES), so callers and tests need no copy of it."""
+    assert B.ar_noalloc_scratch_bytes() == 8 << 20
+    txt = open(HEADER).read()
+    assert "#define AR_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)" in txt
+
+
+def test_device_status_without_gpu(B):
+    """Reading the device error word needs a device: without one the call
+    reports AR_ERR_CUDA (and never AR_ERR_TIMEOUT)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this check needs a machine without a GPU")
+    assert _err(B.ar_device_status) == "AR_ERR_CUDA"
+
+
+def test_lost_copy_hook_checks_precede_launch(B):
+    h = _bank(B)
+    # nothing appended: the site's rows are out of range
+    assert _err(B.ar_route_fwd_lost_copies, h, [0], 4, FAKE, None, FAKE, FAKE, 100,
+                0) == "AR_ERR_INVALID_ARG"
+    assert _err(B.ar_route_fwd_lost_copies, h, [0], 3, FAKE, None, FAKE, FAKE, 100,
+                0) == "AR_ERR_SHAPE"
+    B.ar_bank_destroy(h)
