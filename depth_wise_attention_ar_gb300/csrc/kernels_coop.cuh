@@ -404,15 +404,6 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     }
     const int key0 = (d - r) / 8;
     float qg[CPL][8], U[CPL][8];
-#pragma unroll
-    for (int j = 0; j < CPL; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int c = (LR ? kidx[j] : cidx[j]) * 8 + (e ^ sw) - key0 * 8;
-            const bool have = !LR || mp.key_warp;
-            qg[j][e] = have ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
-            U[j][e] = 0.f;
-        }
     const float inv_width = 1.0f / (float)(a.norm_full ? d : r);
 
     const int64_t GB = gridDim.x, gb = blockIdx.x;
@@ -440,6 +431,17 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         if (++slot_p == S) slot_p = 0;
     };
     for (int s = 0; s < S && issued < hi; ++s) issue_next();
+    // q*g after the first copies are issued, so that their latency starts at
+    // once (delta 8B backward phase 19.50 -> 19.42 ms)
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = (LR ? kidx[j] : cidx[j]) * 8 + (e ^ sw) - key0 * 8;
+            const bool have = !LR || mp.key_warp;
+            qg[j][e] = have ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
+            U[j][e] = 0.f;
+        }
 
     auto fetch_token = [&](int64_t t) {
         const T *grow = static_cast<const T *>(a.dout) + t * d;
