@@ -443,15 +443,17 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             U[j][e] = 0.f;
         }
 
-    auto fetch_token = [&](int64_t t) {
+    auto fetch_token = [&](int64_t t) {   // this thread's chunks, in 16-byte pieces
         const T *grow = static_cast<const T *>(a.dout) + t * d;
         const T *orow = static_cast<const T *>(a.fout) + t * d;
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int off = cidx[j] * 8;
-            cp_async16(tbuf + off, grow + off);
-            cp_async16(tbuf + d + off, orow + off);
-        }
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int k = 0; k < CB / 16; ++k) {
+                const int off = cidx[j] * 8 + k * (16 / (int)sizeof(T));
+                cp_async16(tbuf + off, grow + off);
+                cp_async16(tbuf + d + off, orow + off);
+            }
         cp_async_commit();
     };
     if (kTok && hi > lo) fetch_token(gb);
