@@ -129,6 +129,19 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Named barrier `id` (1..15) over `count` threads of the block (a multiple of
+// 32): bar_sync_named waits for all of them; bar_arrive_named counts this
+// thread's arrival without waiting (a producer signalling waiting consumers;
+// its earlier shared-memory writes are visible to them after their wait).
+__device__ __forceinline__ void bar_sync_named(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_named(int id, int count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---- 8-element chunks ------------------------------------------------------
 // A chunk is 8 consecutive elements of a row: 16 bytes in bf16, 32 in fp32.
 

@@ -12,11 +12,14 @@
 // - r = d (full keys): a warp's key heads are its value heads, so the
 //   forward needs no exchange; the backward sums the RMS coupling term
 //   sum_h dz*zr over the four warps through shared memory.
-// - r < d (sliced keys, r a multiple of CG): the key tail is owned by the last
-//   r/CG warps. They compute every head's raw score and publish it; the
-//   backward also publishes dz per head, and the key-path terms on the tail
-//   are staged in the shared gradient row before the owning lanes write it.
-// Score bits match between the passes (same lanes, same order, dot8 sums).
+// - r < d (sliced keys, r a multiple of CG): the key tail lies in the last
+//   r/CG warps' column groups. In the forward those warps compute every
+//   head's raw score and publish it. In the backward every warp scores its own
+//   heads from their key slices and stages their key-path terms in the shared
+//   gradient row; the warps owning the tail wait for them on a named barrier
+//   before they write it. The forward's and the backward's scores then differ
+//   in summation order (they agree to rounding); with full keys both take the
+//   same lanes and order, so the bits match.
 //
 // The forward takes one block barrier per item and can take the site's append
 // (FRESH): the new row's item stages the row it is formed from, each warp
@@ -37,13 +40,13 @@ constexpr int kCoopFwdStages = 4;
 // Backward stages of (row + fp32 gradient row), and with bf16 rows a block
 // buffer (2 d b bytes) into which each thread fetches its own chunks of the
 // next token's dL/dout and output rows by cp.async while the current token
-// runs. Sliced keys (two blocks per SM at most, by registers) take 3 stages
-// and the buffer; full keys take 2 and the buffer, which leaves room for three
-// blocks of d = 4096. Against 4 stages (sliced) and 3 stages (full) with an L2
-// prefetch of the next token's rows: low-rank block backward 19.00 -> 18.92
-// ms, delta 8B 20.47 -> 19.54 ms. (4 stages and the buffer left one block per
-// SM: 28.9 ms.)
-constexpr int coop_bwd_stages(size_t esize, bool lr) { return esize == 2 ? (lr ? 3 : 2) : 3; }
+// runs. bf16 rows take 2 stages and the buffer, which leaves room for three
+// blocks of d = 4096 (full keys 161 registers, sliced keys 160). Against 3
+// stages with an L2 prefetch of the next token's rows: delta 8B backward
+// 20.47 -> 19.54 ms; low-rank block 19.00 -> 18.44 ms together with the
+// balanced key work below (4 stages and the buffer left one block per SM:
+// 28.9 ms).
+constexpr int coop_bwd_stages(size_t esize, bool lr) { return esize == 2 ? 2 : 3; }
 constexpr bool coop_bwd_tokbuf(size_t esize) { return esize == 2; }
 
 struct CoopMap {
@@ -382,9 +385,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     for (int i = threadIdx.x; i < AR_MAX_SOURCES / 32; i += blockDim.x) s_first[i] = a.first_mask[i];
     unsigned char *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)S * slot_bytes);
-    float *zsm = reinterpret_cast<float *>(bars + S);  // [2][32] raw scores (sliced keys)
-    float *dzs = zsm + 64;                              // [2][32] dz per head (sliced keys)
-    float *cws = dzs + 64;                              // [2][32] per-warp coupling sums
+    float *cws = reinterpret_cast<float *>(bars + S) + 128;  // [2][32] per-warp coupling sums
     constexpr bool kTok = coop_bwd_tokbuf(sizeof(T));
     T *tbuf = reinterpret_cast<T *>(smem + ((size_t)S * slot_bytes + S * 8 + 3 * 2 * 32 * 4 + 15) / 16 * 16);
     if (threadIdx.x == 0) {
@@ -396,14 +397,29 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     const CoopMap mp = coop_map(w, lane, H, d, r);
     const int sw = ((lane >> 2) & 1) * 4;
     const int gchunk = w * CPL * 32;
-    int cidx[CPL], kidx[CPL];
+    int cidx[CPL];
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-        cidx[j] = gchunk + chunk_of<CPL>(mp.hl, mp.sub, mp.LPH, j);
-        kidx[j] = gchunk + chunk_of<CPL>(mp.hk % mp.Hk, mp.ksub, mp.LPHk, j);
-    }
+    for (int j = 0; j < CPL; ++j) cidx[j] = gchunk + chunk_of<CPL>(mp.hl, mp.sub, mp.LPH, j);
     const int key0 = (d - r) / 8;
-    float qg[CPL][8], U[CPL][8];
+    // Sliced keys: every warp scores its own value heads from their key
+    // slices, the LPH lanes of a head taking its ckh key chunks in turn, so no
+    // warp carries the others' key work and no score crosses warps. (Before,
+    // the warps owning the tail scored every head and staged every key-path
+    // term: one block barrier more per item, a third of the block idle at
+    // each, and 255 registers: low-rank block backward 18.89 -> 18.75 ms with
+    // three stages, 18.44 ms with two and three blocks per SM.) A lane holds
+    // r/1024 key chunks, rounded up: the four-warp shapes have r = d/4 or d/2
+    // (coop_supported), so at most half of CPL (KM slots).
+    constexpr int KM = LR ? (CPL + 1) / 2 : CPL;
+    const int ckh = r / 8 / H;
+    int kidx[KM];
+    bool kval[KM];
+#pragma unroll
+    for (int u = 0; u < KM; ++u) {
+        kval[u] = !LR || mp.sub + mp.LPH * u < ckh;
+        kidx[u] = LR ? key0 + mp.h * ckh + mp.sub + mp.LPH * u : cidx[u];
+    }
+    float qg[KM][8], U[KM][8];
     const float inv_width = 1.0f / (float)(a.norm_full ? d : r);
 
     const int64_t GB = gridDim.x, gb = blockIdx.x;
@@ -434,12 +450,11 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     // q*g after the first copies are issued, so that their latency starts at
     // once (delta 8B backward phase 19.50 -> 19.42 ms)
 #pragma unroll
-    for (int j = 0; j < CPL; ++j)
+    for (int j = 0; j < KM; ++j)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const int c = (LR ? kidx[j] : cidx[j]) * 8 + (e ^ sw) - key0 * 8;
-            const bool have = !LR || mp.key_warp;
-            qg[j][e] = have ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
+            const int c = kidx[j] * 8 + (e ^ sw) - key0 * 8;
+            qg[j][e] = kval[j] ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
             U[j][e] = 0.f;
         }
 
@@ -509,7 +524,8 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         float *gb_s = reinterpret_cast<float *>(vb + vbytes);
         const bool first = (s_first[n >> 5] >> (n & 31)) & 1u;
 
-        // pass A: value dots, raw scores
+        // pass A: value dots, raw scores (full keys: over the value chunks;
+        // sliced keys: over this lane's key chunks of its head's key slice)
         float v[CPL][8];
         float P = 0.f, zr = 0.f;
 #pragma unroll
@@ -518,45 +534,37 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             P = __fadd_rn(P, dot8(G[j], v[j]));
             if constexpr (!LR) zr = __fadd_rn(zr, dot8(qg[j], v[j]));
         }
-        P = group_sum(P, mp.LPH);
-        if constexpr (!LR) {
-            zr = group_sum(zr, mp.LPH);
-        } else {
-            if (mp.key_warp) {
-                float zk = 0.f;
+        if constexpr (LR) {
 #pragma unroll
-                for (int j = 0; j < CPL; ++j) {
+            for (int u = 0; u < KM; ++u)
+                if (kval[u]) {
                     float kv[8];
-                    ld_chunk_s_sw(reinterpret_cast<const T *>(vb + kidx[j] * CB), sw, kv);
-                    zk = __fadd_rn(zk, dot8(qg[j], kv));
+                    ld_chunk_s_sw(reinterpret_cast<const T *>(vb + kidx[u] * CB), sw, kv);
+                    zr = __fadd_rn(zr, dot8(qg[u], kv));
                 }
-                zk = group_sum(zk, mp.LPHk);
-                if (mp.ksub == 0) zsm[par * 32 + mp.hk] = zk;
-            }
-            if (__syncthreads_or(!got)) { ok = false; break; }
-            phase ^= 1u << slot;
-            if (i > lo && issued < hi) issue_next();
-            zr = zsm[par * 32 + mp.h];
         }
+        P = group_sum(P, mp.LPH);
+        zr = group_sum(zr, mp.LPH);
         const float wgt = exp2f((__fmul_rn(iv, zr) - lse_h) * kLog2e);
         const float dz = wgt * (P - S_h);
         const float cpart = warp_sum(mp.sub == 0 ? dz * zr : 0.f);
         if (lane == 0) cws[par * 32 + w] = cpart;
-        if (LR && mp.sub == 0) dzs[par * 32 + mp.h] = dz;
+        // the item's one block barrier: the coupling sums, and the stage
+        // wait's outcome (all threads leave together on a timeout); with
+        // sliced keys it also frees the previous item's stage
+        if (__syncthreads_or(!got)) { ok = false; break; }
+        phase ^= 1u << slot;
         if constexpr (LR) {
-            __syncthreads();
-        } else {
-            if (__syncthreads_or(!got)) { ok = false; break; }
-            phase ^= 1u << slot;
+            if (i > lo && issued < hi) issue_next();
         }
         float C = 0.f;
 #pragma unroll
         for (int k = 0; k < kCoopWarps; ++k) C += cws[par * 32 + k];
         const float coef = iv * iv * iv * C * inv_width;
         float *grad_row = a.grad + ((int64_t)s_rows[n] * TT + tok) * d;
+        const float ak = iv * dz;
 
         if constexpr (!LR) {
-            const float ak = iv * dz;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 float nv[8];
@@ -576,31 +584,33 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                 st_grad8(grad_row + cidx[j] * 8, sw, nv, a.grad_v8);
             }
         } else {
-            // key-path terms on the tail, staged in the shared gradient row
-            if (mp.key_warp) {
-                const float ak = iv * dzs[par * 32 + mp.hk];
+            // key-path terms of this lane's key chunks, staged in the shared
+            // gradient row (the tail belongs to the last warps' value columns)
 #pragma unroll
-                for (int j = 0; j < CPL; ++j) {
+            for (int u = 0; u < KM; ++u)
+                if (kval[u]) {
                     float kv[8], nv[8];
-                    ld_chunk_s_sw(reinterpret_cast<const T *>(vb + kidx[j] * CB), sw, kv);
+                    ld_chunk_s_sw(reinterpret_cast<const T *>(vb + kidx[u] * CB), sw, kv);
                     if (first) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) nv[e] = 0.f;
                     } else {
-                        ld_chunk_s_sw(gb_s + kidx[j] * 8, sw, nv);
+                        ld_chunk_s_sw(gb_s + kidx[u] * 8, sw, nv);
                     }
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        nv[e] = fmaf(ak, qg[j][e], nv[e]);
+                        nv[e] = fmaf(ak, qg[u][e], nv[e]);
                         nv[e] = fmaf(-coef, kv[e], nv[e]);
-                        U[j][e] = fmaf(ak, kv[e], U[j][e]);
+                        U[u][e] = fmaf(ak, kv[e], U[u][e]);
                     }
-                    float *dst = gb_s + kidx[j] * 8;
+                    float *dst = gb_s + kidx[u] * 8;
                     *reinterpret_cast<float4 *>(dst + sw) = make_float4(nv[0], nv[1], nv[2], nv[3]);
                     *reinterpret_cast<float4 *>(dst + (sw ^ 4)) = make_float4(nv[4], nv[5], nv[6], nv[7]);
                 }
-                __syncwarp();
-            }
+            // the warps owning tail columns wait for every warp's key-path
+            // terms; the others only signal theirs (named barrier 1)
+            if (mp.key_warp) bar_sync_named(1, kCoopWarps * 32);
+            else bar_arrive_named(1, kCoopWarps * 32);
             // value path (and the radial term off the slice for the full norm)
             const float cv = a.norm_full ? coef : 0.f;
 #pragma unroll
@@ -644,11 +654,11 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     }
     // per-block partial sums U over the key coordinates -> workspace row gb;
     // dL/dalpha partials (one per warp) -> tail
-    if (!LR || mp.key_warp) {
+    {
         float *wrow = a.ws + gb * r;
 #pragma unroll
-        for (int j = 0; j < CPL; ++j)
-            st_f32x8_g_sw(wrow + ((LR ? kidx[j] : cidx[j]) - key0) * 8, sw, U[j]);
+        for (int j = 0; j < KM; ++j)
+            if (kval[j]) st_f32x8_g_sw(wrow + (kidx[j] - key0) * 8, sw, U[j]);
     }
     if (a.dalpha && lane == 0) a.ws[GB * r + gb * 4 + w] = dal;
 }
