@@ -5,6 +5,10 @@ arguments (tensors -> device pointers, lists -> int32 arrays, streams ->
 cudaStream_t). ``Bank`` is a convenience owner of the buffers a bank needs,
 allocated with torch; every computation runs in the library's CUDA kernels.
 There is no fallback: if the library is missing, importing this module raises.
+
+With AR_CHECKED=1 in the environment the range-checked build of the same
+library (libattnres_gb300_checked.so, include/attnres.h: ar_checked_fault) is
+loaded instead; it has the same entry points.
 """
 
 from __future__ import annotations
@@ -15,17 +19,19 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIBPATH = os.path.join(HERE, "libattnres_gb300.so")
+CHECKED = os.environ.get("AR_CHECKED", "") == "1"
+LIBPATH = os.path.join(HERE, "libattnres_gb300_checked.so" if CHECKED else "libattnres_gb300.so")
 
 AR_OK = 0
 STATUS = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_SHAPE", 3: "AR_ERR_ALIGN",
           4: "AR_ERR_CAPACITY", 5: "AR_ERR_ORDER", 6: "AR_ERR_CUDA", 7: "AR_ERR_TIMEOUT",
-          8: "AR_ERR_UNSUPPORTED"}
+          8: "AR_ERR_UNSUPPORTED", 9: "AR_ERR_BOUNDS"}
 AR_F32, AR_BF16 = 0, 1
 AR_NORM_KEY, AR_NORM_FULL = 0, 1
 AR_MAX_SOURCES = 256
 AR_MAX_QUERIES = 8
 AR_DEVERR_WAIT_TIMEOUT = 1
+AR_DEVERR_BOUNDS = 2
 
 # Every function the header declares, with its ctypes signature.
 _P, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -77,11 +83,14 @@ SIGNATURES = {
     "ar_device_status": ([], ctypes.c_int),
     "ar_route_fwd_lost_copies": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, ctypes.c_uint32, _P],
                                  ctypes.c_int),
+    "ar_checked_fault": ([_I32P, ctypes.POINTER(ctypes.c_uint64), _U32P, _U32P], ctypes.c_int),
+    "ar_checked_trim_out": ([_I64], ctypes.c_int),
 }
 
 if not os.path.exists(LIBPATH):
     raise ImportError(
-        f"{LIBPATH} is not built; run depth_wise_attention_ar_gb300.build.build() "
+        f"{LIBPATH} is not built; run depth_wise_attention_ar_gb300.build.build("
+        f"{'checked=True' if CHECKED else ''}) "
         "(nvcc, sm_103a). There is no CPU fallback.")
 
 _lib = ctypes.CDLL(LIBPATH)
@@ -335,8 +344,9 @@ def ar_device_error() -> int:
 
 
 def ar_device_status():
-    """Raises ARError (AR_ERR_TIMEOUT) if a device-side wait ran out since the
-    last read of the device error word; clears the word."""
+    """Raises ARError (AR_ERR_BOUNDS) if a checked build refused an access,
+    else (AR_ERR_TIMEOUT) if a device-side wait ran out, since the last read
+    of the device error word; clears the word."""
     _check("ar_device_status", _lib.ar_device_status())
 
 
@@ -345,6 +355,20 @@ def ar_route_fwd_lost_copies(bank, rows, H, q, g, out, lse, poll_limit: int, str
     _check("ar_route_fwd_lost_copies",
            _lib.ar_route_fwd_lost_copies(bank, arr, n, H, _ptr(q), _ptr(g), _ptr(out), _ptr(lse),
                                          poll_limit, _stream(stream)))
+
+
+def ar_checked_fault():
+    """(checked, address, bytes, kind) of the first access a checked build
+    refused since the last call (kind 0: none); clears the record. checked
+    is 0 in the unchecked library, which touches no device here."""
+    c, a, b, k = ctypes.c_int32(), ctypes.c_uint64(), ctypes.c_uint32(), ctypes.c_uint32()
+    _check("ar_checked_fault", _lib.ar_checked_fault(ctypes.byref(c), ctypes.byref(a),
+                                                     ctypes.byref(b), ctypes.byref(k)))
+    return c.value, a.value, b.value, k.value
+
+
+def ar_checked_trim_out(nbytes: int):
+    _check("ar_checked_trim_out", _lib.ar_checked_trim_out(nbytes))
 
 
 # ---- convenience owner of a bank's buffers -------------------------------------

@@ -9,6 +9,21 @@
 
 namespace ar {
 
+#ifdef AR_CHECKED
+// Range checks of the checked build: the buffers one launch may touch.
+// bank and grad are [cap, T, d] row arrays (an access must lie inside one
+// row the site lists); every other buffer is a span [lo, hi), writable or not.
+constexpr int kCheckSpans = 48;
+struct CheckTable {
+    uint64_t bank, bank_row, grad, grad_row;  // bases and bytes per row
+    int cap;
+    int n;
+    uint64_t lo[kCheckSpans], hi[kCheckSpans];
+    uint8_t wr[kCheckSpans];
+    unsigned long long *fault;  // [taken, address, kind << 32 | bytes]
+};
+#endif
+
 // Everything a routing launch needs, passed by value (kernel parameter space).
 struct RouteArgs {
     const void *bank;      // rows [cap, T, d] of the storage dtype
@@ -52,6 +67,9 @@ struct RouteArgs {
     int has_bias;
     float bias[AR_MAX_SOURCES];
     uint32_t first_mask[AR_MAX_SOURCES / 32];  // backward: bit n set = store (first touch)
+#ifdef AR_CHECKED
+    CheckTable chk;
+#endif
 };
 
 // The multi-query forward's arguments: the shared fields plus one query,
@@ -92,6 +110,10 @@ cudaError_t launch_append(const void *src, const void *prev, void *dst, float *i
 cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
                              bool dst_valid, cudaStream_t s);
 unsigned int *device_error_word();
+#ifdef AR_CHECKED
+// The checked build's record of the first refused access (three words).
+unsigned long long *device_check_fault();
+#endif
 // AR_OK when the current device is the one the bank was created on (or the
 // bank's device is unknown), else AR_ERR_INVALID_ARG: every launch runs on the
 // current device, and the bank's buffers belong to its own.

@@ -137,6 +137,70 @@ void fill_common(ar::RouteArgs &a, const ar_bank *b, const int32_t *rows_in, int
     }
 }
 
+
+// ---- range-check table (checked build) ----------------------------------------
+// The buffers one launch may touch, with the extents this library's header
+// gives them; the kernels refuse any access outside them.
+#ifdef AR_CHECKED
+int64_t g_trim_out = 0;  // ar_checked_trim_out: bytes taken off every out span
+
+void chk_span(ar::RouteArgs &a, const void *p, int64_t bytes, bool writable)
+{
+    if (!p || bytes <= 0 || a.chk.n >= ar::kCheckSpans) return;
+    const uint64_t lo = reinterpret_cast<uint64_t>(p);
+    a.chk.lo[a.chk.n] = lo;
+    a.chk.hi[a.chk.n] = lo + static_cast<uint64_t>(bytes);
+    a.chk.wr[a.chk.n] = writable ? 1 : 0;
+    ++a.chk.n;
+}
+
+int64_t vec_bytes(int r, int64_t stride) { return ((int64_t)(r - 1) * stride + 1) * 4; }
+
+// bwd: the call is a backward (lse and the outputs are read, not written)
+void chk_fill(ar::RouteArgs &a, const ar_bank *b, bool bwd, size_t ws_bytes)
+{
+    ar::CheckTable &c = a.chk;
+    std::memset(&c, 0, sizeof(c));
+    const int64_t TD = b->T * (int64_t)b->d * (int64_t)b->esize;
+    c.bank = reinterpret_cast<uint64_t>(b->rows);
+    c.bank_row = static_cast<uint64_t>(TD);
+    c.grad = reinterpret_cast<uint64_t>(b->grad);
+    c.grad_row = static_cast<uint64_t>(b->T * (int64_t)b->d * 4);
+    c.cap = b->cap;
+    c.fault = ar::device_check_fault();
+    chk_span(a, a.inv, b->T * (int64_t)b->inv_ld * 4, a.fresh1 > 0);
+    chk_span(a, a.q, vec_bytes(b->r, a.q_stride), false);
+    chk_span(a, a.g, vec_bytes(b->r, a.g_stride), false);
+    chk_span(a, a.out, TD - g_trim_out, true);
+    chk_span(a, a.lse, b->T * (int64_t)a.H * 4, !bwd);
+    chk_span(a, a.fout, TD, false);
+    chk_span(a, a.dout, TD, false);
+    chk_span(a, a.ws, static_cast<int64_t>(ws_bytes), true);
+    chk_span(a, a.partial, TD, false);
+    chk_span(a, a.alpha, 4, false);
+    chk_span(a, a.routed, TD, true);
+    chk_span(a, a.dalpha, 4, false);
+    chk_span(a, a.fresh_src, TD, false);
+}
+
+void chk_fill_multi(ar::MultiArgs &m, const ar_bank *b)
+{
+    chk_fill(m.base, b, false, 0);
+    const int64_t TD = b->T * (int64_t)b->d * (int64_t)b->esize;
+    for (int i = 0; i < m.nq; ++i) {
+        chk_span(m.base, m.q[i], vec_bytes(b->r, 1), false);
+        chk_span(m.base, m.g[i], vec_bytes(b->r, 1), false);
+        chk_span(m.base, m.out[i], TD - g_trim_out, true);
+        chk_span(m.base, m.lse[i], b->T * (int64_t)m.base.H * 4, true);
+    }
+}
+#define AR_CHK_FILL(a, b, bwd, ws) chk_fill((a), (b), (bwd), (ws))
+#define AR_CHK_FILL_MULTI(m, b) chk_fill_multi((m), (b))
+#else
+#define AR_CHK_FILL(a, b, bwd, ws) ((void)0)
+#define AR_CHK_FILL_MULTI(m, b) ((void)0)
+#endif
+
 }  // namespace
 
 extern "C" {
@@ -153,6 +217,7 @@ const char *ar_status_string(ar_status s)
     case AR_ERR_CUDA: return "AR_ERR_CUDA";
     case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT";
     case AR_ERR_UNSUPPORTED: return "AR_ERR_UNSUPPORTED";
+    case AR_ERR_BOUNDS: return "AR_ERR_BOUNDS";
     }
     return "AR_ERR_UNKNOWN";
 }
@@ -295,6 +360,7 @@ ar_status route_fwd_impl(ar_bank *bank, const ar_site &st_, const void *partial,
         a.partial = partial;
         a.alpha = alpha;
         a.routed = routed;
+        AR_CHK_FILL(a, bank, false, 0);
         const cudaError_t e = ar::launch_route_fwd(a, bank->dtype, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return from_cuda(e);
     }
@@ -365,6 +431,7 @@ ar_status ar_route_fwd_append(ar_bank *bank, const void *src, int32_t accumulate
             a.acc_row = accumulate_from;
             a.out = out;
             a.lse = lse;
+            AR_CHK_FILL(a, bank, false, 0);
             const cudaError_t e =
                 ar::launch_route_fwd(a, bank->dtype, static_cast<cudaStream_t>(stream));
             if (e != cudaSuccess) {
@@ -430,6 +497,7 @@ ar_status ar_route_fwd_multi(const ar_bank *bank, const int32_t *rows, int32_t n
         m.out[i] = out[i];
         m.lse[i] = lse[i];
     }
+    AR_CHK_FILL_MULTI(m, bank);
     const cudaError_t e = ar::launch_route_fwd_multi(m, bank->dtype, static_cast<cudaStream_t>(stream));
     return from_cuda(e);
 }
@@ -504,6 +572,7 @@ ar_status route_bwd_impl(ar_bank *bank, const ar_site &st_, const void *out, con
         if (e != cudaSuccess) return from_cuda(e);
         if (ws_bytes < (size_t)ws_rows * ((size_t)bank->r + 4) * sizeof(float))
             return AR_ERR_CAPACITY;
+        AR_CHK_FILL(a, bank, true, ws_bytes);
         e = ar::launch_route_bwd(a, bank->dtype, s);
         if (e != cudaSuccess) return from_cuda(e);
         e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), ws_rows, bank->r, q,
@@ -666,6 +735,7 @@ ar_status ar_route_fwd_lost_copies(ar_bank *bank, const int32_t *rows, int32_t n
     a.lse = lse;
     a.wait_limit = poll_limit;
     a.lost_copies = 1;
+    AR_CHK_FILL(a, bank, false, 0);
     return from_cuda(ar::launch_route_fwd(a, bank->dtype, static_cast<cudaStream_t>(stream)));
 }
 
@@ -674,7 +744,46 @@ ar_status ar_device_status(void)
     uint32_t bits = 0;
     const ar_status st = ar_device_error(&bits);
     if (st != AR_OK) return st;
+    if (bits & AR_DEVERR_BOUNDS) return AR_ERR_BOUNDS;
     return (bits & AR_DEVERR_WAIT_TIMEOUT) ? AR_ERR_TIMEOUT : AR_OK;
+}
+
+ar_status ar_checked_fault(int32_t *checked, uint64_t *addr, uint32_t *bytes, uint32_t *kind)
+{
+    if (!checked || !addr || !bytes || !kind) return AR_ERR_INVALID_ARG;
+    *checked = 0;
+    *addr = 0;
+    *bytes = 0;
+    *kind = 0;
+#ifdef AR_CHECKED
+    *checked = 1;
+    unsigned long long *f = ar::device_check_fault();
+    unsigned long long v[3] = {0ull, 0ull, 0ull};
+    if (!f || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(v, f, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(f, 0, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    if (v[0]) {
+        *addr = v[1];
+        *bytes = static_cast<uint32_t>(v[2] & 0xffffffffull);
+        *kind = static_cast<uint32_t>(v[2] >> 32);
+    }
+#endif
+    return AR_OK;
+}
+
+ar_status ar_checked_trim_out(int64_t bytes)
+{
+#ifdef AR_CHECKED
+    if (bytes < 0) return AR_ERR_INVALID_ARG;
+    g_trim_out = bytes;
+    return AR_OK;
+#else
+    (void)bytes;
+    return AR_ERR_UNSUPPORTED;
+#endif
 }
 
 ar_status ar_device_error(uint32_t *bits)

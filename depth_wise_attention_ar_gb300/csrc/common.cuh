@@ -35,6 +35,103 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- range checks (checked build) ---------------------------------------------
+// Built with AR_CHECKED, every global access the helpers below make is first
+// checked against the buffers of the launch (the table the host puts in the
+// arguments), and every staged shared-memory access against the block's
+// dynamic shared memory, both for range and alignment. A refused access is
+// not made: a load gives zeros, a store is dropped, a bulk copy completes its
+// bytes on its mbarrier without copying. The first refusal is recorded and
+// AR_DEVERR_BOUNDS is set in the error word; nothing traps. A kernel names
+// its arguments at entry (chk_enter) or opts out (chk_off). Without
+// AR_CHECKED the checks are the constant true and compile away.
+#ifdef AR_CHECKED
+static __shared__ const RouteArgs *chk_args_s;
+extern __shared__ __align__(16) unsigned char chk_dyn_smem[];
+
+__device__ __forceinline__ void chk_enter(const RouteArgs &a) { chk_args_s = &a; }
+__device__ __forceinline__ void chk_off() { chk_args_s = nullptr; }
+
+enum : uint32_t { kChkLoad = 1, kChkStore = 2, kChkShared = 3 };
+
+static __device__ __noinline__ void chk_record(const RouteArgs *a, uint64_t addr, uint32_t bytes,
+                                        uint32_t kind)
+{
+    unsigned long long *f = a->chk.fault;
+    if (f && atomicCAS(f, 0ull, 1ull) == 0ull) {
+        f[1] = addr;
+        f[2] = (static_cast<unsigned long long>(kind) << 32) | bytes;
+        __threadfence();
+    }
+    if (a->err) atomicOr(a->err, AR_DEVERR_BOUNDS);
+}
+
+// A row of the bank or of the gradient rows that this launch may touch:
+// a listed row; in the bank, a store only into the row the call appends,
+// and a load also from the row a fused partial sum starts from.
+__device__ __forceinline__ bool chk_row_ok(const RouteArgs *a, uint64_t row, bool bank, bool store)
+{
+    if (bank && store) return a->fresh1 > 0 && row == static_cast<uint64_t>(a->rows[a->fresh1 - 1]);
+    for (int i = 0; i < a->n_src; ++i)
+        if (row == static_cast<uint64_t>(a->rows[i])) return true;
+    return bank && a->fresh1 > 0 && a->acc_row >= 0 && row == static_cast<uint64_t>(a->acc_row);
+}
+
+static __device__ __noinline__ bool chk_global(const void *p, uint32_t bytes, bool store, uint32_t align)
+{
+    const RouteArgs *a = chk_args_s;
+    if (!a) return true;
+    const CheckTable &c = a->chk;
+    const uint64_t x = reinterpret_cast<uint64_t>(p), e = x + bytes;
+    const uint32_t kind = store ? kChkStore : kChkLoad;
+    if ((x | bytes) % align != 0) {
+        chk_record(a, x, bytes, kind);
+        return false;
+    }
+    for (int b = 0; b < 2; ++b) {
+        const uint64_t base = b ? c.grad : c.bank, rb = b ? c.grad_row : c.bank_row;
+        if (base && rb && x >= base && x < base + static_cast<uint64_t>(c.cap) * rb) {
+            const uint64_t row = (x - base) / rb;
+            if (e <= base + (row + 1) * rb && chk_row_ok(a, row, b == 0, store)) return true;
+            chk_record(a, x, bytes, kind);
+            return false;
+        }
+    }
+    for (int i = 0; i < c.n; ++i)
+        if (x >= c.lo[i] && e <= c.hi[i] && (!store || c.wr[i])) return true;
+    chk_record(a, x, bytes, kind);
+    return false;
+}
+
+static __device__ __noinline__ bool chk_shared(const void *p, uint32_t bytes, uint32_t align)
+{
+    const RouteArgs *a = chk_args_s;
+    if (!a) return true;
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uint32_t x = smem_u32(p), base = smem_u32(chk_dyn_smem);
+    if (x >= base && x + bytes <= base + dyn && (x | bytes) % align == 0) return true;
+    chk_record(a, x, bytes, kChkShared);
+    return false;
+}
+#define AR_CHK_G(p, n, st, al) ::ar::chk_global((p), (n), (st), (al))
+#define AR_CHK_S(p, n, al) ::ar::chk_shared((p), (n), (al))
+// run the statement(s) after the check's arguments when the access is refused
+#define AR_GUARD_G(p, n, st, al, ...) \
+    if (!::ar::chk_global((p), (n), (st), (al))) { __VA_ARGS__; }
+#define AR_GUARD_S(p, n, al, ...) \
+    if (!::ar::chk_shared((p), (n), (al))) { __VA_ARGS__; }
+#define AR_CHK_ENTER(a) ::ar::chk_enter(a)
+#define AR_CHK_OFF() ::ar::chk_off()
+#else
+#define AR_CHK_G(p, n, st, al) true
+#define AR_CHK_S(p, n, al) true
+#define AR_GUARD_G(p, n, st, al, ...)
+#define AR_GUARD_S(p, n, al, ...)
+#define AR_CHK_ENTER(a) ((void)0)
+#define AR_CHK_OFF() ((void)0)
+#endif
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -65,6 +162,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                          uint64_t policy)
 {
+#ifdef AR_CHECKED
+    if (!chk_global(src, bytes, false, 16) || !chk_shared(dst, bytes, 16)) {
+        // refused: the bytes complete without a copy, so no wait runs out
+        asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(
+                         smem_u32(bar)),
+                     "r"(bytes)
+                     : "memory");
+        return;
+    }
+#endif
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
@@ -83,6 +190,7 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
 // address; nothing waits for it.
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
 {
+    AR_GUARD_G(src, bytes, false, 16, return)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
@@ -123,6 +231,8 @@ __device__ __forceinline__ void report_error(unsigned int *err, unsigned int bit
 // thread's next cp_async_wait_all); both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc)
 {
+    AR_GUARD_G(gsrc, 16, false, 16, return)
+    AR_GUARD_S(smem_dst, 16, 16, return)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
                  : "memory");
 }
@@ -173,6 +283,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 __device__ __forceinline__ uint4 lds128(const void *p)
 {
     uint4 u;
+    AR_GUARD_S(p, 16, 16, return make_uint4(0u, 0u, 0u, 0u))
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
                  : "r"(smem_u32(p))
@@ -196,20 +307,29 @@ __device__ __forceinline__ void ld_chunk_s(const float *p, float v[8])
 }
 
 // Load a chunk from global memory through the read-only path.
+__device__ __forceinline__ void zero8(float v[8])
+{
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+}
 __device__ __forceinline__ void ld_chunk_g(const __nv_bfloat16 *p, float v[8])
 {
+    AR_GUARD_G(p, 16, false, 16, return zero8(v))
     unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(p)), v);
 }
 __device__ __forceinline__ void ld_chunk_g(const float *p, float v[8])
 {
+    AR_GUARD_G(p, 32, false, 16, return zero8(v))
     const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
     const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// Store a chunk (rounded to nearest even for bf16).
-__device__ __forceinline__ void st_chunk_g(__nv_bfloat16 *p, const float v[8])
+// Store a chunk (rounded to nearest even for bf16) through a generic pointer:
+// st_chunk_g into global memory, st_chunk_s into shared memory (the same
+// store; only the checked build tells them apart).
+__device__ __forceinline__ void st_chunk_raw(__nv_bfloat16 *p, const float v[8])
 {
     uint4 u;
     u.x = pack_bf16x2(v[0], v[1]);
@@ -218,10 +338,20 @@ __device__ __forceinline__ void st_chunk_g(__nv_bfloat16 *p, const float v[8])
     u.w = pack_bf16x2(v[6], v[7]);
     *reinterpret_cast<uint4 *>(p) = u;
 }
-__device__ __forceinline__ void st_chunk_g(float *p, const float v[8])
+__device__ __forceinline__ void st_chunk_raw(float *p, const float v[8])
 {
     reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
     reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <typename T> __device__ __forceinline__ void st_chunk_g(T *p, const float v[8])
+{
+    AR_GUARD_G(p, (uint32_t)ChunkBytes<T>::value, true, 16, return)
+    st_chunk_raw(p, v);
+}
+template <typename T> __device__ __forceinline__ void st_chunk_s(T *p, const float v[8])
+{
+    AR_GUARD_S(p, (uint32_t)ChunkBytes<T>::value, 16, return)
+    st_chunk_raw(p, v);
 }
 
 // ---- packed fp32 pairs ---------------------------------------------------------
@@ -320,19 +450,32 @@ __device__ __forceinline__ void ld_chunk_s_sw(const float *p, int sw, float v[8]
 }
 __device__ __forceinline__ void ld_chunk_g_sw(const __nv_bfloat16 *p, int sw, float v[8])
 {
+    AR_GUARD_G(p, 16, false, 16, return zero8(v))
     unpack_bf16x8(swap_halves(__ldg(reinterpret_cast<const uint4 *>(p)), sw), v);
 }
 __device__ __forceinline__ void ld_chunk_g_sw(const float *p, int sw, float v[8])
 {
+    AR_GUARD_G(p, 32, false, 16, return zero8(v))
     const float4 a = __ldg(reinterpret_cast<const float4 *>(p + sw));
     const float4 b = __ldg(reinterpret_cast<const float4 *>(p + (sw ^ 4)));
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
-__device__ __forceinline__ void st_f32x8_g_sw(float *p, int sw, const float v[8])
+__device__ __forceinline__ void st_f32x8_raw_sw(float *p, int sw, const float v[8])
 {
     *reinterpret_cast<float4 *>(p + sw) = make_float4(v[0], v[1], v[2], v[3]);
     *reinterpret_cast<float4 *>(p + (sw ^ 4)) = make_float4(v[4], v[5], v[6], v[7]);
+}
+// ... into global memory / into shared memory
+__device__ __forceinline__ void st_f32x8_g_sw(float *p, int sw, const float v[8])
+{
+    AR_GUARD_G(p, 32, true, 16, return)
+    st_f32x8_raw_sw(p, sw, v);
+}
+__device__ __forceinline__ void st_f32x8_s_sw(float *p, int sw, const float v[8])
+{
+    AR_GUARD_S(p, 32, 16, return)
+    st_f32x8_raw_sw(p, sw, v);
 }
 
 // One fp32 chunk of a gradient row in global memory: a single 256-bit store
@@ -342,6 +485,7 @@ __device__ __forceinline__ void st_f32x8_g_sw(float *p, int sw, const float v[8]
 __device__ __forceinline__ void st_grad8(float *p, int sw, const float v[8], bool v8)
 {
     if (v8) {
+        AR_GUARD_G(p, 32, true, 32, return)
         float x[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -371,6 +515,7 @@ __device__ __forceinline__ int chunk_of(int h, int sub, int LPH, int j)
 __device__ __forceinline__ void ld_f32x8_s(const float *p, float v[8]) { ld_chunk_s(p, v); }
 __device__ __forceinline__ void st_f32x8_s(float *p, const float v[8])
 {
+    AR_GUARD_S(p, 32, 16, return)
     reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
     reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
@@ -401,8 +546,44 @@ __device__ __forceinline__ void store_output(const RouteArgs &a, int64_t off, co
 // One element of the storage dtype, as fp32 / rounded from fp32 (to nearest even).
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ void st_elem(float *p, float v) { *p = v; }
-__device__ __forceinline__ void st_elem(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void st_elem(float *p, float v)
+{
+    AR_GUARD_G(p, 4, true, 4, return)
+    *p = v;
+}
+__device__ __forceinline__ void st_elem(__nv_bfloat16 *p, float v)
+{
+    AR_GUARD_G(p, 2, true, 2, return)
+    *p = __float2bfloat16_rn(v);
+}
+
+// Checked scalar access to global memory (a plain __ldg / store when not
+// built with the checks).
+__device__ __forceinline__ float ldg_chk(const float *p)
+{
+    AR_GUARD_G(p, 4, false, 4, return 0.f)
+    return __ldg(p);
+}
+__device__ __forceinline__ float ld_chk(const float *p)  // plain (coherent) load
+{
+    AR_GUARD_G(p, 4, false, 4, return 0.f)
+    return *p;
+}
+__device__ __forceinline__ uint4 ldg16_chk(const uint4 *p)
+{
+    AR_GUARD_G(p, 16, false, 16, return make_uint4(0u, 0u, 0u, 0u))
+    return __ldg(p);
+}
+__device__ __forceinline__ void st16_chk(void *p, uint4 v)
+{
+    AR_GUARD_G(p, 16, true, 16, return)
+    *reinterpret_cast<uint4 *>(p) = v;
+}
+__device__ __forceinline__ void st_chk(float *p, float v)
+{
+    AR_GUARD_G(p, 4, true, 4, return)
+    *p = v;
+}
 
 // Sum over the `lph` lanes of this lane's aligned group (lph a power of two).
 __device__ __forceinline__ float group_sum(float x, int lph)

@@ -65,6 +65,7 @@ template <typename T, int CPL>
 __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     route_bwd_kernel(const __grid_constant__ RouteArgs a)
 {
+    AR_CHK_ENTER(a);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     __shared__ uint32_t s_first[AR_MAX_SOURCES / 32];
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int c = cidx[j] * 8 + (e ^ sw);
-                qg[j][e] = __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f);
+                qg[j][e] = ldg_chk(a.q + c * a.q_stride) * (a.g ? ldg_chk(a.g + c * a.g_stride) : 1.0f);
             }
     };
     if constexpr (!kQgLate) load_qg();
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
 
     float G[CPL][8];
     float S_h = 0.f, lse_h = 0.f, dal = 0.f;
-    const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
+    const float alpha = a.alpha ? ldg_chk(a.alpha) : 1.0f;
     int64_t tok = gw, i = lo;
     int n = 0, slot = 0;
     uint32_t phase = 0;
@@ -204,10 +205,10 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
             S_h = group_sum(sp, LPH);
             if (tok + GW < TT) fetch_token(tok + GW);      // this lane's chunks are read
             if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted by the warp owning (t, 0)
-            lse_h = __ldg(a.lse + tok * H + h);
+            lse_h = ldg_chk(a.lse + tok * H + h);
             __syncwarp();
             for (int nn = lane; nn < N; nn += 32)
-                cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+                cur_inv[nn] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[nn]);
             __syncwarp();
         }
         const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     __syncthreads();
     float *uw = reinterpret_cast<float *>(ring);
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) st_f32x8_g_sw(uw + cidx[j] * 8, sw, U[j]);
+    for (int j = 0; j < CPL; ++j) st_f32x8_s_sw(uw + cidx[j] * 8, sw, U[j]);
     __shared__ float s_dal[kBwdWarps];
     if (lane == 0) s_dal[warp] = dal;
     __syncthreads();
@@ -287,12 +288,13 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
         float t = 0.f;
 #pragma unroll
         for (int k = 0; k < kBwdWarps; ++k) t += reinterpret_cast<const float *>(rings)[k * wstride + c];
-        a.ws[gb * d + c] = t;
+        st_chk(a.ws + (gb * d + c), t);
     }
     if (a.dalpha && threadIdx.x == 0) {
         float t = 0.f;
 #pragma unroll
         for (int k = 0; k < kBwdWarps; ++k) t += s_dal[k];
+        AR_GUARD_G(a.ws + GB * d + gb * 4, 16, true, 16, return)
         *reinterpret_cast<float4 *>(a.ws + GB * d + gb * 4) = make_float4(t, 0.f, 0.f, 0.f);
     }
 }

@@ -89,6 +89,7 @@ template <typename T, int CPL, bool LR, bool FRESH = false>
 __global__ void __launch_bounds__(kCoopWarps * 32)
     route_fwd_coop_kernel(const __grid_constant__ RouteArgs a)
 {
+    AR_CHK_ENTER(a);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     constexpr int S = kCoopFwdStages;
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         for (int e = 0; e < 8; ++e) {
             const int c = (LR ? kidx[j] : cidx[j]) * 8 + e - key0 * 8;
             const bool have = !LR || mp.key_warp;
-            qg[j][e] = have ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
+            qg[j][e] = have ? ldg_chk(a.q + c * a.q_stride) * (a.g ? ldg_chk(a.g + c * a.g_stride) : 1.0f) : 0.f;
         }
 
     const int64_t GB = gridDim.x, gb = blockIdx.x;
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     int64_t tok = gb, i = 0;
     float m = 0.f, l = 0.f;
     float acc[CPL][8];
-    const float alpha = delta && a.alpha ? __ldg(a.alpha) : 1.0f;
+    const float alpha = delta && a.alpha ? ldg_chk(a.alpha) : 1.0f;
     bool ok = true, bad = false;
     for (; i < total; ++i) {
         float *inv_t = cur_inv + tpar * AR_MAX_SOURCES;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                          &pbars[tpar], pol);
             }
             for (int nn = threadIdx.x; nn < N; nn += blockDim.x)
-                inv_t[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+                inv_t[nn] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[nn]);
         }
         const bool got = mbar_wait(&bars[slot], (phase >> slot) & 1u, kWaitLimit);
         const unsigned char *buf = ring + (size_t)slot * row_bytes;
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
 #pragma unroll
                             for (int e = 0; e < 8; ++e) x[e] += y[e];
                         }
-                        st_chunk_g(reinterpret_cast<T *>(sb + cidx[j] * CB), x);
+                        st_chunk_s(reinterpret_cast<T *>(sb + cidx[j] * CB), x);
                         st_chunk_g(slot_row + cidx[j] * 8, x);
                     }
                     __syncwarp();
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         if (FRESH && fresh) {
             const float sum = ((ssq[par * 4 + 0] + ssq[par * 4 + 1]) + ssq[par * 4 + 2]) + ssq[par * 4 + 3];
             iv = rsqrtf(fmaf(sum, 1.0f / (float)(a.norm_full ? d : r), a.eps));
-            if (threadIdx.x == 0) const_cast<float *>(a.inv)[tok * a.inv_ld + s_rows[n]] = iv;
+            if (threadIdx.x == 0) st_chk(const_cast<float *>(a.inv) + (tok * a.inv_ld + s_rows[n]), iv);
         }
 
 #pragma unroll
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                         store_output<T>(a, off, o);
                     }
                 }
-                if (mp.sub == 0) a.lse[tok * H + mp.h] = m + log2f(l) * kLn2;
+                if (mp.sub == 0) st_chk(a.lse + (tok * H + mp.h), m + log2f(l) * kLn2);
             }
         }
         par ^= 1;
@@ -370,6 +371,7 @@ template <typename T, int CPL, bool LR>
 __global__ void __launch_bounds__(kCoopWarps * 32)
     route_bwd_coop_kernel(const __grid_constant__ RouteArgs a)
 {
+    AR_CHK_ENTER(a);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     __shared__ uint32_t s_first[AR_MAX_SOURCES / 32];
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = kidx[j] * 8 + (e ^ sw) - key0 * 8;
-            qg[j][e] = kval[j] ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
+            qg[j][e] = kval[j] ? ldg_chk(a.q + c * a.q_stride) * (a.g ? ldg_chk(a.g + c * a.g_stride) : 1.0f) : 0.f;
             U[j][e] = 0.f;
         }
 
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
 
     float G[CPL][8];
     float S_h = 0.f, lse_h = 0.f, dal = 0.f;
-    const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
+    const float alpha = a.alpha ? ldg_chk(a.alpha) : 1.0f;
     int64_t tok = gb, i = lo;
     int n = 0, slot = 0, par = 0;
     uint32_t phase = 0;
@@ -510,11 +512,11 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
             S_h = group_sum(sp, mp.LPH);
             if (kTok && tok + GB < TT) fetch_token(tok + GB);   // this thread's chunks are read
             if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted once
-            lse_h = __ldg(a.lse + tok * H + mp.h);
+            lse_h = ldg_chk(a.lse + tok * H + mp.h);
         }
         // the source's inverse RMS (a small, cache-resident table), requested
         // before the wait for the staged row so that its latency hides there
-        const float iv = __ldg(a.inv + tok * a.inv_ld + s_rows[n]);
+        const float iv = ldg_chk(a.inv + tok * a.inv_ld + s_rows[n]);
         // The first block barrier of an item also carries the wait's outcome
         // (all threads leave together on a timeout); with sliced keys it also
         // frees the stage of the previous item, which every warp has finished
@@ -604,6 +606,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                         U[u][e] = fmaf(ak, kv[e], U[u][e]);
                     }
                     float *dst = gb_s + kidx[u] * 8;
+                    AR_GUARD_S(dst, 32, 16, continue)
                     *reinterpret_cast<float4 *>(dst + sw) = make_float4(nv[0], nv[1], nv[2], nv[3]);
                     *reinterpret_cast<float4 *>(dst + (sw ^ 4)) = make_float4(nv[4], nv[5], nv[6], nv[7]);
                 }
@@ -654,7 +657,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         for (int j = 0; j < KM; ++j)
             if (kval[j]) st_f32x8_g_sw(wrow + (kidx[j] - key0) * 8, sw, U[j]);
     }
-    if (a.dalpha && lane == 0) a.ws[GB * r + gb * 4 + w] = dal;
+    if (a.dalpha && lane == 0) st_chk(a.ws + (GB * r + gb * 4 + w), dal);
 }
 
 template <typename T, int CPL, bool LR, bool FRESH>

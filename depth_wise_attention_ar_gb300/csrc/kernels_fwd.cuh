@@ -136,8 +136,8 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int c = kidx[j] * 8 + e - key0 * 8;
-                qg[j][e] = kval[j] ? __ldg(a.q + c * a.q_stride) *
-                                         (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f)
+                qg[j][e] = kval[j] ? ldg_chk(a.q + c * a.q_stride) *
+                                         (a.g ? ldg_chk(a.g + c * a.g_stride) : 1.0f)
                                    : 0.f;
             }
     };
@@ -176,7 +176,7 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
 #pragma unroll
         for (int u = 0; u < AR_MAX_SOURCES / 32; ++u) {
             const int nn = lane + 32 * u;
-            if (nn < N) pre_inv[u] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+            if (nn < N) pre_inv[u] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[nn]);
         }
     };
     if (ntok > 0) prefetch_inv(gw);
@@ -234,7 +234,7 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
                     for (int e = 0; e < 8; ++e) ss = fmaf(v[j][e], v[j][e], ss);
                 ss = warp_sum(ss);
                 ivn = rsqrtf(fmaf(ss, 1.0f / (float)d, a.eps));
-                if (lane == 0) const_cast<float *>(a.inv)[tok * a.inv_ld + s_rows[n]] = ivn;
+                if (lane == 0) st_chk(const_cast<float *>(a.inv) + (tok * a.inv_ld + s_rows[n]), ivn);
             }
         }
         // __fmul_rn keeps the product uncontracted: the backward recomputes
@@ -286,7 +286,7 @@ __device__ __forceinline__ void route_fwd_body(const RouteArgs &a)
                 for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
                 store_output<T>(a, tok * d + cidx[j] * 8, o);
             }
-            if (sub == 0) a.lse[tok * H + h] = m + log2f(l) * kLn2;
+            if (sub == 0) st_chk(a.lse + (tok * H + h), m + log2f(l) * kLn2);
         }
         if (++n == N) { n = 0; tok += GW; }
         if (++slot == S) slot = 0;
@@ -310,6 +310,7 @@ template <typename T, int CPL, bool FRESH = false>
 __global__ void __launch_bounds__(kFwdWarps * 32)
     route_fwd_kernel(const __grid_constant__ RouteArgs a)
 {
+    AR_CHK_ENTER(a);
     route_fwd_body<T, CPL, false, FRESH, CPL>(a);
 }
 
@@ -318,6 +319,7 @@ template <typename T, int CPL, int KM>
 __global__ void __launch_bounds__(kFwdWarps * 32, fwd_min_blocks(sizeof(T) == 2, CPL, KM))
     route_fwd_sk_kernel(const __grid_constant__ RouteArgs a)
 {
+    AR_CHK_ENTER(a);
     route_fwd_body<T, CPL, true, false, KM>(a);
 }
 
@@ -338,6 +340,7 @@ template <typename T, int CPL, bool FRESH = false, int NG = AR_MAX_SOURCES / 32,
 __global__ void __launch_bounds__(kFwdWarps * 32, MINB)
     route_fwd_pair_kernel(const __grid_constant__ RouteArgs a)
 {
+    AR_CHK_ENTER(a);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     constexpr int S = kFwdStages;
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, MINB)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = cidx[j] * 8 + e;
-            qg[j][e] = __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f);
+            qg[j][e] = ldg_chk(a.q + c * a.q_stride) * (a.g ? ldg_chk(a.g + c * a.g_stride) : 1.0f);
         }
 
     // ---- work: token pairs gw, gw + GW, ...
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, MINB)
 #pragma unroll
             for (int v = 0; v < NG; ++v) {
                 const int nn = lane + 32 * v;
-                if (nn < N && t < TT) pre_inv[k][v] = __ldg(a.inv + t * a.inv_ld + s_rows[nn]);
+                if (nn < N && t < TT) pre_inv[k][v] = ldg_chk(a.inv + t * a.inv_ld + s_rows[nn]);
             }
         }
     };
@@ -475,7 +478,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, MINB)
             ivn = rsqrtf(fmaf(ss, 1.0f / (float)d, a.eps));
             const int64_t tk = u * 2 + tt;
             if (fl == 0 && tk < TT)
-                const_cast<float *>(a.inv)[tk * a.inv_ld + s_rows[n]] = ivn;
+                st_chk(const_cast<float *>(a.inv) + (tk * a.inv_ld + s_rows[n]), ivn);
         }
         const float z = __fmul_rn(zr, ivn);
         if (n == 0) {
@@ -514,7 +517,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32, MINB)
                     for (int e = 0; e < 8; ++e) o[e] = acc[j][e] * rl;
                     store_output<T>(a, tok * d + cidx[j] * 8, o);
                 }
-                if (sub == 0) a.lse[tok * H + h] = m + log2f(l) * kLn2;
+                if (sub == 0) st_chk(a.lse + (tok * H + h), m + log2f(l) * kLn2);
             }
         }
         if (++n == N) { n = 0; u += GW; }

@@ -28,22 +28,24 @@
 namespace ar {
 
 template <typename T> __device__ __forceinline__ float gen_ld(const T *p);
-template <> __device__ __forceinline__ float gen_ld<float>(const float *p) { return __ldg(p); }
+template <> __device__ __forceinline__ float gen_ld<float>(const float *p) { return ldg_chk(p); }
 template <> __device__ __forceinline__ float gen_ld<__nv_bfloat16>(const __nv_bfloat16 *p)
 {
+    AR_GUARD_G(p, 2, false, 2, return 0.f)
     const unsigned short u = __ldg(reinterpret_cast<const unsigned short *>(p));
     return __uint_as_float((uint32_t)u << 16);
 }
 
 __device__ __forceinline__ float gen_qg(const RouteArgs &a, int c)
 {
-    return __ldg(a.q + (int64_t)c * a.q_stride) *
-           (a.g ? __ldg(a.g + (int64_t)c * a.g_stride) : 1.0f);
+    return ldg_chk(a.q + (int64_t)c * a.q_stride) *
+           (a.g ? ldg_chk(a.g + (int64_t)c * a.g_stride) : 1.0f);
 }
 
 template <typename T>
 __global__ void route_fwd_generic_kernel(const __grid_constant__ RouteArgs a, int wpb)
 {
+    AR_CHK_ENTER(a);
     extern __shared__ __align__(16) float gsm[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -58,10 +60,10 @@ __global__ void route_fwd_generic_kernel(const __grid_constant__ RouteArgs a, in
     for (int c = threadIdx.x; c < r; c += blockDim.x) qg[c] = gen_qg(a, c);
     __syncthreads();
     const T *bank = static_cast<const T *>(a.bank);
-    const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
+    const float alpha = a.alpha ? ldg_chk(a.alpha) : 1.0f;
 
     for (int64_t t = (int64_t)blockIdx.x * wpb + warp; t < TT; t += (int64_t)gridDim.x * wpb) {
-        for (int n = lane; n < N; n += 32) cinv[n] = __ldg(a.inv + t * a.inv_ld + s_rows[n]);
+        for (int n = lane; n < N; n += 32) cinv[n] = ldg_chk(a.inv + t * a.inv_ld + s_rows[n]);
         __syncwarp();
         // scores, one warp reduction per (row, head)
         for (int n = 0; n < N; ++n) {
@@ -84,7 +86,7 @@ __global__ void route_fwd_generic_kernel(const __grid_constant__ RouteArgs a, in
             for (int n = 0; n < N; ++n) l += exp2f((wz[n * H + h] - m) * kLog2e);
             const float lse = m + log2f(l) * kLn2;
             lse_s[h] = lse;
-            a.lse[t * H + h] = lse;
+            st_chk(a.lse + (t * H + h), lse);
             for (int n = 0; n < N; ++n) wz[n * H + h] = exp2f((wz[n * H + h] - lse) * kLog2e);
         }
         __syncwarp();
@@ -107,6 +109,7 @@ __global__ void route_fwd_generic_kernel(const __grid_constant__ RouteArgs a, in
 template <typename T>
 __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, int wpb)
 {
+    AR_CHK_ENTER(a);
     extern __shared__ __align__(16) float gsm[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -127,7 +130,7 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
     const T *bank = static_cast<const T *>(a.bank);
     const T *dout = static_cast<const T *>(a.dout);
     const T *fout = static_cast<const T *>(a.fout);
-    const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
+    const float alpha = a.alpha ? ldg_chk(a.alpha) : 1.0f;
     const float inv_w = 1.0f / (float)(a.norm_full ? d : r);
     const int64_t gw = (int64_t)blockIdx.x * wpb + warp;
     const int64_t GW = (int64_t)gridDim.x * wpb;
@@ -149,7 +152,7 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
             if (lane == 0) S[h] = sp;
         }
         if (a.dalpha) dal += warp_sum(raw);
-        for (int n = lane; n < N; n += 32) cinv[n] = __ldg(a.inv + t * a.inv_ld + s_rows[n]);
+        for (int n = lane; n < N; n += 32) cinv[n] = ldg_chk(a.inv + t * a.inv_ld + s_rows[n]);
         __syncwarp();
         // per row: value dot P, raw score zr, weight, score gradient, C_n
         for (int n = 0; n < N; ++n) {
@@ -166,7 +169,7 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
                 zr = warp_sum(zr);
                 float z = __fmul_rn(zr, iv);
                 if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
-                const float lse = __ldg(a.lse + t * H + h);
+                const float lse = ldg_chk(a.lse + t * H + h);
                 const float w = exp2f((z - lse) * kLog2e);
                 const float dz = w * (P - S[h]);
                 C = fmaf(dz, zr, C);
@@ -192,7 +195,7 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
                 const int64_t off = ((int64_t)s_rows[n] * TT + t) * d + c;
                 const float sv = gen_ld(bank + off);
                 const bool first = (a.first_mask[n >> 5] >> (n & 31)) & 1u;
-                float v = first ? 0.f : a.grad[off];
+                float v = first ? 0.f : ld_chk(a.grad + off);
                 v = fmaf(W[n * H + hv], Gc, v);
                 const float iv = cinv[n];
                 if (key) {
@@ -201,7 +204,7 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
                     u = fmaf(ak, sv, u);
                 }
                 if (norm) v = fmaf(-(iv * iv * iv * Cn[n] * inv_w), sv, v);
-                a.grad[off] = v;
+                st_chk(a.grad + off, v);
             }
             if (key) U[kc] = u;
         }
@@ -215,7 +218,7 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
     for (int c = threadIdx.x; c < r; c += blockDim.x) {
         float s = 0.f;
         for (int w = 0; w < wpb; ++w) s += U0[(size_t)w * wf + c];
-        a.ws[(int64_t)blockIdx.x * r + c] = s;
+        st_chk(a.ws + ((int64_t)blockIdx.x * r + c), s);
     }
     if (a.dalpha) {
         __shared__ float s_dal[4];
@@ -225,8 +228,10 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
             float s = 0.f;
             for (int w = 0; w < wpb; ++w) s += s_dal[w];
             float *tail = a.ws + (int64_t)gridDim.x * r + (int64_t)blockIdx.x * 4;
-            tail[0] = s;
-            tail[1] = tail[2] = tail[3] = 0.f;
+            st_chk(tail, s);   // scalar stores: r may be odd, so the tail may not be 16-byte aligned
+            st_chk(tail + 1, 0.f);
+            st_chk(tail + 2, 0.f);
+            st_chk(tail + 3, 0.f);
         }
     }
 }

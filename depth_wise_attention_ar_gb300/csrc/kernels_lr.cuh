@@ -38,6 +38,7 @@ namespace ar {
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant__ RouteArgs a)
 {
+    AR_CHK_ENTER(a);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     constexpr int S = kLrFwdStages;
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = kidx[j] * 8 + e;
-            qg[j][e] = kval[j] ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
+            qg[j][e] = kval[j] ? ldg_chk(a.q + c * a.q_stride) * (a.g ? ldg_chk(a.g + c * a.g_stride) : 1.0f) : 0.f;
         }
     }
 
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
     };
     auto load_inv = [&](int64_t k, float *dst) {
         const int64_t tok = gw + k * GW;
-        for (int nn = lane; nn < N; nn += 32) dst[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+        for (int nn = lane; nn < N; nn += 32) dst[nn] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[nn]);
     };
 
     if (ntok > 0) {
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(32) route_fwd_lr_kernel(const __grid_constant_
             for (int n = 0; n < N; ++n) l += exp2f((zs[n * H + h] - m) * kLog2e);
             const float rl = 1.f / l;
             for (int n = 0; n < N; ++n) ws[n * H + h] = exp2f((zs[n * H + h] - m) * kLog2e) * rl;
-            a.lse[tok * H + h] = m + log2f(l) * kLn2;
+            st_chk(a.lse + (tok * H + h), m + log2f(l) * kLn2);
         }
         __syncwarp();
         // the next token's keys and inverse RMS can come in now
@@ -247,6 +248,7 @@ inline size_t lr_bwd_smem_bytes(int d, size_t esize, bool g_in_registers)
 template <typename T, int KMAX, int CPLT = 0>
 __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant__ RouteArgs a)
 {
+    AR_CHK_ENTER(a);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     __shared__ uint32_t s_first[AR_MAX_SOURCES / 32];
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int c = (kidx[j] - key0) * 8 + e;
-            qg[j][e] = kval[j] ? __ldg(a.q + c * a.q_stride) * (a.g ? __ldg(a.g + c * a.g_stride) : 1.0f) : 0.f;
+            qg[j][e] = kval[j] ? ldg_chk(a.q + c * a.q_stride) * (a.g ? ldg_chk(a.g + c * a.g_stride) : 1.0f) : 0.f;
             U[j][e] = 0.f;
         }
     }
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
     // delta form: G = alpha dL/dh enters linearly, so G stays in the storage
     // dtype and alpha scales the dot products and the w G term
     float S_h = 0.f, lse_h = 0.f, dal = 0.f;
-    const float alpha = a.alpha ? __ldg(a.alpha) : 1.0f;
+    const float alpha = a.alpha ? ldg_chk(a.alpha) : 1.0f;
     int64_t tok = lo / N, i = lo;
     int n = (int)(lo - tok * N), slot = 0;
     uint32_t phase = 0;
@@ -357,11 +359,11 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 #pragma unroll
             for (int j = 0; j < CPLT; ++j) {
                 const int c = vbase + LPH * j;
-                preG[j] = __ldg(g4 + c);
-                preO[j] = __ldg(o4 + c);
+                preG[j] = ldg16_chk(g4 + c);
+                preO[j] = ldg16_chk(o4 + c);
             }
-            pre_lse = __ldg(a.lse + t * H + h);
-            if (lane < N) pre_inv = __ldg(a.inv + t * a.inv_ld + s_rows[lane]);
+            pre_lse = ldg_chk(a.lse + t * H + h);
+            if (lane < N) pre_inv = ldg_chk(a.inv + t * a.inv_ld + s_rows[lane]);
         }
     };
     if (tok <= last_tok) prefetch_tok(tok);
@@ -379,13 +381,13 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
                     unpack_bf16x8(preG[j], gv);
                     unpack_bf16x8(preO[j], o);
                 } else {
-                    const uint4 graw = __ldg(reinterpret_cast<const uint4 *>(
+                    const uint4 graw = ldg16_chk(reinterpret_cast<const uint4 *>(
                         reinterpret_cast<const unsigned char *>(grow) + (size_t)c * ChunkBytes<T>::value));
                     if constexpr (sizeof(T) == 2) {
                         if constexpr (CPLT == 0) *reinterpret_cast<uint4 *>(Gs + c * 8) = graw;
                         unpack_bf16x8(graw, gv);
                     } else {
-                        const uint4 g2 = __ldg(reinterpret_cast<const uint4 *>(
+                        const uint4 g2 = ldg16_chk(reinterpret_cast<const uint4 *>(
                             reinterpret_cast<const unsigned char *>(grow) + (size_t)c * 32 + 16));
                         if constexpr (CPLT == 0) {
                             reinterpret_cast<uint4 *>(Gs + c * 8)[0] = graw;
@@ -412,12 +414,12 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
                 lse_h = pre_lse;
                 if (lane < N) cur_inv[lane] = pre_inv;
                 for (int nn = lane + 32; nn < N; nn += 32)
-                    cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+                    cur_inv[nn] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[nn]);
                 if (tok < last_tok) prefetch_tok(tok + 1);
             } else {
-                lse_h = __ldg(a.lse + tok * H + h);
+                lse_h = ldg_chk(a.lse + tok * H + h);
                 for (int nn = lane; nn < N; nn += 32)
-                    cur_inv[nn] = __ldg(a.inv + tok * a.inv_ld + s_rows[nn]);
+                    cur_inv[nn] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[nn]);
             }
             __syncwarp();
         }
@@ -530,8 +532,10 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
         if (kval[j]) st_f32x8_g(wrow + (kidx[j] - key0) * 8, U[j]);
-    if (a.dalpha && lane == 0)
+    if (a.dalpha && lane == 0) {
+        AR_GUARD_G(a.ws + GW * r + gw * 4, 16, true, 16, return)
         *reinterpret_cast<float4 *>(a.ws + GW * r + gw * 4) = make_float4(dal, 0.f, 0.f, 0.f);
+    }
 }
 
 template <typename T, int KMAX>

@@ -63,6 +63,7 @@ template <typename T>
 __global__ void __launch_bounds__(kMultiThreads)
     route_fwd_multi_kernel(const __grid_constant__ MultiArgs m, int nbuf)
 {
+    AR_CHK_ENTER(m.base);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[AR_MAX_SOURCES];
     constexpr int CB = ChunkBytes<T>::value;
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kMultiThreads)
         for (int e = 0; e < 8; ++e) {
             const int c = kc * 8 + e;
             qg[qi][e] = (has_key && qi < nq)
-                            ? __ldg(m.q[qi] + c) * (m.g[qi] ? __ldg(m.g[qi] + c) : 1.0f)
+                            ? ldg_chk(m.q[qi] + c) * (m.g[qi] ? ldg_chk(m.g[qi] + c) : 1.0f)
                             : 0.f;
         }
     __syncthreads();
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kMultiThreads)
     bool ok = true;
     for (int64_t tok = gb; tok < TT; tok += GB) {
         for (int n = tid; n < N; n += kMultiThreads)
-            invs[n] = __ldg(a.inv + tok * a.inv_ld + s_rows[n]);
+            invs[n] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[n]);
         const bool got = mbar_wait(&bars[b], (phase >> b) & 1u, kWaitLimit);
         const unsigned char *buf = bufs + (size_t)b * tok_bytes;
 
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kMultiThreads)
             for (int n = 0; n < N; ++n) l += exp2f((wq[n] - mx) * kLog2e);
             const float lse = mx + log2f(l) * kLn2;
             for (int n = 0; n < N; ++n) wq[n] = exp2f((wq[n] - lse) * kLog2e);
-            m.lse[qi][tok * H + hh] = lse;
+            st_chk(m.lse[qi] + (tok * H + hh), lse);
         }
         __syncthreads();
 

@@ -126,6 +126,7 @@ inline int multi_mma_buffers(int d, int r, int H, int N, size_t *smem)
 __global__ void __launch_bounds__(kMmaThreads)
     route_fwd_multi_mma_kernel(const __grid_constant__ MultiArgs m, int nbuf)
 {
+    AR_CHK_ENTER(m.base);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[kMmaMaxRows];
     constexpr int QM = AR_MAX_QUERIES;
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kMmaThreads)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int c = warp * Kr + ks * 16 + half * 8 + 2 * t4 + e;
-                    v[e] = __ldg(m.q[g8] + c) * (m.g[g8] ? __ldg(m.g[g8] + c) : 1.0f);
+                    v[e] = ldg_chk(m.q[g8] + c) * (m.g[g8] ? ldg_chk(m.g[g8] + c) : 1.0f);
                 }
             }
             const __nv_bfloat162 hi = __floats2bfloat162_rn(v[0], v[1]);
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kMmaThreads)
     int b = 0;
     bool ok = true;
     for (int64_t tok = gb; tok < TT; tok += GB) {
-        if (tid < N) invs[tid] = __ldg(a.inv + tok * a.inv_ld + s_rows[tid]);
+        if (tid < N) invs[tid] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[tid]);
         const bool got = mbar_wait(&bars[b], (phase >> b) & 1u, kWaitLimit);
         if (__syncthreads_or(!got)) { ok = false; break; }
         phase ^= 1u << b;
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kMmaThreads)
                 wh[n] = hi;
                 wl[n] = __float2bfloat16_rn(w - __bfloat162float(hi));
             }
-            m.lse[qi][tok * H + hh] = lse;
+            st_chk(m.lse[qi] + (tok * H + hh), lse);
         }
         __syncthreads();
 
@@ -284,9 +285,8 @@ __global__ void __launch_bounds__(kMmaThreads)
             for (int idx = lane; idx < 64; idx += 32) {
                 const int row = idx >> 3, seg = idx & 7;
                 if (row < nq && t0 + seg < ntile)
-                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(m.out[row]) + tok * d +
-                                               (t0 + seg) * 8) =
-                        *reinterpret_cast<const uint4 *>(stg + row * kStgPitch + seg * 16);
+                    st16_chk(static_cast<__nv_bfloat16 *>(m.out[row]) + tok * d + (t0 + seg) * 8,
+                             *reinterpret_cast<const uint4 *>(stg + row * kStgPitch + seg * 16));
             }
             __syncwarp();
         }
@@ -375,6 +375,7 @@ __device__ __forceinline__ bool ms_bar_or(bool v)
 __global__ void __launch_bounds__(kMsThreads, 2)
     route_fwd_multi_stream_kernel(const __grid_constant__ MultiArgs m, const MsLayout L)
 {
+    AR_CHK_ENTER(m.base);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[kMmaMaxRows];
     __shared__ volatile int s_abort;
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(kMsThreads, 2)
     const uint32_t qgp = L.qg_pitch;
     for (int i = tid; i < QM * r; i += kMsThreads) {
         const int qi = i / r, c = i - qi * r;
-        const float v = qi < nq ? __ldg(m.q[qi] + c) * (m.g[qi] ? __ldg(m.g[qi] + c) : 1.0f) : 0.f;
+        const float v = qi < nq ? ldg_chk(m.q[qi] + c) * (m.g[qi] ? ldg_chk(m.g[qi] + c) : 1.0f) : 0.f;
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);
         *reinterpret_cast<__nv_bfloat16 *>(qgs + (size_t)qi * qgp + c * 2) = hi;
         *reinterpret_cast<__nv_bfloat16 *>(qgs + (size_t)(QM + qi) * qgp + c * 2) =
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(kMsThreads, 2)
     for (int64_t ti = 0; ti < ntok; ++ti) {
         const int64_t tok = gb + ti * GB;
         float *inv_t = invs + (ti & 1) * kMmaMaxRows;
-        if (tid < N) inv_t[tid] = __ldg(a.inv + tok * a.inv_ld + s_rows[tid]);
+        if (tid < N) inv_t[tid] = ldg_chk(a.inv + tok * a.inv_ld + s_rows[tid]);
         bool got = true;
         for (int k = 0; k < nk && got; ++k) {
             int sk = st0 + k, rk = rnd0;
@@ -603,7 +604,7 @@ __global__ void __launch_bounds__(kMsThreads, 2)
                         wl[n] = __float2bfloat16_rn(w - __bfloat162float(hi));
                     }
                 }
-                if (ssub == 0) lse_out[tok * H + sh] = lse;
+                if (ssub == 0) st_chk(lse_out + (tok * H + sh), lse);
             }
         }
         ms_bar();
@@ -678,11 +679,10 @@ __global__ void __launch_bounds__(kMsThreads, 2)
                     __syncwarp();
                     const int64_t o = tok * d + (int64_t)(tile * ntl + lt0 + oseg) * 8;
                     if (out0)
-                        *reinterpret_cast<uint4 *>(out0 + o) =
-                            *reinterpret_cast<const uint4 *>(stg + orow0 * kStgPitch + oseg * 16);
+                        st16_chk(out0 + o, *reinterpret_cast<const uint4 *>(stg + orow0 * kStgPitch + oseg * 16));
                     if (out1)
-                        *reinterpret_cast<uint4 *>(out1 + o) =
-                            *reinterpret_cast<const uint4 *>(stg + (orow0 + 4) * kStgPitch + oseg * 16);
+                        st16_chk(out1 + o,
+                                 *reinterpret_cast<const uint4 *>(stg + (orow0 + 4) * kStgPitch + oseg * 16));
                     __syncwarp();
                 }
             }

@@ -44,6 +44,27 @@ unsigned int *device_error_word()
     return cache[dev];
 }
 
+#ifdef AR_CHECKED
+// The checked build's record of its first refused access: [taken, address,
+// kind << 32 | bytes].
+__device__ unsigned long long g_check_fault[3] = {0ull, 0ull, 0ull};
+
+unsigned long long *device_check_fault()
+{
+    static std::mutex mu;
+    static unsigned long long *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_check_fault) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned long long *>(p);
+    }
+    return cache[dev];
+}
+#endif
+
 // ---- append ----------------------------------------------------------------
 // One warp per token. new = src (copied only when src is not the slot
 // itself), or prev + src in fp32 rounded once to the storage dtype (block
@@ -74,6 +95,7 @@ __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev
                                                      int norm_full, float eps, int64_t ld,
                                                      int64_t es, bool in_place)
 {
+    AR_CHK_OFF();
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -195,6 +217,7 @@ cudaError_t launch_append(const void *src, const void *prev, void *dst, float *i
 __global__ void __launch_bounds__(256) grad_fold_scalar_kernel(float *dst, const float *src,
                                                                int64_t n, int mode)
 {
+    AR_CHK_OFF();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
         dst[i] = ((mode & 1) ? src[i] : 0.f) + ((mode & 2) ? dst[i] : 0.f);
@@ -203,6 +226,7 @@ __global__ void __launch_bounds__(256) grad_fold_scalar_kernel(float *dst, const
 __global__ void __launch_bounds__(256) grad_fold_kernel(float *dst, const float *src, int64_t n4,
                                                         int mode)
 {
+    AR_CHK_OFF();
     float4 *d4 = reinterpret_cast<float4 *>(dst);
     const float4 *s4 = reinterpret_cast<const float4 *>(src);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
@@ -250,6 +274,7 @@ cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_v
 __global__ void __launch_bounds__(256) token_sum_kernel(const float *grad, int64_t TT, int d,
                                                         float *out)
 {
+    AR_CHK_OFF();
     __shared__ float part[8][33];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
@@ -288,6 +313,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const T *oa, const float *la
                                                     const float *lb, T *out, float *lse,
                                                     int64_t TT, int d, int H)
 {
+    AR_CHK_OFF();
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -387,6 +413,7 @@ __global__ void __cluster_dims__(kRedCtas, 1, 1) __launch_bounds__(kRedWarps * 3
     dqdg_reduce_kernel(const float *__restrict__ ws, int rows, int r, const float *q, int64_t qs,
                        const float *g, int64_t gs, float *dq, float *dg, float *dalpha)
 {
+    AR_CHK_OFF();
     __shared__ float part[kRedWarps][32 * V];
     __shared__ float cta_sum[32 * V];
     __shared__ float red[kRedWarps * 32];

@@ -83,7 +83,8 @@ typedef enum {
     AR_ERR_ORDER = 5,       /* backward not in reverse forward order        */
     AR_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed         */
     AR_ERR_TIMEOUT = 7,     /* a device-side wait ran out (see ar_device_error) */
-    AR_ERR_UNSUPPORTED = 8  /* valid, but outside the fused kernels' shapes */
+    AR_ERR_UNSUPPORTED = 8, /* valid, but outside the fused kernels' shapes */
+    AR_ERR_BOUNDS = 9       /* checked build: an access left its buffers     */
 } ar_status;
 
 typedef enum { AR_F32 = 0, AR_BF16 = 1 } ar_dtype;
@@ -97,6 +98,8 @@ typedef enum { AR_NORM_KEY = 0, AR_NORM_FULL = 1 } ar_norm;
 
 /* Device error bits reported by ar_device_error(). */
 #define AR_DEVERR_WAIT_TIMEOUT 1u
+/* Set only by a library built with the range checks (see ar_checked_fault). */
+#define AR_DEVERR_BOUNDS 2u
 
 typedef struct ar_bank ar_bank; /* opaque host-side handle */
 
@@ -496,9 +499,10 @@ ar_status ar_noalloc_scratch_bytes(size_t *bytes);
 ar_status ar_device_error(uint32_t *bits);
 
 /* The device error word as a status: synchronises the device, reads and
- * clears the word, and returns AR_ERR_TIMEOUT if a device-side wait ran out
- * since the last read (AR_DEVERR_WAIT_TIMEOUT), AR_OK if none did, AR_ERR_CUDA
- * if the device could not be read. */
+ * clears the word, and returns AR_ERR_BOUNDS if a checked kernel skipped an
+ * access since the last read (AR_DEVERR_BOUNDS), else AR_ERR_TIMEOUT if a
+ * device-side wait ran out (AR_DEVERR_WAIT_TIMEOUT), AR_OK if neither
+ * happened, AR_ERR_CUDA if the device could not be read. */
 ar_status ar_device_status(void);
 
 /*
@@ -518,6 +522,41 @@ ar_status ar_device_status(void);
 ar_status ar_route_fwd_lost_copies(ar_bank *bank, const int32_t *rows, int32_t n_src,
                                    int32_t H, const float *q, const float *g, void *out,
                                    float *lse, uint32_t poll_limit, void *stream);
+
+/*
+ * Range checks (a debugging aid with no counterpart in the papers; it stands
+ * in for a memory checker). A library built with AR_CHECKED defined
+ * (libattnres_gb300_checked.so) gives every routing kernel a table of the
+ * buffers of its launch: the bank's rows and gradient rows, where an access
+ * must fall inside one row that the site lists (a store into the bank only
+ * inside the row the call appends), and every other buffer the call takes,
+ * read-only where the call only reads it, with the extents stated in this
+ * header. Each global access the kernels make through their load, store and
+ * bulk-copy paths, and each staged shared-memory access, is checked for
+ * range and alignment first. An access that fails is not made (a load gives
+ * zeros, a bulk copy completes its bytes on its mbarrier without copying),
+ * the first one is recorded, and AR_DEVERR_BOUNDS is set in the device error
+ * word. Nothing traps. The bank append, merge, token-sum, gradient-fold and
+ * dq/dg reduction kernels are not checked.
+ *
+ * ar_checked_fault: *checked = 1 in a checked library, else 0. In a checked
+ * library it synchronises the device and returns the first failed access
+ * since the last call: *addr (a global address, or the shared-window offset
+ * for kind 3), *bytes, *kind (0 none, 1 global load, 2 global store,
+ * 3 shared memory), then clears the record. In an unchecked library the
+ * outputs are zero and nothing touches the device. Errors:
+ * AR_ERR_INVALID_ARG (a null pointer), AR_ERR_CUDA.
+ *
+ * ar_checked_trim_out: a test of the checks themselves. The next launches
+ * declare the output buffer out of a forward (each out[i] of a multi-query
+ * read) `bytes` shorter than the call states, so that stores into its tail
+ * are refused although they lie inside the real buffer; 0 restores the
+ * stated extents. Host state of the library,
+ * not thread-safe. AR_ERR_UNSUPPORTED in an unchecked library,
+ * AR_ERR_INVALID_ARG for a negative size.
+ */
+ar_status ar_checked_fault(int32_t *checked, uint64_t *addr, uint32_t *bytes, uint32_t *kind);
+ar_status ar_checked_trim_out(int64_t bytes);
 
 #ifdef __cplusplus
 }

@@ -279,3 +279,21 @@ def test_lost_copy_hook_checks_precede_launch(B):
     assert _err(B.ar_route_fwd_lost_copies, h, [0], 3, FAKE, None, FAKE, FAKE, 100,
                 0) == "AR_ERR_SHAPE"
     B.ar_bank_destroy(h)
+
+
+def test_unchecked_library_reports_no_range_checks(B):
+    """The library the binding loads by default is built without the range
+    checks: ar_checked_fault says so without touching a device, and the
+    trim hook of the checks is refused."""
+    if B.CHECKED:
+        pytest.skip("the range-checked build is loaded")
+    assert B.ar_checked_fault() == (0, 0, 0, 0)
+    assert _err(B.ar_checked_trim_out, 64) == "AR_ERR_UNSUPPORTED"
+
+
+def test_checked_build_has_its_own_library_and_objects():
+    """The range-checked variant builds from the same sources into its own
+    library and object folder, so the two never overwrite each other."""
+    from depth_wise_attention_ar_gb300 import build
+    assert build.LIB != build.LIB_CHECKED and build.BUILD != build.BUILD_CHECKED
+    assert os.path.dirname(build.LIB_CHECKED) == os.path.dirname(build.LIB)
