@@ -21,6 +21,7 @@ struct CheckTable {
     uint64_t lo[kCheckSpans], hi[kCheckSpans];
     uint8_t wr[kCheckSpans];
     unsigned long long *fault;  // [taken, address, kind << 32 | bytes]
+    int off;                    // 1: this launch is not checked
 };
 #endif
 
@@ -96,19 +97,24 @@ cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps);
 // form, the four-warp kernels.
 bool fwd_fuses_append(const RouteArgs &a, ar_dtype dt, bool in_place);
 // dq and dg are written with the strides of q and g respectively.
+// The launches below take, last, the buffer table of the range-checked build
+// (its chk field; ignored by the normal build, and nullptr = not checked).
 cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, int64_t q_stride,
                                const float *g, int64_t g_stride, float *dq, float *dg,
-                               float *dalpha, cudaStream_t s);
+                               float *dalpha, cudaStream_t s, const RouteArgs *chk = nullptr);
 cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const float *lb,
-                         void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s);
-cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cudaStream_t s);
+                         void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s,
+                         const RouteArgs *chk = nullptr);
+cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cudaStream_t s,
+                             const RouteArgs *chk = nullptr);
 // src is a strided [T, d] view: element (t, c) at src[t * ld + c * es]
 // (ld = 0: the same vector for every token).
 cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col,
                           int64_t T, int d, int r, int inv_ld, int norm_full, float eps,
-                          ar_dtype dt, cudaStream_t s, int64_t ld, int64_t es);
+                          ar_dtype dt, cudaStream_t s, int64_t ld, int64_t es,
+                          const RouteArgs *chk = nullptr);
 cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
-                             bool dst_valid, cudaStream_t s);
+                             bool dst_valid, cudaStream_t s, const RouteArgs *chk = nullptr);
 unsigned int *device_error_word();
 #ifdef AR_CHECKED
 // The checked build's record of the first refused access (three words).

@@ -196,9 +196,110 @@ void chk_fill_multi(ar::MultiArgs &m, const ar_bank *b)
 }
 #define AR_CHK_FILL(a, b, bwd, ws) chk_fill((a), (b), (bwd), (ws))
 #define AR_CHK_FILL_MULTI(m, b) chk_fill_multi((m), (b))
+
+// Tables of the launches that take no RouteArgs (append, fold, token sum,
+// merge, dq/dg reduction), filled in a per-thread slot: a launch copies its
+// parameters when it is made.
+ar::RouteArgs &chk_slot(const ar_bank *b, bool bank_rows, bool grad_rows)
+{
+    thread_local ar::RouteArgs a;
+    std::memset(&a, 0, sizeof(a));
+    ar::CheckTable &c = a.chk;
+    if (bank_rows) {
+        c.bank = reinterpret_cast<uint64_t>(b->rows);
+        c.bank_row = static_cast<uint64_t>(b->T * (int64_t)b->d * (int64_t)b->esize);
+    }
+    if (grad_rows) {
+        c.grad = reinterpret_cast<uint64_t>(b->grad);
+        c.grad_row = static_cast<uint64_t>(b->T * (int64_t)b->d * 4);
+    }
+    c.cap = b->cap;
+    c.fault = ar::device_check_fault();
+    a.err = ar::device_error_word();
+    return a;
+}
+
+// append of row new_row (its bank slot the only store target; the partial
+// sum's row acc_from read), from src: a strided [T, d] view of src_bytes
+// bytes, or a row of the bank itself
+const ar::RouteArgs *chk_append(const ar_bank *b, int new_row, int acc_from, const void *src,
+                                int64_t src_bytes)
+{
+    ar::RouteArgs &a = chk_slot(b, true, false);
+    a.rows[0] = new_row;
+    a.n_src = 1;
+    a.fresh1 = 1;
+    a.acc_row = acc_from;
+    const uint64_t x = reinterpret_cast<uint64_t>(src), lo = a.chk.bank;
+    if (a.chk.bank_row && x >= lo && x < lo + (uint64_t)b->cap * a.chk.bank_row) {
+        const int row = static_cast<int>((x - lo) / a.chk.bank_row);
+        if (row != new_row) a.rows[a.n_src++] = row;
+    } else {
+        chk_span(a, src, src_bytes, false);
+    }
+    chk_span(a, b->inv, b->T * (int64_t)b->inv_ld * 4, true);
+    return &a;
+}
+
+const ar::RouteArgs *chk_grad_rows(const ar_bank *b, int row0, int row1, const float *out,
+                                   int64_t out_bytes)
+{
+    ar::RouteArgs &a = chk_slot(b, false, true);
+    a.rows[a.n_src++] = row0;
+    if (row1 >= 0) a.rows[a.n_src++] = row1;
+    chk_span(a, out, out_bytes, true);
+    return &a;
+}
+
+const ar::RouteArgs *chk_merge(const ar_bank *b, int H, const void *oa, const float *la,
+                               const void *ob, const float *lb, const void *out, const float *lse)
+{
+    ar::RouteArgs &a = chk_slot(b, false, false);
+    const int64_t TD = b->T * (int64_t)b->d * (int64_t)b->esize, TH = b->T * (int64_t)H * 4;
+    chk_span(a, out, TD - g_trim_out, true);
+    chk_span(a, lse, TH, true);
+    chk_span(a, oa, TD, false);
+    chk_span(a, ob, TD, false);
+    chk_span(a, la, TH, false);
+    chk_span(a, lb, TH, false);
+    return &a;
+}
+
+const ar::RouteArgs *chk_reduce(const ar_bank *b, const void *ws, size_t ws_bytes, const float *q,
+                                int64_t qs, const float *g, int64_t gs, const float *dq,
+                                const float *dg, const float *dalpha)
+{
+    ar::RouteArgs &a = chk_slot(b, false, false);
+    chk_span(a, dq, vec_bytes(b->r, qs), true);
+    chk_span(a, dg, vec_bytes(b->r, gs), true);
+    chk_span(a, dalpha, 4, true);
+    chk_span(a, ws, static_cast<int64_t>(ws_bytes), false);
+    chk_span(a, q, vec_bytes(b->r, qs), false);
+    chk_span(a, g, vec_bytes(b->r, gs), false);
+    return &a;
+}
 #else
 #define AR_CHK_FILL(a, b, bwd, ws) ((void)0)
 #define AR_CHK_FILL_MULTI(m, b) ((void)0)
+inline const ar::RouteArgs *chk_append(const ar_bank *, int, int, const void *, int64_t)
+{
+    return nullptr;
+}
+inline const ar::RouteArgs *chk_grad_rows(const ar_bank *, int, int, const float *, int64_t)
+{
+    return nullptr;
+}
+inline const ar::RouteArgs *chk_merge(const ar_bank *, int, const void *, const float *,
+                                      const void *, const float *, const void *, const float *)
+{
+    return nullptr;
+}
+inline const ar::RouteArgs *chk_reduce(const ar_bank *, const void *, size_t, const float *,
+                                       int64_t, const float *, int64_t, const float *,
+                                       const float *, const float *)
+{
+    return nullptr;
+}
 #endif
 
 }  // namespace
@@ -301,11 +402,14 @@ ar_status ar_bank_append_strided(ar_bank *bank, const void *src, int64_t token_s
     ar_bank_row_ptr(bank, bank->count, &dst);
     const void *prev = nullptr;
     if (accumulate_from >= 0) ar_bank_row_ptr(bank, accumulate_from, const_cast<void **>(&prev));
-    const cudaError_t e = ar::launch_append(src, prev, dst, bank->inv + bank->count, bank->T,
-                                            bank->d, bank->r, bank->inv_ld, bank->norm_full,
-                                            bank->eps, bank->dtype,
-                                            static_cast<cudaStream_t>(stream), token_stride,
-                                            elem_stride);
+    const int64_t src_bytes =
+        bank->T > 0 ? ((bank->T - 1) * token_stride + (int64_t)(bank->d - 1) * elem_stride + 1) *
+                          (int64_t)bank->esize
+                    : 0;
+    const cudaError_t e = ar::launch_append(
+        src, prev, dst, bank->inv + bank->count, bank->T, bank->d, bank->r, bank->inv_ld,
+        bank->norm_full, bank->eps, bank->dtype, static_cast<cudaStream_t>(stream), token_stride,
+        elem_stride, chk_append(bank, bank->count, accumulate_from, src, src_bytes));
     if (e != cudaSuccess) return from_cuda(e);
     if (out_row) *out_row = bank->count;
     ++bank->count;
@@ -550,9 +654,10 @@ ar_status route_bwd_impl(ar_bank *bank, const ar_site &st_, const void *out, con
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (bank->T == 0) {
         // no tokens: the reduction over zero workspace rows writes zeros
-        const cudaError_t e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), 0, bank->r, q,
-                                                     st_.q_stride, g, st_.g_stride, dq, dg,
-                                                     dalpha, s);
+        const cudaError_t e = ar::launch_dqdg_reduce(
+            static_cast<const float *>(ws), 0, bank->r, q, st_.q_stride, g, st_.g_stride, dq, dg,
+            dalpha, s,
+            chk_reduce(bank, ws, ws_bytes, q, st_.q_stride, g, st_.g_stride, dq, dg, dalpha));
         if (e != cudaSuccess) return from_cuda(e);
     } else {
         ar::RouteArgs a;
@@ -575,8 +680,10 @@ ar_status route_bwd_impl(ar_bank *bank, const ar_site &st_, const void *out, con
         AR_CHK_FILL(a, bank, true, ws_bytes);
         e = ar::launch_route_bwd(a, bank->dtype, s);
         if (e != cudaSuccess) return from_cuda(e);
-        e = ar::launch_dqdg_reduce(static_cast<const float *>(ws), ws_rows, bank->r, q,
-                                   st_.q_stride, g, st_.g_stride, dq, dg, dalpha, s);
+        e = ar::launch_dqdg_reduce(
+            static_cast<const float *>(ws), ws_rows, bank->r, q, st_.q_stride, g, st_.g_stride, dq,
+            dg, dalpha, s,
+            chk_reduce(bank, ws, ws_bytes, q, st_.q_stride, g, st_.g_stride, dq, dg, dalpha));
         if (e != cudaSuccess) return from_cuda(e);
     }
     for (int i = 0; i < n_src; ++i) bank->touched[rows[i]] = 1;
@@ -622,10 +729,10 @@ ar_status ar_bank_append_broadcast(ar_bank *bank, const void *vec, int32_t *out_
     if ((reinterpret_cast<uintptr_t>(vec) % bank->esize) != 0) return AR_ERR_ALIGN;
     void *dst = nullptr;
     ar_bank_row_ptr(bank, bank->count, &dst);
-    const cudaError_t e = ar::launch_append(vec, nullptr, dst, bank->inv + bank->count, bank->T,
-                                            bank->d, bank->r, bank->inv_ld, bank->norm_full,
-                                            bank->eps, bank->dtype,
-                                            static_cast<cudaStream_t>(stream), 0, 1);
+    const cudaError_t e = ar::launch_append(
+        vec, nullptr, dst, bank->inv + bank->count, bank->T, bank->d, bank->r, bank->inv_ld,
+        bank->norm_full, bank->eps, bank->dtype, static_cast<cudaStream_t>(stream), 0, 1,
+        chk_append(bank, bank->count, -1, vec, (int64_t)bank->d * (int64_t)bank->esize));
     if (e != cudaSuccess) return from_cuda(e);
     if (out_row) *out_row = bank->count;
     ++bank->count;
@@ -644,7 +751,7 @@ ar_status ar_bank_grad_token_sum(const ar_bank *bank, int32_t row, float *out, v
         e = cudaMemsetAsync(out, 0, (size_t)bank->d * sizeof(float), s);
     else
         e = ar::launch_token_sum(bank->grad + (int64_t)row * bank->T * bank->d, bank->T, bank->d,
-                                 out, s);
+                                 out, s, chk_grad_rows(bank, row, -1, out, (int64_t)bank->d * 4));
     return e == cudaSuccess ? AR_OK : from_cuda(e);
 }
 
@@ -660,7 +767,8 @@ ar_status ar_bank_grad_fold(ar_bank *bank, int32_t dst_row, int32_t src_row, voi
     const float *src = bank->grad + (int64_t)src_row * n;
     const cudaError_t e = ar::launch_grad_fold(dst, src, n, bank->touched[src_row] != 0,
                                                bank->touched[dst_row] != 0,
-                                               static_cast<cudaStream_t>(stream));
+                                               static_cast<cudaStream_t>(stream),
+                                               chk_grad_rows(bank, dst_row, src_row, nullptr, 0));
     if (e != cudaSuccess) return from_cuda(e);
     bank->touched[dst_row] = 1;
     return AR_OK;
@@ -678,7 +786,8 @@ ar_status ar_route_merge(const ar_bank *bank, int32_t H, const void *out_a, cons
         !aligned4(lse_b) || !aligned4(lse))
         return AR_ERR_ALIGN;
     const cudaError_t e = ar::launch_merge(out_a, lse_a, out_b, lse_b, out, lse, bank->T, bank->d,
-                                           H, bank->dtype, static_cast<cudaStream_t>(stream));
+                                           H, bank->dtype, static_cast<cudaStream_t>(stream),
+                                           chk_merge(bank, H, out_a, lse_a, out_b, lse_b, out, lse));
     return e == cudaSuccess ? AR_OK : from_cuda(e);
 }
 

@@ -49,7 +49,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 static __shared__ const RouteArgs *chk_args_s;
 extern __shared__ __align__(16) unsigned char chk_dyn_smem[];
 
-__device__ __forceinline__ void chk_enter(const RouteArgs &a) { chk_args_s = &a; }
+__device__ __forceinline__ void chk_enter(const RouteArgs &a) { chk_args_s = a.chk.off ? nullptr : &a; }
 __device__ __forceinline__ void chk_off() { chk_args_s = nullptr; }
 
 enum : uint32_t { kChkLoad = 1, kChkStore = 2, kChkShared = 3 };
@@ -123,6 +123,10 @@ static __device__ __noinline__ bool chk_shared(const void *p, uint32_t bytes, ui
     if (!::ar::chk_shared((p), (n), (al))) { __VA_ARGS__; }
 #define AR_CHK_ENTER(a) ::ar::chk_enter(a)
 #define AR_CHK_OFF() ::ar::chk_off()
+// kernels without a RouteArgs parameter take the table as a last parameter
+#define AR_CHK_PARAM , const __grid_constant__ ::ar::RouteArgs chk_args
+#define AR_CHK_PASS(a) , (a)
+#define AR_CHK_ENTER_PARAM() ::ar::chk_enter(chk_args)
 #else
 #define AR_CHK_G(p, n, st, al) true
 #define AR_CHK_S(p, n, al) true
@@ -130,6 +134,9 @@ static __device__ __noinline__ bool chk_shared(const void *p, uint32_t bytes, ui
 #define AR_GUARD_S(p, n, al, ...)
 #define AR_CHK_ENTER(a) ((void)0)
 #define AR_CHK_OFF() ((void)0)
+#define AR_CHK_PARAM
+#define AR_CHK_PASS(a)
+#define AR_CHK_ENTER_PARAM() ((void)0)
 #endif
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
@@ -568,6 +575,18 @@ __device__ __forceinline__ float ld_chk(const float *p)  // plain (coherent) loa
 {
     AR_GUARD_G(p, 4, false, 4, return 0.f)
     return *p;
+}
+// Checked plain load / store of one element of any type through a generic
+// pointer to global memory.
+template <typename E> __device__ __forceinline__ E ld_chk_t(const E *p)
+{
+    AR_GUARD_G(p, (uint32_t)sizeof(E), false, (uint32_t)sizeof(E), return E{})
+    return *p;
+}
+template <typename E> __device__ __forceinline__ void st_chk_t(E *p, E v)
+{
+    AR_GUARD_G(p, (uint32_t)sizeof(E), true, (uint32_t)sizeof(E), return)
+    *p = v;
 }
 __device__ __forceinline__ uint4 ldg16_chk(const uint4 *p)
 {

@@ -93,9 +93,9 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev, T *dst, float *inv,
                                                      int64_t TT, int d, int r, int inv_ld,
                                                      int norm_full, float eps, int64_t ld,
-                                                     int64_t es, bool in_place)
+                                                     int64_t es, bool in_place AR_CHK_PARAM)
 {
-    AR_CHK_OFF();
+    AR_CHK_ENTER_PARAM();
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev
                 for (int e = 0; e < 8; ++e) {
                     const int col = c * 8 + e;
                     if (col < d) {
-                        float v = to_f32(in_place ? o[col] : s[col * es]);
-                        if (prev) v += to_f32(prev[t * d + col]);
+                        float v = to_f32(in_place ? ld_chk_t(o + col) : ld_chk_t(s + col * es));
+                        if (prev) v += to_f32(ld_chk_t(prev + (t * d + col)));
                         if (!in_place) st_elem(o + col, v);
                         // square the stored (rounded) value
                         const float vr = sizeof(T) == 2 ? round_bf16(v) : v;
@@ -159,15 +159,29 @@ __global__ void __launch_bounds__(256) append_kernel(const T *src, const T *prev
             }
         }
         ss = warp_sum(ss);
-        if (lane == 0) inv[t * inv_ld] = rsqrtf(fmaf(ss, inv_w, eps));
+        if (lane == 0) st_chk_t(inv + t * inv_ld, rsqrtf(fmaf(ss, inv_w, eps)));
     }
 }
+
+#ifdef AR_CHECKED
+// The table a launch passes when its caller gave none: not checked.
+static const RouteArgs &chk_or_off(const RouteArgs *chk)
+{
+    static RouteArgs off = [] {
+        RouteArgs a{};
+        a.chk.off = 1;
+        return a;
+    }();
+    return chk ? *chk : off;
+}
+#endif
 
 template <typename E>
 static cudaError_t append_t(const void *src, const void *prev, void *dst, float *inv_col, int64_t T,
                             int d, int r, int inv_ld, int norm_full, float eps, int64_t ld,
-                            int64_t es, cudaStream_t s)
+                            int64_t es, cudaStream_t s, const RouteArgs *chk)
 {
+    (void)chk;
     const bool in_place = src == dst && prev == nullptr && ld == d && es == 1;
     const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
                          reinterpret_cast<uintptr_t>(prev);
@@ -187,25 +201,28 @@ static cudaError_t append_t(const void *src, const void *prev, void *dst, float 
     E *dp = static_cast<E *>(dst);
     if (mode == kInPlace)
         append_kernel<E, kInPlace><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld,
-                                                        norm_full, eps, ld, es, in_place);
+                                                        norm_full, eps, ld, es,
+                                                        in_place AR_CHK_PASS(chk_or_off(chk)));
     else if (mode == kCopy)
         append_kernel<E, kCopy><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld,
-                                                     norm_full, eps, ld, es, in_place);
+                                                     norm_full, eps, ld, es,
+                                                     in_place AR_CHK_PASS(chk_or_off(chk)));
     else
         append_kernel<E, kScalar><<<grid, 256, 0, s>>>(sp, pp, dp, inv_col, T, d, r, inv_ld,
-                                                       norm_full, eps, ld, es, in_place);
+                                                       norm_full, eps, ld, es,
+                                                       in_place AR_CHK_PASS(chk_or_off(chk)));
     return cudaGetLastError();
 }
 
 cudaError_t launch_append(const void *src, const void *prev, void *dst, float *inv_col, int64_t T,
                           int d, int r, int inv_ld, int norm_full, float eps, ar_dtype dt,
-                          cudaStream_t s, int64_t ld, int64_t es)
+                          cudaStream_t s, int64_t ld, int64_t es, const RouteArgs *chk)
 {
     if (T == 0) return cudaSuccess;
     return dt == AR_BF16 ? append_t<__nv_bfloat16>(src, prev, dst, inv_col, T, d, r, inv_ld,
-                                                   norm_full, eps, ld, es, s)
+                                                   norm_full, eps, ld, es, s, chk)
                          : append_t<float>(src, prev, dst, inv_col, T, d, r, inv_ld, norm_full,
-                                           eps, ld, es, s);
+                                           eps, ld, es, s, chk);
 }
 
 // ---- gradient fold (block-sum fan-out) -----------------------------------------
@@ -215,35 +232,36 @@ cudaError_t launch_append(const void *src, const void *prev, void *dst, float *i
 // version t ("Low-Rank Attention Residuals", Appendix B.4: every write of a
 // block receives the block sum's adjoint).
 __global__ void __launch_bounds__(256) grad_fold_scalar_kernel(float *dst, const float *src,
-                                                               int64_t n, int mode)
+                                                               int64_t n, int mode AR_CHK_PARAM)
 {
-    AR_CHK_OFF();
+    AR_CHK_ENTER_PARAM();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
-        dst[i] = ((mode & 1) ? src[i] : 0.f) + ((mode & 2) ? dst[i] : 0.f);
+        st_chk_t(dst + i, ((mode & 1) ? ld_chk_t(src + i) : 0.f) + ((mode & 2) ? ld_chk_t(dst + i) : 0.f));
 }
 
 __global__ void __launch_bounds__(256) grad_fold_kernel(float *dst, const float *src, int64_t n4,
-                                                        int mode)
+                                                        int mode AR_CHK_PARAM)
 {
-    AR_CHK_OFF();
+    AR_CHK_ENTER_PARAM();
     float4 *d4 = reinterpret_cast<float4 *>(dst);
     const float4 *s4 = reinterpret_cast<const float4 *>(src);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
          i += (int64_t)gridDim.x * blockDim.x) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (mode & 1) v = s4[i];                  // src has content
+        if (mode & 1) v = ld_chk_t(s4 + i);       // src has content
         if (mode & 2) {                           // dst has content
-            const float4 o = d4[i];
+            const float4 o = ld_chk_t(d4 + i);
             v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
         }
-        d4[i] = v;
+        st_chk_t(d4 + i, v);
     }
 }
 
 cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_valid,
-                             bool dst_valid, cudaStream_t s)
+                             bool dst_valid, cudaStream_t s, const RouteArgs *chk)
 {
+    (void)chk;
     if (n == 0) return cudaSuccess;
     const int mode = (src_valid ? 1 : 0) | (dst_valid ? 2 : 0);
     int grid = 0;
@@ -254,7 +272,7 @@ cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_v
         if (e != cudaSuccess) return e;
         const int64_t need = (n + 255) / 256;
         if (need < grid) grid = (int)need;
-        grad_fold_scalar_kernel<<<grid, 256, 0, s>>>(dst, src, n, mode);
+        grad_fold_scalar_kernel<<<grid, 256, 0, s>>>(dst, src, n, mode AR_CHK_PASS(chk_or_off(chk)));
         return cudaGetLastError();
     }
     cudaError_t e = persistent_grid(reinterpret_cast<const void *>(&grad_fold_kernel), 256, 0, &grid);
@@ -262,7 +280,7 @@ cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_v
     const int64_t n4 = n / 4;
     const int64_t need = (n4 + 255) / 256;
     if (need < grid) grid = (int)need;
-    grad_fold_kernel<<<grid, 256, 0, s>>>(dst, src, n4, mode);
+    grad_fold_kernel<<<grid, 256, 0, s>>>(dst, src, n4, mode AR_CHK_PASS(chk_or_off(chk)));
     return cudaGetLastError();
 }
 
@@ -272,28 +290,30 @@ cudaError_t launch_grad_fold(float *dst, const float *src, int64_t n, bool src_v
 // of the delta form, "Multi-Head Attention Residuals", Sec. 3.3). One block per
 // 32 columns; warp w sums tokens w, w + 8, ..., then the 8 warps in order.
 __global__ void __launch_bounds__(256) token_sum_kernel(const float *grad, int64_t TT, int d,
-                                                        float *out)
+                                                        float *out AR_CHK_PARAM)
 {
-    AR_CHK_OFF();
+    AR_CHK_ENTER_PARAM();
     __shared__ float part[8][33];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
     float s = 0.f;
     if (c < d)
-        for (int64_t t = w; t < TT; t += 8) s += grad[t * d + c];
+        for (int64_t t = w; t < TT; t += 8) s += ld_chk_t(grad + (t * d + c));
     part[w][lane] = s;
     __syncthreads();
     if (w == 0 && c < d) {
         float t = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) t += part[k][lane];
-        out[c] = t;
+        st_chk_t(out + c, t);
     }
 }
 
-cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cudaStream_t s)
+cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cudaStream_t s,
+                             const RouteArgs *chk)
 {
-    token_sum_kernel<<<(d + 31) / 32, 256, 0, s>>>(grad, T, d, out);
+    (void)chk;
+    token_sum_kernel<<<(d + 31) / 32, 256, 0, s>>>(grad, T, d, out AR_CHK_PASS(chk_or_off(chk)));
     return cudaGetLastError();
 }
 
@@ -311,9 +331,9 @@ cudaError_t launch_token_sum(const float *grad, int64_t T, int d, float *out, cu
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) merge_kernel(const T *oa, const float *la, const T *ob,
                                                     const float *lb, T *out, float *lse,
-                                                    int64_t TT, int d, int H)
+                                                    int64_t TT, int d, int H AR_CHK_PARAM)
 {
-    AR_CHK_OFF();
+    AR_CHK_ENTER_PARAM();
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -321,7 +341,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const T *oa, const float *la
     for (int64_t t = w0; t < TT; t += nw) {
         for (int c = lane; c < nch; c += 32) {
             const int h = (VEC ? c * 8 : c) / K;
-            const float a = la[t * H + h], b = lb[t * H + h];
+            const float a = ld_chk_t(la + (t * H + h)), b = ld_chk_t(lb + (t * H + h));
             const float m = fmaxf(a, b);
             const float ea = exp2f((a - m) * kLog2e), eb = exp2f((b - m) * kLog2e);
             const float inv = 1.f / (ea + eb);
@@ -333,22 +353,24 @@ __global__ void __launch_bounds__(256) merge_kernel(const T *oa, const float *la
                 for (int e = 0; e < 8; ++e) z[e] = fmaf(ea * inv, x[e], eb * inv * y[e]);
                 st_chunk_g(out + t * d + c * 8, z);
             } else {
-                const float x = to_f32(oa[t * d + c]), y = to_f32(ob[t * d + c]);
+                const float x = to_f32(ld_chk_t(oa + (t * d + c))), y = to_f32(ld_chk_t(ob + (t * d + c)));
                 st_elem(out + t * d + c, fmaf(ea * inv, x, eb * inv * y));
             }
         }
         for (int h = lane; h < H; h += 32) {
-            const float a = la[t * H + h], b = lb[t * H + h];
+            const float a = ld_chk_t(la + (t * H + h)), b = ld_chk_t(lb + (t * H + h));
             const float m = fmaxf(a, b);
-            lse[t * H + h] = m + log2f(exp2f((a - m) * kLog2e) + exp2f((b - m) * kLog2e)) * kLn2;
+            st_chk_t(lse + (t * H + h), m + log2f(exp2f((a - m) * kLog2e) + exp2f((b - m) * kLog2e)) * kLn2);
         }
     }
 }
 
 template <typename E>
 static cudaError_t merge_t(const void *oa, const float *la, const void *ob, const float *lb,
-                           void *out, float *lse, int64_t T, int d, int H, cudaStream_t s)
+                           void *out, float *lse, int64_t T, int d, int H, cudaStream_t s,
+                           const RouteArgs *chk)
 {
+    (void)chk;
     const uintptr_t al = reinterpret_cast<uintptr_t>(oa) | reinterpret_cast<uintptr_t>(ob) |
                          reinterpret_cast<uintptr_t>(out);
     const bool vec = d % 8 == 0 && (d / H) % 8 == 0 && (al & 15) == 0;
@@ -362,18 +384,21 @@ static cudaError_t merge_t(const void *oa, const float *la, const void *ob, cons
     const E *a = static_cast<const E *>(oa), *b = static_cast<const E *>(ob);
     E *o = static_cast<E *>(out);
     if (vec)
-        merge_kernel<E, true><<<grid, 256, 0, s>>>(a, la, b, lb, o, lse, T, d, H);
+        merge_kernel<E, true><<<grid, 256, 0, s>>>(a, la, b, lb, o, lse, T, d,
+                                                   H AR_CHK_PASS(chk_or_off(chk)));
     else
-        merge_kernel<E, false><<<grid, 256, 0, s>>>(a, la, b, lb, o, lse, T, d, H);
+        merge_kernel<E, false><<<grid, 256, 0, s>>>(a, la, b, lb, o, lse, T, d,
+                                                    H AR_CHK_PASS(chk_or_off(chk)));
     return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const void *oa, const float *la, const void *ob, const float *lb,
-                         void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s)
+                         void *out, float *lse, int64_t T, int d, int H, ar_dtype dt, cudaStream_t s,
+                         const RouteArgs *chk)
 {
     if (T == 0) return cudaSuccess;
-    return dt == AR_BF16 ? merge_t<__nv_bfloat16>(oa, la, ob, lb, out, lse, T, d, H, s)
-                         : merge_t<float>(oa, la, ob, lb, out, lse, T, d, H, s);
+    return dt == AR_BF16 ? merge_t<__nv_bfloat16>(oa, la, ob, lb, out, lse, T, d, H, s, chk)
+                         : merge_t<float>(oa, la, ob, lb, out, lse, T, d, H, s, chk);
 }
 
 // ---- dq / dg -----------------------------------------------------------------
@@ -398,12 +423,14 @@ template <int V>
 __device__ __forceinline__ void red_load(const float *p, float (&x)[V])
 {
     if constexpr (V == 4) {
+        AR_GUARD_G(p, 16, false, 16, x[0] = x[1] = x[2] = x[3] = 0.f; return)
         const float4 v = __ldcg(reinterpret_cast<const float4 *>(p));
         x[0] = v.x;
         x[1] = v.y;
         x[2] = v.z;
         x[3] = v.w;
     } else {
+        AR_GUARD_G(p, 4, false, 4, x[0] = 0.f; return)
         x[0] = __ldcg(p);
     }
 }
@@ -411,9 +438,10 @@ __device__ __forceinline__ void red_load(const float *p, float (&x)[V])
 template <int V>
 __global__ void __cluster_dims__(kRedCtas, 1, 1) __launch_bounds__(kRedWarps * 32)
     dqdg_reduce_kernel(const float *__restrict__ ws, int rows, int r, const float *q, int64_t qs,
-                       const float *g, int64_t gs, float *dq, float *dg, float *dalpha)
+                       const float *g, int64_t gs, float *dq, float *dg,
+                       float *dalpha AR_CHK_PARAM)
 {
-    AR_CHK_OFF();
+    AR_CHK_ENTER_PARAM();
     __shared__ float part[kRedWarps][32 * V];
     __shared__ float cta_sum[32 * V];
     __shared__ float red[kRedWarps * 32];
@@ -475,22 +503,22 @@ __global__ void __cluster_dims__(kRedCtas, 1, 1) __launch_bounds__(kRedWarps * 3
 #pragma unroll
         for (int e = 0; e < V; ++e) {
             const int c = c0 + e;
-            dq[c * qs] = (g ? g[c * gs] : 1.0f) * t[e];
-            if (dg) dg[c * gs] = q[c * qs] * t[e];
+            st_chk_t(dq + c * qs, (g ? ld_chk_t(g + c * gs) : 1.0f) * t[e]);
+            if (dg) st_chk_t(dg + c * gs, ld_chk_t(q + c * qs) * t[e]);
         }
     }
     if (dalpha && blockIdx.y == 0 && rank == 1) {
         // dL/dalpha of the delta form: the rows * 4 tail partials, fixed order
         const float *tail = ws + (int64_t)rows * r;
         float a = 0.f;
-        for (int k = threadIdx.x; k < rows * 4; k += kRedWarps * 32) a += tail[k];
+        for (int k = threadIdx.x; k < rows * 4; k += kRedWarps * 32) a += ld_chk_t(tail + k);
         red[threadIdx.x] = a;
         __syncthreads();
         for (int o = kRedWarps * 16; o > 0; o >>= 1) {
             if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
             __syncthreads();
         }
-        if (threadIdx.x == 0) *dalpha = red[0];
+        if (threadIdx.x == 0) st_chk_t(dalpha, red[0]);
     }
     // no CTA leaves while CTA 0 may still read its shared memory
     cl.sync();
@@ -498,16 +526,19 @@ __global__ void __cluster_dims__(kRedCtas, 1, 1) __launch_bounds__(kRedWarps * 3
 
 cudaError_t launch_dqdg_reduce(const float *ws, int rows, int r, const float *q, int64_t q_stride,
                                const float *g, int64_t g_stride, float *dq, float *dg,
-                               float *dalpha, cudaStream_t s)
+                               float *dalpha, cudaStream_t s, const RouteArgs *chk)
 {
+    (void)chk;
     if (r % 4 == 0) {
         const dim3 grid(kRedCtas, (r / 4 + 31) / 32);
         dqdg_reduce_kernel<4><<<grid, kRedWarps * 32, 0, s>>>(ws, rows, r, q, q_stride, g,
-                                                             g_stride, dq, dg, dalpha);
+                                                             g_stride, dq, dg,
+                                                             dalpha AR_CHK_PASS(chk_or_off(chk)));
     } else {
         const dim3 grid(kRedCtas, (r + 31) / 32);
         dqdg_reduce_kernel<1><<<grid, kRedWarps * 32, 0, s>>>(ws, rows, r, q, q_stride, g,
-                                                             g_stride, dq, dg, dalpha);
+                                                             g_stride, dq, dg,
+                                                             dalpha AR_CHK_PASS(chk_or_off(chk)));
     }
     return cudaGetLastError();
 }

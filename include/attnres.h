@@ -526,18 +526,19 @@ ar_status ar_route_fwd_lost_copies(ar_bank *bank, const int32_t *rows, int32_t n
 /*
  * Range checks (a debugging aid with no counterpart in the papers; it stands
  * in for a memory checker). A library built with AR_CHECKED defined
- * (libattnres_gb300_checked.so) gives every routing kernel a table of the
+ * (libattnres_gb300_checked.so) gives every kernel launch a table of the
  * buffers of its launch: the bank's rows and gradient rows, where an access
  * must fall inside one row that the site lists (a store into the bank only
  * inside the row the call appends), and every other buffer the call takes,
  * read-only where the call only reads it, with the extents stated in this
  * header. Each global access the kernels make through their load, store and
- * bulk-copy paths, and each staged shared-memory access, is checked for
- * range and alignment first. An access that fails is not made (a load gives
+ * bulk-copy paths, and each access to the rows staged in shared memory
+ * (not the tensor-core tile loads), is checked for range and alignment
+ * first. An access that fails is not made (a load gives
  * zeros, a bulk copy completes its bytes on its mbarrier without copying),
  * the first one is recorded, and AR_DEVERR_BOUNDS is set in the device error
- * word. Nothing traps. The bank append, merge, token-sum, gradient-fold and
- * dq/dg reduction kernels are not checked.
+ * word. Nothing traps. Every kernel of the library is checked, the append,
+ * merge, token-sum, gradient-fold and dq/dg reduction kernels included.
  *
  * ar_checked_fault: *checked = 1 in a checked library, else 0. In a checked
  * library it synchronises the device and returns the first failed access
@@ -548,10 +549,10 @@ ar_status ar_route_fwd_lost_copies(ar_bank *bank, const int32_t *rows, int32_t n
  * AR_ERR_INVALID_ARG (a null pointer), AR_ERR_CUDA.
  *
  * ar_checked_trim_out: a test of the checks themselves. The next launches
- * declare the output buffer out of a forward (each out[i] of a multi-query
- * read) `bytes` shorter than the call states, so that stores into its tail
- * are refused although they lie inside the real buffer; 0 restores the
- * stated extents. Host state of the library,
+ * declare the output buffer out of a forward or a merge (each out[i] of a
+ * multi-query read) `bytes` shorter than the call states, so that stores
+ * into its tail are refused although they lie inside the real buffer; 0
+ * restores the stated extents. Host state of the library,
  * not thread-safe. AR_ERR_UNSUPPORTED in an unchecked library,
  * AR_ERR_INVALID_ARG for a negative size.
  */

@@ -138,3 +138,41 @@ def test_multi_query_stores_past_a_shortened_output_are_refused(B, orc):
         assert _nmax(outs[i][: T - 1].double().cpu().numpy(), ref_out[: T - 1]) < 2e-2
         assert _nmax(lses[i].double().cpu().numpy(), ref_lse) < 2e-2
     bank.close()
+
+
+@pytest.mark.parametrize("d,H", [(1280, 8), (520, 4)])
+def test_merge_stores_past_a_shortened_output_are_refused(B, orc, d, H):
+    """The same check on a kernel that takes its buffer table as a parameter
+    of its own (the merge of two partial reads): the vector path (d = 1280)
+    and the one-column path (d = 520)."""
+    import torch
+    T, N, dt = 301, 4, "bf16"
+    inp = synth.HostInputs(seed=97 + d, q_std=0.5, g_kind="random")
+    bank = B.Bank(T, d, d, N, dt)
+    for j in range(N):
+        bank.append(inp.output(j, T, d, dt))
+    q, g = inp.query(0, d), inp.norm_weight(0, d)
+    out_a, lse_a = bank.route_fwd([0, 1, 2], H, q, g, site_id=0)
+    out_b, lse_b = bank.route_fwd([3], H, q, g, site_id=1)
+    out = torch.full((T, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, H), 7.0, device="cuda")
+    B.ar_device_status()
+    assert B.ar_checked_fault()[3] == 0
+    B.ar_checked_trim_out(d * 2)
+    try:
+        B.ar_route_merge(bank.handle, H, out_a, lse_a, out_b, lse_b, out, lse)
+    finally:
+        B.ar_checked_trim_out(0)
+    checked, addr, nbytes, kind = B.ar_checked_fault()
+    assert checked == 1 and kind == 2
+    base = out.data_ptr() + (T - 1) * d * 2
+    assert base <= addr < base + d * 2
+    with pytest.raises(B.ARError) as e:
+        B.ar_device_status()
+    assert e.value.name == "AR_ERR_BOUNDS"
+    assert torch.all(out[T - 1] == 7.0)
+    host = [inp.host_output(j, T, d, dt) for j in range(N)]
+    ref_out, ref_lse = orc.route_fwd(host, inp.host_query(0, d), inp.host_norm_weight(0, d), H)
+    assert _nmax(out[: T - 1].double().cpu().numpy(), ref_out[: T - 1]) < 2e-2
+    assert _nmax(lse.double().cpu().numpy(), ref_lse) < 2e-2
+    bank.close()
