@@ -491,7 +491,7 @@ ar_status ar_route_bwd_noalloc(ar_bank *bank, const int32_t *rows, int32_t n_src
                                void *stream);
 
 /* The size of ar_route_bwd_noalloc's fixed scratch array in bytes
- * (AR_NOALLOC_SCRATCH_BYTES, as this build of the library has it). */
+ * (AR_NOALLOC_SCRATCH_BYTES, the value the library was compiled with). */
 ar_status ar_noalloc_scratch_bytes(size_t *bytes);
 
 /* Read and clear the device error word of the current device (bit mask of

@@ -47,7 +47,7 @@ typedef double real;
 #define ORC_BAD_ARG 1
 #define ORC_NO_MEMORY 2
 
-/* Bytes of the arithmetic type of this build (8: float64, 4: float32). */
+/* Bytes of the arithmetic type this file was compiled with (8: float64, 4: float32). */
 int orc_real_bytes(void) { return (int)sizeof(real); }
 
 int orc_max_threads(void)
