@@ -9,6 +9,7 @@
 
 #include "ar_internal.h"
 #include "attnres.h"
+#include "checks.h"
 
 namespace ar {
 
@@ -66,40 +67,14 @@ static __device__ __noinline__ void chk_record(const RouteArgs *a, uint64_t addr
     if (a->err) atomicOr(a->err, AR_DEVERR_BOUNDS);
 }
 
-// A row of the bank or of the gradient rows that this launch may touch:
-// a listed row; in the bank, a store only into the row the call appends,
-// and a load also from the row a fused partial sum starts from.
-__device__ __forceinline__ bool chk_row_ok(const RouteArgs *a, uint64_t row, bool bank, bool store)
-{
-    if (bank && store) return a->fresh1 > 0 && row == static_cast<uint64_t>(a->rows[a->fresh1 - 1]);
-    for (int i = 0; i < a->n_src; ++i)
-        if (row == static_cast<uint64_t>(a->rows[i])) return true;
-    return bank && a->fresh1 > 0 && a->acc_row >= 0 && row == static_cast<uint64_t>(a->acc_row);
-}
-
+// The decision itself (chk_decide, checks.h) is shared with a host test.
 static __device__ __noinline__ bool chk_global(const void *p, uint32_t bytes, bool store, uint32_t align)
 {
     const RouteArgs *a = chk_args_s;
     if (!a) return true;
-    const CheckTable &c = a->chk;
-    const uint64_t x = reinterpret_cast<uint64_t>(p), e = x + bytes;
-    const uint32_t kind = store ? kChkStore : kChkLoad;
-    if ((x | bytes) % align != 0) {
-        chk_record(a, x, bytes, kind);
-        return false;
-    }
-    for (int b = 0; b < 2; ++b) {
-        const uint64_t base = b ? c.grad : c.bank, rb = b ? c.grad_row : c.bank_row;
-        if (base && rb && x >= base && x < base + static_cast<uint64_t>(c.cap) * rb) {
-            const uint64_t row = (x - base) / rb;
-            if (e <= base + (row + 1) * rb && chk_row_ok(a, row, b == 0, store)) return true;
-            chk_record(a, x, bytes, kind);
-            return false;
-        }
-    }
-    for (int i = 0; i < c.n; ++i)
-        if (x >= c.lo[i] && e <= c.hi[i] && (!store || c.wr[i])) return true;
-    chk_record(a, x, bytes, kind);
+    const uint64_t x = reinterpret_cast<uint64_t>(p);
+    if (chk_decide(*a, x, bytes, store, align)) return true;
+    chk_record(a, x, bytes, store ? kChkStore : kChkLoad);
     return false;
 }
 
