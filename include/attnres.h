@@ -315,7 +315,15 @@ ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes);
  * ar_bank_zero_grad, an in-place accumulation afterwards — and dL/dq, dL/dg.
  *   rows, n_src, H, q, g : exactly as in the forward of this site
  *   out   : device [T, d], this site's forward output (its per-head dot with
- *           dout is the softmax coupling term)
+ *           dout is the softmax coupling term). The coupling is read from
+ *           this output as stored, in one pass, where MHAR Figure 10 sums it
+ *           over the sources in a first pass: with a bf16 bank its rounding
+ *           enters every routing feedback as w * <dout_h, rounding_h>. That is
+ *           small, but a source that holds nearly all of a head's weight has
+ *           a nearly cancelling feedback. Its key-path gradient can then
+ *           differ from the exact one by a few percent of the row's largest
+ *           gradient: 3.3 % measured on the LR page's 4B shape with peaked
+ *           queries.
  *   dout  : device [T, d] of the bank dtype, dL/dout
  *   lse   : device float [T, H] written by this site's forward
  *   dq    : device float [r], overwritten with dL/dq

@@ -78,7 +78,7 @@ def lib(precision: str = "f64"):
             L.orc_inv_rms.restype = i32
             L.orc_route_fwd.argtypes = [P, i32, i64, i32, i32, i32, i32, f64, P, P, P, P, P]
             L.orc_route_fwd.restype = i32
-            L.orc_route_bwd.argtypes = [P, i32, i64, i32, i32, i32, i32, f64, P, P, P, P, P, P]
+            L.orc_route_bwd.argtypes = [P, i32, i64, i32, i32, i32, i32, f64, P, P, P, P, P, P, P]
             L.orc_route_bwd.restype = i32
             if L.orc_real_bytes() != np.dtype(_NP[precision]).itemsize:
                 raise RuntimeError(f"{_LIBPATHS[precision]} is not the {precision} build")
@@ -151,13 +151,17 @@ def route_fwd(sources, q, g, H: int, r: int | None = None, eps: float = 1e-6,
 
 
 def route_bwd(sources, q, g, dout, H: int, r: int | None = None, eps: float = 1e-6,
-              full_width: bool = False, dsrc=None, precision: str = "f64"):
+              full_width: bool = False, dsrc=None, precision: str = "f64", fwd_out=None):
     """Backward of one routing site.
 
     Returns ``(dsrc, dq, dg)``: ``dsrc`` a list of N [T, d] arrays holding
     dL/ds_n (if ``dsrc`` is given, the site's gradients are ADDED to those
     arrays in place), ``dq`` and ``dg`` [r]; all in the arithmetic type of
     ``precision`` ("f64", the parity reference, or "f32").
+    ``fwd_out`` ([T, d] or None): the forward output whose per-head dot with
+    dout couples the sources in the routing feedback. None recomputes it (the
+    definition); given, it is taken as is (the stored output a one-pass
+    backward reads, e.g. rounded to bf16).
     """
     dt = _NP[precision]
     srcs = [_arr(s, precision) for s in sources]
@@ -174,8 +178,12 @@ def route_bwd(sources, q, g, dout, H: int, r: int | None = None, eps: float = 1e
     G = _arr(dout, precision)
     dq = np.empty(r, dtype=dt)
     dg = np.empty(r, dtype=dt)
+    fo = None if fwd_out is None else _arr(fwd_out, precision)
+    if fo is not None and fo.shape != (T, d):
+        raise ValueError("fwd_out must be [T, d]")
     _check(lib(precision).orc_route_bwd(_ptr_array(srcs), N, T, d, r, H, int(full_width), eps,
                                _ptr(qq), None if gg is None else _ptr(gg), _ptr(G),
+                               None if fo is None else _ptr(fo),
                                _ptr_array(dsrc), _ptr(dq), _ptr(dg)))
     return dsrc, dq, dg
 

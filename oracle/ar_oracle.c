@@ -163,13 +163,20 @@ int orc_route_fwd(const real *const *src, int N, int64_t T, int d, int r, int H,
  * ("Multi-Head Attention Residuals", Appendix E, dq and dg):
  *   dq_c = sum_{t,n} fb_{n,h(c)} inv_n g_c s_{n,c},   dg_c = sum_{t,n} fb_{n,h(c)} inv_n q_c s_{n,c},
  * where fb_{n,h} = alpha_{n,h} <G_[h], s_{n,[h]} - out_[h]> is the routing feedback.
+ *   fwd_out : [T,d] or NULL. NULL: out in the feedback is the read itself,
+ *             recomputed here (the definition). Otherwise out_[h] in the
+ *             feedback is taken from this array: the forward output a
+ *             one-pass backward is given (as stored, e.g. rounded to bf16),
+ *             where "Multi-Head Attention Residuals", Appendix E (Figure 10)
+ *             accumulates the coupling sum_n alpha <G_[h], s_{n,[h]}> over the
+ *             sources in a first pass.
  *   dsrc[n] : [T,d], ADDED to (the caller zeroes it; a row read by several
  *             sites sums their contributions)
  *   dq, dg  : [r], overwritten; dg may be NULL. g may be NULL (= ones).
  */
 int orc_route_bwd(const real *const *src, int N, int64_t T, int d, int r, int H,
                   int full_width, double eps, const real *q, const real *g,
-                  const real *dout, real *const *dsrc, real *dq, real *dg)
+                  const real *dout, const real *fwd_out, real *const *dsrc, real *dq, real *dg)
 {
     if (check_shape(N, T, d, r, H)) return ORC_BAD_ARG;
     const int K = d / H, Kr = r / H, c_key = d - r;
@@ -225,7 +232,7 @@ int orc_route_bwd(const real *const *src, int N, int64_t T, int d, int r, int H,
                 int h = c / K;
                 real acc = (real)0;
                 for (int n = 0; n < N; ++n) acc += a[n * H + h] * src[n][t * d + c];
-                o[c] = acc;
+                o[c] = fwd_out ? fwd_out[t * d + c] : acc;
             }
             /* routing feedback fb_{n,h} = alpha <G_[h], s_[h] - out_[h]>  (Eq. 15, 20) */
             for (int n = 0; n < N; ++n) {

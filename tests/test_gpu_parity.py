@@ -582,17 +582,36 @@ def test_full_size_sampled_tokens(W, orc, name, heads):
     assert nmax(to64(mb.dg[s]), dg) < tol
 
 
-def test_full_size_lr_block_sampled_tokens(W, orc):
-    """The low-rank block workload at full size (T=8192, d=4096, r=1024, H=8,
-    65 sites over 9 completed + partial block sums) in the benchmark's launch
-    configuration: bank rows (bit-exact, oracle rounding of the partial sums),
-    outputs, lse and source gradients of 32 sampled tokens, dq/dg of the last
-    site over all tokens."""
+# The one-pass backward's coupling term is the per-head dot of dL/dout with
+# the forward output it is given, as stored (bf16 here): against the oracle
+# taking the same stored output, only fp32 arithmetic separates them.
+ONE_PASS_TOL = 1e-4
+
+
+@pytest.mark.parametrize("q_std", [0.02, 0.3], ids=["bench-queries", "peaked-queries"])
+@pytest.mark.parametrize("name", ["lr_block", "lr_page_1b", "lr_page_4b"])
+def test_full_size_lr_block_sampled_tokens(W, orc, name, q_std):
+    """The block workloads at full size in the benchmark's launch
+    configuration: low-rank block (T=8192, d=4096, r=1024, H=8, 65 sites over
+    9 completed + partial block sums) and the LR page's 1B and 4B models
+    (T=4096, d=1536 / 2560, r=384 / 640, one head, 49 / 89 sites, 8 blocks):
+    bank rows (bit-exact, oracle rounding of the partial sums), outputs, lse
+    and source gradients of 32 sampled tokens, dq/dg of the last site over all
+    tokens, with random norm weights.
+    - Queries of the benchmark's scale (std 0.02): everything against the
+      oracle's exact definition at the bf16 bound.
+    - Peaked queries (std 0.3: score std up to 7.6 on a 640-wide key slice):
+      outputs and lse against the exact definition at the bf16 bound, the
+      gradients against the oracle's backward with the coupling taken from the
+      stored bf16 forward output (ONE_PASS_TOL). There the stored output's
+      rounding, times the near-cancelling coupling of the dominant source, can
+      move the source gradient beyond the bf16 bound (0.033 on the 4B shape)."""
     import torch
     from oracle import schedule, storage
     _, wl = W
-    cfg = wl.CONFIGS["lr_block"]
-    inputs = synth.DeviceInputs(seed=12, q_std=0.3, g_kind="random")
+    cfg = wl.CONFIGS[name]
+    one_pass = q_std > 0.1
+    inputs = synth.DeviceInputs(seed=12, q_std=q_std, g_kind="random")
     mb = wl.Microbatch(cfg, cfg.H, inputs)
     mb.step()
     torch.cuda.synchronize()
@@ -615,12 +634,24 @@ def test_full_size_lr_block_sampled_tokens(W, orc):
         o, l = orc.route_fwd(src, to64(mb.q[s]), to64(mb.g[s]), H, r=r)
         assert nmax(to64(mb.out[s][ti]), o) < tol, s
         assert nmax(to64(mb.lse[s][ti]), l) < tol, s
+    gtol = ONE_PASS_TOL if one_pass else tol
+    exact = {j: np.zeros((len(toks), d)) for j in range(mb.n_rows)}
     for s in reversed(mb.plan.run_sites):
         src = [rows[j] for j in mb.plan.sites[s]]
         orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][ti]), H, r=r,
-                      dsrc=[dsrc[j] for j in mb.plan.sites[s]])
+                      dsrc=[dsrc[j] for j in mb.plan.sites[s]],
+                      fwd_out=to64(mb.out[s][ti]) if one_pass else None)
+        if one_pass:
+            orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][ti]), H, r=r,
+                          dsrc=[exact[j] for j in mb.plan.sites[s]])
     for j in range(mb.n_rows):
-        assert nmax(to64(mb.bank.grad[j][ti]), dsrc[j]) < tol, j
+        kern = to64(mb.bank.grad[j][ti])
+        assert nmax(kern, dsrc[j]) < gtol, j
+        if one_pass:
+            # against the exact definition: within the bf16 bound, or within
+            # what the stored output's rounding alone accounts for
+            explained = nmax(dsrc[j], exact[j])
+            assert nmax(kern, exact[j]) < max(tol, explained + 2 * ONE_PASS_TOL), (j, explained)
     s = mb.plan.run_sites[-1]
     dq = np.zeros(r)
     dg = np.zeros(r)
@@ -629,8 +660,9 @@ def test_full_size_lr_block_sampled_tokens(W, orc):
         outs_sl = [to64(inputs.output(j, T, d, "bf16")[sl]) for j in range(mb.n_rows)]
         rows_sl = storage.block_bank(outs_sl, oplan, "bf16")
         src = [rows_sl[j] for j in mb.plan.sites[s]]
-        _, a, b = orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][sl]), H, r=r)
+        _, a, b = orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][sl]), H, r=r,
+                                fwd_out=to64(mb.out[s][sl]) if one_pass else None)
         dq += a
         dg += b
-    assert nmax(to64(mb.dq[s]), dq) < tol
-    assert nmax(to64(mb.dg[s]), dg) < tol
+    assert nmax(to64(mb.dq[s]), dq) < gtol
+    assert nmax(to64(mb.dg[s]), dg) < gtol

@@ -461,3 +461,41 @@ def test_float32_build_agrees_with_float64(orc, N, T, d, H, r, fw):
         assert np.all(dq32 == 0) and np.all(dg32 == 0)
     inv32 = orc.inv_rms(srcs32[0], r=r, full_width=fw, precision="f32")
     assert nmax(inv32, orc.inv_rms(srcs32[0], r=r, full_width=fw)) < 1e-6
+
+
+@pytest.mark.parametrize("N,T,d,H,r,fw", [(5, 9, 64, 4, 64, False), (4, 7, 96, 1, 32, False),
+                                          (3, 5, 64, 8, 32, True)])
+def test_backward_coupling_from_a_given_forward_output(orc, N, T, d, H, r, fw):
+    """route_bwd(fwd_out=...): the forward output enters the backward only
+    through its per-head dot with dL/dout (the coupling of the sources in the
+    routing feedback, "Multi-Head Attention Residuals", Appendix E). So:
+    the oracle's own forward output gives the recomputing backward's result;
+    an output changed orthogonally to dL/dout within every head gives the same
+    result again; a change along dL/dout changes the result linearly (twice
+    the change, twice the difference) and not at all the direct value term
+    outside the key slice."""
+    srcs, q, g, G = _case(17, N, T, d, H, r)
+    out, _ = orc.route_fwd(srcs, q, g, H, r=r, full_width=fw)
+    ref = orc.route_bwd(srcs, q, g, G, H, r=r, full_width=fw)
+    same = orc.route_bwd(srcs, q, g, G, H, r=r, full_width=fw, fwd_out=out)
+    for a, b in zip(ref[0] + list(ref[1:]), same[0] + list(same[1:])):
+        assert _nmax(b, a) < 1e-12
+    K = d // H
+    rng = np.random.default_rng(5)
+    X = rng.normal(size=(T, d))
+    for t in range(T):                         # X_[h] orthogonal to G_[h] in every head
+        for h in range(H):
+            sl = slice(h * K, (h + 1) * K)
+            gh = G[t, sl]
+            X[t, sl] -= gh * np.dot(gh, X[t, sl]) / np.dot(gh, gh)
+    orth = orc.route_bwd(srcs, q, g, G, H, r=r, full_width=fw, fwd_out=out + 0.3 * X)
+    for a, b in zip(ref[0] + list(ref[1:]), orth[0] + list(orth[1:])):
+        assert _nmax(b, a) < 1e-10
+    d1 = orc.route_bwd(srcs, q, g, G, H, r=r, full_width=fw, fwd_out=out + 1e-3 * G)
+    d2 = orc.route_bwd(srcs, q, g, G, H, r=r, full_width=fw, fwd_out=out + 2e-3 * G)
+    for n in range(N):
+        e1, e2 = d1[0][n] - ref[0][n], d2[0][n] - ref[0][n]
+        assert np.max(np.abs(e1)) > 0 or N == 1
+        assert np.max(np.abs(e2 - 2 * e1)) <= 1e-8 * max(np.max(np.abs(e2)), 1e-30)
+        if not fw and r < d:                   # only key / RMS coordinates feel the coupling
+            assert np.max(np.abs(e1[:, : d - r])) == 0
