@@ -83,6 +83,7 @@ SIGNATURES = {
     "ar_device_status": ([], ctypes.c_int),
     "ar_route_fwd_lost_copies": ([_P, _I32P, _I32, _I32, _P, _P, _P, _P, ctypes.c_uint32, _P],
                                  ctypes.c_int),
+    "ar_route_bwd_exact": ([_P, _SITEP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "ar_checked_fault": ([_I32P, ctypes.POINTER(ctypes.c_uint64), _U32P, _U32P], ctypes.c_int),
     "ar_checked_trim_out": ([_I64], ctypes.c_int),
 }
@@ -209,6 +210,15 @@ def ar_route_bwd_site(bank, site: ArSite, out, dout, lse, alpha, dq, dg, dalpha,
                                                        _ptr(dout), _ptr(lse), _ptr(alpha),
                                                        _ptr(dq), _ptr(dg), _ptr(dalpha), _ptr(ws),
                                                        ws_bytes, _stream(stream)))
+
+
+def ar_route_bwd_exact(bank, site: ArSite, out, dout, lse, alpha, coupling, dq, dg, dalpha, ws,
+                       ws_bytes, stream=None):
+    _check("ar_route_bwd_exact", _lib.ar_route_bwd_exact(bank, ctypes.byref(site), _ptr(out),
+                                                         _ptr(dout), _ptr(lse), _ptr(alpha),
+                                                         _ptr(coupling), _ptr(dq), _ptr(dg),
+                                                         _ptr(dalpha), _ptr(ws), ws_bytes,
+                                                         _stream(stream)))
 
 
 def ar_bank_zero_grad(bank):
@@ -545,7 +555,9 @@ class Bank:
         return ws
 
     def route_bwd(self, rows, H, q, g, out, dout, lse, dq=None, dg=None, site_id=0,
-                  stream=None, ws=None):
+                  stream=None, ws=None, exact=False):
+        """exact=True: the coupling term summed over the sources first
+        (ar_route_bwd_exact), into a [T, H] scratch allocated here."""
         dev = self.rows.device
         strided = _strided(q, g)
         if dq is None:  # laid out like q (dq is written with q's stride)
@@ -563,6 +575,11 @@ class Bank:
                     raise ValueError(f"{nm} must have the stride of {'q' if nm[-1] == 'q' else 'g'}")
         if ws is None:
             ws = self.workspace(H)
+        if exact:
+            coupling = torch.empty((self.T, H), dtype=torch.float32, device=dev)
+            ar_route_bwd_exact(self.handle, make_site(rows, H, q, g, site_id), out, dout, lse,
+                               None, coupling, dq, dg, None, ws, ws.numel() * 4, stream)
+            return dq, dg
         if strided:
             ar_route_bwd_site(self.handle, make_site(rows, H, q, g, site_id), out, dout, lse, None,
                               dq, dg, None, ws, ws.numel() * 4, stream)

@@ -68,6 +68,9 @@ struct RouteArgs {
     int has_bias;
     float bias[AR_MAX_SOURCES];
     uint32_t first_mask[AR_MAX_SOURCES / 32];  // backward: bit n set = store (first touch)
+    // backward: the coupling term S [T, H] summed exactly over the sources
+    // (route_coupling_kernel), read instead of <G_h, out_h>; nullptr: from out
+    const float *coupling;
 #ifdef AR_CHECKED
     CheckTable chk;
 #endif
@@ -88,6 +91,8 @@ struct MultiArgs {
 // Each returns cudaErrorNotSupported when no instantiation covers the shape.
 cudaError_t launch_route_fwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
 cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s);
+// The exact coupling term of a site's backward into S [T, H] (fp32).
+cudaError_t launch_route_coupling(const RouteArgs &a, float *S, ar_dtype dt, cudaStream_t s);
 cudaError_t launch_route_fwd_multi(const MultiArgs &m, ar_dtype dt, cudaStream_t s);
 cudaError_t dispatch_fwd_multi_mma(const MultiArgs &m, cudaStream_t s);  // bf16 rows
 cudaError_t route_bwd_grid(const RouteArgs &a, ar_dtype dt, int *grid_warps);

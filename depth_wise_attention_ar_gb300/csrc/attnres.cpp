@@ -181,6 +181,14 @@ void chk_fill(ar::RouteArgs &a, const ar_bank *b, bool bwd, size_t ws_bytes)
     chk_span(a, a.routed, TD, true);
     chk_span(a, a.dalpha, 4, false);
     chk_span(a, a.fresh_src, TD, false);
+    chk_span(a, a.coupling, b->T * (int64_t)a.H * 4, false);
+}
+
+// the coupling pre-pass: the backward's table, the coupling buffer writable
+void chk_fill_coupling(ar::RouteArgs &a, const ar_bank *b, float *coupling)
+{
+    chk_fill(a, b, true, 0);
+    chk_span(a, coupling, b->T * (int64_t)a.H * 4, true);
 }
 
 void chk_fill_multi(ar::MultiArgs &m, const ar_bank *b)
@@ -196,6 +204,7 @@ void chk_fill_multi(ar::MultiArgs &m, const ar_bank *b)
 }
 #define AR_CHK_FILL(a, b, bwd, ws) chk_fill((a), (b), (bwd), (ws))
 #define AR_CHK_FILL_MULTI(m, b) chk_fill_multi((m), (b))
+#define AR_CHK_FILL_COUPLING(a, b, c) chk_fill_coupling((a), (b), (c))
 
 // Tables of the launches that take no RouteArgs (append, fold, token sum,
 // merge, dq/dg reduction), filled in a per-thread slot: a launch copies its
@@ -281,6 +290,7 @@ const ar::RouteArgs *chk_reduce(const ar_bank *b, const void *ws, size_t ws_byte
 #else
 #define AR_CHK_FILL(a, b, bwd, ws) ((void)0)
 #define AR_CHK_FILL_MULTI(m, b) ((void)0)
+#define AR_CHK_FILL_COUPLING(a, b, c) ((void)0)
 inline const ar::RouteArgs *chk_append(const ar_bank *, int, int, const void *, int64_t)
 {
     return nullptr;
@@ -620,6 +630,14 @@ ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes)
     int warps = 0;
     cudaError_t e = ar::route_bwd_grid(a, bank->dtype, &warps);
     if (e != cudaSuccess) return from_cuda(e);
+    // the exact-coupling variant of the kernels (ar_route_bwd_exact) may
+    // keep more blocks resident: the workspace serves both
+    static const float kAnyCoupling = 0.f;
+    a.coupling = &kAnyCoupling;
+    int warps_cs = 0;
+    e = ar::route_bwd_grid(a, bank->dtype, &warps_cs);
+    if (e != cudaSuccess) return from_cuda(e);
+    warps = std::max(warps, warps_cs);
     // any site may run on the scalar-access kernels (repeated rows, or more
     // sources than the sliced-key kernels' key cache holds)
     int gw = 0;
@@ -635,7 +653,8 @@ namespace {
 
 ar_status route_bwd_impl(ar_bank *bank, const ar_site &st_, const void *out, const void *dout,
                          const float *lse, const float *alpha, float *dq, float *dg,
-                         float *dalpha, void *ws, size_t ws_bytes, void *stream)
+                         float *dalpha, void *ws, size_t ws_bytes, void *stream,
+                         float *coupling = nullptr)
 {
     const int32_t *rows = st_.rows;
     const int32_t n_src = st_.n_src, H = st_.H;
@@ -670,6 +689,9 @@ ar_status route_bwd_impl(ar_bank *bank, const ar_site &st_, const void *out, con
         a.dalpha = dalpha;
         for (int i = 0; i < a.n_src; ++i)
             if (!bank->touched[a.rows[i]]) a.first_mask[i >> 5] |= 1u << (i & 31);
+        // the kernel variant (and so its grid) depends on where the coupling
+        // term comes from
+        a.coupling = coupling;
         // workspace rows of the family serving this site (at most what
         // ar_route_bwd_workspace reports)
         int ws_rows = 0;
@@ -677,6 +699,13 @@ ar_status route_bwd_impl(ar_bank *bank, const ar_site &st_, const void *out, con
         if (e != cudaSuccess) return from_cuda(e);
         if (ws_bytes < (size_t)ws_rows * ((size_t)bank->r + 4) * sizeof(float))
             return AR_ERR_CAPACITY;
+        if (coupling) {
+            // the coupling term summed over the sources first, then read by
+            // the backward in place of <G_h, out_h>
+            AR_CHK_FILL_COUPLING(a, bank, coupling);
+            e = ar::launch_route_coupling(a, coupling, bank->dtype, s);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
         AR_CHK_FILL(a, bank, true, ws_bytes);
         e = ar::launch_route_bwd(a, bank->dtype, s);
         if (e != cudaSuccess) return from_cuda(e);
@@ -719,6 +748,18 @@ ar_status ar_route_bwd_site(ar_bank *bank, const ar_site *site, const void *out,
 {
     if (!site) return AR_ERR_INVALID_ARG;
     return route_bwd_impl(bank, *site, out, dout, lse, alpha, dq, dg, dalpha, ws, ws_bytes, stream);
+}
+
+ar_status ar_route_bwd_exact(ar_bank *bank, const ar_site *site, const void *out,
+                             const void *dout, const float *lse, const float *alpha,
+                             float *coupling, float *dq, float *dg, float *dalpha, void *ws,
+                             size_t ws_bytes, void *stream)
+{
+    if (!site) return AR_ERR_INVALID_ARG;
+    if (bank && bank->T > 0 && !coupling) return AR_ERR_INVALID_ARG;
+    if (!aligned4(coupling)) return AR_ERR_ALIGN;
+    return route_bwd_impl(bank, *site, out, dout, lse, alpha, dq, dg, dalpha, ws, ws_bytes, stream,
+                          coupling);
 }
 
 ar_status ar_bank_append_broadcast(ar_bank *bank, const void *vec, int32_t *out_row, void *stream)

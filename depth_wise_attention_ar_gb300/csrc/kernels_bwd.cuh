@@ -61,7 +61,10 @@ inline size_t bwd_smem_bytes(int d, size_t esize)
            (size_t)kBwdWarps * 2 * d * esize;
 }
 
-template <typename T, int CPL>
+// CS: the coupling term comes from a.coupling (ar_route_bwd_exact), not from
+// the forward output (a separate instantiation keeps the one-pass kernel as
+// it was)
+template <typename T, int CPL, bool CS = false>
 __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     route_bwd_kernel(const __grid_constant__ RouteArgs a)
 {
@@ -202,7 +205,8 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
                 }
                 sp = __fadd_rn(sp, dot8(G[j], o));
             }
-            S_h = group_sum(sp, LPH);
+            if constexpr (CS) S_h = ldg_chk(a.coupling + (tok * H + h));
+            else S_h = group_sum(sp, LPH);
             if (tok + GW < TT) fetch_token(tok + GW);      // this lane's chunks are read
             if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted by the warp owning (t, 0)
             lse_h = ldg_chk(a.lse + tok * H + h);
@@ -299,10 +303,10 @@ __global__ void __launch_bounds__(kBwdWarps * 32, CPL <= 2 ? 4 : 1)
     }
 }
 
-template <typename T, int CPL>
-cudaError_t bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_rows)
+template <typename T, int CPL, bool CS>
+cudaError_t bwd_inst_cs(const RouteArgs *a, cudaStream_t s, int *grid_rows)
 {
-    const void *k = reinterpret_cast<const void *>(&route_bwd_kernel<T, CPL>);
+    const void *k = reinterpret_cast<const void *>(&route_bwd_kernel<T, CPL, CS>);
     const size_t smem = bwd_smem_bytes(a->d, sizeof(T));
     int grid = 0;
     cudaError_t e = persistent_grid(k, kBwdWarps * 32, smem, &grid);
@@ -311,8 +315,15 @@ cudaError_t bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_rows)
         *grid_rows = grid;  // workspace rows: one per block
         return cudaSuccess;
     }
-    route_bwd_kernel<T, CPL><<<grid, kBwdWarps * 32, smem, s>>>(*a);
+    route_bwd_kernel<T, CPL, CS><<<grid, kBwdWarps * 32, smem, s>>>(*a);
     return cudaGetLastError();
+}
+
+template <typename T, int CPL>
+cudaError_t bwd_inst(const RouteArgs *a, cudaStream_t s, int *grid_rows)
+{
+    return a->coupling ? bwd_inst_cs<T, CPL, true>(a, s, grid_rows)
+                       : bwd_inst_cs<T, CPL, false>(a, s, grid_rows);
 }
 
 // Same shapes as the forward. With grid_rows != nullptr only the grid (in

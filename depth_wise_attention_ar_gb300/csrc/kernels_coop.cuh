@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
                 }
                 sp = __fadd_rn(sp, dot8(G[j], o));
             }
-            S_h = group_sum(sp, mp.LPH);
+            S_h = a.coupling ? ldg_chk(a.coupling + (tok * H + mp.h)) : group_sum(sp, mp.LPH);
             if (kTok && tok + GB < TT) fetch_token(tok + GB);   // this thread's chunks are read
             if (a.dalpha && n == 0) dal += warp_sum(raw);  // each token counted once
             lse_h = ldg_chk(a.lse + tok * H + mp.h);

@@ -149,7 +149,7 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
                 sp = fmaf(alpha * gv, ov, sp);
             }
             sp = warp_sum(sp);
-            if (lane == 0) S[h] = sp;
+            if (lane == 0) S[h] = a.coupling ? ldg_chk(a.coupling + (t * H + h)) : sp;
         }
         if (a.dalpha) dal += warp_sum(raw);
         for (int n = lane; n < N; n += 32) cinv[n] = ldg_chk(a.inv + t * a.inv_ld + s_rows[n]);
@@ -234,6 +234,72 @@ __global__ void route_bwd_generic_kernel(const __grid_constant__ RouteArgs a, in
             st_chk(tail + 3, 0.f);
         }
     }
+}
+
+// The exact coupling term of a site's backward, summed over the sources as in
+// the first sweep of "Multi-Head Attention Residuals", Appendix E (Figure 10):
+//   S[t, h] = alpha * sum_n w_{n,h} <dL/dout_[h], s_{n,[h]}>,  w = exp(z - lse)
+// with the scores recomputed as the forward takes them (z = inv * <q g, key
+// slice h>, plus log k for a row listed k times) and alpha the delta form's
+// gate (1 otherwise). Every shape: one warp per token, the heads in turn,
+// the rows inner, scalar element accesses. The backward kernels read S
+// instead of <G_h, out_h> from the stored forward output, whose rounding
+// (bf16) would otherwise enter every routing feedback.
+template <typename T>
+__global__ void route_coupling_kernel(const __grid_constant__ RouteArgs a, float *S_out, int wpb)
+{
+    AR_CHK_ENTER(a);
+    extern __shared__ __align__(16) float gsm[];
+    __shared__ int s_rows[AR_MAX_SOURCES];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = a.d, r = a.r, H = a.H, N = a.n_src;
+    const int K = d / H, Kr = r / H, kstart = d - r;
+    const int64_t TT = a.T;
+    float *qg = gsm;                                            // [r]
+    for (int i = threadIdx.x; i < N; i += blockDim.x) s_rows[i] = a.rows[i];
+    for (int c = threadIdx.x; c < r; c += blockDim.x) qg[c] = gen_qg(a, c);
+    __syncthreads();
+    const T *bank = static_cast<const T *>(a.bank);
+    const T *dout = static_cast<const T *>(a.dout);
+    const float alpha = a.alpha ? ldg_chk(a.alpha) : 1.0f;
+    const int64_t gw = (int64_t)blockIdx.x * wpb + warp;
+    const int64_t GW = (int64_t)gridDim.x * wpb;
+    for (int64_t t = gw; t < TT; t += GW) {
+        const int64_t trow = t * d;
+        for (int h = 0; h < H; ++h) {
+            const float lse = ldg_chk(a.lse + (t * H + h));
+            float S = 0.f;
+            for (int n = 0; n < N; ++n) {
+                const T *src = bank + ((int64_t)s_rows[n] * TT + t) * d;
+                float P = 0.f, zr = 0.f;
+                for (int k = lane; k < K; k += 32)
+                    P = fmaf(gen_ld(dout + trow + h * K + k), gen_ld(src + h * K + k), P);
+                for (int k = lane; k < Kr; k += 32)
+                    zr = fmaf(qg[h * Kr + k], gen_ld(src + kstart + h * Kr + k), zr);
+                P = warp_sum(P);
+                zr = warp_sum(zr);
+                float z = __fmul_rn(zr, ldg_chk(a.inv + (t * a.inv_ld + s_rows[n])));
+                if (a.has_bias) z = __fadd_rn(z, a.bias[n]);
+                S = fmaf(exp2f((z - lse) * kLog2e), P, S);
+            }
+            if (lane == 0) st_chk(S_out + (t * H + h), alpha * S);
+        }
+    }
+}
+
+template <typename T>
+cudaError_t dispatch_coupling(const RouteArgs &a, float *S, cudaStream_t s)
+{
+    constexpr int wpb = 4;
+    const size_t smem = (size_t)a.r * 4;
+    const void *k = reinterpret_cast<const void *>(&route_coupling_kernel<T>);
+    int grid = 0;
+    cudaError_t e = persistent_grid(k, wpb * 32, smem, &grid);
+    if (e != cudaSuccess) return e;
+    const int64_t need = (a.T + wpb - 1) / wpb;
+    if (need < grid) grid = (int)need;
+    route_coupling_kernel<T><<<grid, wpb * 32, smem, s>>>(a, S, wpb);
+    return cudaGetLastError();
 }
 
 template <typename T>

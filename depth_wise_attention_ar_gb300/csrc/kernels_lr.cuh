@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(32) route_bwd_lr_kernel(const __grid_constant_
             });
             // each token's <dL/dh, routed> counted by the warp owning (t, 0)
             if (a.dalpha && n == 0) dal += warp_sum(sp);
-            S_h = alpha * group_sum(sp, LPH);
+            S_h = a.coupling ? ldg_chk(a.coupling + (tok * H + h)) : alpha * group_sum(sp, LPH);
             if constexpr (kPre) {
                 lse_h = pre_lse;
                 if (lane < N) cur_inv[lane] = pre_inv;

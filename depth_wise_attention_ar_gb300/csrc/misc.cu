@@ -22,6 +22,7 @@ template <typename T> cudaError_t dispatch_coop_fwd(const RouteArgs &a, cudaStre
 template <typename T> cudaError_t dispatch_coop_bwd(const RouteArgs *a, cudaStream_t s, int *grid_rows);
 template <typename T> cudaError_t dispatch_generic_fwd(const RouteArgs &a, cudaStream_t s);
 template <typename T> cudaError_t dispatch_generic_bwd(const RouteArgs *a, cudaStream_t s, int *grid_warps);
+template <typename T> cudaError_t dispatch_coupling(const RouteArgs &a, float *S, cudaStream_t s);
 
 // Device error word; kernels get its address as an argument.
 __device__ unsigned int g_device_error = 0;
@@ -579,6 +580,11 @@ static cudaError_t bwd_any(const RouteArgs &a, ar_dtype dt, cudaStream_t s, int 
                   : dispatch_generic_bwd<float>(&a, s, rows);
     default: return cudaErrorNotSupported;
     }
+}
+
+cudaError_t launch_route_coupling(const RouteArgs &a, float *S, ar_dtype dt, cudaStream_t s)
+{
+    return dt == AR_BF16 ? dispatch_coupling<__nv_bfloat16>(a, S, s) : dispatch_coupling<float>(a, S, s);
 }
 
 cudaError_t launch_route_bwd(const RouteArgs &a, ar_dtype dt, cudaStream_t s)

@@ -297,3 +297,15 @@ def test_checked_build_has_its_own_library_and_objects():
     from depth_wise_attention_ar_gb300 import build
     assert build.LIB != build.LIB_CHECKED and build.BUILD != build.BUILD_CHECKED
     assert os.path.dirname(build.LIB_CHECKED) == os.path.dirname(build.LIB)
+
+
+def test_exact_backward_checks_precede_launch(B):
+    """ar_route_bwd_exact refuses a missing or misaligned coupling buffer
+    before anything is launched."""
+    h = _bank(B)
+    site = B.make_site([0], 4, FAKE, None, 0)
+    assert _err(B.ar_route_bwd_exact, h, site, FAKE, FAKE, FAKE, None, None, FAKE, None, None,
+                FAKE, 1 << 20, 0) == "AR_ERR_INVALID_ARG"
+    assert _err(B.ar_route_bwd_exact, h, site, FAKE, FAKE, FAKE, None, FAKE + 2, FAKE, None, None,
+                FAKE, 1 << 20, 0) == "AR_ERR_ALIGN"
+    B.ar_bank_destroy(h)

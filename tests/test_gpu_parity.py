@@ -582,6 +582,44 @@ def test_full_size_sampled_tokens(W, orc, name, heads):
     assert nmax(to64(mb.dg[s]), dg) < tol
 
 
+@pytest.mark.parametrize("d,r,H,dtype", [(1280, 1280, 1, "bf16"), (1280, 1280, 8, "bf16"),
+                                         (512, 512, 4, "bf16"), (4096, 4096, 8, "bf16"),
+                                         (4096, 1024, 8, "bf16"), (2560, 640, 1, "bf16"),
+                                         (1536, 384, 1, "bf16"), (520, 520, 4, "bf16"),
+                                         (1280, 1280, 8, "f32")])
+def test_exact_coupling_backward(W, orc, d, r, H, dtype):
+    """ar_route_bwd_exact on every backward family (one-warp full keys, the
+    short rows, four warps with full and sliced keys, one-warp sliced keys,
+    scalar access), with peaked queries: the source gradients, dq and dg
+    against the oracle's exact definition, and the one-pass ar_route_bwd of
+    the same site against the oracle taking the coupling from the stored
+    forward output."""
+    import torch
+    B, _ = W
+    T, N = 777, 3
+    tol = 1e-5 if dtype == "f32" else ONE_PASS_TOL
+    inp = synth.HostInputs(seed=31 + d + H, q_std=0.5, g_kind="random")
+    bank = B.Bank(T, d, r, N, dtype)
+    for j in range(N):
+        bank.append(inp.output(j, T, d, dtype))
+    rows = list(range(N))
+    q, g = inp.query(0, r), inp.norm_weight(0, r)
+    host = [inp.host_output(j, T, d, dtype) for j in rows]
+    hq, hg, hG = inp.host_query(0, r), inp.host_norm_weight(0, r), inp.host_dout(0, T, d, dtype)
+    dout = inp.dout(0, T, d, dtype)
+    for exact in (True, False):
+        out, lse = bank.route_fwd(rows, H, q, g, site_id=0)
+        bank.zero_grad()
+        dq, dg = bank.route_bwd(rows, H, q, g, out, dout, lse, site_id=0, exact=exact)
+        torch.cuda.synchronize()
+        ref, rdq, rdg = orc.route_bwd(host, hq, hg, hG, H, r=r,
+                                      fwd_out=None if exact else to64(out))
+        for j in rows:
+            assert nmax(to64(bank.grad[j]), ref[j]) < tol, (exact, j)
+        assert nmax(to64(dq), rdq) < tol and nmax(to64(dg), rdg) < tol, exact
+    bank.close()
+
+
 # The one-pass backward's coupling term is the per-head dot of dL/dout with
 # the forward output it is given, as stored (bf16 here): against the oracle
 # taking the same stored output, only fp32 arithmetic separates them.
