@@ -323,7 +323,8 @@ ar_status ar_route_bwd_workspace(const ar_bank *bank, int32_t H, size_t *bytes);
  *           a nearly cancelling feedback. Its key-path gradient can then
  *           differ from the exact one by a few percent of the row's largest
  *           gradient: 3.3 % measured on the LR page's 4B shape with peaked
- *           queries.
+ *           queries. ar_route_bwd_exact sums the coupling over the sources
+ *           instead.
  *   dout  : device [T, d] of the bank dtype, dL/dout
  *   lse   : device float [T, H] written by this site's forward
  *   dq    : device float [r], overwritten with dL/dq
