@@ -248,8 +248,12 @@ class Microbatch:
                     on_site("fwd", t)
         return appended
 
-    def backward(self, stream=None, on_site=None):
+    def backward(self, stream=None, on_site=None, exact=False):
+        """Every site's backward in reverse; exact=True sums each site's coupling
+        term over its sources first (ar_route_bwd_exact; plain form only)."""
         bank, plan = self.bank, self.plan
+        if exact and self.cfg.delta:
+            raise ValueError("exact coupling is wired for the plain form here")
         bank.zero_grad()
         for t in reversed(plan.run_sites):
             if on_site:
@@ -262,7 +266,7 @@ class Microbatch:
             else:
                 bank.route_bwd(plan.sites[t], self.H, self.q[t], self.g[t], self.out[t],
                                self.dout[t], self.lse[t], self.dq[t], dg, site_id=t,
-                               stream=stream, ws=self.ws)
+                               stream=stream, ws=self.ws, exact=exact)
             if on_site:
                 on_site("bwd_end", t)
         if self.cfg.delta:

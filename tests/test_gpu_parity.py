@@ -704,3 +704,24 @@ def test_full_size_lr_block_sampled_tokens(W, orc, name, q_std):
         dg += b
     assert nmax(to64(mb.dq[s]), dq) < gtol
     assert nmax(to64(mb.dg[s]), dg) < gtol
+    if one_pass:
+        # the same microbatch again with the coupling summed over the sources
+        # (ar_route_bwd_exact): the exact definition at the tight bound
+        mb.forward()
+        mb.backward(exact=True)
+        torch.cuda.synchronize()
+        for j in range(mb.n_rows):
+            assert nmax(to64(mb.bank.grad[j][ti]), exact[j]) < ONE_PASS_TOL, ("exact", j)
+        dq[:] = 0
+        dg[:] = 0
+        for t0 in range(0, T, 1024):
+            sl = slice(t0, min(T, t0 + 1024))
+            outs_sl = [to64(inputs.output(j, T, d, "bf16")[sl]) for j in range(mb.n_rows)]
+            rows_sl = storage.block_bank(outs_sl, oplan, "bf16")
+            src = [rows_sl[j] for j in mb.plan.sites[s]]
+            _, a, b = orc.route_bwd(src, to64(mb.q[s]), to64(mb.g[s]), to64(mb.dout[s][sl]), H,
+                                    r=r)
+            dq += a
+            dg += b
+        assert nmax(to64(mb.dq[s]), dq) < ONE_PASS_TOL
+        assert nmax(to64(mb.dg[s]), dg) < ONE_PASS_TOL
