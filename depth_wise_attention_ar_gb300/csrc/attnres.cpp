@@ -756,6 +756,7 @@ ar_status ar_route_bwd_exact(ar_bank *bank, const ar_site *site, const void *out
                              size_t ws_bytes, void *stream)
 {
     if (!site) return AR_ERR_INVALID_ARG;
+    if (alpha || dalpha) return AR_ERR_UNSUPPORTED;   // the plain form only
     if (bank && bank->T > 0 && !coupling) return AR_ERR_INVALID_ARG;
     if (!aligned4(coupling)) return AR_ERR_ALIGN;
     return route_bwd_impl(bank, *site, out, dout, lse, alpha, dq, dg, dalpha, ws, ws_bytes, stream,

@@ -447,21 +447,23 @@ ar_status ar_route_bwd_site(ar_bank *bank, const ar_site *site, const void *out,
                             const void *dout, const float *lse, const float *alpha, float *dq,
                             float *dg, float *dalpha, void *ws, size_t ws_bytes, void *stream);
 
-/* ar_route_bwd_site with the coupling term summed over the sources, as in the
- * first pass of "Multi-Head Attention Residuals", Appendix E (Figure 10):
- *   coupling[t, h] = alpha * sum_n w_{n,h} <dout_[h], s_{n,[h]}>
- * (alpha = 1 without the delta form) is computed into `coupling` first (one
- * more read of the site's rows), and the backward then uses it in place of the
- * per-head dot of dout with `out`. This makes the source, query and norm-weight
+/* ar_route_bwd_site (plain form) with the coupling term summed over the
+ * sources, as in the first pass of "Multi-Head Attention Residuals", Appendix E
+ * (Figure 10):
+ *   coupling[t, h] = sum_n w_{n,h} <dout_[h], s_{n,[h]}>
+ * is computed into `coupling` first (one more read of the site's rows), and
+ * the backward then uses it in place of the per-head dot of dout with `out`. This makes the source, query and norm-weight
  * gradients exact up to fp32 rounding, whatever the precision of the stored
  * forward output. For a bf16 bank, the one-pass backward (ar_route_bwd and
  * ar_route_bwd_site) carries the output's rounding into the feedback of a
- * dominant source (see ar_route_bwd, `out`). `out` is still read, for dL/dalpha
- * and the token buffers.
+ * dominant source (see ar_route_bwd, `out`). `out` is still read (the token
+ * buffers).
  *   coupling : device float [T, H], written (caller-owned scratch)
+ *   alpha, dalpha : must be NULL (the delta form is not served here)
  *   other arguments as ar_route_bwd_site.
- * Errors: as ar_route_bwd_site; AR_ERR_INVALID_ARG for a NULL coupling when
- * T > 0, AR_ERR_ALIGN for one not 4-byte aligned. */
+ * Errors: as ar_route_bwd_site; AR_ERR_UNSUPPORTED for a non-NULL alpha or
+ * dalpha, AR_ERR_INVALID_ARG for a NULL coupling when T > 0, AR_ERR_ALIGN for
+ * one not 4-byte aligned. */
 ar_status ar_route_bwd_exact(ar_bank *bank, const ar_site *site, const void *out,
                              const void *dout, const float *lse, const float *alpha,
                              float *coupling, float *dq, float *dg, float *dalpha, void *ws,

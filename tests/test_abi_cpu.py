@@ -300,12 +300,14 @@ def test_checked_build_has_its_own_library_and_objects():
 
 
 def test_exact_backward_checks_precede_launch(B):
-    """ar_route_bwd_exact refuses a missing or misaligned coupling buffer
-    before anything is launched."""
+    """ar_route_bwd_exact refuses a missing or misaligned coupling buffer, and
+    the delta form, before anything is launched."""
     h = _bank(B)
     site = B.make_site([0], 4, FAKE, None, 0)
     assert _err(B.ar_route_bwd_exact, h, site, FAKE, FAKE, FAKE, None, None, FAKE, None, None,
                 FAKE, 1 << 20, 0) == "AR_ERR_INVALID_ARG"
     assert _err(B.ar_route_bwd_exact, h, site, FAKE, FAKE, FAKE, None, FAKE + 2, FAKE, None, None,
                 FAKE, 1 << 20, 0) == "AR_ERR_ALIGN"
+    assert _err(B.ar_route_bwd_exact, h, site, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                FAKE, 1 << 20, 0) == "AR_ERR_UNSUPPORTED"      # the delta form
     B.ar_bank_destroy(h)
