@@ -311,3 +311,15 @@ def test_exact_backward_checks_precede_launch(B):
     assert _err(B.ar_route_bwd_exact, h, site, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
                 FAKE, 1 << 20, 0) == "AR_ERR_UNSUPPORTED"      # the delta form
     B.ar_bank_destroy(h)
+
+
+def test_binding_signatures_match_the_header_parameter_counts(B):
+    """Every ctypes signature in the binding takes as many arguments as its C
+    declaration in include/attnres.h has parameters (a parameter added on one
+    side only would shift every argument after it)."""
+    txt = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = dict(re.findall(r"\b(ar_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", txt))
+    for name, (argtypes, _) in B.SIGNATURES.items():
+        params = " ".join(decls[name].split())
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert n == len(argtypes), (name, n, len(argtypes))
