@@ -499,3 +499,8 @@ def test_backward_coupling_from_a_given_forward_output(orc, N, T, d, H, r, fw):
         assert np.max(np.abs(e2 - 2 * e1)) <= 1e-8 * max(np.max(np.abs(e2)), 1e-30)
         if not fw and r < d:                   # only key / RMS coordinates feel the coupling
             assert np.max(np.abs(e1[:, : d - r])) == 0
+    # the float32 build takes the same argument
+    f32 = orc.route_bwd(srcs, q, g, G, H, r=r, full_width=fw, fwd_out=out + 1e-3 * G,
+                        precision="f32")
+    for a, b in zip(d1[0], f32[0]):
+        assert _nmax(b.astype(np.float64), a) < 1e-5
